@@ -1,0 +1,434 @@
+"""Benchmark of the KDA hot path on one GB300 (or N independent replicas).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  prefill : B=1, T=8192, H=12, d=128, initial state ~ N(0, 0.02^2), o in bf16
+  decode  : 256 sequences x 96 heads, one token each, on a 1.6 GB fp32 state updated in place
+value = (prefill + decode) token-heads per second over the whole job; the prefill and
+decode parts are also reported on their own, with their roofline fractions.
+
+Run:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 is launched with torchrun, one rank per GPU, each rank a full replica
+(independent sequences, no collective on the data path: weak scaling).
+--impl reference times the fp64 CPU oracle on this host's cores (a bounded sample of
+the same workload per step).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_attention_serving_02_gb300 import inputs  # noqa: E402
+
+PREFILL_T, PREFILL_H = 8192, 12
+DECODE_N, DECODE_H = 256, 96
+D = 128
+# algorithmic bytes per token-head
+PREFILL_BYTES_PER_TH = 4 * 2 * D + 4 * D + 4          # q, k, v, o (bf16) + z (fp32) + b = 1540
+DECODE_BYTES_PER_TH = 2 * 4 * D * D + 3 * 2 * D + 4 * D + 4 + 4 * D   # S read+write, q,k,v, z, b, o = 132868
+# algorithmic tensor-core flops per token-head of the chunk form (C=64, triangles counted once)
+PREFILL_FLOPS_PER_TH = 5 * 64 * D + 6 * D * D          # 139264
+METRIC = "KDA prefill tokens/s·head & decode tokens/s at d=128 on 1 GB300; % of roofline"
+WORKLOAD = ("prefill B=1 T=8192 H=12 d=128 (S0~N(0,0.02^2), o bf16) + decode N=256 H=96 d=128 "
+            "(1 token/seq, 1.6 GB fp32 state in place)")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# ranks
+# ------------------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------
+# workload
+# ------------------------------------------------------------------------------------
+def make_workload(rank, n_steps):
+    """Prefill inputs (drawn on the host from the seeded generator, so the oracle sees the
+    same tensors) and device-resident decode state and per-step decode inputs."""
+    seed = 1000 * rank
+    pre_cpu = inputs.prefill_inputs(PREFILL_T, PREFILL_H, 1, seed=seed, init_state=True)
+    pre = {k: v.cuda() for k, v in pre_cpu.items()}
+    state = inputs.decode_state(DECODE_N, DECODE_H, seed=seed + 1, device="cuda")
+    dec = [inputs.decode_step_inputs(DECODE_N, DECODE_H, seed=seed + 1, step=i, device="cuda")
+           for i in range(n_steps)]
+    return pre_cpu, pre, state, dec
+
+
+class Flusher:
+    """Writes a buffer larger than L2 (129 MB) between timed steps."""
+
+    def __init__(self, nbytes=512 << 20):
+        self.buf = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def run_ours_device(pre, state, dec, steps, warmup, world):
+    from linear_attention_serving_02_gb300 import kda
+
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(PREFILL_T, 1, PREFILL_H), dtype=torch.uint8, device="cuda")
+    o = torch.empty(pre["q"].shape, dtype=torch.bfloat16, device="cuda")
+    S = torch.empty((1, PREFILL_H, D, D), dtype=torch.float32, device="cuda")
+    o_dec = torch.empty((DECODE_N, DECODE_H, D), dtype=torch.float32, device="cuda")
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        kda.kda_chunk_prefill(pre["q"], pre["k"], pre["v"], pre["z"], pre["A"], pre["b"], initial_state=pre["S0"],
+                              o=o, final_state=S, workspace=ws)
+        d = dec[i]
+        kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["z"], d["A"], d["b"], state, o=o_dec)
+
+    for i in range(warmup):
+        flush()
+        step(i)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush()
+        e0, e1, e2 = ev[j]
+        d = dec[warmup + j]
+        e0.record(stream)
+        kda.kda_chunk_prefill(pre["q"], pre["k"], pre["v"], pre["z"], pre["A"], pre["b"], initial_state=pre["S0"],
+                              o=o, final_state=S, workspace=ws)
+        e1.record(stream)
+        kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["z"], d["A"], d["b"], state, o=o_dec)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    pre_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    finite = bool(torch.isfinite(S).all() and torch.isfinite(o_dec).all())
+    return pre_ms, dec_ms, finite
+
+
+def run_ours_e2e(pre_cpu, dec, steps, warmup, world):
+    """Same step through the public API with host buffers: every step copies its inputs
+    from pinned host memory to the device and its outputs back, inside the timed region.
+    The decode state stays resident on the device (it is the serving-side cache)."""
+    from linear_attention_serving_02_gb300 import kda
+
+    h_pre = {k: v.pin_memory() for k, v in pre_cpu.items()}
+    h_dec = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in dec[:warmup + steps]]
+    d_pre = {k: torch.empty_like(v, device="cuda") for k, v in h_pre.items()}
+    d_dec = {k: torch.empty_like(v, device="cuda") for k, v in h_dec[0].items()}
+    state = inputs.decode_state(DECODE_N, DECODE_H, seed=7, device="cuda")
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(PREFILL_T, 1, PREFILL_H), dtype=torch.uint8, device="cuda")
+    o = torch.empty(h_pre["q"].shape, dtype=torch.bfloat16, device="cuda")
+    S = torch.empty((1, PREFILL_H, D, D), dtype=torch.float32, device="cuda")
+    o_dec = torch.empty((DECODE_N, DECODE_H, D), dtype=torch.float32, device="cuda")
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_S = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    h_od = torch.empty(o_dec.shape, dtype=o_dec.dtype).pin_memory()
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in h_pre.values()) + \
+        sum(t.numel() * t.element_size() for t in h_dec[0].values())
+    d2h = sum(t.numel() * t.element_size() for t in (h_o, h_S, h_od))
+
+    def step(i):
+        for k in d_pre:
+            d_pre[k].copy_(h_pre[k], non_blocking=True)
+        for k in d_dec:
+            d_dec[k].copy_(h_dec[i][k], non_blocking=True)
+        kda.kda_chunk_prefill(d_pre["q"], d_pre["k"], d_pre["v"], d_pre["z"], d_pre["A"], d_pre["b"],
+                              initial_state=d_pre["S0"], o=o, final_state=S, workspace=ws)
+        kda.kda_recurrent_decode(d_dec["q"], d_dec["k"], d_dec["v"], d_dec["z"], d_dec["A"], d_dec["b"], state,
+                                 o=o_dec)
+        h_o.copy_(o, non_blocking=True)
+        h_S.copy_(S, non_blocking=True)
+        h_od.copy_(o_dec, non_blocking=True)
+
+    for i in range(warmup):
+        flush()
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = []
+    for j in range(steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(warmup + j)
+        e1.record(stream)
+        e1.synchronize()   # the host has the step's results before the next step starts
+        ms.append(e0.elapsed_time(e1))
+    barrier(world)
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ------------------------------------------------------------------------------------
+def oracle_sample(pre_cpu, prefill_heads, decode_pairs, seed=0):
+    """Time the fp64 oracle on a sample: the prefill batch restricted to its first
+    prefill_heads heads, plus decode_pairs (sequence, head) pairs of one decode token.
+    Returns (seconds, token-heads processed, threads)."""
+    import oracle
+
+    h = prefill_heads
+    sl = {k: (v[..., :h, :].contiguous() if k in ("q", "k", "v", "z") else v) for k, v in pre_cpu.items()}
+    sl["b"] = pre_cpu["b"][..., :h].contiguous()
+    sl["A"] = pre_cpu["A"][:h].contiguous()
+    sl["S0"] = pre_cpu["S0"][:, :h].contiguous()
+    P = decode_pairs
+    st = inputs.decode_step_inputs(P, 1, seed=seed + 11)
+    S0 = inputs.decode_state(P, 1, seed=seed + 12)
+    threads = oracle.hardware_threads()
+    t0 = time.perf_counter()
+    oracle.kda_forward(sl["q"], sl["k"], sl["v"], sl["z"], sl["A"], sl["b"], S0=sl["S0"])
+    oracle.kda_forward(st["q"].reshape(P, 1, 1, D), st["k"].reshape(P, 1, 1, D), st["v"].reshape(P, 1, 1, D),
+                       st["z"].reshape(P, 1, 1, D), st["A"], st["b"].reshape(P, 1, 1), S0=S0)
+    dt = time.perf_counter() - t0
+    return dt, PREFILL_T * h + P, threads
+
+
+def traffic_record(kernel_file, kernel_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    source of that kernel (else None)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_name)
+        src = b""
+        for fn in rec["sources"]:
+            with open(os.path.join(ROOT, fn), "rb") as f:
+                src += f.read()
+        if hashlib.sha1(src).hexdigest() != rec["sources_sha1"]:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def main_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    pre_cpu = inputs.prefill_inputs(PREFILL_T, PREFILL_H, 1, seed=0, init_state=True)
+    heads, pairs = 2, 1024
+    for _ in range(args.warmup):
+        oracle_sample(pre_cpu, heads, pairs)
+    tot_s, tot_units, threads = 0.0, 0, 1
+    for _ in range(args.steps):
+        dt, units, threads = oracle_sample(pre_cpu, heads, pairs)
+        tot_s += dt
+        tot_units += units
+    value = tot_units / tot_s
+    sample = ("per step: prefill T=8192 restricted to %d of 12 heads (%d token-heads) + %d decode "
+              "(sequence, head) pairs, one token each" % (heads, PREFILL_T * heads, pairs))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "token·head/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "token·head/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "token·head/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main_ours(args, rank, world, local):
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    n_dec = args.warmup + args.steps
+    pre_cpu, pre, state, dec = make_workload(rank, n_dec)
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    t_wall = time.perf_counter()
+    pre_ms, dec_ms, finite = run_ours_device(pre, state, dec, args.steps, args.warmup, world)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop() if clocks else None
+
+    e2e_ms, h2d, d2h = run_ours_e2e(pre_cpu, dec, args.steps, args.warmup, world)
+
+    pre_t = max_over_ranks(sum(pre_ms) / 1e3, world)
+    dec_t = max_over_ranks(sum(dec_ms) / 1e3, world)
+    step_t = max_over_ranks((sum(pre_ms) + sum(dec_ms)) / 1e3, world)
+    e2e_t = max_over_ranks(sum(e2e_ms) / 1e3, world)
+    K = args.steps
+    th_pre = PREFILL_T * PREFILL_H
+    th_dec = DECODE_N * DECODE_H
+    units = world * K * (th_pre + th_dec)
+    value = units / step_t
+
+    # roofline of each part: algorithmic bytes (flops) per launch / average launch time
+    pre_launch = pre_t / K
+    dec_launch = dec_t / K
+    dec_gbs = DECODE_BYTES_PER_TH * th_dec / dec_launch / 1e9
+    pre_gbs = PREFILL_BYTES_PER_TH * th_pre / pre_launch / 1e9
+    pre_tflops = PREFILL_FLOPS_PER_TH * th_pre / pre_launch / 1e12
+    dec_traffic = traffic_record("linear_attention_serving_02_gb300/csrc/kda_decode.cu", "kda_decode_kernel<128>")
+    roof_dec = {"kernel": "kda_decode_kernel<128>", "bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": dec_gbs / hbm, "peak_kind": peak_kind + " (burst copy)",
+                "traffic": dec_traffic, "algorithmic_bytes_per_launch": DECODE_BYTES_PER_TH * th_dec}
+    roof_pre = {"kernel": "kda_chunk_prefill (plan + intra + inter)", "bound": "hbm", "achieved": pre_gbs,
+                "peak": hbm, "unit": "GB/s", "frac": pre_gbs / hbm, "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TH * th_pre,
+                "mma_tflops": pre_tflops, "mma_frac_of_bf16": pre_tflops / tf_burst, "traffic": None}
+    dominant = roof_dec if dec_t >= pre_t else roof_pre
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        dt, cu_units, threads = oracle_sample(pre_cpu, PREFILL_H, 4096)
+        cpu = {"value": cu_units / dt, "unit": "token·head/s", "cores": threads, "kind": "oracle",
+               "sample": "prefill B=1 T=8192 H=12 (all %d token-heads) + 4096 decode (sequence, head) pairs, "
+                         "one token each; %.1f s of host time" % (th_pre, dt)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "token·head/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": 1e3 * step_t / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 operands split hi/lo, fp32 accumulate; decode f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": PREFILL_T,
+                   "parallelism": "replicas x%d" % world, "l2": "flushed between timed steps (512 MB write)"},
+        "prefill": {"value": world * K * th_pre / pre_t, "unit": "token·head/s",
+                    "tokens_per_s": world * K * PREFILL_T / pre_t, "ms": 1e3 * pre_launch, "roofline": roof_pre},
+        "decode": {"value": world * K * DECODE_N / dec_t, "unit": "token/s (one per sequence)",
+                   "token_heads_per_s": world * K * th_dec / dec_t, "ms": 1e3 * dec_launch, "roofline": roof_dec},
+        "roofline": dominant,
+        "cpu_baseline": cpu,
+        "e2e": {"value": units / e2e_t, "unit": "token·head/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+        "outputs_finite": finite,
+        "timed_wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        main_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        main_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

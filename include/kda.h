@@ -1,0 +1,157 @@
+/*
+ * kda.h - C ABI of the GB300 Kimi Delta Attention (KDA) library.
+ *
+ * KDA is the gated delta-rule recurrence, per sequence n and head h, over tokens t:
+ *
+ *   log a_t = -5 * sigmoid(exp(A_h) * z_t)       (a vector over d_k; bounded decay,
+ *                                                 'From Linear Attention to KDA', §5.4)
+ *   beta_t  = sigmoid(b_t)                       (a scalar; same page, §5.3)
+ *   S_t     = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T
+ *   o_t     = S_t^T q_t                          (same page, §5.2; 'Kimi K3 attention deep
+ *                                                 dive', §2.1; 'Kimi K3', section
+ *                                                 "Kimi Delta Attention")
+ *
+ * S is a d_k x d_v fp32 matrix (row index = key channel). The library supports
+ * d_k = d_v = 128 only. Inputs arrive already projected: q and k L2-normalised by the
+ * caller, z and b the raw pre-activations of the decay and write-strength gates.
+ * No 1/sqrt(d_k) scale is applied to q.
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device pointers owned by the caller. The library
+ *     allocates nothing and keeps no pointer after the call returns.
+ *   - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16).
+ *   - Layouts are dense row-major with the last dimension contiguous.
+ *   - 'stream' is a cudaStream_t (NULL = the legacy default stream). Work is enqueued
+ *     asynchronously; a return of KDA_OK means the arguments were valid and the
+ *     kernels were launched, not that they have finished.
+ *   - Errors are returned as kda_status codes; nothing is thrown across the ABI and no
+ *     kernel traps. A failed argument check launches nothing and writes nothing.
+ *   - Every pointer must be 16-byte aligned (the kernels use 128-bit accesses);
+ *     the prefill workspace must be 256-byte aligned.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = -1,        /* a required pointer is NULL */
+    KDA_ERR_SHAPE = -2,       /* a size is negative or inconsistent */
+    KDA_ERR_UNSUPPORTED = -3, /* d_k or d_v other than 128, or an unknown output dtype */
+    KDA_ERR_SEQLENS = -4,     /* cu_seqlens not rising from 0 to the token count */
+    KDA_ERR_ALIGN = -5,       /* a pointer is not 16-byte (workspace: 256-byte) aligned */
+    KDA_ERR_WORKSPACE = -6,   /* workspace smaller than kda_chunk_prefill_workspace_size() */
+    KDA_ERR_CUDA = -7,        /* a CUDA launch or API call failed */
+    KDA_ERR_DEVICE = -8       /* the device lacks what the kernels need (sm_103a, smem) */
+} kda_status;
+
+/* Output element type of the prefill. */
+typedef enum {
+    KDA_OUT_BF16 = 0, /* o rounded to bf16 (round to nearest even) */
+    KDA_OUT_F32 = 1   /* o kept in fp32 */
+} kda_out_dtype;
+
+/* Short English text for a status code (static storage; never NULL). */
+const char *kda_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int kda_version(void);
+
+/*
+ * Bytes of device workspace kda_chunk_prefill() needs for a batch of total_tokens
+ * tokens in num_seqs sequences and num_heads heads. The size is an upper bound that
+ * depends only on these three numbers, so one buffer serves every batch up to them.
+ * Returns 0 for negative arguments.
+ */
+size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t num_heads);
+
+/*
+ * kda_chunk_prefill - chunkwise-parallel KDA over whole sequences.
+ *
+ * Computes, for every sequence and head, all outputs o_t and the final state S_T of the
+ * recurrence above, starting from initial_state. The work is the chunkwise form of
+ * 'From Linear Attention to KDA', §7 (chunks of 64 tokens: per-chunk decayed K K^T and
+ * Q K^T matrices, the UT/WY triangular solve that turns the chain of delta updates
+ * into dense products, then a serial pass that carries S from chunk to chunk), with
+ * the 16-token tiles of §8 inside each chunk. The gate and beta are computed from
+ * z, A, b inside the kernels.
+ *
+ * Batch layouts (tokens packed row by row):
+ *   dense   : cu_seqlens == NULL. batch sequences of seq_len tokens each; num_seqs must
+ *             equal batch. Token (i, t) is row i * seq_len + t.
+ *   varlen  : cu_seqlens != NULL. batch must be 1; seq_len is the total token count;
+ *             sequence n owns rows cu_seqlens[n] .. cu_seqlens[n+1]-1. Empty sequences
+ *             are allowed (their final state equals their initial state).
+ *
+ * Arguments (T_total = batch * seq_len rows, H = num_heads):
+ *   q, k        device bf16 [T_total, H, 128]   queries, L2-normalised keys
+ *   v           device bf16 [T_total, H, 128]   values
+ *   z           device fp32 [T_total, H, 128]   decay pre-activation
+ *   A           device fp32 [H]                 per-head log scale of the decay gate
+ *   b           device fp32 [T_total, H]        write-strength pre-activation
+ *   initial_state device fp32 [num_seqs, H, 128, 128] or NULL (zeros)
+ *   cu_seqlens  device int32 [num_seqs + 1] or NULL (dense layout)
+ *   cu_seqlens_host  host int32 [num_seqs + 1] or NULL. When given it must hold the same
+ *               values as cu_seqlens; it is validated on the host before anything is
+ *               launched (KDA_ERR_SEQLENS). Without it, cu_seqlens is validated on the
+ *               device: a bad table makes the kernels fill final_state with NaN, leave o
+ *               untouched, and record KDA_ERR_SEQLENS for kda_workspace_status().
+ *   o           device [T_total, H, 128], bf16 or fp32 per o_dtype (written)
+ *   final_state device fp32 [num_seqs, H, 128, 128] (written). May alias initial_state.
+ *   workspace   device scratch of at least kda_chunk_prefill_workspace_size() bytes,
+ *               256-byte aligned. Its contents need no initialisation and are dead after
+ *               the kernels finish, except the status word read by kda_workspace_status().
+ *   stream      cudaStream_t
+ *
+ * Calls that share a workspace must be ordered on one stream.
+ */
+int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const float *z, const float *A, const float *b,
+                      const float *initial_state,
+                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                      int32_t batch, int64_t seq_len, int32_t num_seqs, int32_t num_heads,
+                      int32_t d_k, int32_t d_v,
+                      void *o, int32_t o_dtype, float *final_state,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Status recorded on the device by the last kda_chunk_prefill() that used this
+ * workspace (KDA_OK or KDA_ERR_SEQLENS). Synchronises 'stream'.
+ */
+int kda_workspace_status(const void *workspace, void *stream);
+
+/*
+ * kda_recurrent_decode - one token per sequence, the recurrence applied in place.
+ *
+ * For every sequence n and head h: read S = state[n, h], apply
+ *   S' = Diag(a) S;  p = S'^T k;  S = S' + beta k (v - p)^T;  o = S^T q
+ * (the three-step diagonal-plus-low-rank update of 'Kimi K3 attention deep dive', §2.2;
+ * the error form of 'Kimi K3', section "Kimi Delta Attention"), write S back and o out.
+ * All arithmetic is fp32.
+ *
+ * Arguments (N = num_seqs, H = num_heads):
+ *   q, k, v   device bf16 [N, H, 128]
+ *   z         device fp32 [N, H, 128]
+ *   A         device fp32 [H]
+ *   b         device fp32 [N, H]
+ *   state     device fp32 [N, H, 128, 128], read and overwritten in place
+ *   o         device fp32 [N, H, 128] (written)
+ *   stream    cudaStream_t
+ */
+int kda_recurrent_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const float *z, const float *A, const float *b,
+                         float *state, float *o,
+                         int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
+                         void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,157 @@
+// Device helpers shared by the KDA kernels: the gate, tile geometry, the layout of
+// the per-chunk record that the intra-chunk kernel writes and the inter-chunk kernel
+// reads, and thin wrappers over the PTX used (mma.sync, ldmatrix, cp.async).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kD = 128;        // d_k = d_v
+constexpr int kC = 64;         // chunk length (tokens)
+constexpr int kTile = 16;      // sub-chunk tile ('From Linear Attention to KDA', §8)
+constexpr float kGMin = -5.0f; // lower bound of log a (same page, §5.4)
+
+// Row strides (in bf16 elements) of the 16-bit tiles kept in shared memory and in the
+// chunk record. The 16-byte pad staggers rows across banks so that ldmatrix reads of
+// 8 consecutive rows hit 32 distinct banks.
+constexpr int kLd128 = kD + 8;  // 128-wide tiles: 272 B per row
+constexpr int kLd64 = kC + 8;   // 64-wide tiles: 144 B per row
+
+// ---------------------------------------------------------------------------------
+// Chunk record: everything the serial inter-chunk pass needs about one (chunk, head),
+// stored as the exact byte image of its shared-memory tiles so that it is copied with
+// plain 16-byte moves. Split-bf16 operands are stored as a hi plane then a lo plane.
+//   Wn   [2][64][kLd128] bf16   -W = -T' Khat        (rows: token i, cols: key channel)
+//   Qh   [2][64][kLd128] bf16   q_i * exp(G_i)
+//   KeT  [2][128][kLd64] bf16   k_j * exp(G_last - G_j), transposed (row: channel)
+//   Aqk  [2][64][kLd64]  bf16   decayed causal Q K^T, diagonal included
+//   gam  [128]           fp32   exp(G_last), the chunk's total decay
+//   Up   [8][64][16]     fp32   U' = T' V, in blocks of 16 value columns
+// ---------------------------------------------------------------------------------
+constexpr size_t kRecWn = 0;
+constexpr size_t kRecQh = kRecWn + 2ull * kC * kLd128 * 2;
+constexpr size_t kRecKeT = kRecQh + 2ull * kC * kLd128 * 2;
+constexpr size_t kRecAqk = kRecKeT + 2ull * kD * kLd64 * 2;
+constexpr size_t kRecGam = kRecAqk + 2ull * kC * kLd64 * 2;
+constexpr size_t kRecUp = kRecGam + kD * 4;
+constexpr size_t kRecBytes = kRecUp + (size_t)kC * kD * 4;
+static_assert(kRecBytes % 128 == 0, "chunk records must stay 128-byte aligned");
+static_assert(kRecQh % 16 == 0 && kRecKeT % 16 == 0 && kRecAqk % 16 == 0 && kRecGam % 16 == 0 &&
+              kRecUp % 16 == 0, "record fields must be 16-byte aligned");
+
+// Workspace: [0, 256) header (int32 status at offset 0), then seq_cu[N+1] and
+// chunk_off[N+1] (int32, 256-byte aligned each), then the chunk records.
+constexpr size_t kWsHeader = 256;
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline size_t ws_table_bytes(int64_t num_seqs) {
+    return align_up((size_t)(num_seqs + 1) * 4, 256);
+}
+__host__ __device__ inline int64_t chunk_bound(int64_t total_tokens, int64_t num_seqs) {
+    // sum_n ceil(len_n / C) <= (total + (C-1) * N) / C
+    return (total_tokens + (int64_t)(kC - 1) * num_seqs) / kC;
+}
+
+// ---------------------------------------------------------------------------------
+// Gate: log a = g_min * sigmoid(exp(A_h) * z), beta = sigmoid(b)
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ float gate_log_decay(float eA, float z) {
+    return kGMin / (1.0f + expf(-eA * z));
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------------------------
+// Split-bf16: x = hi + lo with hi = bf16(x), lo = bf16(x - hi). A product of two split
+// operands is taken as hi*hi + hi*lo + lo*hi, which carries about 16 mantissa bits.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat162 v) {
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &hi, uint32_t &lo) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    float2 hf = __bfloat1622float2(h);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = pack_bf16x2(h);
+    lo = pack_bf16x2(l);
+}
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    return __bfloat1622float2(h);
+}
+
+// ---------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// split-bf16 product: d += ah*bh + ah*bl + al*bh
+__device__ __forceinline__ void mma_split3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                           uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+    mma_bf16(d, al, bh0, bh1);
+    mma_bf16(d, ah, bl0, bl1);
+    mma_bf16(d, ah, bh0, bh1);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t &r0, uint32_t &r1, const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(smem_u32(p)));
+}
+
+// A fragment (16x16) of a row-major bf16 tile at (row0, col0), row stride ld elements.
+__device__ __forceinline__ void load_a(uint32_t (&r)[4], const __nv_bfloat16 *base, int ld, int row0, int col0,
+                                       int lane) {
+    ldsm_x4(r, base + (size_t)(row0 + (lane & 15)) * ld + col0 + ((lane >> 4) << 3));
+}
+// B fragments of two adjacent n8 tiles (cols n0..n0+15), k rows k0..k0+15, from a tile
+// stored [k][n] row-major: r[0],r[1] = tile n0; r[2],r[3] = tile n0+8.
+__device__ __forceinline__ void load_b_kn(uint32_t (&r)[4], const __nv_bfloat16 *base, int ld, int k0, int n0,
+                                          int lane) {
+    ldsm_x4_t(r, base + (size_t)(k0 + (lane & 7) + (((lane >> 3) & 1) << 3)) * ld + n0 + ((lane >> 4) << 3));
+}
+// B fragment of one n8 tile (rows n0..n0+7 of a tile stored [n][k] row-major), k0..k0+15.
+__device__ __forceinline__ void load_b_nk(uint32_t &r0, uint32_t &r1, const __nv_bfloat16 *base, int ld, int n0,
+                                          int k0, int lane) {
+    ldsm_x2(r0, r1, base + (size_t)(n0 + (lane & 7)) * ld + k0 + (((lane >> 3) & 1) << 3));
+}
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Cooperative copy of nbytes (a multiple of 16) by nthreads threads.
+__device__ __forceinline__ void cp_async_block(void *dst, const void *src, size_t nbytes, int tid, int nthreads) {
+    char *d = static_cast<char *>(dst);
+    const char *s = static_cast<const char *>(src);
+    for (size_t off = (size_t)tid * 16; off < nbytes; off += (size_t)nthreads * 16) cp_async16(d + off, s + off);
+}
+
+}  // namespace kda

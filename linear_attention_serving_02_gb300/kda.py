@@ -1,0 +1,163 @@
+"""Python binding of the KDA C ABI (include/kda.h): argument marshalling only.
+
+Each function here has the name of the C entry point it calls. Tensors are torch
+CUDA tensors; the binding checks dtypes and shapes, passes raw pointers, sizes and the
+current CUDA stream, and raises KdaError on a non-zero status. Every step of the
+computation runs in the CUDA library; if the library cannot be built or loaded the
+import fails loudly. There is no other code path.
+"""
+import ctypes
+
+import torch
+
+from . import build as _build
+
+D = 128
+KDA_OUT_BF16 = 0
+KDA_OUT_F32 = 1
+
+_LIB = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (fn, status_string(status), status))
+
+
+def library():
+    """The loaded CUDA library (built in-tree on first use if missing or stale)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_version.argtypes = []
+        lib.kda_version.restype = ctypes.c_int
+        lib.kda_chunk_prefill_workspace_size.argtypes = [i64, i32, i32]
+        lib.kda_chunk_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          i32, i64, i32, i32, i32, i32,
+                                          vp, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.kda_chunk_prefill.restype = ctypes.c_int
+        lib.kda_workspace_status.argtypes = [vp, vp]
+        lib.kda_workspace_status.restype = ctypes.c_int
+        lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        lib.kda_recurrent_decode.restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def status_string(status):
+    return library().kda_status_string(int(status)).decode()
+
+
+kda_status_string = status_string
+
+
+def kda_version():
+    return library().kda_version()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, cuda=True):
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if cuda and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def kda_chunk_prefill_workspace_size(total_tokens, num_seqs, num_heads):
+    return int(library().kda_chunk_prefill_workspace_size(int(total_tokens), int(num_seqs), int(num_heads)))
+
+
+def kda_chunk_prefill(q, k, v, z, A, b, initial_state=None, cu_seqlens=None, cu_seqlens_host=None,
+                      o=None, final_state=None, workspace=None, o_dtype=torch.bfloat16, stream=None):
+    """Chunkwise KDA prefill. Returns (o, final_state).
+
+    q, k, v: bf16 [B, T, H, 128] (dense batch) or [T_total, H, 128] with cu_seqlens;
+    z: fp32 like q; A: fp32 [H]; b: fp32 [..., H]; initial_state: fp32 [N, H, 128, 128]
+    or None; cu_seqlens: int32 CUDA [N+1] or None; cu_seqlens_host: optional CPU int32
+    copy of it (validated on the host). o / final_state / workspace are allocated with
+    torch when not given.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    _need(z, "z", torch.float32)
+    _need(A, "A", torch.float32)
+    _need(b, "b", torch.float32)
+    H = q.shape[-2]
+    if q.shape[-1] != D or v.shape[-1] != D:
+        raise ValueError("head size must be 128")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        batch, seq_len = 1, q.numel() // (H * D)
+        num_seqs = cu_seqlens.numel() - 1
+    else:
+        if q.dim() != 4:
+            raise ValueError("dense batch wants q as [B, T, H, 128]")
+        batch, seq_len = q.shape[0], q.shape[1]
+        num_seqs = batch
+    total = batch * seq_len
+    hc = None
+    if cu_seqlens_host is not None:
+        hc = cu_seqlens_host.to(torch.int32).contiguous()
+        if hc.is_cuda or hc.numel() != num_seqs + 1:
+            raise ValueError("cu_seqlens_host must be a CPU tensor of num_seqs + 1 entries")
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32)
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bf16 or fp32")
+    if final_state is None:
+        final_state = torch.empty((num_seqs, H, D, D), dtype=torch.float32, device=q.device)
+    _need(final_state, "final_state", torch.float32)
+    need = kda_chunk_prefill_workspace_size(total, num_seqs, H)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = library().kda_chunk_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(b), _ptr(initial_state), _ptr(cu_seqlens),
+        _ptr(hc),
+        batch, seq_len, num_seqs, H, D, D,
+        _ptr(o), KDA_OUT_F32 if o.dtype == torch.float32 else KDA_OUT_BF16, _ptr(final_state),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != 0:
+        raise KdaError("kda_chunk_prefill", rc)
+    return o, final_state
+
+
+def kda_workspace_status(workspace, stream=None):
+    """Device-side status of the last prefill that used this workspace (synchronises)."""
+    return int(library().kda_workspace_status(_ptr(workspace), _stream(stream)))
+
+
+def kda_recurrent_decode(q, k, v, z, A, b, state, o=None, stream=None):
+    """One decode token per sequence; state [N, H, 128, 128] fp32 is updated in place. Returns o (fp32)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    _need(z, "z", torch.float32)
+    _need(A, "A", torch.float32)
+    _need(b, "b", torch.float32)
+    _need(state, "state", torch.float32)
+    N, H = q.shape[0], q.shape[1]
+    if o is None:
+        o = torch.empty((N, H, D), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32)
+    rc = library().kda_recurrent_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(b), _ptr(state), _ptr(o),
+                                        N, H, D, D, _stream(stream))
+    if rc != 0:
+        raise KdaError("kda_recurrent_decode", rc)
+    return o

@@ -1,0 +1,136 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every entry point that
+include/*.h declares, and its host-side argument checks return the documented status
+codes. No compute call is made here; the checks reject every case before any CUDA
+call, so fake (never dereferenced) device pointers are safe to pass.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from linear_attention_serving_02_gb300 import kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+KDA_OK, KDA_ERR_NULL, KDA_ERR_SHAPE, KDA_ERR_UNSUPPORTED = 0, -1, -2, -3
+KDA_ERR_SEQLENS, KDA_ERR_ALIGN, KDA_ERR_WORKSPACE = -4, -5, -6
+FAKE = 1 << 20  # 256-byte aligned fake device address, never dereferenced
+
+
+def declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(kda_[A-Za-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_chunk_prefill_workspace_size",
+                     "kda_status_string", "kda_workspace_status", "kda_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(kda.library()._name)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, "not exported: %s" % missing
+
+
+def test_status_strings_and_version():
+    assert kda.kda_status_string(0) == "ok"
+    for code in range(-8, 0):
+        assert kda.kda_status_string(code) != "unknown status"
+    assert kda.kda_status_string(12345) == "unknown status"
+    assert kda.kda_version() >= 100
+
+
+def test_workspace_size():
+    ws = kda.kda_chunk_prefill_workspace_size
+    assert ws(-1, 1, 1) == 0
+    a = ws(8192, 1, 12)
+    b = ws(8192 * 2, 1, 12)
+    assert 0 < a < b
+    assert ws(8192, 1, 24) > a
+    # one more sequence can add a partial chunk per head
+    assert ws(8192, 2, 12) > a
+
+
+def _prefill(**over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, A=FAKE, b=FAKE, initial_state=None, cu=None, cu_host=None,
+                batch=1, seq_len=256, num_seqs=1, num_heads=2, d_k=128, d_v=128, o=FAKE, o_dtype=0,
+                final_state=FAKE, workspace=FAKE, workspace_bytes=1 << 40, stream=None)
+    args.update(over)
+    return kda.library().kda_chunk_prefill(
+        args["q"], args["k"], args["v"], args["z"], args["A"], args["b"], args["initial_state"], args["cu"],
+        args["cu_host"], args["batch"], args["seq_len"], args["num_seqs"], args["num_heads"], args["d_k"],
+        args["d_v"], args["o"], args["o_dtype"], args["final_state"], args["workspace"], args["workspace_bytes"],
+        args["stream"])
+
+
+def _host_cu(vals):
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d_k=64), KDA_ERR_UNSUPPORTED),
+    (dict(d_v=256), KDA_ERR_UNSUPPORTED),
+    (dict(o_dtype=7), KDA_ERR_UNSUPPORTED),
+    (dict(num_heads=0), KDA_ERR_SHAPE),
+    (dict(seq_len=-1), KDA_ERR_SHAPE),
+    (dict(batch=2, num_seqs=1), KDA_ERR_SHAPE),
+    (dict(batch=2, num_seqs=2, cu=FAKE), KDA_ERR_SHAPE),
+    (dict(seq_len=1 << 31), KDA_ERR_SHAPE),
+    (dict(q=None), KDA_ERR_NULL),
+    (dict(final_state=None), KDA_ERR_NULL),
+    (dict(workspace=None), KDA_ERR_NULL),
+    (dict(A=None), KDA_ERR_NULL),
+    (dict(q=FAKE + 8), KDA_ERR_ALIGN),
+    (dict(z=FAKE + 4), KDA_ERR_ALIGN),
+    (dict(initial_state=FAKE + 8), KDA_ERR_ALIGN),
+    (dict(workspace=FAKE + 16), KDA_ERR_ALIGN),
+    (dict(workspace_bytes=1024), KDA_ERR_WORKSPACE),
+])
+def test_prefill_argument_checks(over, code):
+    assert _prefill(**over) == code
+
+
+def test_prefill_host_cu_seqlens_checks():
+    for vals, code in (([0, 100, 90, 256], KDA_ERR_SEQLENS),   # falls
+                       ([1, 100, 200, 256], KDA_ERR_SEQLENS),  # does not start at 0
+                       ([0, 100, 200, 255], KDA_ERR_SEQLENS)): # does not end at the token count
+        ptr, keep = _host_cu(vals)
+        assert _prefill(cu=FAKE, cu_host=ptr, num_seqs=3) == code
+
+
+def test_prefill_empty_batch_is_ok():
+    assert _prefill(batch=0, num_seqs=0, q=None, k=None, v=None, z=None, b=None, o=None) == KDA_OK
+
+
+def _decode(**over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, A=FAKE, b=FAKE, state=FAKE, o=FAKE, num_seqs=4, num_heads=2,
+                d_k=128, d_v=128, stream=None)
+    args.update(over)
+    return kda.library().kda_recurrent_decode(
+        args["q"], args["k"], args["v"], args["z"], args["A"], args["b"], args["state"], args["o"],
+        args["num_seqs"], args["num_heads"], args["d_k"], args["d_v"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d_k=96), KDA_ERR_UNSUPPORTED),
+    (dict(num_heads=0), KDA_ERR_SHAPE),
+    (dict(num_seqs=-3), KDA_ERR_SHAPE),
+    (dict(state=None), KDA_ERR_NULL),
+    (dict(o=None), KDA_ERR_NULL),
+    (dict(v=FAKE + 2), KDA_ERR_ALIGN),
+    (dict(state=FAKE + 8), KDA_ERR_ALIGN),
+    (dict(num_seqs=0), KDA_OK),
+])
+def test_decode_argument_checks(over, code):
+    assert _decode(**over) == code

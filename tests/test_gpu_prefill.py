@@ -1,0 +1,172 @@
+"""Chunkwise prefill on the GPU against the fp64 oracle, through the C ABI.
+
+Small cases are compared element by element at sizes that span several 64-token
+chunks and 16-token tiles with ragged tails; the full-size workloads are compared in
+full (single long sequence) or on sampled (sequence, head) units.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_serving_02_gb300 import inputs, kda
+from tests.gpu_util import assert_prefill_close, np64, oracle_units
+
+pytestmark = pytest.mark.gpu
+
+
+def _cuda(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def gpu_prefill(inp, cu=None, cu_host=True, o_dtype=torch.float32, S0="inp"):
+    g = _cuda(inp)
+    s0 = g["S0"] if S0 == "inp" else S0
+    cu_d = None if cu is None else torch.tensor(cu, dtype=torch.int32, device="cuda")
+    cu_h = None if (cu is None or not cu_host) else torch.tensor(cu, dtype=torch.int32)
+    o, S = kda.kda_chunk_prefill(g["q"], g["k"], g["v"], g["z"], g["A"], g["b"], initial_state=s0,
+                                 cu_seqlens=cu_d, cu_seqlens_host=cu_h, o_dtype=o_dtype)
+    torch.cuda.synchronize()
+    return o.cpu(), S.cpu()
+
+
+def test_tiny_config():
+    """B=1, T=256, H=2, zero initial state: four chunks, every output compared."""
+    inp = inputs.prefill_inputs(256, 2, 1, seed=0)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"])
+    for dt in (torch.float32, torch.bfloat16):
+        o, S = gpu_prefill(inp, o_dtype=dt)
+        assert o.dtype == dt
+        assert_prefill_close(o, S, o_ref, S_ref, "tiny %s" % dt)
+
+
+@pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 130, 200])
+def test_dense_batch_ragged_lengths(T):
+    B, H = 2, 3
+    inp = inputs.prefill_inputs(B * T, H, B, seed=10 + T, init_state=True, batch_rows=B)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"])
+    o, S = gpu_prefill(inp)
+    assert_prefill_close(o, S, o_ref, S_ref, "T=%d" % T)
+
+
+@pytest.mark.parametrize("cu_host", [True, False])
+def test_packed_varlen_with_empty_and_short_sequences(cu_host):
+    lens = [0, 1, 64, 100, 300, 17, 0, 129]
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    H = 2
+    inp = inputs.prefill_inputs(cu[-1], H, len(lens), seed=3, init_state=True)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu, cu_host=cu_host)
+    assert_prefill_close(o, S, o_ref, S_ref, "varlen")
+    for n, L in enumerate(lens):
+        if L == 0:
+            assert torch.equal(S[n], inp["S0"][n]), "an empty sequence must return its initial state"
+
+
+def test_packed_equals_separate_runs():
+    """Chunks restart at every sequence start, so a packed batch gives each sequence
+    exactly the result of running it alone."""
+    lens = [70, 5, 128]
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    H = 3
+    inp = inputs.prefill_inputs(cu[-1], H, len(lens), seed=4, init_state=True)
+    o, S = gpu_prefill(inp, cu=cu)
+    for n in range(len(lens)):
+        a, e = cu[n], cu[n + 1]
+        part = {k: (v[:, a:e].contiguous() if k in ("q", "k", "v", "z", "b") else v) for k, v in inp.items()}
+        part["S0"] = inp["S0"][n:n + 1].contiguous()
+        on, Sn = gpu_prefill(part)
+        assert torch.equal(on[0], o[0, a:e]) and torch.equal(Sn[0], S[n]), "sequence %d" % n
+
+
+def test_head_permutation_equivariance():
+    T, H = 150, 4
+    inp = inputs.prefill_inputs(T, H, 1, seed=6, init_state=True)
+    o, S = gpu_prefill(inp)
+    perm = [2, 0, 3, 1]
+    pinp = {k: (v[..., perm, :].contiguous() if k in ("q", "k", "v", "z") else v) for k, v in inp.items()}
+    pinp["b"] = inp["b"][..., perm].contiguous()
+    pinp["A"] = inp["A"][perm].contiguous()
+    pinp["S0"] = inp["S0"][:, perm].contiguous()
+    op, Sp = gpu_prefill(pinp)
+    assert torch.equal(op, o[..., perm, :]) and torch.equal(Sp, S[:, perm])
+
+
+def test_no_decay_no_write_keeps_state():
+    """z = -inf gives a = 1 exactly and b = -inf gives beta = 0: the state passes
+    through unchanged and o_t = S0^T q_t."""
+    T, H = 130, 2
+    inp = inputs.prefill_inputs(T, H, 1, seed=7, init_state=True)
+    inp["z"] = torch.full_like(inp["z"], -float("inf"))
+    inp["b"] = torch.full_like(inp["b"], -float("inf"))
+    o, S = gpu_prefill(inp)
+    assert torch.equal(S, inp["S0"]), "state must pass through bit-identical"
+    o_ref = np.einsum("thc,hcj->thj", np64(inp["q"][0]), np64(inp["S0"][0]))
+    assert_prefill_close(o[0], None, o_ref, None, "identity")
+
+
+def test_strongest_decay_everywhere():
+    """z = +inf puts every token at the decay bound log a = -5: inside a 64-token chunk the
+    decay spans e^-315, and the tile factors reach e^75; nothing may overflow."""
+    T, H = 200, 2
+    inp = inputs.prefill_inputs(T, H, 1, seed=8, init_state=True)
+    inp["z"] = torch.full_like(inp["z"], float("inf"))
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"])
+    o, S = gpu_prefill(inp)
+    assert torch.isfinite(o).all() and torch.isfinite(S).all()
+    assert_prefill_close(o, S, o_ref, S_ref, "decay bound")
+
+
+def test_invalid_device_cu_seqlens_is_reported():
+    """Without a host copy, a falling cu_seqlens is caught on the device: the workspace
+    status says so, final_state is NaN and o is left untouched."""
+    cu = [0, 100, 50, 256]
+    H = 2
+    inp = _cuda(inputs.prefill_inputs(256, H, 3, seed=9, init_state=True))
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o = torch.full(inp["q"].shape, 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(256, 3, H), dtype=torch.uint8, device="cuda")
+    _, S = kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"],
+                                 initial_state=inp["S0"], cu_seqlens=cu_d, o=o, workspace=ws)
+    assert kda.kda_workspace_status(ws) == -4
+    assert torch.isnan(S).all()
+    assert (o == 7.0).all()
+    # the same workspace then serves a valid call and reports ok
+    cu_d = torch.tensor([0, 50, 100, 256], dtype=torch.int32, device="cuda")
+    kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"],
+                          initial_state=inp["S0"], cu_seqlens=cu_d, o=o, workspace=ws)
+    assert kda.kda_workspace_status(ws) == 0
+
+
+def test_host_cu_seqlens_rejected_before_launch():
+    H = 2
+    inp = _cuda(inputs.prefill_inputs(256, H, 3, seed=9))
+    cu_d = torch.tensor([0, 100, 50, 256], dtype=torch.int32, device="cuda")
+    with pytest.raises(kda.KdaError) as ei:
+        kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], cu_seqlens=cu_d,
+                              cu_seqlens_host=cu_d.cpu())
+    assert ei.value.status == -4
+
+
+def test_prefill_then_decode_equals_longer_prefill():
+    """The chunked and the recurrent path agree on the state ('Kimi K3' page: both
+    paths must give the same state-update semantics)."""
+    T, m, H = 200, 9, 3
+    inp = inputs.prefill_inputs(T + m, H, 1, seed=11, init_state=True)
+    g = _cuda(inp)
+    o_long, S_long = kda.kda_chunk_prefill(g["q"], g["k"], g["v"], g["z"], g["A"], g["b"],
+                                           initial_state=g["S0"], o_dtype=torch.float32)
+    head = {k: (v[:, :T].contiguous() if k in ("q", "k", "v", "z", "b") else v) for k, v in g.items()}
+    o1, S = kda.kda_chunk_prefill(head["q"], head["k"], head["v"], head["z"], head["A"], head["b"],
+                                  initial_state=g["S0"], o_dtype=torch.float32)
+    state = S.clone()
+    outs = [o1[0]]
+    for t in range(T, T + m):
+        ot = kda.kda_recurrent_decode(g["q"][:, t].contiguous(), g["k"][:, t].contiguous(), g["v"][:, t].contiguous(),
+                                      g["z"][:, t].contiguous(), g["A"], g["b"][:, t].contiguous(), state)
+        outs.append(ot)
+    o_split = torch.cat(outs, 0)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"])
+    assert_prefill_close(o_split.cpu(), state.cpu(), o_ref[0], S_ref, "prefill + decode vs oracle")
+    assert_prefill_close(o_split.cpu(), state.cpu(), np64(o_long[0]), np64(S_long), "prefill + decode vs long")
