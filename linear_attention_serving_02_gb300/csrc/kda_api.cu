@@ -3,8 +3,9 @@
 // synchronisation (except kda_workspace_status), no exceptions.
 
 #include <cuda_runtime.h>
+#include <stdlib.h>
 
-#include "../../include/kda.h"
+#include "kda.h"
 #include "kda_common.cuh"
 
 namespace kda {
@@ -56,6 +57,14 @@ int device_info(DeviceInfo &info) {
 // Value-column slice of the inter-chunk walk: narrow slices when there are few
 // (sequence, head) chains to spread over the SMs, wide slices otherwise.
 int choose_slice(int64_t chains, int sms) {
+    // KDA_INTER_COLS (16, 32 or 64) overrides the choice; a tuning aid, read once
+    static int forced = -1;
+    if (forced < 0) {
+        const char *e = getenv("KDA_INTER_COLS");
+        const int v = e ? atoi(e) : 0;
+        forced = (v == 16 || v == 32 || v == 64) ? v : 0;
+    }
+    if (forced) return forced;
     if (chains * 2 >= sms) return 64;
     if (chains * 4 >= sms) return 32;
     return 16;

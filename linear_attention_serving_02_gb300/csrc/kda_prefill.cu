@@ -98,12 +98,15 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
 // intra-chunk kernel
 // ---------------------------------------------------------------------------------
 struct IntraSmem {
-    float G[kC][kD + 4];  // cumulative log decay inside the chunk
+    float G[kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay
     float beta[kC];
     float Akk[kC][kC + 1];
     float Aqk[kC][kC + 1];
     float T[kC][kC + 1];
     float X[3][kTile][kTile + 1];  // off-diagonal block products of the solve
+    __nv_bfloat16 qs[kC][kLd128];  // the chunk's q, k, v (rows past the sequence end are zero)
+    __nv_bfloat16 ks[kC][kLd128];
+    __nv_bfloat16 vs[kC][kLd128];
     union {
         struct {  // operands of the decayed Gram products of one tile row
             __nv_bfloat16 aq[2][kTile][kLd128];
@@ -112,7 +115,6 @@ struct IntraSmem {
         } g;
         struct {  // operands of W = T' Khat and U' = T' V
             __nv_bfloat16 kh[2][kC][kLd128];
-            __nv_bfloat16 v[kC][kLd128];
             __nv_bfloat16 t[2][kC][kLd64];
         } w;
     } u;
@@ -152,25 +154,47 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     const int64_t hoff = (int64_t)h * kD;
     uint8_t *rec = records + ((int64_t)slot * H + h) * (int64_t)kRecBytes;
 
-    // ---- gate, cumulative log decay, beta --------------------------------------
-    if (tid < kD) {
-        const float eA = expf(A[h]);
-        const float *zc = z + t0 * rowstride + hoff + tid;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < kC; ++i) {
-            float la = 0.f;
-            if (i < L) la = gate_log_decay(eA, zc[(int64_t)i * rowstride]);
-            acc += la;
-            s.G[i][tid] = acc;
-        }
-    } else if (tid < kD + kC) {
+    // ---- stage z, q, k, v of the chunk in shared memory (all requests in flight at once) ----
+    for (int e = tid; e < kC * (kD / 4); e += kIntraThreads) {  // z: 32 x 16 B per row
+        const int i = e / (kD / 4), c = (e % (kD / 4)) * 4;
+        float *dst = &s.G[i][c];
+        if (i < L)
+            cp_async16(dst, z + (t0 + i) * rowstride + hoff + c);
+        else
+            *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int e = tid; e < 3 * kC * (kD / 8); e += kIntraThreads) {  // q, k, v: 16 x 16 B per row
+        const int which = e / (kC * (kD / 8));
+        const int r = e % (kC * (kD / 8));
+        const int i = r / (kD / 8), c = (r % (kD / 8)) * 8;
+        const __nv_bfloat16 *src = which == 0 ? q : (which == 1 ? k : v);
+        __nv_bfloat16 *dst = which == 0 ? &s.qs[i][c] : (which == 1 ? &s.ks[i][c] : &s.vs[i][c]);
+        if (i < L)
+            cp_async16(dst, src + (t0 + i) * rowstride + hoff + c);
+        else
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_commit();
+    if (tid >= kD && tid < kD + kC) {
         const int i = tid - kD;
         s.beta[i] = (i < L) ? sigmoid_f(bgate[(t0 + i) * H + h]) : 0.f;
     }
     for (int e = tid; e < kC * (kC + 1); e += kIntraThreads) {
         (&s.Akk[0][0])[e] = 0.f;
         (&s.Aqk[0][0])[e] = 0.f;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
+    if (tid < kD) {
+        const float eA = expf(A[h]);
+        float acc = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < kC; ++i) {
+            if (i < L) acc += gate_log_decay(eA, s.G[i][tid]);
+            s.G[i][tid] = acc;
+        }
     }
     __syncthreads();
 
@@ -187,19 +211,17 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             __nv_bfloat16 *dhi, *dlo;
             bool fwd;  // factor exp(G_tok - G_r) (true) or exp(G_r - G_tok) (false)
             if (row < kTile) {
-                tok = r + row; src = q; fwd = true;
+                tok = r + row; src = &s.qs[tok][c]; fwd = true;
                 dhi = &s.u.g.aq[0][row][c]; dlo = &s.u.g.aq[1][row][c];
             } else if (row < 2 * kTile) {
-                tok = r + row - kTile; src = k; fwd = true;
+                tok = r + row - kTile; src = &s.ks[tok][c]; fwd = true;
                 dhi = &s.u.g.ak[0][row - kTile][c]; dlo = &s.u.g.ak[1][row - kTile][c];
             } else {
-                tok = row - 2 * kTile; src = k; fwd = false;
+                tok = row - 2 * kTile; src = &s.ks[tok][c]; fwd = false;
                 dhi = &s.u.g.bk[0][tok][c]; dlo = &s.u.g.bk[1][tok][c];
             }
-            float2 x = make_float2(0.f, 0.f);
-            if (tok < L) {
-                x = __bfloat1622float2(
-                    *reinterpret_cast<const __nv_bfloat162 *>(src + (t0 + tok) * rowstride + hoff + c));
+            float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(src));
+            {
                 const float d0 = fwd ? s.G[tok][c] - s.G[r][c] : s.G[r][c] - s.G[tok][c];
                 const float d1 = fwd ? s.G[tok][c + 1] - s.G[r][c + 1] : s.G[r][c + 1] - s.G[tok][c + 1];
                 x.x *= expf(d0);
@@ -300,17 +322,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     }
     for (int e = tid; e < kC * (kD / 2); e += kIntraThreads) {
         const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
-        float2 kk = make_float2(0.f, 0.f);
-        uint32_t vv = 0u;
-        if (i < L) {
-            kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(k + (t0 + i) * rowstride + hoff + c));
-            vv = *reinterpret_cast<const uint32_t *>(v + (t0 + i) * rowstride + hoff + c);
-        }
+        const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
         uint32_t hi, lo;
         split_bf16x2(kk.x * expf(s.G[i][c]), kk.y * expf(s.G[i][c + 1]), hi, lo);
         *reinterpret_cast<uint32_t *>(&s.u.w.kh[0][i][c]) = hi;
         *reinterpret_cast<uint32_t *>(&s.u.w.kh[1][i][c]) = lo;
-        *reinterpret_cast<uint32_t *>(&s.u.w.v[i][c]) = vv;
     }
     __syncthreads();
 
@@ -338,7 +354,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 load_a(tl, &s.u.w.t[1][0][0], kLd64, a * 16, ks * 16, lane);
                 load_b_kn(kh, &s.u.w.kh[0][0][0], kLd128, ks * 16, n0, lane);
                 load_b_kn(kl, &s.u.w.kh[1][0][0], kLd128, ks * 16, n0, lane);
-                load_b_kn(vb, &s.u.w.v[0][0], kLd128, ks * 16, n0, lane);
+                load_b_kn(vb, &s.vs[0][0], kLd128, ks * 16, n0, lane);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     mma_split3(accW[a][nt], th, tl, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
@@ -373,9 +389,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         __nv_bfloat16 *Qh = reinterpret_cast<__nv_bfloat16 *>(rec + kRecQh);
         for (int e = tid; e < kC * (kD / 2); e += kIntraThreads) {
             const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
-            float2 qq = make_float2(0.f, 0.f);
-            if (i < L)
-                qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(q + (t0 + i) * rowstride + hoff + c));
+            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
             uint32_t hi, lo;
             split_bf16x2(qq.x * expf(s.G[i][c]), qq.y * expf(s.G[i][c + 1]), hi, lo);
             *reinterpret_cast<uint32_t *>(Qh + (size_t)i * kLd128 + c) = hi;
@@ -384,9 +398,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         __nv_bfloat16 *KeT = reinterpret_cast<__nv_bfloat16 *>(rec + kRecKeT);
         for (int e = tid; e < kD * (kC / 2); e += kIntraThreads) {
             const int c = e / (kC / 2), j = (e % (kC / 2)) * 2;
-            float k0 = 0.f, k1 = 0.f;
-            if (j < L) k0 = __bfloat162float(k[(t0 + j) * rowstride + hoff + c]);
-            if (j + 1 < L) k1 = __bfloat162float(k[(t0 + j + 1) * rowstride + hoff + c]);
+            const float k0 = __bfloat162float(s.ks[j][c]);
+            const float k1 = __bfloat162float(s.ks[j + 1][c]);
             const float gl = s.G[kC - 1][c];
             uint32_t hi, lo;
             split_bf16x2(k0 * expf(gl - s.G[j][c]), k1 * expf(gl - s.G[j + 1][c]), hi, lo);
@@ -421,19 +434,47 @@ struct InterSmem {
     __nv_bfloat16 U[2][kC][CW + 8];  // corrected values, split, [token][value column]
 };
 
-constexpr int kInterThreads = 128;
+constexpr int kInterThreads = 256;
 
+// B fragments of NTW adjacent n8 tiles (columns n0 .. n0 + 8*NTW - 1), k rows k0 .. k0+15,
+// from a tile stored [k][n] row-major.
+template <int NTW>
+__device__ __forceinline__ void load_b_tiles(uint32_t (&r)[NTW][2], const __nv_bfloat16 *base, int ld, int k0,
+                                             int n0, int lane) {
+    if constexpr (NTW == 1) {
+        ldsm_x2_t(r[0][0], r[0][1], base + (size_t)(k0 + (lane & 15)) * ld + n0);
+    } else {
+#pragma unroll
+        for (int p = 0; p < NTW / 2; ++p) {
+            uint32_t t[4];
+            load_b_kn(t, base, ld, k0, n0 + 16 * p, lane);
+            r[2 * p][0] = t[0];
+            r[2 * p][1] = t[1];
+            r[2 * p + 1][0] = t[2];
+            r[2 * p + 1][1] = t[3];
+        }
+    }
+}
+
+// Eight warps. In the 64-row products (U, O) warp w owns rows 16*(w%4) .. +15 and half of
+// the slice's columns; in the state update it owns key channels 16w .. 16w+15, all columns.
+// The three split-bf16 products (hi*hi, hi*lo, lo*hi) accumulate separately, so each
+// dependent chain of MMAs is one product per k-step long.
 template <int CW>
 __global__ void __launch_bounds__(kInterThreads, 1)
     kda_inter_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
                      const int32_t *__restrict__ chunk_off, int32_t H, const uint8_t *__restrict__ records,
                      const float *__restrict__ S0, float *__restrict__ Sout, void *__restrict__ o, int o_f32) {
     static_assert(CW % 16 == 0 && CW >= 16 && CW <= 64, "column slice");
-    constexpr int NT = CW / 8;  // n8 tiles per slice
+    constexpr int NT = CW / 8;   // n8 tiles in the slice
+    constexpr int NTW = NT / 2;  // n8 tiles per warp in the 64-row products
     extern __shared__ __align__(16) unsigned char smem_raw[];
     InterSmem<CW> &s = *reinterpret_cast<InterSmem<CW> *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t4 = lane & 3;
+    const int mrow = (warp & 3) * 16;         // rows of U and O owned by this warp
+    const int ncol = (warp >> 2) * NTW * 8;   // first slice column of those
+    const int srow = warp * 16;               // key channels of S owned by this warp
     const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * CW;
     const int64_t sbase = ((int64_t)n * H + h) * kD * kD;
 
@@ -445,21 +486,18 @@ __global__ void __launch_bounds__(kInterThreads, 1)
     const int c_begin = chunk_off[n], c_end = chunk_off[n + 1];
     const int64_t t_begin = seq_cu[n], t_end = seq_cu[n + 1];
 
-    // state slice in registers: warp w owns key channels 32w..32w+31 (two m16 tiles)
-    float Sacc[2][NT][4];
+    float Sacc[NT][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = warp * 32 + mt * 16 + g + hr * 8;
-                const int col = col0 + nt * 8 + 2 * t4;
-                float2 x = make_float2(0.f, 0.f);
-                if (S0) x = *reinterpret_cast<const float2 *>(S0 + sbase + (int64_t)row * kD + col);
-                Sacc[mt][nt][2 * hr] = x.x;
-                Sacc[mt][nt][2 * hr + 1] = x.y;
-            }
+        for (int hr = 0; hr < 2; ++hr) {
+            const int row = srow + g + hr * 8;
+            const int col = col0 + nt * 8 + 2 * t4;
+            float2 x = make_float2(0.f, 0.f);
+            if (S0) x = *reinterpret_cast<const float2 *>(S0 + sbase + (int64_t)row * kD + col);
+            Sacc[nt][2 * hr] = x.x;
+            Sacc[nt][2 * hr + 1] = x.y;
+        }
 
     auto rec_of = [&](int c) { return records + ((int64_t)c * H + h) * (int64_t)kRecBytes; };
     auto issue_W = [&](int c) {
@@ -490,18 +528,16 @@ __global__ void __launch_bounds__(kInterThreads, 1)
     };
     auto store_state_split = [&]() {
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int row = warp * 32 + mt * 16 + g + hr * 8;
-                    const int col = nt * 8 + 2 * t4;
-                    uint32_t hi, lo;
-                    split_bf16x2(Sacc[mt][nt][2 * hr], Sacc[mt][nt][2 * hr + 1], hi, lo);
-                    *reinterpret_cast<uint32_t *>(&s.S[0][row][col]) = hi;
-                    *reinterpret_cast<uint32_t *>(&s.S[1][row][col]) = lo;
-                }
+            for (int hr = 0; hr < 2; ++hr) {
+                const int row = srow + g + hr * 8;
+                const int col = nt * 8 + 2 * t4;
+                uint32_t hi, lo;
+                split_bf16x2(Sacc[nt][2 * hr], Sacc[nt][2 * hr + 1], hi, lo);
+                *reinterpret_cast<uint32_t *>(&s.S[0][row][col]) = hi;
+                *reinterpret_cast<uint32_t *>(&s.S[1][row][col]) = lo;
+            }
     };
 
     issue_W(c_begin);
@@ -513,44 +549,47 @@ __global__ void __launch_bounds__(kInterThreads, 1)
         const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
         const int L = (int)min((int64_t)kC, t_end - t0);
 
-        // ---- U = U' - W S (rows 16w .. 16w+15) ----
+        // ---- U = U' - W S (W is stored negated) ----
         cp_async_wait<2>();
         __syncthreads();
-        float Uacc[NT][4];
+        float ua[3][NTW][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
-                const int row = warp * 16 + g + hr * 8;
-                const int col = nt * 8 + 2 * t4;
+                const int row = mrow + g + hr * 8;
+                const int col = ncol + nt * 8 + 2 * t4;
                 const float2 u = *reinterpret_cast<const float2 *>(&s.Up[col >> 4][row][col & 15]);
-                Uacc[nt][2 * hr] = u.x;
-                Uacc[nt][2 * hr + 1] = u.y;
+                ua[0][nt][2 * hr] = u.x;
+                ua[0][nt][2 * hr + 1] = u.y;
+                ua[1][nt][2 * hr] = ua[1][nt][2 * hr + 1] = 0.f;
+                ua[2][nt][2 * hr] = ua[2][nt][2 * hr + 1] = 0.f;
             }
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-            uint32_t ah[4], al[4];
-            load_a(ah, &s.Wn[0][0][0], kLd128, warp * 16, ks * 16, lane);
-            load_a(al, &s.Wn[1][0][0], kLd128, warp * 16, ks * 16, lane);
+            uint32_t ah[4], al[4], bh[NTW][2], bl[NTW][2];
+            load_a(ah, &s.Wn[0][0][0], kLd128, mrow, ks * 16, lane);
+            load_a(al, &s.Wn[1][0][0], kLd128, mrow, ks * 16, lane);
+            load_b_tiles<NTW>(bh, &s.S[0][0][0], CW + 8, ks * 16, ncol, lane);
+            load_b_tiles<NTW>(bl, &s.S[1][0][0], CW + 8, ks * 16, ncol, lane);
 #pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                uint32_t bh[4], bl[4];
-                load_b_kn(bh, &s.S[0][0][0], CW + 8, ks * 16, np * 16, lane);
-                load_b_kn(bl, &s.S[1][0][0], CW + 8, ks * 16, np * 16, lane);
-                mma_split3(Uacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                mma_split3(Uacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+            for (int nt = 0; nt < NTW; ++nt) {
+                mma_bf16(ua[0][nt], ah, bh[nt][0], bh[nt][1]);
+                mma_bf16(ua[1][nt], ah, bl[nt][0], bl[nt][1]);
+                mma_bf16(ua[2][nt], al, bh[nt][0], bh[nt][1]);
             }
         }
         __syncthreads();
         issue_W(c + 1);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
-                const int row = warp * 16 + g + hr * 8;
-                const int col = nt * 8 + 2 * t4;
+                const int row = mrow + g + hr * 8;
+                const int col = ncol + nt * 8 + 2 * t4;
                 uint32_t hi, lo;
-                split_bf16x2(Uacc[nt][2 * hr], Uacc[nt][2 * hr + 1], hi, lo);
+                split_bf16x2(ua[0][nt][2 * hr] + (ua[1][nt][2 * hr] + ua[2][nt][2 * hr]),
+                             ua[0][nt][2 * hr + 1] + (ua[1][nt][2 * hr + 1] + ua[2][nt][2 * hr + 1]), hi, lo);
                 *reinterpret_cast<uint32_t *>(&s.U[0][row][col]) = hi;
                 *reinterpret_cast<uint32_t *>(&s.U[1][row][col]) = lo;
             }
@@ -559,54 +598,56 @@ __global__ void __launch_bounds__(kInterThreads, 1)
         cp_async_wait<2>();
         __syncthreads();
         {
-            float Oacc[NT][4];
+            float oa[3][NTW][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int p = 0; p < 3; ++p)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) Oacc[nt][e] = 0.f;
+                for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) oa[p][nt][e] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
-                uint32_t ah[4], al[4];
-                load_a(ah, &s.Qh[0][0][0], kLd128, warp * 16, ks * 16, lane);
-                load_a(al, &s.Qh[1][0][0], kLd128, warp * 16, ks * 16, lane);
+                uint32_t ah[4], al[4], bh[NTW][2], bl[NTW][2];
+                load_a(ah, &s.Qh[0][0][0], kLd128, mrow, ks * 16, lane);
+                load_a(al, &s.Qh[1][0][0], kLd128, mrow, ks * 16, lane);
+                load_b_tiles<NTW>(bh, &s.S[0][0][0], CW + 8, ks * 16, ncol, lane);
+                load_b_tiles<NTW>(bl, &s.S[1][0][0], CW + 8, ks * 16, ncol, lane);
 #pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                    uint32_t bh[4], bl[4];
-                    load_b_kn(bh, &s.S[0][0][0], CW + 8, ks * 16, np * 16, lane);
-                    load_b_kn(bl, &s.S[1][0][0], CW + 8, ks * 16, np * 16, lane);
-                    mma_split3(Oacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                    mma_split3(Oacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+                for (int nt = 0; nt < NTW; ++nt) {
+                    mma_bf16(oa[0][nt], ah, bh[nt][0], bh[nt][1]);
+                    mma_bf16(oa[1][nt], ah, bl[nt][0], bl[nt][1]);
+                    mma_bf16(oa[2][nt], al, bh[nt][0], bh[nt][1]);
                 }
             }
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks) {
-                if (ks > warp) break;  // A_qk is lower triangular
-                uint32_t ah[4], al[4];
-                load_a(ah, &s.Aqk[0][0][0], kLd64, warp * 16, ks * 16, lane);
-                load_a(al, &s.Aqk[1][0][0], kLd64, warp * 16, ks * 16, lane);
+                if (ks > (warp & 3)) break;  // A_qk is lower triangular
+                uint32_t ah[4], al[4], bh[NTW][2], bl[NTW][2];
+                load_a(ah, &s.Aqk[0][0][0], kLd64, mrow, ks * 16, lane);
+                load_a(al, &s.Aqk[1][0][0], kLd64, mrow, ks * 16, lane);
+                load_b_tiles<NTW>(bh, &s.U[0][0][0], CW + 8, ks * 16, ncol, lane);
+                load_b_tiles<NTW>(bl, &s.U[1][0][0], CW + 8, ks * 16, ncol, lane);
 #pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                    uint32_t bh[4], bl[4];
-                    load_b_kn(bh, &s.U[0][0][0], CW + 8, ks * 16, np * 16, lane);
-                    load_b_kn(bl, &s.U[1][0][0], CW + 8, ks * 16, np * 16, lane);
-                    mma_split3(Oacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                    mma_split3(Oacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+                for (int nt = 0; nt < NTW; ++nt) {
+                    mma_bf16(oa[0][nt], ah, bh[nt][0], bh[nt][1]);
+                    mma_bf16(oa[1][nt], ah, bl[nt][0], bl[nt][1]);
+                    mma_bf16(oa[2][nt], al, bh[nt][0], bh[nt][1]);
                 }
             }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int row = warp * 16 + g + hr * 8;
+                    const int row = mrow + g + hr * 8;
                     if (row < L) {
-                        const int64_t off = ((t0 + row) * H + h) * (int64_t)kD + col0 + nt * 8 + 2 * t4;
-                        if (o_f32) {
-                            *reinterpret_cast<float2 *>(static_cast<float *>(o) + off) =
-                                make_float2(Oacc[nt][2 * hr], Oacc[nt][2 * hr + 1]);
-                        } else {
+                        const float o0 = oa[0][nt][2 * hr] + (oa[1][nt][2 * hr] + oa[2][nt][2 * hr]);
+                        const float o1 = oa[0][nt][2 * hr + 1] + (oa[1][nt][2 * hr + 1] + oa[2][nt][2 * hr + 1]);
+                        const int64_t off = ((t0 + row) * H + h) * (int64_t)kD + col0 + ncol + nt * 8 + 2 * t4;
+                        if (o_f32)
+                            *reinterpret_cast<float2 *>(static_cast<float *>(o) + off) = make_float2(o0, o1);
+                        else
                             *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(o) + off) =
-                                __floats2bfloat162_rn(Oacc[nt][2 * hr], Oacc[nt][2 * hr + 1]);
-                        }
+                                __floats2bfloat162_rn(o0, o1);
                     }
                 }
         }
@@ -616,31 +657,36 @@ __global__ void __launch_bounds__(kInterThreads, 1)
         // ---- S = Diag(gamma) S + Kend^T U ----
         cp_async_wait<2>();
         __syncthreads();
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        {
+            float sx[NT][4];
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
-                const float gm = s.gam[warp * 32 + mt * 16 + g + hr * 8];
+                const float gm = s.gam[srow + g + hr * 8];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    Sacc[mt][nt][2 * hr] *= gm;
-                    Sacc[mt][nt][2 * hr + 1] *= gm;
+                    Sacc[nt][2 * hr] *= gm;
+                    Sacc[nt][2 * hr + 1] *= gm;
+                    sx[nt][2 * hr] = sx[nt][2 * hr + 1] = 0.f;
                 }
             }
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks) {
-                uint32_t ah[4], al[4];
-                load_a(ah, &s.KeT[0][0][0], kLd64, warp * 32 + mt * 16, ks * 16, lane);
-                load_a(al, &s.KeT[1][0][0], kLd64, warp * 32 + mt * 16, ks * 16, lane);
+                uint32_t ah[4], al[4], bh[NT][2], bl[NT][2];
+                load_a(ah, &s.KeT[0][0][0], kLd64, srow, ks * 16, lane);
+                load_a(al, &s.KeT[1][0][0], kLd64, srow, ks * 16, lane);
+                load_b_tiles<NT>(bh, &s.U[0][0][0], CW + 8, ks * 16, 0, lane);
+                load_b_tiles<NT>(bl, &s.U[1][0][0], CW + 8, ks * 16, 0, lane);
 #pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                    uint32_t bh[4], bl[4];
-                    load_b_kn(bh, &s.U[0][0][0], CW + 8, ks * 16, np * 16, lane);
-                    load_b_kn(bl, &s.U[1][0][0], CW + 8, ks * 16, np * 16, lane);
-                    mma_split3(Sacc[mt][2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                    mma_split3(Sacc[mt][2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_bf16(sx[nt], ah, bl[nt][0], bl[nt][1]);
+                    mma_bf16(sx[nt], al, bh[nt][0], bh[nt][1]);
+                    mma_bf16(Sacc[nt], ah, bh[nt][0], bh[nt][1]);
                 }
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Sacc[nt][e] += sx[nt][e];
         }
         __syncthreads();
         issue_K(c + 1);
@@ -649,16 +695,14 @@ __global__ void __launch_bounds__(kInterThreads, 1)
     cp_async_wait<0>();
 
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = warp * 32 + mt * 16 + g + hr * 8;
-                const int col = col0 + nt * 8 + 2 * t4;
-                *reinterpret_cast<float2 *>(Sout + sbase + (int64_t)row * kD + col) =
-                    make_float2(Sacc[mt][nt][2 * hr], Sacc[mt][nt][2 * hr + 1]);
-            }
+        for (int hr = 0; hr < 2; ++hr) {
+            const int row = srow + g + hr * 8;
+            const int col = col0 + nt * 8 + 2 * t4;
+            *reinterpret_cast<float2 *>(Sout + sbase + (int64_t)row * kD + col) =
+                make_float2(Sacc[nt][2 * hr], Sacc[nt][2 * hr + 1]);
+        }
 }
 
 // ---------------------------------------------------------------------------------
