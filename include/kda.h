@@ -127,6 +127,42 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 int kda_workspace_status(const void *workspace, void *stream);
 
 /*
+ * kda_chunk_prefill_noalloc - the same prefill, for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers that cannot
+ * provide the device workspace kda_chunk_prefill() asks for: a plugin running inside an
+ * engine that owns all device memory and passes it only the call's tensors, or code on
+ * a latency-critical path where cudaMalloc, which may synchronise the whole device, is
+ * not allowed. Instead of a workspace it uses a scratch area of
+ * KDA_NOALLOC_SCRATCH_BYTES compiled into the library: a static device array that exists
+ * on every GPU that loads the library, from load until process exit. The library still
+ * allocates nothing at call time. Arguments, results and error codes are those of
+ * kda_chunk_prefill() without the two workspace arguments; inputs and outputs are still
+ * the caller's.
+ *
+ *   - A batch whose workspace (kda_chunk_prefill_workspace_size(total_tokens, num_seqs,
+ *     num_heads)) exceeds KDA_NOALLOC_SCRATCH_BYTES is refused with KDA_ERR_WORKSPACE
+ *     before anything is launched. 64 MiB holds, for example, 2048 tokens x 12 heads.
+ *   - The first call on a device looks up the scratch's device address on that device
+ *     (cudaGetSymbolAddress, with the device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one scratch area and it keeps the last call's contents. The
+ *     kernels need nothing in it to start at zero, but calls whose GPU work overlaps in
+ *     time (different streams, or threads without ordering) race on it: order them.
+ *   - The device-side cu_seqlens check still fills final_state with NaN on a bad table;
+ *     there is no workspace to pass to kda_workspace_status(), so pass cu_seqlens_host
+ *     to have the table checked on the host instead.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int kda_chunk_prefill_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const float *z, const float *A, const float *b,
+                              const float *initial_state,
+                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                              int32_t batch, int64_t seq_len, int32_t num_seqs, int32_t num_heads,
+                              int32_t d_k, int32_t d_v,
+                              void *o, int32_t o_dtype, float *final_state, void *stream);
+
+/*
  * kda_recurrent_decode - one token per sequence, the recurrence applied in place.
  *
  * For every sequence n and head h: read S = state[n, h], apply

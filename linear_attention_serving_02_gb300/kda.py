@@ -161,3 +161,42 @@ def kda_recurrent_decode(q, k, v, z, A, b, state, o=None, stream=None):
     if rc != 0:
         raise KdaError("kda_recurrent_decode", rc)
     return o
+
+
+def kda_chunk_prefill_noalloc(q, k, v, z, A, b, initial_state=None, cu_seqlens=None, cu_seqlens_host=None,
+                              o=None, final_state=None, o_dtype=torch.bfloat16, stream=None):
+    """kda_chunk_prefill on the library's built-in scratch instead of a caller workspace,
+    for callers that may not allocate device memory. Same arguments and results as
+    kda_chunk_prefill without `workspace` (o and final_state are still allocated here when
+    not given; pass them to allocate nothing). Batches larger than the built-in scratch
+    raise KdaError with status KDA_ERR_WORKSPACE."""
+    lib = library()
+    fn = lib.kda_chunk_prefill_noalloc
+    if fn.restype is not ctypes.c_int:
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp, i32, vp, vp]
+        fn.restype = ctypes.c_int
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    _need(z, "z", torch.float32)
+    _need(A, "A", torch.float32)
+    _need(b, "b", torch.float32)
+    H = q.shape[-2]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        batch, seq_len = 1, q.numel() // (H * D)
+        num_seqs = cu_seqlens.numel() - 1
+    else:
+        batch, seq_len = q.shape[0], q.shape[1]
+        num_seqs = batch
+    hc = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+    if final_state is None:
+        final_state = torch.empty((num_seqs, H, D, D), dtype=torch.float32, device=q.device)
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(b), _ptr(initial_state), _ptr(cu_seqlens), _ptr(hc),
+            batch, seq_len, num_seqs, H, D, D, _ptr(o), KDA_OUT_F32 if o.dtype == torch.float32 else KDA_OUT_BF16,
+            _ptr(final_state), _stream(stream))
+    if rc != 0:
+        raise KdaError("kda_chunk_prefill_noalloc", rc)
+    return o, final_state
