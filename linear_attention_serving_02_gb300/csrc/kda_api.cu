@@ -3,7 +3,6 @@
 // synchronisation (except kda_workspace_status), no exceptions.
 
 #include <cuda_runtime.h>
-#include <stdlib.h>
 
 #include "kda.h"
 #include "kda_common.cuh"
@@ -15,9 +14,8 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
                          const float *A, const float *b, const int32_t *status, const int32_t *seq_cu,
                          const int32_t *chunk_off, int32_t N, int32_t H, int64_t nslots, uint8_t *records,
                          cudaStream_t st);
-cudaError_t launch_inter(int cw, const int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N,
-                         int32_t H, const uint8_t *records, const float *S0, float *Sout, void *o, int o_f32,
-                         cudaStream_t st);
+cudaError_t launch_walk(int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N, int32_t H,
+                        const uint8_t *records, const float *S0, float *Sout, void *o, int o_f32, cudaStream_t st);
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                           const float *A, const float *b, float *state, float *o, int32_t N, int32_t H,
                           int num_sms, cudaStream_t st);
@@ -52,22 +50,6 @@ int device_info(DeviceInfo &info) {
     }
     info = cache[dev];
     return KDA_OK;
-}
-
-// Value-column slice of the inter-chunk walk: narrow slices when there are few
-// (sequence, head) chains to spread over the SMs, wide slices otherwise.
-int choose_slice(int64_t chains, int sms) {
-    // KDA_INTER_COLS (16, 32 or 64) overrides the choice; a tuning aid, read once
-    static int forced = -1;
-    if (forced < 0) {
-        const char *e = getenv("KDA_INTER_COLS");
-        const int v = e ? atoi(e) : 0;
-        forced = (v == 16 || v == 32 || v == 64) ? v : 0;
-    }
-    if (forced) return forced;
-    if (chains * 2 >= sms) return 64;
-    if (chains * 4 >= sms) return 32;
-    return 16;
 }
 
 }  // namespace
@@ -145,9 +127,8 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                           reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, status, seq_cu, chunk_off, num_seqs,
                           num_heads, nslots, records, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    const int cw = choose_slice((int64_t)num_seqs * num_heads, dev.sms);
-    if (kda::launch_inter(cw, status, seq_cu, chunk_off, num_seqs, num_heads, records, initial_state, final_state, o,
-                          o_f32, st) != cudaSuccess)
+    if (kda::launch_walk(status, seq_cu, chunk_off, num_seqs, num_heads, records, initial_state, final_state, o, o_f32,
+                         st) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -21,26 +21,35 @@ constexpr int kLd128 = kD + 8;  // 128-wide tiles: 272 B per row
 constexpr int kLd64 = kC + 8;   // 64-wide tiles: 144 B per row
 
 // ---------------------------------------------------------------------------------
-// Chunk record: everything the serial inter-chunk pass needs about one (chunk, head),
-// stored as the exact byte image of its shared-memory tiles so that it is copied with
-// plain 16-byte moves. Split-bf16 operands are stored as a hi plane then a lo plane.
-//   Wn   [2][64][kLd128] bf16   -W = -T' Khat        (rows: token i, cols: key channel)
-//   Qh   [2][64][kLd128] bf16   q_i * exp(G_i)
-//   KeT  [2][128][kLd64] bf16   k_j * exp(G_last - G_j), transposed (row: channel)
-//   Aqk  [2][64][kLd64]  bf16   decayed causal Q K^T, diagonal included
-//   gam  [128]           fp32   exp(G_last), the chunk's total decay
-//   Up   [8][64][16]     fp32   U' = T' V, in blocks of 16 value columns
+// Chunk record: everything the serial state walk needs about one (chunk, head). The
+// operand tiles are stored as the exact shared-memory images the tensor core reads
+// (interleaved K-major core-matrix layout, see kda_tc.cuh), a hi plane then a lo plane
+// for split-bf16 operands, so that the walk fetches them with bulk copies.
+//   Wn   [2][64 x 128]  bf16   -W = -T' Khat      (rows: token i, K: key channel c)
+//   Qh   [2][64 x 128]  bf16   q_i * exp(G_i)     (rows: token i, K: key channel c)
+//   KeT  [2][128 x 64]  bf16   k_j * exp(G_last - G_j), transposed (rows: c, K: token j)
+//   Aqk  [2][64 x 64]   bf16   decayed causal Q K^T, diagonal included (rows: i, K: j)
+//   gam  [128]          fp32   exp(G_last), the chunk's total decay
+//   Up   [64][128]      fp32   U' = T' V, token-major (row i, column = value channel)
 // ---------------------------------------------------------------------------------
+constexpr size_t kPlaneQK = (size_t)kC * kD * 2;   // 64 x 128 bf16 tile
+constexpr size_t kPlaneKT = (size_t)kD * kC * 2;   // 128 x 64 bf16 tile
+constexpr size_t kPlaneCC = (size_t)kC * kC * 2;   // 64 x 64 bf16 tile
 constexpr size_t kRecWn = 0;
-constexpr size_t kRecQh = kRecWn + 2ull * kC * kLd128 * 2;
-constexpr size_t kRecKeT = kRecQh + 2ull * kC * kLd128 * 2;
-constexpr size_t kRecAqk = kRecKeT + 2ull * kD * kLd64 * 2;
-constexpr size_t kRecGam = kRecAqk + 2ull * kC * kLd64 * 2;
+constexpr size_t kRecQh = kRecWn + 2 * kPlaneQK;
+constexpr size_t kRecKeT = kRecQh + 2 * kPlaneQK;
+constexpr size_t kRecAqk = kRecKeT + 2 * kPlaneKT;
+constexpr size_t kRecGam = kRecAqk + 2 * kPlaneCC;
 constexpr size_t kRecUp = kRecGam + kD * 4;
 constexpr size_t kRecBytes = kRecUp + (size_t)kC * kD * 4;
 static_assert(kRecBytes % 128 == 0, "chunk records must stay 128-byte aligned");
 static_assert(kRecQh % 16 == 0 && kRecKeT % 16 == 0 && kRecAqk % 16 == 0 && kRecGam % 16 == 0 &&
               kRecUp % 16 == 0, "record fields must be 16-byte aligned");
+
+// byte offset of element (r, k) in an interleaved K-major tile with K elements per row
+__host__ __device__ constexpr uint32_t il_off(int r, int k, int K) {
+    return (uint32_t)((r >> 3) * (K >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
 
 // Workspace: [0, 256) header (int32 status at offset 0), then seq_cu[N+1] and
 // chunk_off[N+1] (int32, 256-byte aligned each), then the chunk records.

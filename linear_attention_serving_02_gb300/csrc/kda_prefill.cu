@@ -4,8 +4,8 @@
 //   kda_intra_kernel  one CTA per (chunk, head), all chunks in parallel: gate and
 //                     cumulative decay, decayed K K^T / Q K^T per 16-token tile row,
 //                     UT transform T = (I + A_kk)^-1, W = T' Khat and U' = T' V
-//   kda_inter_kernel  one CTA per (sequence, head, slice of value columns): walks the
-//                     chunks in order with the state slice held in registers,
+//   kda_walk_kernel   one CTA per (sequence, head): walks the chunks in order with the
+//                     full state on chip, on tcgen05 tensor cores (TMEM accumulators),
 //                     U = U' - W S;  O = Qhat S + A_qk U;  S = Diag(gamma) S + Kend^T U
 //
 // The algebra is the chunkwise form of 'From Linear Attention to KDA' (blog), §7.1-7.3
@@ -18,8 +18,9 @@
 //   W = T' (k * exp(G)),  U' = T' v,  U = U' - W S_0
 //   O = (q * exp(G)) S_0 + A_qk U,   S_C = Diag(exp(G_C)) S_0 + (k * exp(G_C - G))^T U
 //
-// Every product runs on the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate)
-// with both operands split into bf16 hi + lo planes (three products per tile). A plain
+// Every product runs on the tensor cores (mma.sync m16n8k16 in the intra kernel, tcgen05
+// in the walk; bf16 inputs, fp32 accumulate) with both operands split into bf16 hi + lo
+// planes (three products per tile). A plain
 // bf16 operand would cost about 2^-9 of relative error per product, which the
 // prediction-error cancellation in U = U' - W S amplifies beyond the accuracy the
 // outputs are held to; the split keeps about 16 mantissa bits.
@@ -30,6 +31,7 @@
 // -5 each, §5.4 of the blog) inside the diagonal tile, within bf16/fp32 range.
 
 #include "kda_common.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -363,8 +365,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 }
             }
         }
-        // write -W (split) and U' (fp32, blocks of 16 columns) to the record
-        __nv_bfloat16 *Wn = reinterpret_cast<__nv_bfloat16 *>(rec + kRecWn);
+        // write -W (split, interleaved tiles) and U' (fp32, token-major) to the record
+        uint8_t *Wn = rec + kRecWn;
         float *Up = reinterpret_cast<float *>(rec + kRecUp);
         const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
@@ -377,25 +379,25 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                     const int c = n0 + nt * 8 + 2 * t4;
                     uint32_t hi, lo;
                     split_bf16x2(-accW[a][nt][2 * hr], -accW[a][nt][2 * hr + 1], hi, lo);
-                    *reinterpret_cast<uint32_t *>(Wn + (size_t)i * kLd128 + c) = hi;
-                    *reinterpret_cast<uint32_t *>(Wn + (size_t)kC * kLd128 + (size_t)i * kLd128 + c) = lo;
-                    *reinterpret_cast<float2 *>(Up + (size_t)warp * kC * 16 + i * 16 + nt * 8 + 2 * t4) =
+                    *reinterpret_cast<uint32_t *>(Wn + il_off(i, c, kD)) = hi;
+                    *reinterpret_cast<uint32_t *>(Wn + kPlaneQK + il_off(i, c, kD)) = lo;
+                    *reinterpret_cast<float2 *>(Up + (size_t)i * kD + c) =
                         make_float2(accU[a][nt][2 * hr], accU[a][nt][2 * hr + 1]);
                 }
     }
 
     // ---- Qhat, Kend^T, A_qk, gamma (elementwise) --------------------------------
     {
-        __nv_bfloat16 *Qh = reinterpret_cast<__nv_bfloat16 *>(rec + kRecQh);
+        uint8_t *Qh = rec + kRecQh;
         for (int e = tid; e < kC * (kD / 2); e += kIntraThreads) {
             const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
             const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
             uint32_t hi, lo;
             split_bf16x2(qq.x * expf(s.G[i][c]), qq.y * expf(s.G[i][c + 1]), hi, lo);
-            *reinterpret_cast<uint32_t *>(Qh + (size_t)i * kLd128 + c) = hi;
-            *reinterpret_cast<uint32_t *>(Qh + (size_t)kC * kLd128 + (size_t)i * kLd128 + c) = lo;
+            *reinterpret_cast<uint32_t *>(Qh + il_off(i, c, kD)) = hi;
+            *reinterpret_cast<uint32_t *>(Qh + kPlaneQK + il_off(i, c, kD)) = lo;
         }
-        __nv_bfloat16 *KeT = reinterpret_cast<__nv_bfloat16 *>(rec + kRecKeT);
+        uint8_t *KeT = rec + kRecKeT;
         for (int e = tid; e < kD * (kC / 2); e += kIntraThreads) {
             const int c = e / (kC / 2), j = (e % (kC / 2)) * 2;
             const float k0 = __bfloat162float(s.ks[j][c]);
@@ -403,16 +405,16 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const float gl = s.G[kC - 1][c];
             uint32_t hi, lo;
             split_bf16x2(k0 * expf(gl - s.G[j][c]), k1 * expf(gl - s.G[j + 1][c]), hi, lo);
-            *reinterpret_cast<uint32_t *>(KeT + (size_t)c * kLd64 + j) = hi;
-            *reinterpret_cast<uint32_t *>(KeT + (size_t)kD * kLd64 + (size_t)c * kLd64 + j) = lo;
+            *reinterpret_cast<uint32_t *>(KeT + il_off(c, j, kC)) = hi;
+            *reinterpret_cast<uint32_t *>(KeT + kPlaneKT + il_off(c, j, kC)) = lo;
         }
-        __nv_bfloat16 *Aq = reinterpret_cast<__nv_bfloat16 *>(rec + kRecAqk);
+        uint8_t *Aq = rec + kRecAqk;
         for (int e = tid; e < kC * (kC / 2); e += kIntraThreads) {
             const int i = e / (kC / 2), j = (e % (kC / 2)) * 2;
             uint32_t hi, lo;
             split_bf16x2(s.Aqk[i][j], s.Aqk[i][j + 1], hi, lo);
-            *reinterpret_cast<uint32_t *>(Aq + (size_t)i * kLd64 + j) = hi;
-            *reinterpret_cast<uint32_t *>(Aq + (size_t)kC * kLd64 + (size_t)i * kLd64 + j) = lo;
+            *reinterpret_cast<uint32_t *>(Aq + il_off(i, j, kC)) = hi;
+            *reinterpret_cast<uint32_t *>(Aq + kPlaneCC + il_off(i, j, kC)) = lo;
         }
         float *gam = reinterpret_cast<float *>(rec + kRecGam);
         if (tid < kD) gam[tid] = expf(s.G[kC - 1][tid]);
@@ -420,300 +422,262 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------
-// inter-chunk kernel: the serial state walk of one (sequence, head, column slice)
+// state walk: one CTA per (sequence, head) carries the full 128 x 128 state through
+// the chunks of its sequence, on the tensor cores (tcgen05, accumulators in TMEM).
+//
+// Transposed orientation, so that the 128 value channels are the MMA's M = 128 rows
+// and every accumulator row is one TMEM lane:
+//   D_U = S^T (-W)^T          [128 x 64]   then U^T = U'^T + D_U       (per thread)
+//   D_O = S^T Qhat^T          [128 x 64]
+//   D_O += U^T A_qk^T                      then o = D_O^T
+//   D_S = U^T Kend             [128 x 128]  then S^T = S^T Diag(gamma) + D_S
+// Each product is split-bf16 (hi*hi + hi*lo + lo*hi). S^T and U^T go to shared memory as
+// split planes (the A operands); the record tiles are the B operands, fetched with bulk
+// copies one chunk ahead: W and Qhat as soon as the first group of MMAs has finished
+// with them, Kend, A_qk and gamma once the state update has.
+//
+// Thread t of warp w owns value channel dv = 32 (w % 4) + lane (TMEM lane dv) and half
+// hf = w / 4 of the columns: tokens 32 hf .. 32 hf + 31 of D_U / D_O, key channels
+// 64 hf .. 64 hf + 63 of the state, which it keeps in registers in fp32.
 // ---------------------------------------------------------------------------------
-template <int CW>
-struct InterSmem {
-    __nv_bfloat16 Wn[2][kC][kLd128];
-    __nv_bfloat16 Qh[2][kC][kLd128];
-    __nv_bfloat16 KeT[2][kD][kLd64];
-    __nv_bfloat16 Aqk[2][kC][kLd64];
-    float gam[kD];
-    float Up[CW / 16][kC][16];
-    __nv_bfloat16 S[2][kD][CW + 8];  // state slice, split, [key channel][value column]
-    __nv_bfloat16 U[2][kC][CW + 8];  // corrected values, split, [token][value column]
+struct WalkSmem {
+    unsigned char wq[2 * kPlaneQK + 2 * kPlaneQK];             // Wn hi, lo | Qh hi, lo
+    unsigned char ka[2 * kPlaneKT + 2 * kPlaneCC + kD * 4];    // KeT hi, lo | Aqk hi, lo | gamma
+    unsigned char st[2 * 128 * kD * 2];                        // S^T hi, lo   (M 128 x K 128)
+    unsigned char ut[2 * 128 * kC * 2];                        // U^T hi, lo   (M 128 x K 64)
+    uint64_t bar_wq, bar_ka, bar_m1, bar_m2;
+    uint32_t tmem_base;
+    int fail;
 };
+static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
 
-constexpr int kInterThreads = 256;
+constexpr int kWalkThreads = 256;
+constexpr uint32_t kWalkTmemCols = 256;  // D_U [0,64) | D_O [64,128) | D_S [128,256)
 
-// B fragments of NTW adjacent n8 tiles (columns n0 .. n0 + 8*NTW - 1), k rows k0 .. k0+15,
-// from a tile stored [k][n] row-major.
-template <int NTW>
-__device__ __forceinline__ void load_b_tiles(uint32_t (&r)[NTW][2], const __nv_bfloat16 *base, int ld, int k0,
-                                             int n0, int lane) {
-    if constexpr (NTW == 1) {
-        ldsm_x2_t(r[0][0], r[0][1], base + (size_t)(k0 + (lane & 15)) * ld + n0);
-    } else {
+// 8 consecutive fp32 values -> one 16-byte chunk of the hi plane and one of the lo plane
+__device__ __forceinline__ void split8_store(const float *x, unsigned char *hi_plane, unsigned char *lo_plane,
+                                             uint32_t off) {
+    uint32_t h[4], l[4];
 #pragma unroll
-        for (int p = 0; p < NTW / 2; ++p) {
-            uint32_t t[4];
-            load_b_kn(t, base, ld, k0, n0 + 16 * p, lane);
-            r[2 * p][0] = t[0];
-            r[2 * p][1] = t[1];
-            r[2 * p + 1][0] = t[2];
-            r[2 * p + 1][1] = t[3];
-        }
-    }
+    for (int j = 0; j < 4; ++j) split_bf16x2(x[2 * j], x[2 * j + 1], h[j], l[j]);
+    *reinterpret_cast<uint4 *>(hi_plane + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo_plane + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Eight warps. In the 64-row products (U, O) warp w owns rows 16*(w%4) .. +15 and half of
-// the slice's columns; in the state update it owns key channels 16w .. 16w+15, all columns.
-// The three split-bf16 products (hi*hi, hi*lo, lo*hi) accumulate separately, so each
-// dependent chain of MMAs is one product per k-step long.
-template <int CW>
-__global__ void __launch_bounds__(kInterThreads, 1)
-    kda_inter_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
-                     const int32_t *__restrict__ chunk_off, int32_t H, const uint8_t *__restrict__ records,
-                     const float *__restrict__ S0, float *__restrict__ Sout, void *__restrict__ o, int o_f32) {
-    static_assert(CW % 16 == 0 && CW >= 16 && CW <= 64, "column slice");
-    constexpr int NT = CW / 8;   // n8 tiles in the slice
-    constexpr int NTW = NT / 2;  // n8 tiles per warp in the 64-row products
+__global__ void __launch_bounds__(kWalkThreads, 1)
+    kda_walk_kernel(int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
+                    const int32_t *__restrict__ chunk_off, int32_t H, const uint8_t *__restrict__ records,
+                    const float *__restrict__ S0, float *__restrict__ Sout, void *__restrict__ o, int o_f32) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    InterSmem<CW> &s = *reinterpret_cast<InterSmem<CW> *>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int mrow = (warp & 3) * 16;         // rows of U and O owned by this warp
-    const int ncol = (warp >> 2) * NTW * 8;   // first slice column of those
-    const int srow = warp * 16;               // key channels of S owned by this warp
-    const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * CW;
+    WalkSmem &s = *reinterpret_cast<WalkSmem *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int dv = 32 * q4 + lane;
+    const int n = blockIdx.x, h = blockIdx.y;
     const int64_t sbase = ((int64_t)n * H + h) * kD * kD;
 
     if (*status != 0) {  // invalid batch table: make the failure visible in final_state
-        for (int e = tid; e < kD * CW; e += kInterThreads)
-            Sout[sbase + (int64_t)(e / CW) * kD + col0 + e % CW] = __int_as_float(0x7fc00000);
+        for (int c = hf * 64; c < hf * 64 + 64; ++c) Sout[sbase + (int64_t)c * kD + dv] = __int_as_float(0x7fc00000);
         return;
     }
     const int c_begin = chunk_off[n], c_end = chunk_off[n + 1];
     const int64_t t_begin = seq_cu[n], t_end = seq_cu[n + 1];
-
-    float Sacc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int row = srow + g + hr * 8;
-            const int col = col0 + nt * 8 + 2 * t4;
-            float2 x = make_float2(0.f, 0.f);
-            if (S0) x = *reinterpret_cast<const float2 *>(S0 + sbase + (int64_t)row * kD + col);
-            Sacc[nt][2 * hr] = x.x;
-            Sacc[nt][2 * hr + 1] = x.y;
-        }
-
     auto rec_of = [&](int c) { return records + ((int64_t)c * H + h) * (int64_t)kRecBytes; };
-    auto issue_W = [&](int c) {
-        if (c < c_end) {
-            const uint8_t *r = rec_of(c);
-            cp_async_block(&s.Wn[0][0][0], r + kRecWn, sizeof(s.Wn), tid, kInterThreads);
-            for (int bblk = 0; bblk < CW / 16; ++bblk)
-                cp_async_block(&s.Up[bblk][0][0], r + kRecUp + (size_t)(col0 / 16 + bblk) * kC * 16 * 4,
-                               (size_t)kC * 16 * 4, tid, kInterThreads);
-        }
-        cp_async_commit();
-    };
-    auto issue_QA = [&](int c) {
-        if (c < c_end) {
-            const uint8_t *r = rec_of(c);
-            cp_async_block(&s.Qh[0][0][0], r + kRecQh, sizeof(s.Qh), tid, kInterThreads);
-            cp_async_block(&s.Aqk[0][0][0], r + kRecAqk, sizeof(s.Aqk), tid, kInterThreads);
-        }
-        cp_async_commit();
-    };
-    auto issue_K = [&](int c) {
-        if (c < c_end) {
-            const uint8_t *r = rec_of(c);
-            cp_async_block(&s.KeT[0][0][0], r + kRecKeT, sizeof(s.KeT), tid, kInterThreads);
-            cp_async_block(&s.gam[0], r + kRecGam, sizeof(s.gam), tid, kInterThreads);
-        }
-        cp_async_commit();
-    };
-    auto store_state_split = [&]() {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = srow + g + hr * 8;
-                const int col = nt * 8 + 2 * t4;
-                uint32_t hi, lo;
-                split_bf16x2(Sacc[nt][2 * hr], Sacc[nt][2 * hr + 1], hi, lo);
-                *reinterpret_cast<uint32_t *>(&s.S[0][row][col]) = hi;
-                *reinterpret_cast<uint32_t *>(&s.S[1][row][col]) = lo;
-            }
-    };
 
-    issue_W(c_begin);
-    issue_QA(c_begin);
-    issue_K(c_begin);
-    store_state_split();
+    if (tid == 0) {
+        tc::mbar_init(&s.bar_wq, 1);
+        tc::mbar_init(&s.bar_ka, 1);
+        tc::mbar_init(&s.bar_m1, 1);
+        tc::mbar_init(&s.bar_m2, 1);
+        tc::mbar_init_fence();
+        s.fail = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s.tmem_base, kWalkTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s.tmem_base;
+    const uint32_t lanes = (uint32_t)(32 * q4) << 16;
+    const uint32_t D_U = tmem, D_O = tmem + 64, D_S = tmem + 128;
 
+    auto issue_wq = [&](int c) {
+        tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(4 * kPlaneQK));
+        tc::bulk_g2s(s.wq, rec_of(c) + kRecWn, (uint32_t)(4 * kPlaneQK), &s.bar_wq);
+    };
+    auto issue_ka = [&](int c) {
+        const uint32_t bytes = (uint32_t)(2 * kPlaneKT + 2 * kPlaneCC + kD * 4);
+        tc::mbar_arrive_expect_tx(&s.bar_ka, bytes);
+        tc::bulk_g2s(s.ka, rec_of(c) + kRecKeT, bytes, &s.bar_ka);
+    };
+    if (tid == 0 && c_begin < c_end) {
+        issue_wq(c_begin);
+        issue_ka(c_begin);
+    }
+
+    // state: S[c][dv] for this thread's 64 key channels, in fp32
+    float Sr[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) Sr[j] = S0 ? S0[sbase + (int64_t)(hf * 64 + j) * kD + dv] : 0.f;
+    auto store_state = [&]() {
+#pragma unroll
+        for (int j = 0; j < 64; j += 8)
+            split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, hf * 64 + j, kD));
+    };
+    store_state();
+    // U' of the first chunk: U'[i][dv] for this thread's 32 tokens
+    float Upr[32];
+    auto load_up = [&](int c) {
+        const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) Upr[j] = up[(hf * 32 + j) * kD + dv];
+    };
+    if (c_begin < c_end) load_up(c_begin);
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    constexpr uint32_t kId64 = tc::idesc_bf16_m128(64);
+    constexpr uint32_t kId128 = tc::idesc_bf16_m128(128);
+    volatile int &fail = s.fail;
+    // completed-phase counts, used to drain in-flight work if a wait ever gives up
+    int n_wq = (c_begin < c_end) ? 1 : 0, n_ka = n_wq, w_wq = 0, w_ka = 0, n_m1 = 0, n_m2 = 0;
     for (int c = c_begin; c < c_end; ++c) {
+        const uint32_t ph = (uint32_t)((c - c_begin) & 1);
         const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
         const int L = (int)min((int64_t)kC, t_end - t0);
 
-        // ---- U = U' - W S (W is stored negated) ----
-        cp_async_wait<2>();
-        __syncthreads();
-        float ua[3][NTW][4];
-#pragma unroll
-        for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = mrow + g + hr * 8;
-                const int col = ncol + nt * 8 + 2 * t4;
-                const float2 u = *reinterpret_cast<const float2 *>(&s.Up[col >> 4][row][col & 15]);
-                ua[0][nt][2 * hr] = u.x;
-                ua[0][nt][2 * hr + 1] = u.y;
-                ua[1][nt][2 * hr] = ua[1][nt][2 * hr + 1] = 0.f;
-                ua[2][nt][2 * hr] = ua[2][nt][2 * hr + 1] = 0.f;
-            }
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            uint32_t ah[4], al[4], bh[NTW][2], bl[NTW][2];
-            load_a(ah, &s.Wn[0][0][0], kLd128, mrow, ks * 16, lane);
-            load_a(al, &s.Wn[1][0][0], kLd128, mrow, ks * 16, lane);
-            load_b_tiles<NTW>(bh, &s.S[0][0][0], CW + 8, ks * 16, ncol, lane);
-            load_b_tiles<NTW>(bl, &s.S[1][0][0], CW + 8, ks * 16, ncol, lane);
-#pragma unroll
-            for (int nt = 0; nt < NTW; ++nt) {
-                mma_bf16(ua[0][nt], ah, bh[nt][0], bh[nt][1]);
-                mma_bf16(ua[1][nt], ah, bl[nt][0], bl[nt][1]);
-                mma_bf16(ua[2][nt], al, bh[nt][0], bh[nt][1]);
+        // ---- group 1: D_U = S^T (-W)^T, D_O = S^T Qhat^T ----
+        if (tid == 0) {
+            tc::fence_after_sync();
+            if (tc::mbar_wait(&s.bar_wq, ph)) {
+                ++w_wq;
+                const uint32_t s0 = tc::smem_addr(s.st), s1 = s0 + 128 * kD * 2;
+                const uint32_t w0 = tc::smem_addr(s.wq), w1 = w0 + kPlaneQK;
+                const uint32_t q0 = w0 + 2 * kPlaneQK, q1 = q0 + kPlaneQK;
+#pragma unroll 1
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint64_t a0 = tc::desc_k(s0, kD, ks), a1 = tc::desc_k(s1, kD, ks);
+                    tc::mma(D_U, a0, tc::desc_k(w0, kD, ks), kId64, ks > 0);
+                    tc::mma(D_U, a0, tc::desc_k(w1, kD, ks), kId64, 1);
+                    tc::mma(D_U, a1, tc::desc_k(w0, kD, ks), kId64, 1);
+                    tc::mma(D_O, a0, tc::desc_k(q0, kD, ks), kId64, ks > 0);
+                    tc::mma(D_O, a0, tc::desc_k(q1, kD, ks), kId64, 1);
+                    tc::mma(D_O, a1, tc::desc_k(q0, kD, ks), kId64, 1);
+                }
+                tc::commit(&s.bar_m1);
+            } else {
+                fail = 1;
             }
         }
-        __syncthreads();
-        issue_W(c + 1);
-#pragma unroll
-        for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = mrow + g + hr * 8;
-                const int col = ncol + nt * 8 + 2 * t4;
-                uint32_t hi, lo;
-                split_bf16x2(ua[0][nt][2 * hr] + (ua[1][nt][2 * hr] + ua[2][nt][2 * hr]),
-                             ua[0][nt][2 * hr + 1] + (ua[1][nt][2 * hr + 1] + ua[2][nt][2 * hr + 1]), hi, lo);
-                *reinterpret_cast<uint32_t *>(&s.U[0][row][col]) = hi;
-                *reinterpret_cast<uint32_t *>(&s.U[1][row][col]) = lo;
-            }
-
-        // ---- O = Qhat S + A_qk U ----
-        cp_async_wait<2>();
-        __syncthreads();
+        if (tc::mbar_wait(&s.bar_m1, ph)) ++n_m1; else fail = 1;
+        tc::fence_after_sync();
         {
-            float oa[3][NTW][4];
+            float d[32], u[32];
+            tc::tmem_ld32(D_U + lanes + hf * 32, d);
 #pragma unroll
-            for (int p = 0; p < 3; ++p)
+            for (int j = 0; j < 32; ++j) u[j] = Upr[j] + d[j];
 #pragma unroll
-                for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) oa[p][nt][e] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                uint32_t ah[4], al[4], bh[NTW][2], bl[NTW][2];
-                load_a(ah, &s.Qh[0][0][0], kLd128, mrow, ks * 16, lane);
-                load_a(al, &s.Qh[1][0][0], kLd128, mrow, ks * 16, lane);
-                load_b_tiles<NTW>(bh, &s.S[0][0][0], CW + 8, ks * 16, ncol, lane);
-                load_b_tiles<NTW>(bl, &s.S[1][0][0], CW + 8, ks * 16, ncol, lane);
-#pragma unroll
-                for (int nt = 0; nt < NTW; ++nt) {
-                    mma_bf16(oa[0][nt], ah, bh[nt][0], bh[nt][1]);
-                    mma_bf16(oa[1][nt], ah, bl[nt][0], bl[nt][1]);
-                    mma_bf16(oa[2][nt], al, bh[nt][0], bh[nt][1]);
-                }
-            }
-#pragma unroll
-            for (int ks = 0; ks < kC / 16; ++ks) {
-                if (ks > (warp & 3)) break;  // A_qk is lower triangular
-                uint32_t ah[4], al[4], bh[NTW][2], bl[NTW][2];
-                load_a(ah, &s.Aqk[0][0][0], kLd64, mrow, ks * 16, lane);
-                load_a(al, &s.Aqk[1][0][0], kLd64, mrow, ks * 16, lane);
-                load_b_tiles<NTW>(bh, &s.U[0][0][0], CW + 8, ks * 16, ncol, lane);
-                load_b_tiles<NTW>(bl, &s.U[1][0][0], CW + 8, ks * 16, ncol, lane);
-#pragma unroll
-                for (int nt = 0; nt < NTW; ++nt) {
-                    mma_bf16(oa[0][nt], ah, bh[nt][0], bh[nt][1]);
-                    mma_bf16(oa[1][nt], ah, bl[nt][0], bl[nt][1]);
-                    mma_bf16(oa[2][nt], al, bh[nt][0], bh[nt][1]);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int row = mrow + g + hr * 8;
-                    if (row < L) {
-                        const float o0 = oa[0][nt][2 * hr] + (oa[1][nt][2 * hr] + oa[2][nt][2 * hr]);
-                        const float o1 = oa[0][nt][2 * hr + 1] + (oa[1][nt][2 * hr + 1] + oa[2][nt][2 * hr + 1]);
-                        const int64_t off = ((t0 + row) * H + h) * (int64_t)kD + col0 + ncol + nt * 8 + 2 * t4;
-                        if (o_f32)
-                            *reinterpret_cast<float2 *>(static_cast<float *>(o) + off) = make_float2(o0, o1);
-                        else
-                            *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(o) + off) =
-                                __floats2bfloat162_rn(o0, o1);
-                    }
-                }
+            for (int j = 0; j < 32; j += 8) split8_store(&u[j], s.ut, s.ut + 128 * kC * 2, il_off(dv, hf * 32 + j, kC));
         }
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
         __syncthreads();
-        issue_QA(c + 1);
+        if (fail) break;
 
-        // ---- S = Diag(gamma) S + Kend^T U ----
-        cp_async_wait<2>();
-        __syncthreads();
-        {
-            float sx[NT][4];
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const float gm = s.gam[srow + g + hr * 8];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    Sacc[nt][2 * hr] *= gm;
-                    Sacc[nt][2 * hr + 1] *= gm;
-                    sx[nt][2 * hr] = sx[nt][2 * hr + 1] = 0.f;
-                }
+        // ---- group 2: D_O += U^T A_qk^T, D_S = U^T Kend ----
+        if (tid == 0) {
+            tc::fence_after_sync();
+            if (c + 1 < c_end) {
+                issue_wq(c + 1);  // group 1 is done with W and Qhat
+                ++n_wq;
             }
-#pragma unroll
-            for (int ks = 0; ks < kC / 16; ++ks) {
-                uint32_t ah[4], al[4], bh[NT][2], bl[NT][2];
-                load_a(ah, &s.KeT[0][0][0], kLd64, srow, ks * 16, lane);
-                load_a(al, &s.KeT[1][0][0], kLd64, srow, ks * 16, lane);
-                load_b_tiles<NT>(bh, &s.U[0][0][0], CW + 8, ks * 16, 0, lane);
-                load_b_tiles<NT>(bl, &s.U[1][0][0], CW + 8, ks * 16, 0, lane);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    mma_bf16(sx[nt], ah, bl[nt][0], bl[nt][1]);
-                    mma_bf16(sx[nt], al, bh[nt][0], bh[nt][1]);
-                    mma_bf16(Sacc[nt], ah, bh[nt][0], bh[nt][1]);
+            if (tc::mbar_wait(&s.bar_ka, ph)) {
+                ++w_ka;
+                const uint32_t u0 = tc::smem_addr(s.ut), u1 = u0 + 128 * kC * 2;
+                const uint32_t k0 = tc::smem_addr(s.ka), k1 = k0 + kPlaneKT;
+                const uint32_t a0q = k0 + 2 * kPlaneKT, a1q = a0q + kPlaneCC;
+#pragma unroll 1
+                for (int ks = 0; ks < kC / 16; ++ks) {
+                    const uint64_t a0 = tc::desc_k(u0, kC, ks), a1 = tc::desc_k(u1, kC, ks);
+                    tc::mma(D_O, a0, tc::desc_k(a0q, kC, ks), kId64, 1);
+                    tc::mma(D_O, a0, tc::desc_k(a1q, kC, ks), kId64, 1);
+                    tc::mma(D_O, a1, tc::desc_k(a0q, kC, ks), kId64, 1);
+                    tc::mma(D_S, a0, tc::desc_k(k0, kC, ks), kId128, ks > 0);
+                    tc::mma(D_S, a0, tc::desc_k(k1, kC, ks), kId128, 1);
+                    tc::mma(D_S, a1, tc::desc_k(k0, kC, ks), kId128, 1);
                 }
+                tc::commit(&s.bar_m2);
+            } else {
+                fail = 1;
             }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) Sacc[nt][e] += sx[nt][e];
         }
+        if (c + 1 < c_end) load_up(c + 1);  // next chunk's U', hidden behind group 2
+        if (tc::mbar_wait(&s.bar_m2, ph)) ++n_m2; else fail = 1;
+        tc::fence_after_sync();
+        {
+            float d[32];
+            tc::tmem_ld32(D_O + lanes + hf * 32, d);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int i = hf * 32 + j;
+                if (i < L) {
+                    const int64_t off = ((t0 + i) * H + h) * (int64_t)kD + dv;
+                    if (o_f32)
+                        static_cast<float *>(o)[off] = d[j];
+                    else
+                        static_cast<__nv_bfloat16 *>(o)[off] = __float2bfloat16_rn(d[j]);
+                }
+            }
+        }
+        {
+            const float *gam = reinterpret_cast<const float *>(s.ka + 2 * kPlaneKT + 2 * kPlaneCC);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                float d[32];
+                tc::tmem_ld32(D_S + lanes + hf * 64 + part * 32, d);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int cc = part * 32 + j;
+                    Sr[cc] = gam[hf * 64 + cc] * Sr[cc] + d[j];
+                }
+            }
+        }
+        store_state();
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
         __syncthreads();
-        issue_K(c + 1);
-        store_state_split();
+        if (fail) break;
+        if (tid == 0 && c + 1 < c_end) {
+            issue_ka(c + 1);  // the state update is done with Kend, A_qk and gamma
+            ++n_ka;
+        }
     }
-    cp_async_wait<0>();
 
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int row = srow + g + hr * 8;
-            const int col = col0 + nt * 8 + 2 * t4;
-            *reinterpret_cast<float2 *>(Sout + sbase + (int64_t)row * kD + col) =
-                make_float2(Sacc[nt][2 * hr], Sacc[nt][2 * hr + 1]);
+    if (fail) {
+        // a wait gave up: let the copies and MMAs in flight land (bounded) before the
+        // shared memory and TMEM are released, and report through the status word
+        if (tid == 0) {
+            if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
+            if (n_ka > w_ka) tc::mbar_wait(&s.bar_ka, (uint32_t)(w_ka & 1));
+            tc::mbar_wait(&s.bar_m1, (uint32_t)(n_m1 & 1));
+            tc::mbar_wait(&s.bar_m2, (uint32_t)(n_m2 & 1));
+            atomicExch(status, -7);
         }
+#pragma unroll
+        for (int j = 0; j < 64; ++j) Sr[j] = __int_as_float(0x7fc00000);
+    }
+#pragma unroll
+    for (int j = 0; j < 64; ++j) Sout[sbase + (int64_t)(hf * 64 + j) * kD + dv] = Sr[j];
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kWalkTmemCols);
 }
 
 // ---------------------------------------------------------------------------------
 // host-side launchers (called from kda_api.cu)
 // ---------------------------------------------------------------------------------
 size_t intra_smem_bytes() { return sizeof(IntraSmem); }
-template <int CW>
-size_t inter_smem_bytes() {
-    return sizeof(InterSmem<CW>);
-}
-
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, cudaStream_t st) {
     kda_plan_kernel<<<1, 256, 0, st>>>(cu, N, seq_len, total, status, seq_cu, chunk_off);
@@ -738,32 +702,20 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
     return cudaGetLastError();
 }
 
-template <int CW>
-static cudaError_t launch_inter_cw(const int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off,
-                                   int32_t N, int32_t H, const uint8_t *records, const float *S0, float *Sout,
-                                   void *o, int o_f32, cudaStream_t st) {
+cudaError_t launch_walk(int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N, int32_t H,
+                        const uint8_t *records, const float *S0, float *Sout, void *o, int o_f32, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kda_inter_kernel<CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sizeof(InterSmem<CW>));
+        cudaError_t e = cudaFuncSetAttribute(kda_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)sizeof(WalkSmem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid((unsigned)N, (unsigned)H, (unsigned)(kD / CW));
-    kda_inter_kernel<CW><<<grid, kInterThreads, sizeof(InterSmem<CW>), st>>>(status, seq_cu, chunk_off, H, records,
-                                                                            S0, Sout, o, o_f32);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_inter(int cw, const int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N,
-                         int32_t H, const uint8_t *records, const float *S0, float *Sout, void *o, int o_f32,
-                         cudaStream_t st) {
     if (N <= 0) return cudaSuccess;
-    switch (cw) {
-        case 16: return launch_inter_cw<16>(status, seq_cu, chunk_off, N, H, records, S0, Sout, o, o_f32, st);
-        case 32: return launch_inter_cw<32>(status, seq_cu, chunk_off, N, H, records, S0, Sout, o, o_f32, st);
-        default: return launch_inter_cw<64>(status, seq_cu, chunk_off, N, H, records, S0, Sout, o, o_f32, st);
-    }
+    dim3 grid((unsigned)N, (unsigned)H);
+    kda_walk_kernel<<<grid, kWalkThreads, sizeof(WalkSmem), st>>>(status, seq_cu, chunk_off, H, records, S0, Sout,
+                                                                   o, o_f32);
+    return cudaGetLastError();
 }
 
 }  // namespace kda
