@@ -23,28 +23,35 @@ constexpr int kLd64 = kC + 8;   // 64-wide tiles: 144 B per row
 // ---------------------------------------------------------------------------------
 // Chunk record: everything the serial state walk needs about one (chunk, head). The
 // operand tiles are stored as the exact shared-memory images the tensor core reads
-// (interleaved K-major core-matrix layout, see kda_tc.cuh), a hi plane then a lo plane
-// for split-bf16 operands, so that the walk fetches them with bulk copies.
-//   Wn   [2][64 x 128]  bf16   -W = -T' Khat      (rows: token i, K: key channel c)
-//   Qh   [2][64 x 128]  bf16   q_i * exp(G_i)     (rows: token i, K: key channel c)
-//   KeT  [2][128 x 64]  bf16   k_j * exp(G_last - G_j), transposed (rows: c, K: token j)
-//   Aqk  [2][64 x 64]   bf16   decayed causal Q K^T, diagonal included (rows: i, K: j)
-//   gam  [128]          fp32   exp(G_last), the chunk's total decay
-//   Up   [64][128]      fp32   U' = T' V, token-major (row i, column = value channel)
+// (interleaved K-major core-matrix layout, see kda_tc.cuh). Split-bf16 operands have a
+// hi and a lo plane. Tiles that one MMA reads together are stacked along the row
+// (N) dimension, so that each MMA group of the walk is one wide instruction chain:
+//   WQ   [hi | lo] of the 128 x 128 stack  [ -W ; Qhat ]
+//          rows 0..63   -W = -T' Khat      (row: token i, K: key channel c)
+//          rows 64..127 q_i * exp(G_i)      (row: token i, K: key channel c)
+//   AK   [hi | lo] of the 192 x 64 stack   [ A_qk ; Kend^T ]
+//          rows 0..63   decayed causal Q K^T, diagonal included (row: i, K: token j)
+//          rows 64..191 k_j * exp(G_last - G_j), transposed      (row: c, K: token j)
+//   gam  [128]   fp32   exp(G_last), the chunk's total decay
+//   Up   [64][128] fp32 U' = T' V, token-major (row i, column = value channel)
 // ---------------------------------------------------------------------------------
 constexpr size_t kPlaneQK = (size_t)kC * kD * 2;   // 64 x 128 bf16 tile
 constexpr size_t kPlaneKT = (size_t)kD * kC * 2;   // 128 x 64 bf16 tile
 constexpr size_t kPlaneCC = (size_t)kC * kC * 2;   // 64 x 64 bf16 tile
-constexpr size_t kRecWn = 0;
-constexpr size_t kRecQh = kRecWn + 2 * kPlaneQK;
-constexpr size_t kRecKeT = kRecQh + 2 * kPlaneQK;
-constexpr size_t kRecAqk = kRecKeT + 2 * kPlaneKT;
-constexpr size_t kRecGam = kRecAqk + 2 * kPlaneCC;
+constexpr size_t kStackWQ = 2 * kPlaneQK;          // one plane of [ -W ; Qhat ]: 128 x 128
+constexpr size_t kStackAK = kPlaneCC + kPlaneKT;   // one plane of [ A_qk ; Kend^T ]: 192 x 64
+constexpr size_t kRecWQ = 0;
+constexpr size_t kRecAK = kRecWQ + 2 * kStackWQ;
+constexpr size_t kRecGam = kRecAK + 2 * kStackAK;
 constexpr size_t kRecUp = kRecGam + kD * 4;
 constexpr size_t kRecBytes = kRecUp + (size_t)kC * kD * 4;
+// where each tile's hi plane starts; its lo plane is one stack further
+constexpr size_t kRecWn = kRecWQ;
+constexpr size_t kRecQh = kRecWQ + kPlaneQK;
+constexpr size_t kRecAqk = kRecAK;
+constexpr size_t kRecKeT = kRecAK + kPlaneCC;
 static_assert(kRecBytes % 128 == 0, "chunk records must stay 128-byte aligned");
-static_assert(kRecQh % 16 == 0 && kRecKeT % 16 == 0 && kRecAqk % 16 == 0 && kRecGam % 16 == 0 &&
-              kRecUp % 16 == 0, "record fields must be 16-byte aligned");
+static_assert(kRecAK % 16 == 0 && kRecGam % 16 == 0 && kRecUp % 16 == 0, "record fields must be 16-byte aligned");
 
 // byte offset of element (r, k) in an interleaved K-major tile with K elements per row
 __host__ __device__ constexpr uint32_t il_off(int r, int k, int K) {

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                     uint32_t hi, lo;
                     split_bf16x2(-accW[a][nt][2 * hr], -accW[a][nt][2 * hr + 1], hi, lo);
                     *reinterpret_cast<uint32_t *>(Wn + il_off(i, c, kD)) = hi;
-                    *reinterpret_cast<uint32_t *>(Wn + kPlaneQK + il_off(i, c, kD)) = lo;
+                    *reinterpret_cast<uint32_t *>(Wn + kStackWQ + il_off(i, c, kD)) = lo;
                     *reinterpret_cast<float2 *>(Up + (size_t)i * kD + c) =
                         make_float2(accU[a][nt][2 * hr], accU[a][nt][2 * hr + 1]);
                 }
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             uint32_t hi, lo;
             split_bf16x2(qq.x * expf(s.G[i][c]), qq.y * expf(s.G[i][c + 1]), hi, lo);
             *reinterpret_cast<uint32_t *>(Qh + il_off(i, c, kD)) = hi;
-            *reinterpret_cast<uint32_t *>(Qh + kPlaneQK + il_off(i, c, kD)) = lo;
+            *reinterpret_cast<uint32_t *>(Qh + kStackWQ + il_off(i, c, kD)) = lo;
         }
         uint8_t *KeT = rec + kRecKeT;
         for (int e = tid; e < kD * (kC / 2); e += kIntraThreads) {
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             uint32_t hi, lo;
             split_bf16x2(k0 * expf(gl - s.G[j][c]), k1 * expf(gl - s.G[j + 1][c]), hi, lo);
             *reinterpret_cast<uint32_t *>(KeT + il_off(c, j, kC)) = hi;
-            *reinterpret_cast<uint32_t *>(KeT + kPlaneKT + il_off(c, j, kC)) = lo;
+            *reinterpret_cast<uint32_t *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
         }
         uint8_t *Aq = rec + kRecAqk;
         for (int e = tid; e < kC * (kC / 2); e += kIntraThreads) {
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             uint32_t hi, lo;
             split_bf16x2(s.Aqk[i][j], s.Aqk[i][j + 1], hi, lo);
             *reinterpret_cast<uint32_t *>(Aq + il_off(i, j, kC)) = hi;
-            *reinterpret_cast<uint32_t *>(Aq + kPlaneCC + il_off(i, j, kC)) = lo;
+            *reinterpret_cast<uint32_t *>(Aq + kStackAK + il_off(i, j, kC)) = lo;
         }
         float *gam = reinterpret_cast<float *>(rec + kRecGam);
         if (tid < kD) gam[tid] = expf(s.G[kC - 1][tid]);
@@ -423,36 +423,48 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 
 // ---------------------------------------------------------------------------------
 // state walk: one CTA per (sequence, head) carries the full 128 x 128 state through
-// the chunks of its sequence, on the tensor cores (tcgen05, accumulators in TMEM).
+// the chunks of its sequence on the tcgen05 tensor cores, accumulators in TMEM.
 //
 // Transposed orientation, so that the 128 value channels are the MMA's M = 128 rows
-// and every accumulator row is one TMEM lane:
-//   D_U = S^T (-W)^T          [128 x 64]   then U^T = U'^T + D_U       (per thread)
-//   D_O = S^T Qhat^T          [128 x 64]
-//   D_O += U^T A_qk^T                      then o = D_O^T
-//   D_S = U^T Kend             [128 x 128]  then S^T = S^T Diag(gamma) + D_S
-// Each product is split-bf16 (hi*hi + hi*lo + lo*hi). S^T and U^T go to shared memory as
-// split planes (the A operands); the record tiles are the B operands, fetched with bulk
-// copies one chunk ahead: W and Qhat as soon as the first group of MMAs has finished
-// with them, Kend, A_qk and gamma once the state update has.
+// and every accumulator row is one TMEM lane. Per chunk, two MMA groups:
+//   group 1   [D_U | D_O1] = S^T [ -W ; Qhat ]^T          N = 128, K = 128
+//   group 2   [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T      N = 192, K = 64
+// with U^T = U'^T + D_U, o = (D_O1 + D_O2)^T and S^T <- S^T Diag(gamma) + D_S.
+// Every product is split-bf16 (hi*hi + hi*lo + lo*hi); S^T and U^T are written to
+// shared memory as split planes (A operands), the record tiles are the B operands.
 //
-// Thread t of warp w owns value channel dv = 32 (w % 4) + lane (TMEM lane dv) and half
-// hf = w / 4 of the columns: tokens 32 hf .. 32 hf + 31 of D_U / D_O, key channels
-// 64 hf .. 64 hf + 63 of the state, which it keeps in registers in fp32.
+// Nine warps with fixed roles:
+//   warps 0-3  U and O: thread = value channel dv (TMEM lane dv); build U^T after
+//              group 1, then read the output accumulators and store o, which
+//              overlaps the next chunk's group 1
+//   warps 4-7  state: thread = value channel dv, its 128 state entries in fp32
+//              registers; update S after group 2 and write the next S^T planes
+//   warp 8     issue: bulk copies of the record tiles one chunk ahead, and the MMAs
+// Named barriers hand the steps over: BAR_S (state planes ready), BAR_OR (output
+// accumulators read), BAR_U (U^T planes ready), each 128 arrivals + the issue warp.
+// Every role runs the same barrier sequence whatever happens: a wait that gives up
+// marks the CTA failed and the rest of the walk skips its work but keeps the sequence.
 // ---------------------------------------------------------------------------------
 struct WalkSmem {
-    unsigned char wq[2 * kPlaneQK + 2 * kPlaneQK];             // Wn hi, lo | Qh hi, lo
-    unsigned char ka[2 * kPlaneKT + 2 * kPlaneCC + kD * 4];    // KeT hi, lo | Aqk hi, lo | gamma
-    unsigned char st[2 * 128 * kD * 2];                        // S^T hi, lo   (M 128 x K 128)
-    unsigned char ut[2 * 128 * kC * 2];                        // U^T hi, lo   (M 128 x K 64)
-    uint64_t bar_wq, bar_ka, bar_m1, bar_m2;
+    unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
+    unsigned char ak[2 * kStackAK];      // [ A_qk ; Kend^T ] hi | lo
+    alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1)
+    unsigned char st[2 * 128 * kD * 2];  // S^T hi | lo   (M 128 x K 128)
+    unsigned char ut[2 * 128 * kC * 2];  // U^T hi | lo   (M 128 x K 64)
+    uint64_t bar_wq, bar_ak, bar_m1, bar_m2;
     uint32_t tmem_base;
     int fail;
 };
 static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
 
 constexpr int kWalkThreads = 256;
-constexpr uint32_t kWalkTmemCols = 256;  // D_U [0,64) | D_O [64,128) | D_S [128,256)
+constexpr uint32_t kWalkTmemCols = 512;  // D_U [0,64) D_O1 [64,128) D_O2 [128,192) D_S [192,320)
+constexpr int kBarS = 1, kBarU = 3;
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n));
+}
 
 // 8 consecutive fp32 values -> one 16-byte chunk of the hi plane and one of the lo plane
 __device__ __forceinline__ void split8_store(const float *x, unsigned char *hi_plane, unsigned char *lo_plane,
@@ -464,6 +476,14 @@ __device__ __forceinline__ void split8_store(const float *x, unsigned char *hi_p
     *reinterpret_cast<uint4 *>(lo_plane + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// bounded wait that gives up at once when the CTA has already failed
+__device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int &fail) {
+    if (fail) return false;
+    if (tc::mbar_wait(bar, parity)) return true;
+    fail = 1;
+    return false;
+}
+
 __global__ void __launch_bounds__(kWalkThreads, 1)
     kda_walk_kernel(int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
                     const int32_t *__restrict__ chunk_off, int32_t H, const uint8_t *__restrict__ records,
@@ -471,203 +491,245 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hf = warp >> 2;
-    const int dv = 32 * q4 + lane;
     const int n = blockIdx.x, h = blockIdx.y;
     const int64_t sbase = ((int64_t)n * H + h) * kD * kD;
+    const int dv = (warp & 3) * 32 + lane;  // value channel = TMEM lane (warps 0-7)
 
     if (*status != 0) {  // invalid batch table: make the failure visible in final_state
-        for (int c = hf * 64; c < hf * 64 + 64; ++c) Sout[sbase + (int64_t)c * kD + dv] = __int_as_float(0x7fc00000);
+        if (warp >= 4)
+            for (int c = 0; c < kD; ++c) Sout[sbase + (int64_t)c * kD + dv] = __int_as_float(0x7fc00000);
         return;
     }
     const int c_begin = chunk_off[n], c_end = chunk_off[n + 1];
     const int64_t t_begin = seq_cu[n], t_end = seq_cu[n + 1];
     auto rec_of = [&](int c) { return records + ((int64_t)c * H + h) * (int64_t)kRecBytes; };
 
-    if (tid == 0) {
-        tc::mbar_init(&s.bar_wq, 1);
-        tc::mbar_init(&s.bar_ka, 1);
-        tc::mbar_init(&s.bar_m1, 1);
-        tc::mbar_init(&s.bar_m2, 1);
-        tc::mbar_init_fence();
-        s.fail = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::mbar_init(&s.bar_wq, 1);
+            tc::mbar_init(&s.bar_ak, 1);
+            tc::mbar_init(&s.bar_m1, 1);
+            tc::mbar_init(&s.bar_m2, 1);
+            tc::mbar_init_fence();
+            s.fail = 0;
+        }
+        __syncwarp();
+        tc::tmem_alloc(&s.tmem_base, kWalkTmemCols);
     }
-    if (warp == 0) tc::tmem_alloc(&s.tmem_base, kWalkTmemCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = s.tmem_base;
-    const uint32_t lanes = (uint32_t)(32 * q4) << 16;
-    const uint32_t D_U = tmem, D_O = tmem + 64, D_S = tmem + 128;
-
-    auto issue_wq = [&](int c) {
-        tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(4 * kPlaneQK));
-        tc::bulk_g2s(s.wq, rec_of(c) + kRecWn, (uint32_t)(4 * kPlaneQK), &s.bar_wq);
-    };
-    auto issue_ka = [&](int c) {
-        const uint32_t bytes = (uint32_t)(2 * kPlaneKT + 2 * kPlaneCC + kD * 4);
-        tc::mbar_arrive_expect_tx(&s.bar_ka, bytes);
-        tc::bulk_g2s(s.ka, rec_of(c) + kRecKeT, bytes, &s.bar_ka);
-    };
-    if (tid == 0 && c_begin < c_end) {
-        issue_wq(c_begin);
-        issue_ka(c_begin);
-    }
-
-    // state: S[c][dv] for this thread's 64 key channels, in fp32
-    float Sr[64];
-#pragma unroll
-    for (int j = 0; j < 64; ++j) Sr[j] = S0 ? S0[sbase + (int64_t)(hf * 64 + j) * kD + dv] : 0.f;
-    auto store_state = [&]() {
-#pragma unroll
-        for (int j = 0; j < 64; j += 8)
-            split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, hf * 64 + j, kD));
-    };
-    store_state();
-    // U' of the first chunk: U'[i][dv] for this thread's 32 tokens
-    float Upr[32];
-    auto load_up = [&](int c) {
-        const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) Upr[j] = up[(hf * 32 + j) * kD + dv];
-    };
-    if (c_begin < c_end) load_up(c_begin);
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    constexpr uint32_t kId64 = tc::idesc_bf16_m128(64);
-    constexpr uint32_t kId128 = tc::idesc_bf16_m128(128);
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t D_UO = tmem, D_AK = tmem + 128;
     volatile int &fail = s.fail;
-    // completed-phase counts, used to drain in-flight work if a wait ever gives up
-    int n_wq = (c_begin < c_end) ? 1 : 0, n_ka = n_wq, w_wq = 0, w_ka = 0, n_m1 = 0, n_m2 = 0;
-    for (int c = c_begin; c < c_end; ++c) {
-        const uint32_t ph = (uint32_t)((c - c_begin) & 1);
-        const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
-        const int L = (int)min((int64_t)kC, t_end - t0);
 
-        // ---- group 1: D_U = S^T (-W)^T, D_O = S^T Qhat^T ----
-        if (tid == 0) {
+    if (warp < 4) {
+        // ------------------ U and O warps (thread 0 issues) -------------------
+        constexpr uint32_t kId128 = tc::idesc_bf16_m128(128), kId192 = tc::idesc_bf16_m128(192);
+        int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (thread 0)
+        auto issue_wq = [&](int c) {
+            tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
+            tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
+            ++n_wq;
+        };
+        auto issue_ak = [&](int c) {
+            tc::mbar_arrive_expect_tx(&s.bar_ak, (uint32_t)(2 * kStackAK));
+            tc::bulk_g2s(s.ak, rec_of(c) + kRecAK, (uint32_t)(2 * kStackAK), &s.bar_ak);
+            ++n_ak;
+        };
+        // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
+        auto issue_g1 = [&](int c) {
+            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
-            if (tc::mbar_wait(&s.bar_wq, ph)) {
-                ++w_wq;
-                const uint32_t s0 = tc::smem_addr(s.st), s1 = s0 + 128 * kD * 2;
-                const uint32_t w0 = tc::smem_addr(s.wq), w1 = w0 + kPlaneQK;
-                const uint32_t q0 = w0 + 2 * kPlaneQK, q1 = q0 + kPlaneQK;
+            if (c + 2 < c_end) tc::prefetch_l2(rec_of(c + 2), (uint32_t)kRecBytes);
+            if (!wait_or_fail(&s.bar_wq, ph, fail)) return;
+            ++w_wq;
+            const uint32_t a0s = tc::smem_addr(s.st), a1s = a0s + 128 * kD * 2;
+            const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
 #pragma unroll 1
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint64_t a0 = tc::desc_k(s0, kD, ks), a1 = tc::desc_k(s1, kD, ks);
-                    tc::mma(D_U, a0, tc::desc_k(w0, kD, ks), kId64, ks > 0);
-                    tc::mma(D_U, a0, tc::desc_k(w1, kD, ks), kId64, 1);
-                    tc::mma(D_U, a1, tc::desc_k(w0, kD, ks), kId64, 1);
-                    tc::mma(D_O, a0, tc::desc_k(q0, kD, ks), kId64, ks > 0);
-                    tc::mma(D_O, a0, tc::desc_k(q1, kD, ks), kId64, 1);
-                    tc::mma(D_O, a1, tc::desc_k(q0, kD, ks), kId64, 1);
-                }
-                tc::commit(&s.bar_m1);
-            } else {
-                fail = 1;
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint64_t a0 = tc::desc_k(a0s, kD, ks), a1 = tc::desc_k(a1s, kD, ks);
+                const uint64_t b0 = tc::desc_k(b0s, kD, ks), b1 = tc::desc_k(b1s, kD, ks);
+                tc::mma(D_UO, a0, b0, kId128, ks > 0);
+                tc::mma(D_UO, a0, b1, kId128, 1);
+                tc::mma(D_UO, a1, b0, kId128, 1);
             }
-        }
-        if (tc::mbar_wait(&s.bar_m1, ph)) ++n_m1; else fail = 1;
-        tc::fence_after_sync();
-        {
-            float d[32], u[32];
-            tc::tmem_ld32(D_U + lanes + hf * 32, d);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] = Upr[j] + d[j];
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) split8_store(&u[j], s.ut, s.ut + 128 * kC * 2, il_off(dv, hf * 32 + j, kC));
-        }
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (fail) break;
+            tc::commit(&s.bar_m1);
+            ++n_m1;
+        };
+        // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T
+        auto issue_g2 = [&](int c) {
+            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
+            tc::fence_after_sync();
+            if (!wait_or_fail(&s.bar_ak, ph, fail)) return;
+            ++w_ak;
+            const uint32_t a0s = tc::smem_addr(s.ut), a1s = a0s + 128 * kC * 2;
+            const uint32_t b0s = tc::smem_addr(s.ak), b1s = b0s + (uint32_t)kStackAK;
+#pragma unroll 1
+            for (int ks = 0; ks < kC / 16; ++ks) {
+                const uint64_t a0 = tc::desc_k(a0s, kC, ks), a1 = tc::desc_k(a1s, kC, ks);
+                const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
+                tc::mma(D_AK, a0, b0, kId192, ks > 0);
+                tc::mma(D_AK, a0, b1, kId192, 1);
+                tc::mma(D_AK, a1, b0, kId192, 1);
+            }
+            tc::commit(&s.bar_m2);
+            ++n_m2;
+        };
 
-        // ---- group 2: D_O += U^T A_qk^T, D_S = U^T Kend ----
-        if (tid == 0) {
-            tc::fence_after_sync();
-            if (c + 1 < c_end) {
-                issue_wq(c + 1);  // group 1 is done with W and Qhat
-                ++n_wq;
-            }
-            if (tc::mbar_wait(&s.bar_ka, ph)) {
-                ++w_ka;
-                const uint32_t u0 = tc::smem_addr(s.ut), u1 = u0 + 128 * kC * 2;
-                const uint32_t k0 = tc::smem_addr(s.ka), k1 = k0 + kPlaneKT;
-                const uint32_t a0q = k0 + 2 * kPlaneKT, a1q = a0q + kPlaneCC;
-#pragma unroll 1
-                for (int ks = 0; ks < kC / 16; ++ks) {
-                    const uint64_t a0 = tc::desc_k(u0, kC, ks), a1 = tc::desc_k(u1, kC, ks);
-                    tc::mma(D_O, a0, tc::desc_k(a0q, kC, ks), kId64, 1);
-                    tc::mma(D_O, a0, tc::desc_k(a1q, kC, ks), kId64, 1);
-                    tc::mma(D_O, a1, tc::desc_k(a0q, kC, ks), kId64, 1);
-                    tc::mma(D_S, a0, tc::desc_k(k0, kC, ks), kId128, ks > 0);
-                    tc::mma(D_S, a0, tc::desc_k(k1, kC, ks), kId128, 1);
-                    tc::mma(D_S, a1, tc::desc_k(k0, kC, ks), kId128, 1);
-                }
-                tc::commit(&s.bar_m2);
-            } else {
-                fail = 1;
-            }
-        }
-        if (c + 1 < c_end) load_up(c + 1);  // next chunk's U', hidden behind group 2
-        if (tc::mbar_wait(&s.bar_m2, ph)) ++n_m2; else fail = 1;
-        tc::fence_after_sync();
-        {
-            float d[32];
-            tc::tmem_ld32(D_O + lanes + hf * 32, d);
+        float Upr[64];
+        auto load_up = [&](int c) {
+            const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int i = hf * 32 + j;
-                if (i < L) {
-                    const int64_t off = ((t0 + i) * H + h) * (int64_t)kD + dv;
-                    if (o_f32)
-                        static_cast<float *>(o)[off] = d[j];
-                    else
-                        static_cast<__nv_bfloat16 *>(o)[off] = __float2bfloat16_rn(d[j]);
-                }
-            }
+            for (int j = 0; j < 64; ++j) Upr[j] = up[j * kD + dv];
+        };
+        if (tid == 0 && c_begin < c_end) {
+            issue_wq(c_begin);
+            issue_ak(c_begin);
+            if (c_begin + 1 < c_end) tc::prefetch_l2(rec_of(c_begin + 1), (uint32_t)kRecBytes);
         }
-        {
-            const float *gam = reinterpret_cast<const float *>(s.ka + 2 * kPlaneKT + 2 * kPlaneCC);
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                float d[32];
-                tc::tmem_ld32(D_S + lanes + hf * 64 + part * 32, d);
+        if (c_begin < c_end) load_up(c_begin);
+        named_sync(kBarS, 256);  // initial S^T planes written by the state warps
+        if (tid == 0 && c_begin < c_end) issue_g1(c_begin);
+        __syncwarp();
+        for (int c = c_begin; c < c_end; ++c) {
+            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
+            const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
+            const int L = (int)min((int64_t)kC, t_end - t0);
+            // U^T = U'^T + D_U, written as split planes for group 2
+            if (wait_or_fail(&s.bar_m1, ph, fail)) {
+                tc::fence_after_sync();
+                uint32_t d0[32], d1[32];
+                tc::tmem_ld32_nowait(D_UO + lanes, d0);
+                tc::tmem_ld32_nowait(D_UO + lanes + 32, d1);
+                tc::tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int cc = part * 32 + j;
-                    Sr[cc] = gam[hf * 64 + cc] * Sr[cc] + d[j];
+                    Upr[j] += __uint_as_float(d0[j]);
+                    Upr[32 + j] += __uint_as_float(d1[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 64; j += 8) split8_store(&Upr[j], s.ut, s.ut + 128 * kC * 2, il_off(dv, j, kC));
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            named_sync(kBarU, 128);  // U^T planes complete; group 1 is done with [ -W ; Qhat ]
+            if (tid == 0) {
+                if (c + 1 < c_end && !fail) issue_wq(c + 1);
+                issue_g2(c);
+            }
+            __syncwarp();
+            if (c + 1 < c_end) load_up(c + 1);  // next chunk's U', hidden behind group 2
+            // o = (D_O1 + D_O2)^T for this thread's value channel
+            float ov[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) ov[j] = 0.f;
+            const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
+            if (ok) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t d1[32], d2[32];
+                    tc::tmem_ld32_nowait(D_UO + lanes + 64 + 32 * half, d1);
+                    tc::tmem_ld32_nowait(D_AK + lanes + 32 * half, d2);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[32 * half + j] = __uint_as_float(d1[j]) + __uint_as_float(d2[j]);
                 }
             }
+            if (tid == 0 && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
+            __syncwarp();
+            tc::fence_before_sync();
+            named_sync(kBarS, 256);  // next S^T planes written; the output accumulators are read
+            if (tid == 0 && c + 1 < c_end) issue_g1(c + 1);
+            __syncwarp();
+            // stage o as [token][channel] in the U^T buffer (free until the next U epilogue)
+            // and write it out in 16-byte row chunks while group 1 runs
+            float *stage = reinterpret_cast<float *>(s.ut);
+#pragma unroll
+            for (int i = 0; i < kC; ++i) {
+                if (o_f32)
+                    stage[i * kD + dv] = ov[i];
+                else
+                    reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov[i]);
+            }
+            named_sync(5, 128);
+            if (ok) {
+                const int chunks_per_row = o_f32 ? kD / 4 : kD / 8;  // 16-byte chunks
+                for (int e = tid; e < L * chunks_per_row; e += 128) {
+                    const int i = e / chunks_per_row, ch = e % chunks_per_row;
+                    const int64_t row = ((t0 + i) * H + h) * (int64_t)kD;
+                    if (o_f32)
+                        reinterpret_cast<uint4 *>(static_cast<float *>(o) + row)[ch] =
+                            reinterpret_cast<const uint4 *>(stage + i * kD)[ch];
+                    else
+                        reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + row)[ch] =
+                            reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(stage) + i * kD)[ch];
+                }
+            }
+            named_sync(5, 128);  // staged tile read out before the next U^T planes land here
         }
-        store_state();
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (fail) break;
-        if (tid == 0 && c + 1 < c_end) {
-            issue_ka(c + 1);  // the state update is done with Kend, A_qk and gamma
-            ++n_ka;
-        }
-    }
-
-    if (fail) {
-        // a wait gave up: let the copies and MMAs in flight land (bounded) before the
-        // shared memory and TMEM are released, and report through the status word
-        if (tid == 0) {
+        if (tid == 0 && fail) {
+            // a wait gave up: let copies and MMAs still in flight land (bounded) before
+            // shared memory and TMEM are released, and report through the status word
             if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
-            if (n_ka > w_ka) tc::mbar_wait(&s.bar_ka, (uint32_t)(w_ka & 1));
-            tc::mbar_wait(&s.bar_m1, (uint32_t)(n_m1 & 1));
-            tc::mbar_wait(&s.bar_m2, (uint32_t)(n_m2 & 1));
+            if (n_ak > w_ak) tc::mbar_wait(&s.bar_ak, (uint32_t)(w_ak & 1));
+            if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
+            if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
             atomicExch(status, -7);
         }
+    } else {
+        // ----------------------------- state warps ------------------------------
+        float Sr[128];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) Sr[j] = __int_as_float(0x7fc00000);
+        for (int j = 0; j < kD; ++j) Sr[j] = S0 ? S0[sbase + (int64_t)j * kD + dv] : 0.f;
+#pragma unroll
+        for (int j = 0; j < kD; j += 8) split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, j, kD));
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        named_arrive(kBarS, 256);
+        for (int c = c_begin; c < c_end; ++c) {
+            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
+            const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
+            const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
+            s.gam[ph][dv] = gnext;
+            named_sync(4, 128);  // the state warps' own barrier: gamma of this chunk in place
+            if (ok) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int part = 0; part < 4; part += 2) {
+                    uint32_t d0[32], d1[32];
+                    tc::tmem_ld32_nowait(D_AK + lanes + 64 + 32 * part, d0);
+                    tc::tmem_ld32_nowait(D_AK + lanes + 64 + 32 * part + 32, d1);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const int cc = 32 * part + j;
+                        const float4 g0 = *reinterpret_cast<const float4 *>(&s.gam[ph][cc]);
+                        const float4 g1 = *reinterpret_cast<const float4 *>(&s.gam[ph][cc + 32]);
+                        Sr[cc] = g0.x * Sr[cc] + __uint_as_float(d0[j]);
+                        Sr[cc + 1] = g0.y * Sr[cc + 1] + __uint_as_float(d0[j + 1]);
+                        Sr[cc + 2] = g0.z * Sr[cc + 2] + __uint_as_float(d0[j + 2]);
+                        Sr[cc + 3] = g0.w * Sr[cc + 3] + __uint_as_float(d0[j + 3]);
+                        Sr[cc + 32] = g1.x * Sr[cc + 32] + __uint_as_float(d1[j]);
+                        Sr[cc + 33] = g1.y * Sr[cc + 33] + __uint_as_float(d1[j + 1]);
+                        Sr[cc + 34] = g1.z * Sr[cc + 34] + __uint_as_float(d1[j + 2]);
+                        Sr[cc + 35] = g1.w * Sr[cc + 35] + __uint_as_float(d1[j + 3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kD; j += 8) split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, j, kD));
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            named_arrive(kBarS, 256);
+        }
+        const bool failed = fail;
+#pragma unroll
+        for (int j = 0; j < kD; ++j)
+            Sout[sbase + (int64_t)j * kD + dv] = failed ? __int_as_float(0x7fc00000) : Sr[j];
     }
-#pragma unroll
-    for (int j = 0; j < 64; ++j) Sout[sbase + (int64_t)(hf * 64 + j) * kD + dv] = Sr[j];
 
     tc::fence_before_sync();
     __syncthreads();
