@@ -189,16 +189,29 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     __syncthreads();
 
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
-    if (tid < kD) {
+    {
         const float eA = expf(A[h]);
+        for (int e = tid; e < kC * kD; e += kIntraThreads) {
+            const int i = e / kD, c = e % kD;
+            s.G[i][c] = (i < L) ? gate_log_decay(eA, s.G[i][c]) : 0.f;
+        }
+        __syncthreads();
+        // column scan: thread (c, half) sums 32 rows, then the upper half adds the lower total
+        const int c = tid % kD, half = tid / kD;
         float acc = 0.f;
 #pragma unroll 8
-        for (int i = 0; i < kC; ++i) {
-            if (i < L) acc += gate_log_decay(eA, s.G[i][tid]);
-            s.G[i][tid] = acc;
+        for (int i = half * 32; i < half * 32 + 32; ++i) {
+            acc += s.G[i][c];
+            s.G[i][c] = acc;
         }
+        __syncthreads();
+        if (half == 1) {
+            const float lower = s.G[31][c];
+#pragma unroll 8
+            for (int i = 32; i < kC; ++i) s.G[i][c] += lower;
+        }
+        __syncthreads();
     }
-    __syncthreads();
 
     // ---- decayed Gram matrices, one 16-token tile row at a time -----------------
     for (int a = 0; a < kC / kTile; ++a) {
@@ -226,8 +239,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             {
                 const float d0 = fwd ? s.G[tok][c] - s.G[r][c] : s.G[r][c] - s.G[tok][c];
                 const float d1 = fwd ? s.G[tok][c + 1] - s.G[r][c + 1] : s.G[r][c + 1] - s.G[tok][c + 1];
-                x.x *= expf(d0);
-                x.y *= expf(d1);
+                x.x *= __expf(d0);
+                x.y *= __expf(d1);
             }
             uint32_t hi, lo;
             split_bf16x2(x.x, x.y, hi, lo);
@@ -266,25 +279,25 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     }
 
     // ---- UT transform: T = (I + A_kk)^-1, unit lower triangular -----------------
-    // diagonal 16x16 blocks by forward substitution, one column per thread
-    if (tid < 64) {
-        const int a = tid >> 4, j = tid & 15, base = a * kTile;
+    // diagonal 16x16 blocks by forward substitution: warp a solves block a, lane j (and
+    // j + 16, a duplicate) its column j, in registers; row i reads A[i][*] as a broadcast
+    if (warp < 4) {
+        const int base = warp * kTile, j = lane & 15;
+        float x[kTile];
+#pragma unroll
         for (int i = 0; i < kTile; ++i) {
-            float val;
-            if (i < j) {
-                val = 0.f;
-            } else if (i == j) {
-                val = 1.f;
-            } else {
-                float acc = 0.f;
-                for (int m = j; m < i; ++m) acc += s.Akk[base + i][base + m] * s.T[base + m][base + j];
-                val = -acc;
-            }
-            s.T[base + i][base + j] = val;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) acc += s.Akk[base + i][base + m] * x[m];  // x[m] = 0 for m < j
+            x[i] = (i < j) ? 0.f : ((i == j) ? 1.f : -acc);
+        }
+        if (lane < kTile) {
+#pragma unroll
+            for (int i = 0; i < kTile; ++i) s.T[base + i][base + j] = x[i];
         }
     } else {
         // zero the blocks above the diagonal
-        for (int e = tid - 64; e < kC * kC; e += kIntraThreads - 64) {
+        for (int e = tid - 128; e < kC * kC; e += kIntraThreads - 128) {
             const int i = e / kC, j = e % kC;
             if ((j >> 4) > (i >> 4)) s.T[i][j] = 0.f;
         }
@@ -326,7 +339,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
         const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
         uint32_t hi, lo;
-        split_bf16x2(kk.x * expf(s.G[i][c]), kk.y * expf(s.G[i][c + 1]), hi, lo);
+        split_bf16x2(kk.x * __expf(s.G[i][c]), kk.y * __expf(s.G[i][c + 1]), hi, lo);
         *reinterpret_cast<uint32_t *>(&s.u.w.kh[0][i][c]) = hi;
         *reinterpret_cast<uint32_t *>(&s.u.w.kh[1][i][c]) = lo;
     }
@@ -393,18 +406,18 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
             const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
             uint32_t hi, lo;
-            split_bf16x2(qq.x * expf(s.G[i][c]), qq.y * expf(s.G[i][c + 1]), hi, lo);
+            split_bf16x2(qq.x * __expf(s.G[i][c]), qq.y * __expf(s.G[i][c + 1]), hi, lo);
             *reinterpret_cast<uint32_t *>(Qh + il_off(i, c, kD)) = hi;
             *reinterpret_cast<uint32_t *>(Qh + kStackWQ + il_off(i, c, kD)) = lo;
         }
         uint8_t *KeT = rec + kRecKeT;
         for (int e = tid; e < kD * (kC / 2); e += kIntraThreads) {
-            const int c = e / (kC / 2), j = (e % (kC / 2)) * 2;
+            const int c = e % kD, j = (e / kD) * 2;  // consecutive threads: consecutive channels
             const float k0 = __bfloat162float(s.ks[j][c]);
             const float k1 = __bfloat162float(s.ks[j + 1][c]);
             const float gl = s.G[kC - 1][c];
             uint32_t hi, lo;
-            split_bf16x2(k0 * expf(gl - s.G[j][c]), k1 * expf(gl - s.G[j + 1][c]), hi, lo);
+            split_bf16x2(k0 * __expf(gl - s.G[j][c]), k1 * __expf(gl - s.G[j + 1][c]), hi, lo);
             *reinterpret_cast<uint32_t *>(KeT + il_off(c, j, kC)) = hi;
             *reinterpret_cast<uint32_t *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
         }
