@@ -217,35 +217,32 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     for (int a = 0; a < kC / kTile; ++a) {
         const int r = a * kTile;  // reference token of this tile row
         const int nb = r + kTile; // key rows j = 0 .. r+15
-        const int items = (2 * kTile + nb) * (kD / 2);
-        for (int e = tid; e < items; e += kIntraThreads) {
-            const int row = e / (kD / 2);
-            const int c = (e % (kD / 2)) * 2;
-            int tok;
-            const __nv_bfloat16 *src;
-            __nv_bfloat16 *dhi, *dlo;
-            bool fwd;  // factor exp(G_tok - G_r) (true) or exp(G_r - G_tok) (false)
-            if (row < kTile) {
-                tok = r + row; src = &s.qs[tok][c]; fwd = true;
-                dhi = &s.u.g.aq[0][row][c]; dlo = &s.u.g.aq[1][row][c];
-            } else if (row < 2 * kTile) {
-                tok = r + row - kTile; src = &s.ks[tok][c]; fwd = true;
-                dhi = &s.u.g.ak[0][row - kTile][c]; dlo = &s.u.g.ak[1][row - kTile][c];
-            } else {
-                tok = row - 2 * kTile; src = &s.ks[tok][c]; fwd = false;
-                dhi = &s.u.g.bk[0][tok][c]; dlo = &s.u.g.bk[1][tok][c];
-            }
-            float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(src));
-            {
-                const float d0 = fwd ? s.G[tok][c] - s.G[r][c] : s.G[r][c] - s.G[tok][c];
-                const float d1 = fwd ? s.G[tok][c + 1] - s.G[r][c + 1] : s.G[r][c + 1] - s.G[tok][c + 1];
-                x.x *= __expf(d0);
-                x.y *= __expf(d1);
-            }
+        // A operands: q and k of the tile row share the factor exp(G_i - G_r)
+        for (int e = tid; e < kTile * (kD / 2); e += kIntraThreads) {
+            const int row = e / (kD / 2), c = (e % (kD / 2)) * 2, i = r + row;
+            const float2 g = *reinterpret_cast<const float2 *>(&s.G[i][c]);
+            const float2 gr = *reinterpret_cast<const float2 *>(&s.G[r][c]);
+            const float f0 = __expf(g.x - gr.x), f1 = __expf(g.y - gr.y);
+            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
+            const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
             uint32_t hi, lo;
-            split_bf16x2(x.x, x.y, hi, lo);
-            *reinterpret_cast<uint32_t *>(dhi) = hi;
-            *reinterpret_cast<uint32_t *>(dlo) = lo;
+            split_bf16x2(qq.x * f0, qq.y * f1, hi, lo);
+            *reinterpret_cast<uint32_t *>(&s.u.g.aq[0][row][c]) = hi;
+            *reinterpret_cast<uint32_t *>(&s.u.g.aq[1][row][c]) = lo;
+            split_bf16x2(kk.x * f0, kk.y * f1, hi, lo);
+            *reinterpret_cast<uint32_t *>(&s.u.g.ak[0][row][c]) = hi;
+            *reinterpret_cast<uint32_t *>(&s.u.g.ak[1][row][c]) = lo;
+        }
+        // B operand: keys j = 0 .. r+15 with the factor exp(G_r - G_j)
+        for (int e = tid; e < nb * (kD / 2); e += kIntraThreads) {
+            const int j = e / (kD / 2), c = (e % (kD / 2)) * 2;
+            const float2 g = *reinterpret_cast<const float2 *>(&s.G[j][c]);
+            const float2 gr = *reinterpret_cast<const float2 *>(&s.G[r][c]);
+            const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[j][c]));
+            uint32_t hi, lo;
+            split_bf16x2(kk.x * __expf(gr.x - g.x), kk.y * __expf(gr.y - g.y), hi, lo);
+            *reinterpret_cast<uint32_t *>(&s.u.g.bk[0][j][c]) = hi;
+            *reinterpret_cast<uint32_t *>(&s.u.g.bk[1][j][c]) = lo;
         }
         __syncthreads();
         const int ntiles = nb / 8;  // n8 tiles of key rows
@@ -254,7 +251,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const int nt = p % ntiles;
             const __nv_bfloat16 *ah_base = mat ? &s.u.g.ak[0][0][0] : &s.u.g.aq[0][0][0];
             const __nv_bfloat16 *al_base = mat ? &s.u.g.ak[1][0][0] : &s.u.g.aq[1][0][0];
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
                 uint32_t ah[4], al[4], bh0, bh1, bl0, bl1;
@@ -262,8 +259,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 load_a(al, al_base, kLd128, 0, ks * 16, lane);
                 load_b_nk(bh0, bh1, &s.u.g.bk[0][0][0], kLd128, nt * 8, ks * 16, lane);
                 load_b_nk(bl0, bl1, &s.u.g.bk[1][0][0], kLd128, nt * 8, ks * 16, lane);
-                mma_split3(acc, ah, al, bh0, bh1, bl0, bl1);
+                mma_bf16(a0, ah, bh0, bh1);  // the three split products in separate chains
+                mma_bf16(a1, ah, bl0, bl1);
+                mma_bf16(a2, al, bh0, bh1);
             }
+            float acc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = a0[e] + (a1[e] + a2[e]);
             const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
