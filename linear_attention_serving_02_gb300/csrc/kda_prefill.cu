@@ -448,17 +448,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // Every product is split-bf16 (hi*hi + hi*lo + lo*hi); S^T and U^T are written to
 // shared memory as split planes (A operands), the record tiles are the B operands.
 //
-// Nine warps with fixed roles:
-//   warps 0-3  U and O: thread = value channel dv (TMEM lane dv); build U^T after
-//              group 1, then read the output accumulators and store o, which
-//              overlaps the next chunk's group 1
+// Eight warps with fixed roles:
+//   warps 0-3  U and O: thread = value channel dv (TMEM lane dv). After group 1 they
+//              build U^T; after group 2 they read the output accumulators, then stage
+//              o through shared memory and store it in 16-byte row chunks while the
+//              next chunk's group 1 runs.
 //   warps 4-7  state: thread = value channel dv, its 128 state entries in fp32
-//              registers; update S after group 2 and write the next S^T planes
-//   warp 8     issue: bulk copies of the record tiles one chunk ahead, and the MMAs
-// Named barriers hand the steps over: BAR_S (state planes ready), BAR_OR (output
-// accumulators read), BAR_U (U^T planes ready), each 128 arrivals + the issue warp.
-// Every role runs the same barrier sequence whatever happens: a wait that gives up
-// marks the CTA failed and the rest of the walk skips its work but keeps the sequence.
+//              registers. After group 2 they update S and write the next S^T planes.
+//              Thread 128 also issues the bulk copies (one chunk ahead, with an L2
+//              prefetch two chunks ahead) and the MMAs.
+// Named barriers hand the steps over: BAR_U (U^T planes ready), BAR_OR (output
+// accumulators read), and a state-warp barrier (S^T planes ready). Every role runs the
+// same barrier sequence whatever happens: a wait that gives up marks the CTA failed and
+// the rest of the walk skips its work but keeps the sequence.
 // ---------------------------------------------------------------------------------
 struct WalkSmem {
     unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
@@ -474,7 +476,7 @@ static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
 
 constexpr int kWalkThreads = 256;
 constexpr uint32_t kWalkTmemCols = 512;  // D_U [0,64) D_O1 [64,128) D_O2 [128,192) D_S [192,320)
-constexpr int kBarS = 1, kBarU = 3;
+constexpr int kBarOR = 2, kBarU = 3;
 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
 __device__ __forceinline__ void named_arrive(int id, int n) {
@@ -540,9 +542,89 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     volatile int &fail = s.fail;
 
     if (warp < 4) {
-        // ------------------ U and O warps (thread 0 issues) -------------------
+        // ----------------------------- U and O warps -----------------------------
+        float Upr[64];
+        auto load_up = [&](int c) {
+            const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) Upr[j] = up[j * kD + dv];
+        };
+        if (c_begin < c_end) load_up(c_begin);
+        tc::fence_before_sync();
+        named_arrive(kBarOR, 256);  // nothing to read yet: group 1 of the first chunk may start
+        for (int c = c_begin; c < c_end; ++c) {
+            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
+            const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
+            const int L = (int)min((int64_t)kC, t_end - t0);
+            // U^T = U'^T + D_U, written as split planes for group 2
+            if (wait_or_fail(&s.bar_m1, ph, fail)) {
+                tc::fence_after_sync();
+                uint32_t d0[32], d1[32];
+                tc::tmem_ld32_nowait(D_UO + lanes, d0);
+                tc::tmem_ld32_nowait(D_UO + lanes + 32, d1);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    Upr[j] += __uint_as_float(d0[j]);
+                    Upr[32 + j] += __uint_as_float(d1[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 64; j += 8) split8_store(&Upr[j], s.ut, s.ut + 128 * kC * 2, il_off(dv, j, kC));
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            named_arrive(kBarU, 256);  // U^T planes complete; group 1 is done with [ -W ; Qhat ]
+            // o = (D_O1 + D_O2)^T for this thread's value channel
+            float ov[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) ov[j] = 0.f;
+            const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
+            if (ok) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t d1[32], d2[32];
+                    tc::tmem_ld32_nowait(D_UO + lanes + 64 + 32 * half, d1);
+                    tc::tmem_ld32_nowait(D_AK + lanes + 32 * half, d2);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[32 * half + j] = __uint_as_float(d1[j]) + __uint_as_float(d2[j]);
+                }
+            }
+            tc::fence_before_sync();
+            named_arrive(kBarOR, 256);  // output accumulators read: the next group 1 may overwrite them
+            // stage o as [token][channel] in the U^T buffer (free until the next U epilogue)
+            // and write it out in 16-byte row chunks while the next group 1 runs
+            float *stage = reinterpret_cast<float *>(s.ut);
+#pragma unroll
+            for (int i = 0; i < kC; ++i) {
+                if (o_f32)
+                    stage[i * kD + dv] = ov[i];
+                else
+                    reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov[i]);
+            }
+            named_sync(5, 128);
+            if (ok) {
+                const int chunks_per_row = o_f32 ? kD / 4 : kD / 8;  // 16-byte chunks
+                for (int e = tid; e < L * chunks_per_row; e += 128) {
+                    const int i = e / chunks_per_row, ch = e % chunks_per_row;
+                    const int64_t row = ((t0 + i) * H + h) * (int64_t)kD;
+                    if (o_f32)
+                        reinterpret_cast<uint4 *>(static_cast<float *>(o) + row)[ch] =
+                            reinterpret_cast<const uint4 *>(stage + i * kD)[ch];
+                    else
+                        reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + row)[ch] =
+                            reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(stage) + i * kD)[ch];
+                }
+            }
+            named_sync(5, 128);  // staged tile read out before the next U^T planes land here
+            if (c + 1 < c_end) load_up(c + 1);
+        }
+    } else {
+        // ----------------- state warps (thread 128 issues the MMAs) -----------------
+        const bool issuer = (tid == 128);
         constexpr uint32_t kId128 = tc::idesc_bf16_m128(128), kId192 = tc::idesc_bf16_m128(192);
-        int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (thread 0)
+        int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (issuer)
         auto issue_wq = [&](int c) {
             tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
             tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
@@ -593,109 +675,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++n_m2;
         };
 
-        float Upr[64];
-        auto load_up = [&](int c) {
-            const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
-#pragma unroll
-            for (int j = 0; j < 64; ++j) Upr[j] = up[j * kD + dv];
-        };
-        if (tid == 0 && c_begin < c_end) {
-            issue_wq(c_begin);
-            issue_ak(c_begin);
-            if (c_begin + 1 < c_end) tc::prefetch_l2(rec_of(c_begin + 1), (uint32_t)kRecBytes);
-        }
-        if (c_begin < c_end) load_up(c_begin);
-        named_sync(kBarS, 256);  // initial S^T planes written by the state warps
-        if (tid == 0 && c_begin < c_end) issue_g1(c_begin);
-        __syncwarp();
-        for (int c = c_begin; c < c_end; ++c) {
-            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
-            const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
-            const int L = (int)min((int64_t)kC, t_end - t0);
-            // U^T = U'^T + D_U, written as split planes for group 2
-            if (wait_or_fail(&s.bar_m1, ph, fail)) {
-                tc::fence_after_sync();
-                uint32_t d0[32], d1[32];
-                tc::tmem_ld32_nowait(D_UO + lanes, d0);
-                tc::tmem_ld32_nowait(D_UO + lanes + 32, d1);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    Upr[j] += __uint_as_float(d0[j]);
-                    Upr[32 + j] += __uint_as_float(d1[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < 64; j += 8) split8_store(&Upr[j], s.ut, s.ut + 128 * kC * 2, il_off(dv, j, kC));
-            }
-            tc::fence_proxy_async();
-            tc::fence_before_sync();
-            named_sync(kBarU, 128);  // U^T planes complete; group 1 is done with [ -W ; Qhat ]
-            if (tid == 0) {
-                if (c + 1 < c_end && !fail) issue_wq(c + 1);
-                issue_g2(c);
-            }
-            __syncwarp();
-            if (c + 1 < c_end) load_up(c + 1);  // next chunk's U', hidden behind group 2
-            // o = (D_O1 + D_O2)^T for this thread's value channel
-            float ov[64];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) ov[j] = 0.f;
-            const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
-            if (ok) {
-                tc::fence_after_sync();
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t d1[32], d2[32];
-                    tc::tmem_ld32_nowait(D_UO + lanes + 64 + 32 * half, d1);
-                    tc::tmem_ld32_nowait(D_AK + lanes + 32 * half, d2);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) ov[32 * half + j] = __uint_as_float(d1[j]) + __uint_as_float(d2[j]);
-                }
-            }
-            if (tid == 0 && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
-            __syncwarp();
-            tc::fence_before_sync();
-            named_sync(kBarS, 256);  // next S^T planes written; the output accumulators are read
-            if (tid == 0 && c + 1 < c_end) issue_g1(c + 1);
-            __syncwarp();
-            // stage o as [token][channel] in the U^T buffer (free until the next U epilogue)
-            // and write it out in 16-byte row chunks while group 1 runs
-            float *stage = reinterpret_cast<float *>(s.ut);
-#pragma unroll
-            for (int i = 0; i < kC; ++i) {
-                if (o_f32)
-                    stage[i * kD + dv] = ov[i];
-                else
-                    reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov[i]);
-            }
-            named_sync(5, 128);
-            if (ok) {
-                const int chunks_per_row = o_f32 ? kD / 4 : kD / 8;  // 16-byte chunks
-                for (int e = tid; e < L * chunks_per_row; e += 128) {
-                    const int i = e / chunks_per_row, ch = e % chunks_per_row;
-                    const int64_t row = ((t0 + i) * H + h) * (int64_t)kD;
-                    if (o_f32)
-                        reinterpret_cast<uint4 *>(static_cast<float *>(o) + row)[ch] =
-                            reinterpret_cast<const uint4 *>(stage + i * kD)[ch];
-                    else
-                        reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + row)[ch] =
-                            reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(stage) + i * kD)[ch];
-                }
-            }
-            named_sync(5, 128);  // staged tile read out before the next U^T planes land here
-        }
-        if (tid == 0 && fail) {
-            // a wait gave up: let copies and MMAs still in flight land (bounded) before
-            // shared memory and TMEM are released, and report through the status word
-            if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
-            if (n_ak > w_ak) tc::mbar_wait(&s.bar_ak, (uint32_t)(w_ak & 1));
-            if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
-            if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
-            atomicExch(status, -7);
-        }
-    } else {
-        // ----------------------------- state warps ------------------------------
         float Sr[128];
 #pragma unroll
         for (int j = 0; j < kD; ++j) Sr[j] = S0 ? S0[sbase + (int64_t)j * kD + dv] : 0.f;
@@ -703,13 +682,28 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         for (int j = 0; j < kD; j += 8) split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, j, kD));
         tc::fence_proxy_async();
         tc::fence_before_sync();
-        named_arrive(kBarS, 256);
+        named_sync(4, 128);  // initial S^T planes complete
+        if (issuer && c_begin < c_end) {
+            issue_wq(c_begin);
+            issue_ak(c_begin);
+            if (c_begin + 1 < c_end) tc::prefetch_l2(rec_of(c_begin + 1), (uint32_t)kRecBytes);
+        }
+        named_sync(kBarOR, 256);
+        if (issuer && c_begin < c_end) issue_g1(c_begin);
+        __syncwarp();
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
+            named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
+            if (issuer) {
+                if (c + 1 < c_end && !fail) issue_wq(c + 1);  // group 1 is done with [ -W ; Qhat ]
+                issue_g2(c);
+            }
+            __syncwarp();
             const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
+            if (issuer && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
             s.gam[ph][dv] = gnext;
-            named_sync(4, 128);  // the state warps' own barrier: gamma of this chunk in place
+            named_sync(4, 128);  // gamma of this chunk in place
             if (ok) {
                 tc::fence_after_sync();
 #pragma unroll
@@ -738,7 +732,19 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             for (int j = 0; j < kD; j += 8) split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, j, kD));
             tc::fence_proxy_async();
             tc::fence_before_sync();
-            named_arrive(kBarS, 256);
+            named_sync(4, 128);       // next S^T planes complete, D_S read
+            named_sync(kBarOR, 256);  // the U and O warps have read this chunk's output accumulators
+            if (issuer && c + 1 < c_end) issue_g1(c + 1);
+            __syncwarp();
+        }
+        if (issuer && fail) {
+            // a wait gave up: let copies and MMAs still in flight land (bounded) before
+            // shared memory and TMEM are released, and report through the status word
+            if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
+            if (n_ak > w_ak) tc::mbar_wait(&s.bar_ak, (uint32_t)(w_ak & 1));
+            if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
+            if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
+            atomicExch(status, -7);
         }
         const bool failed = fail;
 #pragma unroll
