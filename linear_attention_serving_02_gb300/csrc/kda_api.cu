@@ -8,14 +8,22 @@
 #include "kda_common.cuh"
 
 namespace kda {
+struct WalkUnit;
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
-                        int32_t *seq_cu, int32_t *chunk_off, cudaStream_t st);
+                        int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
+                        int32_t *n_units, cudaStream_t st);
+cudaError_t launch_segment_plan(const int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N,
+                                int32_t H, int32_t P, const float *S0, float *Sout, float *Sin, float *Mseg,
+                                float *Rseg, WalkUnit *unitsA, int32_t *nA, WalkUnit *unitsC, int32_t *nC,
+                                int32_t *chains, cudaStream_t st);
+cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
+                           const float *Mseg, const float *Rseg, cudaStream_t st);
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                          const float *A, const float *b, const int32_t *status, const int32_t *seq_cu,
                          const int32_t *chunk_off, int32_t N, int32_t H, int64_t nslots, uint8_t *records,
                          cudaStream_t st);
-cudaError_t launch_walk(int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N, int32_t H,
-                        const uint8_t *records, const float *S0, float *Sout, void *o, int o_f32, cudaStream_t st);
+cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
+                        int32_t H, const uint8_t *records, void *o, int o_f32, cudaStream_t st);
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                           const float *A, const float *b, float *state, float *o, int32_t N, int32_t H,
                           int num_sms, cudaStream_t st);
@@ -23,6 +31,47 @@ size_t intra_smem_bytes();
 }  // namespace kda
 
 namespace {
+
+// Byte offsets of everything kda_chunk_prefill keeps in its workspace, a pure function of
+// (total tokens, sequences, heads) shared by the size query and the call.
+struct WsLayout {
+    size_t seq_cu, chunk_off, records, units, unitsA, unitsC, chains, sin, mseg, rseg, total;
+    int64_t nslots, seg_bound;
+    int P;
+};
+WsLayout ws_layout(int64_t total_tokens, int64_t N, int64_t H) {
+    using kda::align_up;
+    WsLayout w;
+    w.nslots = kda::chunk_bound(total_tokens, N);
+    w.P = kda::walk_segment_chunks(total_tokens, N, H);
+    w.seg_bound = w.P ? kda::segment_bound(total_tokens, N, w.P) : 0;
+    const size_t unit_bytes = sizeof(kda::WalkUnit);
+    size_t off = kda::kWsHeader;
+    w.seq_cu = off;
+    off += kda::ws_table_bytes(N);
+    w.chunk_off = off;
+    off += kda::ws_table_bytes(N);
+    w.records = off;
+    off += (size_t)w.nslots * H * kda::kRecBytes;
+    w.units = off;
+    off += align_up((size_t)N * unit_bytes, 256);
+    w.unitsA = off;
+    off += align_up((size_t)2 * w.seg_bound * unit_bytes, 256);
+    w.unitsC = off;
+    off += align_up((size_t)w.seg_bound * unit_bytes, 256);
+    w.chains = off;
+    off += align_up((size_t)(w.P ? 2 * N : 0) * 4, 256);
+    const size_t states = (size_t)w.seg_bound * H * kda::kStateFloats * 4;
+    w.sin = off;
+    off += states;
+    w.mseg = off;
+    off += states;
+    w.rseg = off;
+    off += states;
+    w.total = off;
+    return w;
+}
+
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -75,8 +124,7 @@ int kda_version(void) { return 100; }
 
 size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
     if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return 0;
-    const int64_t slots = kda::chunk_bound(total_tokens, num_seqs);
-    return kda::kWsHeader + 2 * kda::ws_table_bytes(num_seqs) + (size_t)slots * num_heads * kda::kRecBytes;
+    return ws_layout(total_tokens, num_seqs, num_heads).total;
 }
 
 int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
@@ -114,21 +162,43 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const WsLayout w = ws_layout(total, num_seqs, num_heads);
     int32_t *status = reinterpret_cast<int32_t *>(ws);
-    int32_t *seq_cu = reinterpret_cast<int32_t *>(ws + kda::kWsHeader);
-    int32_t *chunk_off = reinterpret_cast<int32_t *>(ws + kda::kWsHeader + kda::ws_table_bytes(num_seqs));
-    uint8_t *records = ws + kda::kWsHeader + 2 * kda::ws_table_bytes(num_seqs);
-    const int64_t nslots = kda::chunk_bound(total, num_seqs);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + 16);  // units of the plain walk, phase A, phase C
+    int32_t *seq_cu = reinterpret_cast<int32_t *>(ws + w.seq_cu);
+    int32_t *chunk_off = reinterpret_cast<int32_t *>(ws + w.chunk_off);
+    uint8_t *records = ws + w.records;
+    kda::WalkUnit *units = reinterpret_cast<kda::WalkUnit *>(ws + w.units);
     const int o_f32 = (o_dtype == KDA_OUT_F32) ? 1 : 0;
 
-    if (kda::launch_plan(cu_seqlens, num_seqs, seq_len, total, status, seq_cu, chunk_off, st) != cudaSuccess)
+    if (kda::launch_plan(cu_seqlens, num_seqs, seq_len, total, status, seq_cu, chunk_off, num_heads, initial_state,
+                         final_state, units, counts, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (kda::launch_intra(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k),
                           reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, status, seq_cu, chunk_off, num_seqs,
-                          num_heads, nslots, records, st) != cudaSuccess)
+                          num_heads, w.nslots, records, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_walk(status, seq_cu, chunk_off, num_seqs, num_heads, records, initial_state, final_state, o, o_f32,
-                         st) != cudaSuccess)
+    if (w.P == 0) {
+        if (kda::launch_walk(status, units, counts, num_seqs, num_heads, records, o, o_f32, st) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        return KDA_OK;
+    }
+    // segmented walk: phase A (segment maps), phase B (chain them), phase C (outputs)
+    kda::WalkUnit *unitsA = reinterpret_cast<kda::WalkUnit *>(ws + w.unitsA);
+    kda::WalkUnit *unitsC = reinterpret_cast<kda::WalkUnit *>(ws + w.unitsC);
+    int32_t *chains = reinterpret_cast<int32_t *>(ws + w.chains);
+    float *sin = reinterpret_cast<float *>(ws + w.sin);
+    float *mseg = reinterpret_cast<float *>(ws + w.mseg);
+    float *rseg = reinterpret_cast<float *>(ws + w.rseg);
+    if (kda::launch_segment_plan(status, seq_cu, chunk_off, num_seqs, num_heads, w.P, initial_state, final_state, sin,
+                                 mseg, rseg, unitsA, counts + 1, unitsC, counts + 2, chains, st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (kda::launch_walk(status, unitsA, counts + 1, 2 * w.seg_bound, num_heads, records, o, o_f32, st) !=
+        cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (kda::launch_combine(status, chains, num_seqs, num_heads, sin, mseg, rseg, st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (kda::launch_walk(status, unitsC, counts + 2, w.seg_bound, num_heads, records, o, o_f32, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -71,6 +71,49 @@ __host__ __device__ inline int64_t chunk_bound(int64_t total_tokens, int64_t num
 }
 
 // ---------------------------------------------------------------------------------
+// Walk units: one CTA of the state walk (per head, blockIdx.y) carries a state across a
+// run of chunks of one sequence. A plain walk has one unit per sequence. With few long
+// sequences the chunks are cut into segments that run in parallel (the single-GPU form
+// of KDA context parallelism): each segment's affine state map S_out = M S_in + R is
+// found from walks started at zero and at the identity, the maps are chained per
+// sequence, and every segment is walked again from its true input state.
+// ---------------------------------------------------------------------------------
+struct WalkUnit {
+    const float *in;  // state at the start for head 0 ([128][128], row = key channel), head h
+                      // at in + h * 128 * 128; nullptr: zero (or the identity, see flags)
+    float *out;       // state at the end, same layout; nullptr: not kept
+    int32_t c_begin, c_end;  // chunk-record slots
+    int32_t t_begin, t_end;  // tokens of those chunks (the last chunk may be partial)
+    int32_t flags;
+    int32_t pad;
+};
+constexpr int kUnitWriteO = 1;    // write the outputs o of these chunks
+constexpr int kUnitAddUp = 2;     // U = U' - W S (else U = -W S: the homogeneous map)
+constexpr int kUnitIdentity = 4;  // start from the identity when in == nullptr
+constexpr size_t kStateFloats = (size_t)kD * kD;
+
+// Segment length (in chunks) of the segmented walk, or 0 for a plain walk. A pure
+// function of the batch size, so that the workspace size can be computed without a
+// device: segments pay when there are fewer (sequence, head) chains than about a wave
+// of the GPU's 152 SMs and the chains are long.
+__host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
+    const int64_t chains = num_seqs * num_heads;
+    if (chains <= 0) return 0;
+    const int64_t slots = chunk_bound(total_tokens, num_seqs);
+    const int64_t avg = slots / num_seqs;
+    if (chains * 2 >= 152 || avg < 24) return 0;
+    // phase A runs 2 S - 3 walks per chain: aim for about one wave (10 % slack)
+    int64_t S = (167 / chains + 3) / 2;
+    if (S < 2) S = 2;
+    int64_t P = (avg + S - 1) / S;
+    if (P < 4) P = 4;
+    return (int)P;
+}
+__host__ __device__ inline int64_t segment_bound(int64_t total_tokens, int64_t num_seqs, int P) {
+    return (chunk_bound(total_tokens, num_seqs) + (int64_t)(P - 1) * num_seqs) / P;
+}
+
+// ---------------------------------------------------------------------------------
 // Gate: log a = g_min * sigmoid(exp(A_h) * z), beta = sigmoid(b)
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ float gate_log_decay(float eA, float z) {

@@ -40,7 +40,8 @@ namespace kda {
 // ---------------------------------------------------------------------------------
 __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t N, int64_t seq_len,
                                 int64_t total_tokens, int32_t *__restrict__ status, int32_t *__restrict__ seq_cu,
-                                int32_t *__restrict__ chunk_off) {
+                                int32_t *__restrict__ chunk_off, int32_t H, const float *S0, float *Sout,
+                                WalkUnit *__restrict__ units, int32_t *__restrict__ n_units) {
     __shared__ int32_t carry;
     __shared__ int32_t bad;
     __shared__ int32_t scan[256];
@@ -61,14 +62,30 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
     }
     __syncthreads();
     if (bad) {
+        // empty walks whose only job is to mark each final state invalid (NaN)
         for (int64_t n = tid; n <= N; n += blockDim.x) {
             seq_cu[n] = 0;
             chunk_off[n] = 0;
+            if (n < N) {
+                WalkUnit u;
+                u.in = nullptr;
+                u.out = Sout + (size_t)n * H * kStateFloats;
+                u.c_begin = u.c_end = u.t_begin = u.t_end = 0;
+                u.flags = 0;
+                u.pad = 0;
+                units[n] = u;
+            }
         }
-        if (tid == 0) *status = -4;  // KDA_ERR_SEQLENS
+        if (tid == 0) {
+            *status = -4;  // KDA_ERR_SEQLENS
+            *n_units = N;
+        }
         return;
     }
-    if (tid == 0) *status = 0;
+    if (tid == 0) {
+        *status = 0;
+        *n_units = N;
+    }
     for (int64_t base = 0; base <= N; base += 256) {
         const int64_t n = base + tid;
         int32_t start = 0, len = 0;
@@ -91,8 +108,145 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
         // exclusive offset of sequence n = carry + inclusive(n) - len(n)
         if (n <= N) chunk_off[n] = carry + scan[tid] - len;
         __syncthreads();
+        // the plain walk: one unit per sequence (read after this kernel, so the table
+        // entries of n + 1 written in the same pass are complete by then)
+        if (n < N) {
+            WalkUnit u;
+            u.in = S0 ? S0 + (size_t)n * H * kStateFloats : nullptr;
+            u.out = Sout + (size_t)n * H * kStateFloats;
+            u.c_begin = chunk_off[n];
+            u.c_end = chunk_off[n] + len;
+            u.t_begin = start;
+            u.t_end = cu_seqlens ? cu_seqlens[n + 1] : (int32_t)((n + 1) * seq_len);
+            u.flags = kUnitWriteO | kUnitAddUp;
+            u.pad = 0;
+            units[n] = u;
+        }
         if (tid == 255) carry += scan[255];
         __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// segmented walk: tables of the three phases (one thread; used only when there are few
+// sequences). Segment g of the batch is segment sigma of sequence n, g = seg_base[n] + sigma.
+//   phase A  segment 0 from the initial state       -> Sin[g0 + 1]       (the next input)
+//            segment sigma (1 .. S-2) from zero     -> R[g],  with U'
+//            segment sigma (1 .. S-2) from identity -> M[g],  without U'
+//   phase B  Sin[g + 1] = M[g] Sin[g] + R[g]  for sigma = 1 .. S-2 (kda_combine_kernel)
+//   phase C  every segment from its input state (Sin[g], or the initial state for
+//            sigma = 0), writing o; the last one writes the final state
+// ---------------------------------------------------------------------------------
+__global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
+                                        const int32_t *__restrict__ chunk_off, int32_t N, int32_t H, int32_t P,
+                                        const float *S0, float *Sout, float *Sin, float *Mseg, float *Rseg,
+                                        WalkUnit *__restrict__ unitsA, int32_t *__restrict__ nA,
+                                        WalkUnit *__restrict__ unitsC, int32_t *__restrict__ nC,
+                                        int32_t *__restrict__ chains) {
+    if (threadIdx.x != 0) return;
+    if (*status != 0) {
+        // no maps to build; phase C only marks each final state invalid (NaN)
+        for (int32_t n = 0; n < N; ++n) {
+            chains[2 * n] = 0;
+            chains[2 * n + 1] = 0;
+            WalkUnit u;
+            u.in = nullptr;
+            u.out = Sout + (size_t)n * H * kStateFloats;
+            u.c_begin = u.c_end = u.t_begin = u.t_end = 0;
+            u.flags = 0;
+            u.pad = 0;
+            unitsC[n] = u;
+        }
+        *nA = 0;
+        *nC = N;
+        return;
+    }
+    const size_t seg_stride = (size_t)H * kStateFloats;  // one segment's states for all heads
+    int32_t a = 0, g = 0;
+    for (int32_t n = 0; n < N; ++n) {
+        const int32_t c0 = chunk_off[n], c1 = chunk_off[n + 1];
+        const int32_t t0 = seq_cu[n], t1 = seq_cu[n + 1];
+        const int32_t S = (c1 - c0 + P - 1) / P;
+        chains[2 * n] = g;
+        chains[2 * n + 1] = S;
+        const float *init = S0 ? S0 + (size_t)n * seg_stride : nullptr;
+        for (int32_t sg = 0; sg < S; ++sg) {
+            WalkUnit u;
+            u.c_begin = c0 + sg * P;
+            u.c_end = min(c1, c0 + (sg + 1) * P);
+            u.t_begin = t0 + sg * P * kC;
+            u.t_end = min(t1, t0 + (sg + 1) * P * kC);
+            u.pad = 0;
+            // phase C
+            u.in = sg == 0 ? init : Sin + (size_t)(g + sg) * seg_stride;
+            u.out = sg == S - 1 ? Sout + (size_t)n * seg_stride : nullptr;
+            u.flags = kUnitWriteO | kUnitAddUp;
+            unitsC[g + sg] = u;
+            // phase A
+            if (S >= 2 && sg == 0) {
+                u.in = init;
+                u.out = Sin + (size_t)(g + 1) * seg_stride;
+                u.flags = kUnitAddUp;
+                unitsA[a++] = u;
+            } else if (sg >= 1 && sg <= S - 2) {
+                u.in = nullptr;
+                u.out = Rseg + (size_t)(g + sg) * seg_stride;
+                u.flags = kUnitAddUp;
+                unitsA[a++] = u;
+                u.out = Mseg + (size_t)(g + sg) * seg_stride;
+                u.flags = kUnitIdentity;
+                unitsA[a++] = u;
+            }
+        }
+        g += S;
+    }
+    *nA = a;
+    *nC = g;
+}
+
+// Phase B: Sin[g + 1] = M[g] Sin[g] + R[g] along each sequence's segments, in fp32 on the
+// CUDA cores (exact accumulation, a short serial chain). One CTA per (sequence, head,
+// 16 value columns); thread t computes row t / 2, columns 8 (t % 2) .. +7 of its slice.
+__global__ void __launch_bounds__(256)
+    kda_combine_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ chains, int32_t H,
+                       float *__restrict__ Sin, const float *__restrict__ Mseg, const float *__restrict__ Rseg) {
+    __shared__ __align__(16) float xs[kD][16];
+    if (*status != 0) return;
+    const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * 16;
+    const int g0 = chains[2 * n], S = chains[2 * n + 1];
+    const int tid = threadIdx.x, row = tid >> 1, cpart = (tid & 1) * 8;
+    const size_t seg_stride = (size_t)H * kStateFloats, hoff = (size_t)h * kStateFloats;
+    for (int sg = 1; sg <= S - 2; ++sg) {
+        const float *X = Sin + (size_t)(g0 + sg) * seg_stride + hoff;
+        const float *M = Mseg + (size_t)(g0 + sg) * seg_stride + hoff;
+        const float *R = Rseg + (size_t)(g0 + sg) * seg_stride + hoff;
+        float *Y = Sin + (size_t)(g0 + sg + 1) * seg_stride + hoff;
+        *reinterpret_cast<float4 *>(&xs[row][cpart]) = *reinterpret_cast<const float4 *>(X + row * kD + col0 + cpart);
+        *reinterpret_cast<float4 *>(&xs[row][cpart + 4]) =
+            *reinterpret_cast<const float4 *>(X + row * kD + col0 + cpart + 4);
+        __syncthreads();
+        float acc[8];
+        const float4 r0 = *reinterpret_cast<const float4 *>(R + row * kD + col0 + cpart);
+        const float4 r1 = *reinterpret_cast<const float4 *>(R + row * kD + col0 + cpart + 4);
+        acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
+        acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
+        const float4 *mrow = reinterpret_cast<const float4 *>(M + row * kD);
+#pragma unroll 4
+        for (int k4 = 0; k4 < kD / 4; ++k4) {
+            const float4 m = mrow[k4];
+            const float mk[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 x0 = *reinterpret_cast<const float4 *>(&xs[4 * k4 + q][cpart]);
+                const float4 x1 = *reinterpret_cast<const float4 *>(&xs[4 * k4 + q][cpart + 4]);
+                acc[0] += mk[q] * x0.x; acc[1] += mk[q] * x0.y; acc[2] += mk[q] * x0.z; acc[3] += mk[q] * x0.w;
+                acc[4] += mk[q] * x1.x; acc[5] += mk[q] * x1.y; acc[6] += mk[q] * x1.z; acc[7] += mk[q] * x1.w;
+            }
+        }
+        *reinterpret_cast<float4 *>(Y + row * kD + col0 + cpart) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(Y + row * kD + col0 + cpart + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        __threadfence_block();
+        __syncthreads();  // this slice of Y is the next step's X, written by this CTA alone
     }
 }
 
@@ -502,23 +656,29 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
 }
 
 __global__ void __launch_bounds__(kWalkThreads, 1)
-    kda_walk_kernel(int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
-                    const int32_t *__restrict__ chunk_off, int32_t H, const uint8_t *__restrict__ records,
-                    const float *__restrict__ S0, float *__restrict__ Sout, void *__restrict__ o, int o_f32) {
+    kda_walk_kernel(int32_t *__restrict__ status, const WalkUnit *__restrict__ units,
+                    const int32_t *__restrict__ n_units, int32_t H, const uint8_t *__restrict__ records,
+                    void *__restrict__ o, int o_f32) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = blockIdx.x, h = blockIdx.y;
-    const int64_t sbase = ((int64_t)n * H + h) * kD * kD;
+    const int h = blockIdx.y;
+    if ((int)blockIdx.x >= *n_units) return;
+    const WalkUnit unit = units[blockIdx.x];
+    const float *S0 = unit.in ? unit.in + (size_t)h * kStateFloats : nullptr;
+    float *Sout = unit.out ? unit.out + (size_t)h * kStateFloats : nullptr;
+    const bool write_o = (unit.flags & kUnitWriteO) != 0;
+    const bool add_up = (unit.flags & kUnitAddUp) != 0;
+    const bool identity = (unit.flags & kUnitIdentity) != 0;
     const int dv = (warp & 3) * 32 + lane;  // value channel = TMEM lane (warps 0-7)
 
     if (*status != 0) {  // invalid batch table: make the failure visible in final_state
-        if (warp >= 4)
-            for (int c = 0; c < kD; ++c) Sout[sbase + (int64_t)c * kD + dv] = __int_as_float(0x7fc00000);
+        if (warp >= 4 && Sout)
+            for (int c = 0; c < kD; ++c) Sout[(int64_t)c * kD + dv] = __int_as_float(0x7fc00000);
         return;
     }
-    const int c_begin = chunk_off[n], c_end = chunk_off[n + 1];
-    const int64_t t_begin = seq_cu[n], t_end = seq_cu[n + 1];
+    const int c_begin = unit.c_begin, c_end = unit.c_end;
+    const int64_t t_begin = unit.t_begin, t_end = unit.t_end;
     auto rec_of = [&](int c) { return records + ((int64_t)c * H + h) * (int64_t)kRecBytes; };
 
     if (warp == 0) {
@@ -547,7 +707,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         auto load_up = [&](int c) {
             const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) Upr[j] = up[j * kD + dv];
+            for (int j = 0; j < 64; ++j) Upr[j] = add_up ? up[j * kD + dv] : 0.f;
         };
         if (c_begin < c_end) load_up(c_begin);
         tc::fence_before_sync();
@@ -578,7 +738,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             float ov[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) ov[j] = 0.f;
-            const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
+            const bool ok = wait_or_fail(&s.bar_m2, ph, fail) && write_o;
             if (ok) {
                 tc::fence_after_sync();
 #pragma unroll
@@ -677,7 +837,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 
         float Sr[128];
 #pragma unroll
-        for (int j = 0; j < kD; ++j) Sr[j] = S0 ? S0[sbase + (int64_t)j * kD + dv] : 0.f;
+        for (int j = 0; j < kD; ++j) Sr[j] = S0 ? S0[(int64_t)j * kD + dv] : ((identity && j == dv) ? 1.f : 0.f);
 #pragma unroll
         for (int j = 0; j < kD; j += 8) split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, j, kD));
         tc::fence_proxy_async();
@@ -747,9 +907,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             atomicExch(status, -7);
         }
         const bool failed = fail;
+        if (Sout) {
 #pragma unroll
-        for (int j = 0; j < kD; ++j)
-            Sout[sbase + (int64_t)j * kD + dv] = failed ? __int_as_float(0x7fc00000) : Sr[j];
+            for (int j = 0; j < kD; ++j) Sout[(int64_t)j * kD + dv] = failed ? __int_as_float(0x7fc00000) : Sr[j];
+        }
     }
 
     tc::fence_before_sync();
@@ -762,8 +923,26 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 // ---------------------------------------------------------------------------------
 size_t intra_smem_bytes() { return sizeof(IntraSmem); }
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
-                        int32_t *seq_cu, int32_t *chunk_off, cudaStream_t st) {
-    kda_plan_kernel<<<1, 256, 0, st>>>(cu, N, seq_len, total, status, seq_cu, chunk_off);
+                        int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
+                        int32_t *n_units, cudaStream_t st) {
+    kda_plan_kernel<<<1, 256, 0, st>>>(cu, N, seq_len, total, status, seq_cu, chunk_off, H, S0, Sout, units,
+                                       n_units);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_segment_plan(const int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N,
+                                int32_t H, int32_t P, const float *S0, float *Sout, float *Sin, float *Mseg,
+                                float *Rseg, WalkUnit *unitsA, int32_t *nA, WalkUnit *unitsC, int32_t *nC,
+                                int32_t *chains, cudaStream_t st) {
+    kda_segment_plan_kernel<<<1, 32, 0, st>>>(status, seq_cu, chunk_off, N, H, P, S0, Sout, Sin, Mseg, Rseg, unitsA,
+                                              nA, unitsC, nC, chains);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
+                           const float *Mseg, const float *Rseg, cudaStream_t st) {
+    dim3 grid((unsigned)N, (unsigned)H, kD / 16);
+    kda_combine_kernel<<<grid, 256, 0, st>>>(status, chains, H, Sin, Mseg, Rseg);
     return cudaGetLastError();
 }
 
@@ -785,8 +964,8 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
     return cudaGetLastError();
 }
 
-cudaError_t launch_walk(int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N, int32_t H,
-                        const uint8_t *records, const float *S0, float *Sout, void *o, int o_f32, cudaStream_t st) {
+cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
+                        int32_t H, const uint8_t *records, void *o, int o_f32, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kda_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -794,10 +973,9 @@ cudaError_t launch_walk(int32_t *status, const int32_t *seq_cu, const int32_t *c
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    if (N <= 0) return cudaSuccess;
-    dim3 grid((unsigned)N, (unsigned)H);
-    kda_walk_kernel<<<grid, kWalkThreads, sizeof(WalkSmem), st>>>(status, seq_cu, chunk_off, H, records, S0, Sout,
-                                                                   o, o_f32);
+    if (max_units <= 0) return cudaSuccess;
+    dim3 grid((unsigned)max_units, (unsigned)H);
+    kda_walk_kernel<<<grid, kWalkThreads, sizeof(WalkSmem), st>>>(status, units, n_units, H, records, o, o_f32);
     return cudaGetLastError();
 }
 

@@ -170,3 +170,17 @@ def test_prefill_then_decode_equals_longer_prefill():
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"])
     assert_prefill_close(o_split.cpu(), state.cpu(), o_ref[0], S_ref, "prefill + decode vs oracle")
     assert_prefill_close(o_split.cpu(), state.cpu(), np64(o_long[0]), np64(S_long), "prefill + decode vs long")
+
+
+@pytest.mark.parametrize("lens,H", [([3000, 1700, 0, 900], 2), ([2000], 1)])
+def test_segmented_walk(lens, H):
+    """Few long sequences take the segmented walk: per-segment affine state maps from
+    walks started at zero and at the identity, chained per sequence, then every segment
+    walked again from its true input state. Ragged segment tails, an empty sequence and
+    a one-segment sequence included."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    inp = inputs.prefill_inputs(cu[-1], H, len(lens), seed=13, init_state=True)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu)
+    assert_prefill_close(o, S, o_ref, S_ref, "segmented %s" % lens)
