@@ -56,7 +56,7 @@ WsLayout ws_layout(int64_t total_tokens, int64_t N, int64_t H) {
     w.units = off;
     off += align_up((size_t)N * unit_bytes, 256);
     w.unitsA = off;
-    off += align_up((size_t)2 * w.seg_bound * unit_bytes, 256);
+    off += align_up((size_t)3 * w.seg_bound * unit_bytes, 256);  // 2 S - 3 per sequence, 1 if empty
     w.unitsC = off;
     off += align_up((size_t)w.seg_bound * unit_bytes, 256);
     w.chains = off;
@@ -193,7 +193,7 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
     if (kda::launch_segment_plan(status, seq_cu, chunk_off, num_seqs, num_heads, w.P, initial_state, final_state, sin,
                                  mseg, rseg, unitsA, counts + 1, unitsC, counts + 2, chains, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_walk(status, unitsA, counts + 1, 2 * w.seg_bound, num_heads, records, o, o_f32, st) !=
+    if (kda::launch_walk(status, unitsA, counts + 1, 3 * w.seg_bound, num_heads, records, o, o_f32, st) !=
         cudaSuccess)
         return KDA_ERR_CUDA;
     if (kda::launch_combine(status, chains, num_seqs, num_heads, sin, mseg, rseg, st) != cudaSuccess)

@@ -102,8 +102,8 @@ __host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t
     const int64_t slots = chunk_bound(total_tokens, num_seqs);
     const int64_t avg = slots / num_seqs;
     if (chains * 2 >= 152 || avg < 24) return 0;
-    // phase A runs 2 S - 3 walks per chain: aim for about one wave (10 % slack)
-    int64_t S = (167 / chains + 3) / 2;
+    // phase A runs 2 S - 3 walks per chain: at most one wave
+    int64_t S = (152 / chains + 3) / 2;
     if (S < 2) S = 2;
     int64_t P = (avg + S - 1) / S;
     if (P < 4) P = 4;

@@ -130,12 +130,13 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
 // ---------------------------------------------------------------------------------
 // segmented walk: tables of the three phases (one thread; used only when there are few
 // sequences). Segment g of the batch is segment sigma of sequence n, g = seg_base[n] + sigma.
-//   phase A  segment 0 from the initial state       -> Sin[g0 + 1]       (the next input)
+//   phase A  segment 0 from the initial state, writing o -> Sin[g0 + 1] (the next input,
+//            or the final state when the sequence has one segment)
 //            segment sigma (1 .. S-2) from zero     -> R[g],  with U'
 //            segment sigma (1 .. S-2) from identity -> M[g],  without U'
 //   phase B  Sin[g + 1] = M[g] Sin[g] + R[g]  for sigma = 1 .. S-2 (kda_combine_kernel)
-//   phase C  every segment from its input state (Sin[g], or the initial state for
-//            sigma = 0), writing o; the last one writes the final state
+//   phase C  segments 1 .. S-1 from their input states Sin[g], writing o; the last one
+//            writes the final state
 // ---------------------------------------------------------------------------------
 __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
                                         const int32_t *__restrict__ chunk_off, int32_t N, int32_t H, int32_t P,
@@ -162,7 +163,7 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
         return;
     }
     const size_t seg_stride = (size_t)H * kStateFloats;  // one segment's states for all heads
-    int32_t a = 0, g = 0;
+    int32_t a = 0, cc = 0, g = 0;
     for (int32_t n = 0; n < N; ++n) {
         const int32_t c0 = chunk_off[n], c1 = chunk_off[n + 1];
         const int32_t t0 = seq_cu[n], t1 = seq_cu[n + 1];
@@ -170,6 +171,16 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
         chains[2 * n] = g;
         chains[2 * n + 1] = S;
         const float *init = S0 ? S0 + (size_t)n * seg_stride : nullptr;
+        if (S == 0) {  // an empty sequence: its final state is its initial state
+            WalkUnit u;
+            u.in = init;
+            u.out = Sout + (size_t)n * seg_stride;
+            u.c_begin = u.c_end = c0;
+            u.t_begin = u.t_end = t0;
+            u.flags = 0;
+            u.pad = 0;
+            unitsA[a++] = u;
+        }
         for (int32_t sg = 0; sg < S; ++sg) {
             WalkUnit u;
             u.c_begin = c0 + sg * P;
@@ -177,18 +188,20 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
             u.t_begin = t0 + sg * P * kC;
             u.t_end = min(t1, t0 + (sg + 1) * P * kC);
             u.pad = 0;
+            if (sg == 0) {  // phase A, with outputs: the only walk of segment 0
+                u.in = init;
+                u.out = S == 1 ? Sout + (size_t)n * seg_stride : Sin + (size_t)(g + 1) * seg_stride;
+                u.flags = kUnitWriteO | kUnitAddUp;
+                unitsA[a++] = u;
+                continue;
+            }
             // phase C
-            u.in = sg == 0 ? init : Sin + (size_t)(g + sg) * seg_stride;
+            u.in = Sin + (size_t)(g + sg) * seg_stride;
             u.out = sg == S - 1 ? Sout + (size_t)n * seg_stride : nullptr;
             u.flags = kUnitWriteO | kUnitAddUp;
-            unitsC[g + sg] = u;
+            unitsC[cc++] = u;
             // phase A
-            if (S >= 2 && sg == 0) {
-                u.in = init;
-                u.out = Sin + (size_t)(g + 1) * seg_stride;
-                u.flags = kUnitAddUp;
-                unitsA[a++] = u;
-            } else if (sg >= 1 && sg <= S - 2) {
+            if (sg <= S - 2) {
                 u.in = nullptr;
                 u.out = Rseg + (size_t)(g + sg) * seg_stride;
                 u.flags = kUnitAddUp;
@@ -201,7 +214,7 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
         g += S;
     }
     *nA = a;
-    *nC = g;
+    *nC = cc;
 }
 
 // Phase B: Sin[g + 1] = M[g] Sin[g] + R[g] along each sequence's segments, in fp32 on the

@@ -172,7 +172,7 @@ def test_prefill_then_decode_equals_longer_prefill():
     assert_prefill_close(o_split.cpu(), state.cpu(), np64(o_long[0]), np64(S_long), "prefill + decode vs long")
 
 
-@pytest.mark.parametrize("lens,H", [([3000, 1700, 0, 900], 2), ([2000], 1)])
+@pytest.mark.parametrize("lens,H", [([4000, 2000, 0, 900], 2), ([2000], 1), ([1700, 3000], 3)])
 def test_segmented_walk(lens, H):
     """Few long sequences take the segmented walk: per-segment affine state maps from
     walks started at zero and at the identity, chained per sequence, then every segment
