@@ -270,7 +270,6 @@ struct IntraSmem {
     float G[kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay
     float beta[kC];
     float Akk[kC][kC + 1];
-    float Aqk[kC][kC + 1];
     float T[kC][kC + 1];
     float X[3][kTile][kTile + 1];  // off-diagonal block products of the solve
     __nv_bfloat16 qs[kC][kLd128];  // the chunk's q, k, v (rows past the sequence end are zero)
@@ -289,7 +288,7 @@ struct IntraSmem {
     } u;
 };
 
-constexpr int kIntraThreads = 256;
+constexpr int kIntraThreads = 512;
 
 __device__ __forceinline__ int find_seq(const int32_t *chunk_off, int32_t N, int32_t slot) {
     // largest n with chunk_off[n] <= slot (empty sequences share an offset and are skipped)
@@ -348,9 +347,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int i = tid - kD;
         s.beta[i] = (i < L) ? sigmoid_f(bgate[(t0 + i) * H + h]) : 0.f;
     }
-    for (int e = tid; e < kC * (kC + 1); e += kIntraThreads) {
-        (&s.Akk[0][0])[e] = 0.f;
-        (&s.Aqk[0][0])[e] = 0.f;
+    for (int e = tid; e < kC * (kC + 1); e += kIntraThreads) (&s.Akk[0][0])[e] = 0.f;
+    // A_qk goes to the record straight from the MMA fragments; the blocks above the
+    // diagonal stay zero (ordered before those stores by the barriers in between)
+    for (int e = tid; e < (int)(2 * kPlaneCC / 16); e += kIntraThreads) {  // the hi and the lo plane
+        const int plane = e / (int)(kPlaneCC / 16), off = e % (int)(kPlaneCC / 16);
+        *reinterpret_cast<uint4 *>(rec + kRecAqk + plane * kStackAK + (size_t)off * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     cp_async_wait<0>();
     __syncthreads();
@@ -363,19 +365,22 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             s.G[i][c] = (i < L) ? gate_log_decay(eA, s.G[i][c]) : 0.f;
         }
         __syncthreads();
-        // column scan: thread (c, half) sums 32 rows, then the upper half adds the lower total
-        const int c = tid % kD, half = tid / kD;
+        // column scan: thread (c, quarter) sums its 16 rows, then adds the totals of the
+        // quarters below it
+        const int c = tid % kD, qt = tid / kD;
         float acc = 0.f;
-#pragma unroll 8
-        for (int i = half * 32; i < half * 32 + 32; ++i) {
+#pragma unroll
+        for (int i = qt * 16; i < qt * 16 + 16; ++i) {
             acc += s.G[i][c];
             s.G[i][c] = acc;
         }
         __syncthreads();
-        if (half == 1) {
-            const float lower = s.G[31][c];
-#pragma unroll 8
-            for (int i = 32; i < kC; ++i) s.G[i][c] += lower;
+        float below = 0.f;
+        for (int p = 0; p < qt; ++p) below += s.G[p * 16 + 15][c];
+        __syncthreads();
+        if (qt > 0) {
+#pragma unroll
+            for (int i = qt * 16; i < qt * 16 + 16; ++i) s.G[i][c] += below;
         }
         __syncthreads();
     }
@@ -434,14 +439,22 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[e] = a0[e] + (a1[e] + a2[e]);
             const int g = lane >> 2, t4 = lane & 3;
+            if (mat == 0) {  // A_qk (diagonal included), split, into the record
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = r + g + ((e >> 1) << 3);
-                const int j = nt * 8 + 2 * t4 + (e & 1);
-                if (mat == 0)
-                    s.Aqk[i][j] = (j <= i) ? acc[e] : 0.f;
-                else
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int i = r + g + hr * 8, j = nt * 8 + 2 * t4;
+                    uint32_t hi, lo;
+                    split_bf16x2(j <= i ? acc[2 * hr] : 0.f, j + 1 <= i ? acc[2 * hr + 1] : 0.f, hi, lo);
+                    *reinterpret_cast<uint32_t *>(rec + kRecAqk + il_off(i, j, kC)) = hi;
+                    *reinterpret_cast<uint32_t *>(rec + kRecAqk + kStackAK + il_off(i, j, kC)) = lo;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = r + g + ((e >> 1) << 3);
+                    const int j = nt * 8 + 2 * t4 + (e & 1);
                     s.Akk[i][j] = (j < i) ? s.beta[i] * acc[e] : 0.f;
+                }
             }
         }
         __syncthreads();
@@ -515,21 +528,24 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     __syncthreads();
 
     // ---- W = T' Khat (split x split), U' = T' V (split x exact bf16) ------------
-    // warp w owns output columns 16w .. 16w+15 (two n8 tiles) for all 64 rows
+    // warp w owns output columns 16 (w % 8) .. +15; the two halves of the warps split the
+    // 16-row tiles of the triangle evenly: rows {0, 3} and {1, 2} (k-steps 0..a each)
     {
-        float accW[4][2][4], accU[4][2][4];
+        float accW[2][2][4], accU[2][2][4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int ai = 0; ai < 2; ++ai)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    accW[a][nt][e] = 0.f;
-                    accU[a][nt][e] = 0.f;
+                    accW[ai][nt][e] = 0.f;
+                    accU[ai][nt][e] = 0.f;
                 }
-        const int n0 = warp * 16;
+        const int n0 = (warp & 7) * 16;
+        const int half = warp >> 3;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int ai = 0; ai < 2; ++ai) {
+            const int a = half == 0 ? (ai == 0 ? 0 : 3) : (ai == 0 ? 1 : 2);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 if (ks > a) break;  // T' is lower triangular
@@ -541,9 +557,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 load_b_kn(vb, &s.vs[0][0], kLd128, ks * 16, n0, lane);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    mma_split3(accW[a][nt], th, tl, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
-                    mma_bf16(accU[a][nt], tl, vb[2 * nt], vb[2 * nt + 1]);
-                    mma_bf16(accU[a][nt], th, vb[2 * nt], vb[2 * nt + 1]);
+                    mma_split3(accW[ai][nt], th, tl, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
+                    mma_bf16(accU[ai][nt], tl, vb[2 * nt], vb[2 * nt + 1]);
+                    mma_bf16(accU[ai][nt], th, vb[2 * nt], vb[2 * nt + 1]);
                 }
             }
         }
@@ -552,7 +568,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         float *Up = reinterpret_cast<float *>(rec + kRecUp);
         const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int ai = 0; ai < 2; ++ai) {
+            const int a = half == 0 ? (ai == 0 ? 0 : 3) : (ai == 0 ? 1 : 2);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -560,12 +577,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                     const int i = a * 16 + g + hr * 8;
                     const int c = n0 + nt * 8 + 2 * t4;
                     uint32_t hi, lo;
-                    split_bf16x2(-accW[a][nt][2 * hr], -accW[a][nt][2 * hr + 1], hi, lo);
+                    split_bf16x2(-accW[ai][nt][2 * hr], -accW[ai][nt][2 * hr + 1], hi, lo);
                     *reinterpret_cast<uint32_t *>(Wn + il_off(i, c, kD)) = hi;
                     *reinterpret_cast<uint32_t *>(Wn + kStackWQ + il_off(i, c, kD)) = lo;
                     *reinterpret_cast<float2 *>(Up + (size_t)i * kD + c) =
-                        make_float2(accU[a][nt][2 * hr], accU[a][nt][2 * hr + 1]);
+                        make_float2(accU[ai][nt][2 * hr], accU[ai][nt][2 * hr + 1]);
                 }
+        }
     }
 
     // ---- Qhat, Kend^T, A_qk, gamma (elementwise) --------------------------------
@@ -589,14 +607,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             split_bf16x2(k0 * __expf(gl - s.G[j][c]), k1 * __expf(gl - s.G[j + 1][c]), hi, lo);
             *reinterpret_cast<uint32_t *>(KeT + il_off(c, j, kC)) = hi;
             *reinterpret_cast<uint32_t *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
-        }
-        uint8_t *Aq = rec + kRecAqk;
-        for (int e = tid; e < kC * (kC / 2); e += kIntraThreads) {
-            const int i = e / (kC / 2), j = (e % (kC / 2)) * 2;
-            uint32_t hi, lo;
-            split_bf16x2(s.Aqk[i][j], s.Aqk[i][j + 1], hi, lo);
-            *reinterpret_cast<uint32_t *>(Aq + il_off(i, j, kC)) = hi;
-            *reinterpret_cast<uint32_t *>(Aq + kStackAK + il_off(i, j, kC)) = lo;
         }
         float *gam = reinterpret_cast<float *>(rec + kRecGam);
         if (tid < kD) gam[tid] = expf(s.G[kC - 1][tid]);
