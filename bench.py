@@ -341,6 +341,8 @@ def main_reference(args, rank, world):
 
 
 def main_ours(args, rank, world, local):
+    from linear_attention_serving_02_gb300 import kda
+
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     pre_cpu, pre, state, dec = make_workload(rank)
 
@@ -406,7 +408,7 @@ def main_ours(args, rank, world, local):
         "roofline": dominant,
         "cpu_baseline": cpu,
         "e2e": {"value": units / e2e_t, "unit": "token·head/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * K,
+        "gpu_launches": K * (kda.kda_chunk_prefill_launch_count(PREFILL_T, 1, PREFILL_H) + 1),
         "clocks": clk,
         "outputs_finite": finite,
         "timed_wall_s": wall,

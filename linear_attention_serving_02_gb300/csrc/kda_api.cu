@@ -127,6 +127,12 @@ size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, 
     return ws_layout(total_tokens, num_seqs, num_heads).total;
 }
 
+int32_t kda_chunk_prefill_launch_count(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
+    if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return -1;
+    if (num_seqs == 0) return 0;
+    return kda::walk_segment_chunks(total_tokens, num_seqs, num_heads) ? 6 : 3;
+}
+
 int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
                       const float *b, const float *initial_state, const int32_t *cu_seqlens,
                       const int32_t *cu_seqlens_host, int32_t batch, int64_t seq_len, int32_t num_seqs,

@@ -38,6 +38,8 @@ def library():
         lib.kda_version.restype = ctypes.c_int
         lib.kda_chunk_prefill_workspace_size.argtypes = [i64, i32, i32]
         lib.kda_chunk_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.kda_chunk_prefill_launch_count.argtypes = [i64, i32, i32]
+        lib.kda_chunk_prefill_launch_count.restype = i32
         lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                           i32, i64, i32, i32, i32, i32,
                                           vp, i32, vp, vp, ctypes.c_size_t, vp]
@@ -81,6 +83,11 @@ def _need(t, name, dtype, cuda=True):
 
 def kda_chunk_prefill_workspace_size(total_tokens, num_seqs, num_heads):
     return int(library().kda_chunk_prefill_workspace_size(int(total_tokens), int(num_seqs), int(num_heads)))
+
+
+def kda_chunk_prefill_launch_count(total_tokens, num_seqs, num_heads):
+    """Kernels one kda_chunk_prefill call with these sizes launches (3, or 6 for a segmented walk)."""
+    return int(library().kda_chunk_prefill_launch_count(int(total_tokens), int(num_seqs), int(num_heads)))
 
 
 def kda_chunk_prefill(q, k, v, z, A, b, initial_state=None, cu_seqlens=None, cu_seqlens_host=None,

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_chunk_prefill_workspace_size",
-                     "kda_status_string", "kda_workspace_status", "kda_version"):
+                     "kda_status_string", "kda_workspace_status", "kda_version",
+                     "kda_chunk_prefill_launch_count"):
         assert required in names
 
 
@@ -59,6 +60,19 @@ def test_workspace_size():
     assert ws(8192, 1, 24) > a
     # one more sequence can add a partial chunk per head
     assert ws(8192, 2, 12) > a
+
+
+def test_launch_count():
+    lc = kda.kda_chunk_prefill_launch_count
+    assert lc(-1, 1, 1) == -1
+    assert lc(0, 0, 4) == 0
+    # many (sequence, head) chains fill the GPU: one walk pass
+    assert lc(8192 * 64, 64, 32) == 3
+    # short chains are not worth splitting
+    assert lc(256, 1, 2) == 3
+    # one long sequence over few heads: segmented walk
+    assert lc(8192, 1, 12) == 6
+    assert lc(1 << 20, 1, 12) == 6
 
 
 def _prefill(**over):
