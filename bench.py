@@ -266,6 +266,78 @@ def run_ours_e2e(pre_cpu, dec, steps, warmup, world):
     return ms, h2d, d2h
 
 
+SPEC_M = 8  # tokens per verified draft window: the last accepted token + 7 drafts
+# algorithmic bytes: verify reads the state once and, per token, q, k, v, z, b and writes
+# o and the gate log (gk fp32, beta); fold reads and writes the state of every (sequence,
+# head) with at least one accepted token and reads k, v, gk, beta of the accepted tokens
+VERIFY_BYTES_PER_TOKEN = 3 * 2 * D + 4 * D + 4 + 4 * D + 4 * D + 4     # 2312
+FOLD_BYTES_PER_TOKEN = 2 * 2 * D + 4 * D + 4                           # 1028
+
+
+def run_speculative(steps, warmup, world, seed):
+    """Speculative decoding on the decode workload's shape (256 sequences x 96 heads):
+    verify of an SPEC_M-token window from the checkpoint, then the ReplaySSM fold of the
+    accepted prefixes, whose lengths are drawn uniformly from 1..SPEC_M (mean 4.5; the
+    pages report 2.6-4.7 accepted tokens per step)."""
+    from linear_attention_serving_02_gb300 import kda
+
+    N, H, m = DECODE_N, DECODE_H, SPEC_M
+    wins = []
+    for w in range(2):
+        steps_in = [inputs.decode_step_inputs(N, H, seed=seed + 50 + w, step=t, device="cuda") for t in range(m)]
+        win = {}
+        for key in ("q", "k", "v", "z", "b"):
+            x = torch.stack([st[key] for st in steps_in], dim=1)
+            win[key] = x.reshape((N * m,) + tuple(x.shape[2:])).contiguous()
+        win["A"] = steps_in[0]["A"]
+        wins.append(win)
+    state = inputs.decode_state(N, H, seed=seed + 60, device="cuda")
+    g = torch.Generator().manual_seed(seed + 61)
+    acc = torch.randint(1, m + 1, (N,), generator=g, dtype=torch.int32)
+    acc_mean = float(acc.float().mean())
+    acc = acc.cuda()
+    o = torch.empty((N * m, H, D), dtype=torch.float32, device="cuda")
+    gk = torch.empty((N * m, H, D), dtype=torch.float32, device="cuda")
+    beta = torch.empty((N * m, H), dtype=torch.float32, device="cuda")
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+
+    def one(i, ev=None):
+        w = wins[i % 2]
+        if ev:
+            ev[0].record(stream)
+        kda.kda_recurrent_verify(w["q"], w["k"], w["v"], w["z"], w["A"], w["b"], state, m, o=o, gk_log=gk,
+                                 beta_log=beta)
+        if ev:
+            ev[1].record(stream)
+        kda.kda_replay_fold(w["k"], w["v"], gk, beta, acc, state, m)
+        if ev:
+            ev[2].record(stream)
+
+    for i in range(warmup):
+        flush()
+        one(i)
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush()
+        one(warmup + j, evs[j])
+    torch.cuda.synchronize()
+    barrier(world)
+    ver = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b, _ in evs) * 1e-3, world)
+    fol = max_over_ranks(statistics.mean(b.elapsed_time(c) for _, b, c in evs) * 1e-3, world)
+    pairs = N * H
+    ver_bytes = pairs * (4 * D * D + m * VERIFY_BYTES_PER_TOKEN)
+    fold_bytes = pairs * (2 * 4 * D * D + acc_mean * FOLD_BYTES_PER_TOKEN) + 4 * N
+    return {"window": m, "accepted_mean": acc_mean, "sequences": N, "heads": H,
+            "verify": {"ms": 1e3 * ver, "token_heads_per_s": world * pairs * m / ver,
+                       "bytes_per_launch": ver_bytes, "achieved_gbs": ver_bytes / ver / 1e9},
+            "fold": {"ms": 1e3 * fol, "bytes_per_launch": fold_bytes, "achieved_gbs": fold_bytes / fol / 1e9},
+            "accepted_token_heads_per_s": world * pairs * acc_mean / (ver + fol),
+            "finite": bool(torch.isfinite(state).all() and torch.isfinite(o).all())}
+
+
 # ------------------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ------------------------------------------------------------------------------------
@@ -355,6 +427,9 @@ def main_ours(args, rank, world, local):
     clk = clocks.stop() if clocks else None
 
     e2e_ms, h2d, d2h = run_ours_e2e(pre_cpu, dec, args.steps, args.warmup, world)
+    spec = run_speculative(max(1, min(args.steps, 50)), args.warmup, world, seed=1000 * rank)
+    for part in ("verify", "fold"):
+        spec[part]["frac_of_hbm"] = spec[part]["achieved_gbs"] / hbm
 
     pre_t = max_over_ranks(sum(pre_ms) / 1e3, world)
     dec_t = max_over_ranks(sum(dec_ms) / 1e3, world)
@@ -376,7 +451,7 @@ def main_ours(args, rank, world, local):
     roof_dec = {"kernel": "kda_decode_kernel<128>", "bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": dec_gbs / hbm, "peak_kind": peak_kind + " (burst copy)",
                 "traffic": dec_traffic, "algorithmic_bytes_per_launch": DECODE_BYTES_PER_TH * th_dec}
-    roof_pre = {"kernel": "kda_chunk_prefill (plan + intra + inter)", "bound": "hbm", "achieved": pre_gbs,
+    roof_pre = {"kernel": "kda_chunk_prefill (all its kernels)", "bound": "hbm", "achieved": pre_gbs,
                 "peak": hbm, "unit": "GB/s", "frac": pre_gbs / hbm, "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TH * th_pre,
                 "mma_tflops": pre_tflops, "mma_frac_of_bf16": pre_tflops / tf_burst, "traffic": None}
@@ -405,6 +480,7 @@ def main_ours(args, rank, world, local):
                     "tokens_per_s": world * K * PREFILL_T / pre_t, "ms": 1e3 * pre_launch, "roofline": roof_pre},
         "decode": {"value": world * K * DECODE_N / dec_t, "unit": "token/s (one per sequence)",
                    "token_heads_per_s": world * K * th_dec / dec_t, "ms": 1e3 * dec_launch, "roofline": roof_dec},
+        "speculative": spec,
         "roofline": dominant,
         "cpu_baseline": cpu,
         "e2e": {"value": units / e2e_t, "unit": "token·head/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

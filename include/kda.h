@@ -197,6 +197,70 @@ int kda_recurrent_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
                          void *stream);
 
+/* Most draft tokens one kda_recurrent_verify() or kda_replay_fold() call takes. */
+#define KDA_MAX_REPLAY_TOKENS 16
+
+/*
+ * kda_recurrent_verify - several tokens per sequence from a checkpoint state, with the
+ * gate values logged for a later replay (ReplaySSM, 'Kimi K3 attention deep dive', §6.2).
+ *
+ * For every sequence n and head h, starting from S = state[n, h], the decode update of
+ * kda_recurrent_decode() is applied to the m tokens of the sequence in order, and each
+ * token's output o = S^T q (after its own write) is written. The checkpoint `state` is
+ * only read. With state_out = state this is multi-token decode in place.
+ *
+ * Token t of sequence n is row n * m + t of the token-major inputs (m = num_tokens):
+ *   q, k, v   device bf16 [N * m, H, 128]
+ *   z         device fp32 [N * m, H, 128]
+ *   A         device fp32 [H]
+ *   b         device fp32 [N * m, H]
+ *   state     device fp32 [N, H, 128, 128], read only
+ *   state_out device fp32 [N, H, 128, 128] or NULL: the state after all m tokens
+ *             (may be `state` itself)
+ *   o         device fp32 [N * m, H, 128] (written)
+ *   gk_log    device fp32 [N * m, H, 128] or NULL: each token's log a = -5 sigmoid(e^A z)
+ *   beta_log  device fp32 [N * m, H] or NULL: each token's beta = sigmoid(b)
+ *   num_tokens 0 .. KDA_MAX_REPLAY_TOKENS (larger: KDA_ERR_UNSUPPORTED)
+ *
+ * The per-element arithmetic, the column split and the order of the reductions are
+ * those of kda_recurrent_decode() for the same num_seqs and num_heads, so o of token t
+ * equals, bit for bit, the output of the (t+1)-th of m kda_recurrent_decode() calls on
+ * a copy of the checkpoint, and state_out equals the state after the m-th call. That
+ * (the ReplaySSM requirement) holds on one device for one (num_seqs, num_heads).
+ * Pointers need 16-byte alignment (A, b, beta_log: 4). Stream-ordered, asynchronous.
+ */
+int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const float *z, const float *A, const float *b,
+                         const float *state, float *state_out, float *o,
+                         float *gk_log, float *beta_log,
+                         int32_t num_seqs, int32_t num_heads, int32_t num_tokens,
+                         int32_t d_k, int32_t d_v, void *stream);
+
+/*
+ * kda_replay_fold - commit the accepted prefix of a verified draft window to the state.
+ *
+ * For every sequence n, the first a_n = clamp(num_accepted[n], 0, m) tokens of the
+ * window are replayed, in order, on state[n, :] in place, from the caller's k, v and
+ * the gate values that kda_recurrent_verify() logged (the fused fold of 'Kimi K3
+ * attention deep dive', §6.2). The state must be the checkpoint the window was verified
+ * from. No output is produced, and a sequence with a_n = 0 is not touched.
+ *
+ *   k, v          device bf16 [N * m, H, 128], the window's tokens as given to verify
+ *   gk_log        device fp32 [N * m, H, 128] from kda_recurrent_verify()
+ *   beta_log      device fp32 [N * m, H]      from kda_recurrent_verify()
+ *   num_accepted  device int32 [N]
+ *   state         device fp32 [N, H, 128, 128], updated in place
+ *   num_tokens    the window length m, 0 .. KDA_MAX_REPLAY_TOKENS
+ *
+ * The result equals, bit for bit, a_n kda_recurrent_decode() calls with the same
+ * (num_seqs, num_heads) on that sequence's tokens. Alignment: 16 bytes (beta_log and
+ * num_accepted: 4).
+ */
+int kda_replay_fold(const uint16_t *k, const uint16_t *v, const float *gk_log, const float *beta_log,
+                    const int32_t *num_accepted, float *state,
+                    int32_t num_seqs, int32_t num_heads, int32_t num_tokens,
+                    int32_t d_k, int32_t d_v, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

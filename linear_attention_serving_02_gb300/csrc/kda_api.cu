@@ -27,6 +27,13 @@ cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                           const float *A, const float *b, float *state, float *o, int32_t N, int32_t H,
                           int num_sms, cudaStream_t st);
+cudaError_t launch_verify(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
+                          const float *A, const float *b, const float *state, float *state_out, float *o,
+                          float *gk_log, float *beta_log, int32_t N, int32_t H, int32_t m, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_fold(const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *gk_log, const float *beta_log,
+                        const int32_t *accepted, float *state, int32_t N, int32_t H, int32_t m, int num_sms,
+                        cudaStream_t st);
 size_t intra_smem_bytes();
 }  // namespace kda
 
@@ -235,6 +242,51 @@ int kda_recurrent_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v
     if (kda::launch_decode(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k),
                            reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, state, o, num_seqs, num_heads,
                            dev.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
+                         const float *b, const float *state, float *state_out, float *o, float *gk_log,
+                         float *beta_log, int32_t num_seqs, int32_t num_heads, int32_t num_tokens, int32_t d_k,
+                         int32_t d_v, void *stream) {
+    if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_heads <= 0 || num_tokens < 0) return KDA_ERR_SHAPE;
+    if (num_tokens > KDA_MAX_REPLAY_TOKENS) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_tokens == 0) return KDA_OK;
+    if (!q || !k || !v || !z || !A || !b || !state || !o) return KDA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) || !aligned(state, 16) ||
+        !aligned(state_out, 16) || !aligned(o, 16) || !aligned(gk_log, 16) || !aligned(A, 4) || !aligned(b, 4) ||
+        !aligned(beta_log, 4))
+        return KDA_ERR_ALIGN;
+    DeviceInfo dev;
+    int rc = device_info(dev);
+    if (rc != KDA_OK) return rc;
+    if (kda::launch_verify(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k),
+                           reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, state, state_out, o, gk_log, beta_log,
+                           num_seqs, num_heads, num_tokens, dev.sms, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+int kda_replay_fold(const uint16_t *k, const uint16_t *v, const float *gk_log, const float *beta_log,
+                    const int32_t *num_accepted, float *state, int32_t num_seqs, int32_t num_heads,
+                    int32_t num_tokens, int32_t d_k, int32_t d_v, void *stream) {
+    if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_heads <= 0 || num_tokens < 0) return KDA_ERR_SHAPE;
+    if (num_tokens > KDA_MAX_REPLAY_TOKENS) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_tokens == 0) return KDA_OK;
+    if (!k || !v || !gk_log || !beta_log || !num_accepted || !state) return KDA_ERR_NULL;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(gk_log, 16) || !aligned(state, 16) || !aligned(beta_log, 4) ||
+        !aligned(num_accepted, 4))
+        return KDA_ERR_ALIGN;
+    DeviceInfo dev;
+    int rc = device_info(dev);
+    if (rc != KDA_OK) return rc;
+    if (kda::launch_fold(reinterpret_cast<const __nv_bfloat16 *>(k), reinterpret_cast<const __nv_bfloat16 *>(v),
+                         gk_log, beta_log, num_accepted, state, num_seqs, num_heads, num_tokens, dev.sms,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
 }

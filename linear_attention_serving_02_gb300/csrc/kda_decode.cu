@@ -1,4 +1,6 @@
-// KDA recurrent decode: one token per (sequence, head), the state updated in place.
+// KDA recurrent decode: one token per (sequence, head), the state updated in place; and
+// its speculative-decoding pair, verify (several draft tokens from a checkpoint) and
+// fold (replay of the accepted prefix).
 //
 // The three-step diagonal-plus-low-rank update of 'Kimi K3 attention deep dive'
 // (forceinjection.github.io), §2.2, in the error form of 'Kimi K3' (llm.rainlin.net),
@@ -8,19 +10,79 @@
 //   S  = S' + beta k (v - p)^T
 //   o  = S^T q
 // No d_k x d_k matrix is formed. The work is a read-modify-write of the 64 KB fp32
-// state per (sequence, head): memory bound, so the kernel streams S once with 128-bit
+// state per (sequence, head): memory bound, so the kernels stream S once with 128-bit
 // coalesced loads and stores (evict-first: the state is not reused before it leaves
-// L2) and keeps it in registers between the two reductions over key channels.
+// L2) and keep it in registers between the reductions over key channels.
 //
 // Thread layout: a CTA of 256 threads covers a slice of CWD value columns. Each thread
 // owns 4 consecutive columns (one float4) of RPT key rows; the rows of the 256 threads
 // interleave so that every warp-wide access is one contiguous run of a row.
+//
+// ReplaySSM ('Kimi K3 attention deep dive', §6.2): instead of a 64 KB state snapshot per
+// draft token, the verify kernel logs each token's gate values (log a, beta) next to the
+// caller's k and v, about 1 KB per token and head; once the sampler has accepted a prefix,
+// the fold kernel replays just that prefix on the checkpoint. The three kernels share
+// the per-element arithmetic below, written with explicitly rounded intrinsics, the same
+// column slice for the same (sequence, head) count, and the same reduction order, so a
+// fold of a tokens leaves exactly the bits that a calls of the decode kernel leave, and
+// verify's outputs are exactly the decode kernel's.
 
+#include "kda.h"
 #include "kda_common.cuh"
 
 namespace kda {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kMaxReplay = KDA_MAX_REPLAY_TOKENS;  // draft tokens per verify / fold call
+
+template <int CWD>
+struct DecodeGeom {
+    static constexpr int LPR = CWD / 4;              // threads per row (one float4 each)
+    static constexpr int RG = kDecodeThreads / LPR;  // row groups
+    static constexpr int RPT = kD / RG;              // rows per thread
+    static_assert(RG * LPR == kDecodeThreads && RPT * RG == kD, "decode layout");
+};
+
+// ---- the per-element arithmetic every kernel here shares ----
+
+// S' = a S on one row of this thread, and its term of the projection p += k_r S'_r
+__device__ __forceinline__ void decay_project(float4 &s, float a, float kr, float4 &p) {
+    s.x = __fmul_rn(s.x, a); s.y = __fmul_rn(s.y, a); s.z = __fmul_rn(s.z, a); s.w = __fmul_rn(s.w, a);
+    p.x = __fmaf_rn(kr, s.x, p.x); p.y = __fmaf_rn(kr, s.y, p.y);
+    p.z = __fmaf_rn(kr, s.z, p.z); p.w = __fmaf_rn(kr, s.w, p.w);
+}
+// e = beta (v - p)
+__device__ __forceinline__ float4 delta_error(float beta, float4 v, float4 p) {
+    return make_float4(__fmul_rn(beta, __fsub_rn(v.x, p.x)), __fmul_rn(beta, __fsub_rn(v.y, p.y)),
+                       __fmul_rn(beta, __fsub_rn(v.z, p.z)), __fmul_rn(beta, __fsub_rn(v.w, p.w)));
+}
+// S = S' + k_r e on one row
+__device__ __forceinline__ void rank1(float4 &s, float kr, float4 e) {
+    s.x = __fmaf_rn(kr, e.x, s.x); s.y = __fmaf_rn(kr, e.y, s.y);
+    s.z = __fmaf_rn(kr, e.z, s.z); s.w = __fmaf_rn(kr, e.w, s.w);
+}
+// o += q_r S_r
+__device__ __forceinline__ void readout(const float4 &s, float qr, float4 &o) {
+    o.x = __fmaf_rn(qr, s.x, o.x); o.y = __fmaf_rn(qr, s.y, o.y);
+    o.z = __fmaf_rn(qr, s.z, o.z); o.w = __fmaf_rn(qr, s.w, o.w);
+}
+// sum of the RG row-group partials of this thread's four columns, in row-group order
+template <int CWD>
+__device__ __forceinline__ float4 sum_partials(const float (*red)[CWD], int cq) {
+    constexpr int RG = DecodeGeom<CWD>::RG;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int r = 0; r < RG; ++r) {
+        const float4 x = *reinterpret_cast<const float4 *>(&red[r][4 * cq]);
+        acc.x = __fadd_rn(acc.x, x.x); acc.y = __fadd_rn(acc.y, x.y);
+        acc.z = __fadd_rn(acc.z, x.z); acc.w = __fadd_rn(acc.w, x.w);
+    }
+    return acc;
+}
+// the gate of one key channel, as every kernel here computes it
+__device__ __forceinline__ float decode_log_decay(const float *A, int h, float z) {
+    return gate_log_decay(expf(A[h]), z);
+}
 
 // Three CTAs per SM (registers capped accordingly, a few spilled): each CTA has its
 // 64 KB of state in flight, and the third CTA keeps loads outstanding while the others
@@ -30,10 +92,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     kda_decode_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                       const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
                       const float *__restrict__ bgate, float *__restrict__ state, float *__restrict__ o, int32_t H) {
-    constexpr int LPR = CWD / 4;             // threads per row (one float4 each)
-    constexpr int RG = kDecodeThreads / LPR; // row groups
-    constexpr int RPT = kD / RG;             // rows per thread
-    static_assert(RG * LPR == kDecodeThreads && RPT * RG == kD, "decode layout");
+    using G = DecodeGeom<CWD>;
+    constexpr int LPR = G::LPR, RG = G::RG, RPT = G::RPT;
 
     __shared__ float s_alpha[kD], s_k[kD], s_q[kD];
     __shared__ __align__(16) float s_red[RG][CWD];
@@ -52,8 +112,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
 
     if (tid < kD) {
-        const float eA = expf(A[h]);
-        s_alpha[tid] = expf(gate_log_decay(eA, z[nh * kD + tid]));
+        s_alpha[tid] = expf(decode_log_decay(A, h, z[nh * kD + tid]));
         s_k[tid] = __bfloat162float(k[nh * kD + tid]);
         s_q[tid] = __bfloat162float(q[nh * kD + tid]);
     } else if (tid == kD) {
@@ -68,59 +127,225 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int row = rg + i * RG;
-        const float a = s_alpha[row], kr = s_k[row];
-        sv[i].x *= a; sv[i].y *= a; sv[i].z *= a; sv[i].w *= a;
-        p.x += kr * sv[i].x; p.y += kr * sv[i].y; p.z += kr * sv[i].z; p.w += kr * sv[i].w;
+        decay_project(sv[i], s_alpha[row], s_k[row], p);
     }
     *reinterpret_cast<float4 *>(&s_red[rg][4 * cq]) = p;
     __syncthreads();
-    float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int r = 0; r < RG; ++r) {
-        const float4 x = *reinterpret_cast<const float4 *>(&s_red[r][4 * cq]);
-        P.x += x.x; P.y += x.y; P.z += x.z; P.w += x.w;
-    }
+    const float4 P = sum_partials<CWD>(s_red, cq);
     __syncthreads();  // s_red is reused below
 
     // S = S' + beta k (v - p)^T, then o = S^T q
-    const float beta = s_beta;
-    const float4 e = make_float4(beta * (v01.x - P.x), beta * (v01.y - P.y), beta * (v23.x - P.z),
-                                 beta * (v23.y - P.w));
+    const float4 e = delta_error(s_beta, make_float4(v01.x, v01.y, v23.x, v23.y), P);
     float4 oq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int row = rg + i * RG;
-        const float kr = s_k[row], qr = s_q[row];
-        sv[i].x += kr * e.x; sv[i].y += kr * e.y; sv[i].z += kr * e.z; sv[i].w += kr * e.w;
+        rank1(sv[i], s_k[row], e);
         __stcs(reinterpret_cast<float4 *>(S + row * kD + col), sv[i]);
-        oq.x += qr * sv[i].x; oq.y += qr * sv[i].y; oq.z += qr * sv[i].z; oq.w += qr * sv[i].w;
+        readout(sv[i], s_q[row], oq);
     }
     *reinterpret_cast<float4 *>(&s_red[rg][4 * cq]) = oq;
     __syncthreads();
-    if (rg == 0) {
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int r = 0; r < RG; ++r) {
-            const float4 x = *reinterpret_cast<const float4 *>(&s_red[r][4 * cq]);
-            O.x += x.x; O.y += x.y; O.z += x.z; O.w += x.w;
-        }
-        *reinterpret_cast<float4 *>(o + nh * kD + col) = O;
+    if (rg == 0) *reinterpret_cast<float4 *>(o + nh * kD + col) = sum_partials<CWD>(s_red, cq);
+}
+
+// Verify: m draft tokens of every (sequence, head) from the checkpoint state, which is
+// only read. Token t of sequence n sits at row n * m + t of the [N * m, H, ...] inputs.
+// Writes every token's output, and, when the pointers are given, the token's gate
+// values (the ReplaySSM log) and the state after all m tokens (state_out may be the
+// checkpoint itself: each CTA reads its whole slice before it writes any of it).
+template <int CWD>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+    kda_verify_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
+                      const float *__restrict__ bgate, const float *state, float *state_out, float *__restrict__ o,
+                      float *__restrict__ gk_log, float *__restrict__ beta_log, int32_t H, int32_t m) {
+    using G = DecodeGeom<CWD>;
+    constexpr int LPR = G::LPR, RG = G::RG, RPT = G::RPT;
+
+    // v stays bf16 in shared memory (each thread converts only its own four columns),
+    // which keeps the static total under 48 KB
+    __shared__ float s_alpha[kMaxReplay][kD], s_k[kMaxReplay][kD], s_q[kMaxReplay][kD];
+    __shared__ __align__(16) __nv_bfloat16 s_v[kMaxReplay][kD];
+    __shared__ float s_beta[kMaxReplay];
+    __shared__ __align__(16) float s_redp[2][RG][CWD];
+    __shared__ __align__(16) float s_redo[2][RG][CWD];
+
+    const int tid = threadIdx.x;
+    const int64_t nh = blockIdx.x;
+    const int64_t n = nh / H;
+    const int h = (int)(nh % H);
+    const int cq = tid % LPR, rg = tid / LPR;
+    const int col = blockIdx.y * CWD + 4 * cq;
+    const float *S = state + nh * (kD * kD);
+
+    float4 sv[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+
+    // stage every token's gate, k, q, v (and write the log while at it)
+    for (int idx = tid; idx < m * kD; idx += kDecodeThreads) {
+        const int t = idx / kD, c = idx % kD;
+        const int64_t row = ((n * m + t) * H + h) * kD + c;
+        const float la = decode_log_decay(A, h, z[row]);
+        s_alpha[t][c] = expf(la);
+        s_k[t][c] = __bfloat162float(k[row]);
+        s_q[t][c] = __bfloat162float(q[row]);
+        s_v[t][c] = v[row];
+        if (gk_log) gk_log[row] = la;
     }
+    if (tid < m) {
+        const int64_t tok = (n * m + tid) * H + h;
+        const float beta = sigmoid_f(bgate[tok]);
+        s_beta[tid] = beta;
+        if (beta_log) beta_log[tok] = beta;
+    }
+    __syncthreads();
+
+    // One barrier per token: partials alternate between two buffers, and the output of
+    // token t is summed after the barrier of token t + 1.
+    for (int t = 0; t < m; ++t) {
+        float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int row = rg + i * RG;
+            decay_project(sv[i], s_alpha[t][row], s_k[t][row], p);
+        }
+        *reinterpret_cast<float4 *>(&s_redp[t & 1][rg][4 * cq]) = p;
+        __syncthreads();
+        if (t > 0 && rg == 0)
+            *reinterpret_cast<float4 *>(o + ((n * m + t - 1) * H + h) * kD + col) =
+                sum_partials<CWD>(s_redo[(t - 1) & 1], cq);
+        const float4 P = sum_partials<CWD>(s_redp[t & 1], cq);
+        const uint2 vraw = *reinterpret_cast<const uint2 *>(&s_v[t][col]);
+        const float2 v01 = bf16x2_to_float2(vraw.x), v23 = bf16x2_to_float2(vraw.y);
+        const float4 e = delta_error(s_beta[t], make_float4(v01.x, v01.y, v23.x, v23.y), P);
+        float4 oq = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int row = rg + i * RG;
+            rank1(sv[i], s_k[t][row], e);
+            readout(sv[i], s_q[t][row], oq);
+        }
+        *reinterpret_cast<float4 *>(&s_redo[t & 1][rg][4 * cq]) = oq;
+    }
+    __syncthreads();
+    if (m > 0 && rg == 0)
+        *reinterpret_cast<float4 *>(o + ((n * m + m - 1) * H + h) * kD + col) =
+            sum_partials<CWD>(s_redo[(m - 1) & 1], cq);
+    if (state_out) {
+        float *So = state_out + nh * (kD * kD);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(So + (rg + i * RG) * kD + col), sv[i]);
+    }
+}
+
+// Fold: sequence n replays the first accepted[n] (clamped to [0, m]) logged tokens on its
+// checkpoint state, in place. A sequence with nothing accepted is not touched.
+template <int CWD>
+__global__ void __launch_bounds__(kDecodeThreads, 3)
+    kda_fold_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                    const float *__restrict__ gk_log, const float *__restrict__ beta_log,
+                    const int32_t *__restrict__ accepted, float *__restrict__ state, int32_t H, int32_t m) {
+    using G = DecodeGeom<CWD>;
+    constexpr int LPR = G::LPR, RG = G::RG, RPT = G::RPT;
+
+    __shared__ float s_alpha[kMaxReplay][kD], s_k[kMaxReplay][kD], s_v[kMaxReplay][kD];
+    __shared__ float s_beta[kMaxReplay];
+    __shared__ __align__(16) float s_redp[2][RG][CWD];
+
+    const int tid = threadIdx.x;
+    const int64_t nh = blockIdx.x;
+    const int64_t n = nh / H;
+    const int h = (int)(nh % H);
+    const int a = min(max(accepted[n], 0), m);
+    if (a == 0) return;  // uniform over the CTA
+    const int cq = tid % LPR, rg = tid / LPR;
+    const int col = blockIdx.y * CWD + 4 * cq;
+    float *S = state + nh * (kD * kD);
+
+    float4 sv[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+
+    for (int idx = tid; idx < a * kD; idx += kDecodeThreads) {
+        const int t = idx / kD, c = idx % kD;
+        const int64_t row = ((n * m + t) * H + h) * kD + c;
+        s_alpha[t][c] = expf(gk_log[row]);
+        s_k[t][c] = __bfloat162float(k[row]);
+        s_v[t][c] = __bfloat162float(v[row]);
+    }
+    if (tid < a) s_beta[tid] = beta_log[(n * m + tid) * H + h];
+    __syncthreads();
+
+    for (int t = 0; t < a; ++t) {
+        float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int row = rg + i * RG;
+            decay_project(sv[i], s_alpha[t][row], s_k[t][row], p);
+        }
+        *reinterpret_cast<float4 *>(&s_redp[t & 1][rg][4 * cq]) = p;
+        __syncthreads();
+        const float4 P = sum_partials<CWD>(s_redp[t & 1], cq);
+        const float4 e = delta_error(s_beta[t], *reinterpret_cast<const float4 *>(&s_v[t][col]), P);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) rank1(sv[i], s_k[t][rg + i * RG], e);
+    }
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(S + (rg + i * RG) * kD + col), sv[i]);
 }
 
 // Column slice per CTA: whole rows when there are enough (sequence, head) pairs to
 // fill the GPU, otherwise quarter rows so that small batches still spread over SMs.
+// Verify and fold take the same choice for the same pair count, which keeps them
+// bit-identical to the decode kernel.
+static bool whole_rows(int64_t pairs, int num_sms) { return pairs >= 4ll * num_sms; }
+
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                           const float *A, const float *b, float *state, float *o, int32_t N, int32_t H,
                           int num_sms, cudaStream_t st) {
     const int64_t pairs = (int64_t)N * H;
     if (pairs == 0) return cudaSuccess;
-    if (pairs >= 4ll * num_sms) {
+    if (whole_rows(pairs, num_sms)) {
         dim3 grid((unsigned)pairs, 1);
         kda_decode_kernel<128><<<grid, kDecodeThreads, 0, st>>>(q, k, v, z, A, b, state, o, H);
     } else {
         dim3 grid((unsigned)pairs, kD / 32);
         kda_decode_kernel<32><<<grid, kDecodeThreads, 0, st>>>(q, k, v, z, A, b, state, o, H);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
+                          const float *A, const float *b, const float *state, float *state_out, float *o,
+                          float *gk_log, float *beta_log, int32_t N, int32_t H, int32_t m, int num_sms,
+                          cudaStream_t st) {
+    const int64_t pairs = (int64_t)N * H;
+    if (pairs == 0 || m == 0) return cudaSuccess;
+    if (whole_rows(pairs, num_sms)) {
+        dim3 grid((unsigned)pairs, 1);
+        kda_verify_kernel<128><<<grid, kDecodeThreads, 0, st>>>(q, k, v, z, A, b, state, state_out, o, gk_log,
+                                                                beta_log, H, m);
+    } else {
+        dim3 grid((unsigned)pairs, kD / 32);
+        kda_verify_kernel<32><<<grid, kDecodeThreads, 0, st>>>(q, k, v, z, A, b, state, state_out, o, gk_log,
+                                                               beta_log, H, m);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fold(const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *gk_log, const float *beta_log,
+                        const int32_t *accepted, float *state, int32_t N, int32_t H, int32_t m, int num_sms,
+                        cudaStream_t st) {
+    const int64_t pairs = (int64_t)N * H;
+    if (pairs == 0 || m == 0) return cudaSuccess;
+    if (whole_rows(pairs, num_sms)) {
+        dim3 grid((unsigned)pairs, 1);
+        kda_fold_kernel<128><<<grid, kDecodeThreads, 0, st>>>(k, v, gk_log, beta_log, accepted, state, H, m);
+    } else {
+        dim3 grid((unsigned)pairs, kD / 32);
+        kda_fold_kernel<32><<<grid, kDecodeThreads, 0, st>>>(k, v, gk_log, beta_log, accepted, state, H, m);
     }
     return cudaGetLastError();
 }

@@ -48,6 +48,10 @@ def library():
         lib.kda_workspace_status.restype = ctypes.c_int
         lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
         lib.kda_recurrent_decode.restype = ctypes.c_int
+        lib.kda_recurrent_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.kda_recurrent_verify.restype = ctypes.c_int
+        lib.kda_replay_fold.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.kda_replay_fold.restype = ctypes.c_int
         _LIB = lib
     return _LIB
 
@@ -168,6 +172,64 @@ def kda_recurrent_decode(q, k, v, z, A, b, state, o=None, stream=None):
     if rc != 0:
         raise KdaError("kda_recurrent_decode", rc)
     return o
+
+
+MAX_REPLAY_TOKENS = 16  # KDA_MAX_REPLAY_TOKENS
+
+
+def kda_recurrent_verify(q, k, v, z, A, b, state, num_tokens, o=None, state_out=None, gk_log=None, beta_log=None,
+                         log=True, stream=None):
+    """num_tokens draft tokens per sequence from the checkpoint `state` (read only).
+
+    q, k, v: bf16 [N * m, H, 128] token-major (token t of sequence n at row n * m + t);
+    z fp32 like q; b fp32 [N * m, H]; state fp32 [N, H, 128, 128]. With log=True the
+    gate values are logged (allocated here unless given). state_out (may be `state`)
+    receives the state after all m tokens. Returns (o, gk_log, beta_log); o is fp32
+    [N * m, H, 128].
+    """
+    m = int(num_tokens)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    _need(z, "z", torch.float32)
+    _need(A, "A", torch.float32)
+    _need(b, "b", torch.float32)
+    _need(state, "state", torch.float32)
+    N, H = state.shape[0], state.shape[1]
+    if q.shape[0] != N * m:
+        raise ValueError("q has %d rows, expected num_seqs * num_tokens = %d" % (q.shape[0], N * m))
+    if o is None:
+        o = torch.empty((N * m, H, D), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32)
+    if log and gk_log is None:
+        gk_log = torch.empty((N * m, H, D), dtype=torch.float32, device=q.device)
+    if log and beta_log is None:
+        beta_log = torch.empty((N * m, H), dtype=torch.float32, device=q.device)
+    for name, t in (("gk_log", gk_log), ("beta_log", beta_log), ("state_out", state_out)):
+        if t is not None:
+            _need(t, name, torch.float32)
+    rc = library().kda_recurrent_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(b), _ptr(state),
+                                        _ptr(state_out), _ptr(o), _ptr(gk_log), _ptr(beta_log), N, H, m, D, D,
+                                        _stream(stream))
+    if rc != 0:
+        raise KdaError("kda_recurrent_verify", rc)
+    return o, gk_log, beta_log
+
+
+def kda_replay_fold(k, v, gk_log, beta_log, num_accepted, state, num_tokens, stream=None):
+    """Replay the first num_accepted[n] logged tokens of each sequence on `state` in place."""
+    m = int(num_tokens)
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    _need(gk_log, "gk_log", torch.float32)
+    _need(beta_log, "beta_log", torch.float32)
+    _need(num_accepted, "num_accepted", torch.int32)
+    _need(state, "state", torch.float32)
+    N, H = state.shape[0], state.shape[1]
+    rc = library().kda_replay_fold(_ptr(k), _ptr(v), _ptr(gk_log), _ptr(beta_log), _ptr(num_accepted), _ptr(state),
+                                   N, H, m, D, D, _stream(stream))
+    if rc != 0:
+        raise KdaError("kda_replay_fold", rc)
+    return state
 
 
 def kda_chunk_prefill_noalloc(q, k, v, z, A, b, initial_state=None, cu_seqlens=None, cu_seqlens_host=None,

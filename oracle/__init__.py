@@ -16,6 +16,10 @@ kda_forward(q, k, v, z, A, b, S0, cu_seqlens)
     gate + recurrence from the raw inputs, each first converted exactly (bf16 or
     fp32 -> fp64) as the GPU receives them. This is the oracle the CUDA path is
     compared with.
+verify(q, k, v, z, A, b, S0, num_tokens) / replay_fold(k, v, la, beta, S0, accepted, num_tokens)
+    the speculative-decoding pair of ReplaySSM ('Kimi K3 attention deep dive', §6.2):
+    num_tokens draft tokens per sequence from a checkpoint, and the replay of each
+    sequence's accepted prefix on that checkpoint from the logged gate values.
 chunkwise(...)
     (oracle.chunkwise) the chunk algebra of the blog's §7 in fp64, used to pin the
     chunk decomposition against the recurrence.
@@ -194,3 +198,36 @@ def recurrence(q, k, v, la, beta, S0=None, cu_seqlens=None, delta=True, threads=
 def kda_forward(q, k, v, z, A, b, S0=None, cu_seqlens=None, threads=0):
     """The oracle for the CUDA path: gate then recurrence, fp64, from the exact inputs."""
     return default().kda_forward(q, k, v, z, A, b, S0=S0, cu_seqlens=cu_seqlens, threads=threads)
+
+
+def verify(q, k, v, z, A, b, S0, num_tokens):
+    """Draft window of num_tokens tokens per sequence, read from the checkpoint S0 [N, H, dk, dv].
+
+    Inputs are token-major, token t of sequence n at row n * m + t ([N * m, H, ...]).
+    Returns (o, S_after, la, beta) in fp64: every token's output, the state after all m
+    tokens, and the logged gate values ('Kimi K3 attention deep dive', §6.2: the verify
+    pass stores the gate values its fold will replay).
+    """
+    m = int(num_tokens)
+    N = np.asarray(_as_f64(S0)).shape[0]
+    la, beta = gate(z, A, b)
+    cu = np.arange(N + 1, dtype=np.int64) * m
+    o, S = recurrence(q, k, v, la, beta, S0=S0, cu_seqlens=cu)
+    return o, S, la, beta
+
+
+def replay_fold(k, v, la, beta, S0, accepted, num_tokens):
+    """State after each sequence replays the first clamp(accepted[n], 0, m) tokens of its
+    window on the checkpoint S0 ('Kimi K3 attention deep dive', §6.2): the recurrence run
+    over exactly the accepted prefix, fp64. Returns S [N, H, dk, dv]."""
+    m = int(num_tokens)
+    k = _as_f64(k); v = _as_f64(v); la = _as_f64(la); beta = _as_f64(beta)
+    s0 = _as_f64(S0)
+    N = s0.shape[0]
+    acc = np.clip(np.asarray(accepted, dtype=np.int64).reshape(N), 0, m)
+    rows = np.concatenate([np.arange(n * m, n * m + acc[n], dtype=np.int64) for n in range(N)] +
+                          [np.zeros(0, dtype=np.int64)])
+    cu = np.concatenate([[0], np.cumsum(acc)]).astype(np.int64)
+    q0 = np.zeros_like(k[rows])
+    _, S = recurrence(q0, k[rows], v[rows], la[rows], beta[rows], S0=s0, cu_seqlens=cu)
+    return S

@@ -290,6 +290,39 @@ def pin_prefill_then_decode(orc):
     assert np.array_equal(np.concatenate(outs), o) and np.array_equal(S1, S), "split run differs"
 
 
+def pin_replay_fold_matches_snapshots(orc):
+    """ReplaySSM ('Kimi K3 attention deep dive', §6.2): replaying the accepted prefix of a
+    draft window from the checkpoint gives the state that a snapshot taken after that many
+    single-token steps holds, for every accepted count (clamped to the window)."""
+    import oracle as oracle_mod
+    N, H, m, dk, dv = 3, 2, 5, 8, 8
+    rng = np.random.default_rng(91)
+    q = _unit_rows(rng.standard_normal((N * m, H, dk)))
+    k = _unit_rows(rng.standard_normal((N * m, H, dk)))
+    v = rng.standard_normal((N * m, H, dv))
+    z = rng.standard_normal((N * m, H, dk)).astype(np.float32)
+    A = np.log(rng.uniform(1, 16, H)).astype(np.float32)
+    b = rng.standard_normal((N * m, H)).astype(np.float32)
+    S0 = 0.1 * rng.standard_normal((N, H, dk, dv))
+    o, S_all, la, beta = oracle_mod.verify(q, k, v, z, A, b, S0, m)
+    # snapshots: one token at a time per sequence
+    snaps = np.empty((m + 1, N, H, dk, dv))
+    snaps[0] = S0
+    for n in range(N):
+        S = S0[n:n + 1]
+        for t in range(m):
+            r = slice(n * m + t, n * m + t + 1)
+            ot, S = orc.recurrence(q[r], k[r], v[r], la[r], beta[r], S0=S)
+            assert np.array_equal(ot, o[r]), "verify output differs from the single-token step"
+            snaps[t + 1, n] = S[0]
+    assert np.array_equal(snaps[m], S_all), "verify end state"
+    for accepted in ([0, 0, 0], [1, 2, 3], [5, 0, 4], [m + 3, -2, 2]):
+        S = oracle_mod.replay_fold(k, v, la, beta, S0, accepted, m)
+        for n in range(N):
+            a = min(max(accepted[n], 0), m)
+            assert np.array_equal(S[n], snaps[a, n]), "fold of %d tokens (seq %d)" % (a, n)
+
+
 ALL_PINS = [
     pin_linear_attention_worked_example,
     pin_deltanet_worked_example,
@@ -304,4 +337,5 @@ ALL_PINS = [
     pin_chunkwise_equals_recurrence,
     pin_packing_and_splits,
     pin_prefill_then_decode,
+    pin_replay_fold_matches_snapshots,
 ]

@@ -17,6 +17,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 KDA_OK, KDA_ERR_NULL, KDA_ERR_SHAPE, KDA_ERR_UNSUPPORTED = 0, -1, -2, -3
 KDA_ERR_SEQLENS, KDA_ERR_ALIGN, KDA_ERR_WORKSPACE = -4, -5, -6
 FAKE = 1 << 20  # 256-byte aligned fake device address, never dereferenced
+KDA_MAX_REPLAY = 16
 
 
 def declared_functions():
@@ -33,7 +34,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_chunk_prefill_workspace_size",
                      "kda_status_string", "kda_workspace_status", "kda_version",
-                     "kda_chunk_prefill_launch_count"):
+                     "kda_chunk_prefill_launch_count", "kda_recurrent_verify", "kda_replay_fold"):
         assert required in names
 
 
@@ -148,3 +149,59 @@ def _decode(**over):
 ])
 def test_decode_argument_checks(over, code):
     assert _decode(**over) == code
+
+
+def _verify(**over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, A=FAKE, b=FAKE, state=FAKE, state_out=None, o=FAKE, gk=FAKE,
+                beta=FAKE, num_seqs=4, num_heads=2, m=8, d_k=128, d_v=128, stream=None)
+    args.update(over)
+    return kda.library().kda_recurrent_verify(
+        args["q"], args["k"], args["v"], args["z"], args["A"], args["b"], args["state"], args["state_out"],
+        args["o"], args["gk"], args["beta"], args["num_seqs"], args["num_heads"], args["m"], args["d_k"],
+        args["d_v"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d_v=64), KDA_ERR_UNSUPPORTED),
+    (dict(m=17), KDA_ERR_UNSUPPORTED),
+    (dict(m=-1), KDA_ERR_SHAPE),
+    (dict(num_heads=0), KDA_ERR_SHAPE),
+    (dict(state=None), KDA_ERR_NULL),
+    (dict(z=None), KDA_ERR_NULL),
+    (dict(o=FAKE + 4), KDA_ERR_ALIGN),
+    (dict(gk=FAKE + 8), KDA_ERR_ALIGN),
+    (dict(state_out=FAKE + 8), KDA_ERR_ALIGN),
+    (dict(m=0), KDA_OK),
+    (dict(num_seqs=0), KDA_OK),
+])
+def test_verify_argument_checks(over, code):
+    assert _verify(**over) == code
+
+
+def _fold(**over):
+    args = dict(k=FAKE, v=FAKE, gk=FAKE, beta=FAKE, acc=FAKE, state=FAKE, num_seqs=4, num_heads=2, m=8,
+                d_k=128, d_v=128, stream=None)
+    args.update(over)
+    return kda.library().kda_replay_fold(
+        args["k"], args["v"], args["gk"], args["beta"], args["acc"], args["state"], args["num_seqs"],
+        args["num_heads"], args["m"], args["d_k"], args["d_v"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d_k=256), KDA_ERR_UNSUPPORTED),
+    (dict(m=KDA_MAX_REPLAY + 1), KDA_ERR_UNSUPPORTED),
+    (dict(num_seqs=-1), KDA_ERR_SHAPE),
+    (dict(acc=None), KDA_ERR_NULL),
+    (dict(gk=None), KDA_ERR_NULL),
+    (dict(acc=FAKE + 2), KDA_ERR_ALIGN),
+    (dict(k=FAKE + 8), KDA_ERR_ALIGN),
+    (dict(m=0), KDA_OK),
+])
+def test_fold_argument_checks(over, code):
+    assert _fold(**over) == code
+
+
+def test_max_replay_constant_matches_header():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    m = re.search(r"#define KDA_MAX_REPLAY_TOKENS (\d+)", text)
+    assert m and int(m.group(1)) == KDA_MAX_REPLAY == kda.MAX_REPLAY_TOKENS
