@@ -499,6 +499,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", choices=["all", "speculative"], default="all",
+                    help="'speculative' times only the verify + fold pair (about 3 GB on the device; "
+                         "for profiling) and prints its object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -508,6 +511,11 @@ def main():
         return
     rank, world, local = dist_setup(args.gpus)
     try:
+        if args.part == "speculative":
+            spec = run_speculative(args.steps, args.warmup, world, seed=1000 * rank)
+            if rank == 0:
+                print(json.dumps({"speculative": spec}), flush=True)
+            return
         main_ours(args, rank, world, local)
     finally:
         if world > 1:
