@@ -323,6 +323,95 @@ def pin_replay_fold_matches_snapshots(orc):
             assert np.array_equal(S[n], snaps[a, n]), "fold of %d tokens (seq %d)" % (a, n)
 
 
+def pin_layer_short_conv_matches_numpy_convolve(orc):
+    """ShortConv ('Kimi K3 attention deep dive', §2.3: depthwise causal convolution, kernel
+    size 4) streamed in pieces with its state equals np.convolve over the whole sequence,
+    and its impulse response reads back the taps, newest input on the last tap."""
+    from oracle import layer
+    rng = np.random.default_rng(101)
+    T, C = 13, 5
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, 4))
+    ys, st = [], np.zeros((3, C))
+    for piece in (slice(0, 1), slice(1, 5), slice(5, 13)):
+        y, st = layer.short_conv(x[piece], w, st)
+        ys.append(y)
+    y = np.concatenate(ys)
+    for c in range(C):
+        ref = np.convolve(x[:, c], w[c, ::-1])[:T]
+        _close(y[:, c], ref, 1e-13, "conv channel %d" % c)
+    assert np.array_equal(st, x[T - 3:]), "conv state must hold the last three inputs"
+    imp = np.zeros((4, C))
+    imp[0] = 1.0
+    y, _ = layer.short_conv(imp, w, np.zeros((3, C)))
+    for t in range(4):
+        assert np.array_equal(y[t], w[:, 3 - t]), "impulse response at %d" % t
+
+
+def pin_layer_activation_closed_forms(orc):
+    """Swish(x) = x sigmoid(x), L2Norm and the gated per-head RMSNorm (same page, §2.3):
+    closed forms."""
+    from oracle import layer
+    assert layer.swish(np.array([0.0]))[0] == 0.0
+    _close(layer.swish(np.array([np.log(3.0)])), [0.75 * np.log(3.0)], 1e-15, "swish(ln 3)")
+    x = np.linspace(-4, 4, 17)
+    _close(layer.swish(x) - layer.swish(-x), x, 1e-14, "swish odd part")
+    _close(layer.l2norm(np.array([3.0, 4.0]), 0.0), [0.6, 0.8], 1e-15, "l2norm (3, 4)")
+    r = np.random.default_rng(5).standard_normal((4, 9))
+    _close(np.linalg.norm(layer.l2norm(r, 0.0), axis=-1), np.ones(4), 1e-14, "unit rows")
+    s = np.sum(r[0] ** 2)
+    _close(np.sum(layer.l2norm(r[0], 0.5) ** 2), [s / (s + 0.5)], 1e-14, "l2norm epsilon")
+    o = np.array([2.0, -2.0, 2.0, -2.0])
+    w = np.array([1.0, 2.0, 3.0, 4.0])
+    _close(layer.gated_rmsnorm(o, w, np.full(4, np.log(3.0)), 0.0), [0.75, -1.5, 2.25, -3.0], 1e-15,
+           "gated rmsnorm")
+    _close(layer.gated_rmsnorm(7.0 * r, np.ones(9), np.zeros(9), 0.0),
+           0.5 * r / np.sqrt(np.mean(r ** 2, axis=-1, keepdims=True)), 1e-14, "scale invariance, half gate")
+
+
+def pin_layer_streamed_decode_equals_whole_sequence(orc):
+    """Fused decode over T tokens, carrying the recurrent and the conv state, equals the
+    whole-sequence form: np.convolve of each channel, Swish, L2Norm, the recurrence over
+    all T tokens, then the gated RMSNorm of every output ('Kimi K3', llm.rainlin.net:
+    the chunk and recurrent paths must agree, conv state included)."""
+    import oracle as oracle_mod
+    from oracle import layer
+    rng = np.random.default_rng(102)
+    N, H, D, T = 2, 2, 8, 6
+    X = [rng.standard_normal((N, T, H, D)) for _ in range(3)]
+    cw = rng.standard_normal((3, H, D, 4)) * 0.5
+    z = rng.standard_normal((N, T, H, D)).astype(np.float32)
+    A = np.log(rng.uniform(1, 16, H)).astype(np.float32)
+    b = rng.standard_normal((N, T, H)).astype(np.float32)
+    g = rng.standard_normal((N, T, H, D))
+    nw = 1.0 + 0.1 * rng.standard_normal(D)
+    S0 = 0.1 * rng.standard_normal((N, H, D, D))
+    eps1, eps2 = 1e-6, 1e-5
+    # streamed
+    S, cs, ys = S0.copy(), np.zeros((N, 3, 3, H, D)), []
+    for t in range(T):
+        y, S, cs = layer.fused_decode(X[0][:, t], X[1][:, t], X[2][:, t], cs, cw, z[:, t], A, b[:, t], g[:, t], nw,
+                                      S, eps1, eps2)
+        ys.append(y)
+    # whole sequence
+    act = []
+    for s in range(3):
+        a = np.empty((N, T, H, D))
+        for n in range(N):
+            for h in range(H):
+                for c in range(D):
+                    a[n, :, h, c] = np.convolve(X[s][n, :, h, c], cw[s, h, c, ::-1])[:T]
+        act.append(layer.swish(a))
+    q, k, v = layer.l2norm(act[0], eps1), layer.l2norm(act[1], eps1), act[2]
+    la, beta = oracle_mod.gate(z, A, b)
+    o, S_ref = orc.recurrence(q, k, v, la, beta, S0=S0)
+    y_ref = layer.gated_rmsnorm(o, nw, g, eps2)
+    _close(np.stack(ys, axis=1), y_ref, 1e-12, "fused decode outputs")
+    _close(S, S_ref, 1e-12, "fused decode state")
+    for s in range(3):
+        assert np.array_equal(cs[:, s], X[s][:, T - 3:]), "conv state stream %d" % s
+
+
 ALL_PINS = [
     pin_linear_attention_worked_example,
     pin_deltanet_worked_example,
@@ -338,4 +427,7 @@ ALL_PINS = [
     pin_packing_and_splits,
     pin_prefill_then_decode,
     pin_replay_fold_matches_snapshots,
+    pin_layer_short_conv_matches_numpy_convolve,
+    pin_layer_activation_closed_forms,
+    pin_layer_streamed_decode_equals_whole_sequence,
 ]

@@ -79,3 +79,42 @@ def test_mutant_is_caught(tmp_path, name):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, "planted mistake %r passed every pin" % name
+
+
+# ---- planted mistakes in the layer steps around the fused decode (oracle/layer.py) ----
+LAYER_MUTANTS = {
+    "conv_taps_reversed": ("y[t] += w[:, j] * window[t + j]", "y[t] += w[:, CONV_TAPS - 1 - j] * window[t + j]"),
+    "conv_state_oldest_kept": ("window[T:T + CONV_TAPS - 1]", "window[:CONV_TAPS - 1]"),
+    "swish_sign": ("return x / (1.0 + np.exp(-x))", "return x / (1.0 + np.exp(x))"),
+    "l2norm_without_sqrt": ("np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)",
+                            "(np.sum(x * x, axis=-1, keepdims=True) + eps)"),
+    "rmsnorm_sum_not_mean": ("np.mean(o * o, axis=-1, keepdims=True)", "np.sum(o * o, axis=-1, keepdims=True)"),
+    "output_gate_ungated": ("/ (1.0 + np.exp(-g))", "* 1.0"),
+    "value_normalised": ("v = act[2]", "v = l2norm(act[2], eps_l2)"),
+    "query_not_normalised": ("q = l2norm(act[0], eps_l2)", "q = act[0]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAYER_MUTANTS))
+def test_layer_mutant_is_caught(monkeypatch, name):
+    import importlib.util
+
+    from oracle import layer
+    old, new = LAYER_MUTANTS[name]
+    src = open(layer.__file__).read()
+    assert src.count(old) == 1, "mutation anchor not found once: %r" % old
+    spec = importlib.util.spec_from_loader("oracle._layer_mutant", loader=None, origin=layer.__file__)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    exec(compile(src.replace(old, new), layer.__file__, "exec"), mod.__dict__)
+    for fn in ("short_conv", "swish", "l2norm", "gated_rmsnorm", "fused_decode"):
+        monkeypatch.setattr(layer, fn, getattr(mod, fn))
+    caught = []
+    for pin in ALL_PINS:
+        if not pin.__name__.startswith("pin_layer_"):
+            continue
+        try:
+            pin(oracle.default())
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, "planted mistake %r passed every layer pin" % name
