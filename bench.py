@@ -338,6 +338,51 @@ def run_speculative(steps, warmup, world, seed):
             "finite": bool(torch.isfinite(state).all() and torch.isfinite(o).all())}
 
 
+# fused decode: per (sequence, head) token the state read + write, x_q, x_k, x_v (bf16),
+# the conv state read + write (3 streams x 3 inputs, bf16), z, b, g and y (fp32); the conv
+# taps and the norm weight are read once per head
+FUSED_BYTES_PER_TH = 2 * 4 * D * D + 3 * 2 * D + 2 * 9 * 2 * D + 4 * D + 4 + 4 * D + 4 * D   # 138500
+FUSED_BYTES_PER_HEAD = 3 * D * 4 * 4
+
+
+def run_fused_decode(steps, warmup, world, seed):
+    """The fused decode layer step on the decode workload's shape (256 x 96, 1.6 GB state)."""
+    from linear_attention_serving_02_gb300 import kda
+
+    N, H = DECODE_N, DECODE_H
+    prm = inputs.fused_decode_params(H, seed=seed + 70, device="cuda")
+    pool = [inputs.fused_decode_step_inputs(N, H, seed=seed + 70, step=i, device="cuda") for i in range(4)]
+    state = inputs.decode_state(N, H, seed=seed + 71, device="cuda")
+    cs = torch.zeros((N, 3, 3, H, D), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((N, H, D), dtype=torch.float32, device="cuda")
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+
+    def one(i):
+        st = pool[i % len(pool)]
+        kda.kda_fused_decode(st["x_q"], st["x_k"], st["x_v"], cs, prm["conv_w"], st["z"], st["A"], st["b"], st["g"],
+                             prm["norm_w"], state, y=y)
+
+    for i in range(warmup):
+        flush()
+        one(i)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush()
+        evs[j][0].record(stream)
+        one(warmup + j)
+        evs[j][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e-3, world)
+    nbytes = N * H * FUSED_BYTES_PER_TH + H * FUSED_BYTES_PER_HEAD + 4 * D
+    return {"sequences": N, "heads": H, "ms": 1e3 * t, "token_heads_per_s": world * N * H / t,
+            "bytes_per_launch": nbytes, "achieved_gbs": nbytes / t / 1e9,
+            "finite": bool(torch.isfinite(state).all() and torch.isfinite(y).all())}
+
+
 # ------------------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ------------------------------------------------------------------------------------
@@ -430,6 +475,8 @@ def main_ours(args, rank, world, local):
     spec = run_speculative(max(1, min(args.steps, 50)), args.warmup, world, seed=1000 * rank)
     for part in ("verify", "fold"):
         spec[part]["frac_of_hbm"] = spec[part]["achieved_gbs"] / hbm
+    fused = run_fused_decode(max(1, min(args.steps, 50)), args.warmup, world, seed=1000 * rank)
+    fused["frac_of_hbm"] = fused["achieved_gbs"] / hbm
 
     pre_t = max_over_ranks(sum(pre_ms) / 1e3, world)
     dec_t = max_over_ranks(sum(dec_ms) / 1e3, world)
@@ -481,6 +528,7 @@ def main_ours(args, rank, world, local):
         "decode": {"value": world * K * DECODE_N / dec_t, "unit": "token/s (one per sequence)",
                    "token_heads_per_s": world * K * th_dec / dec_t, "ms": 1e3 * dec_launch, "roofline": roof_dec},
         "speculative": spec,
+        "fused_decode": fused,
         "roofline": dominant,
         "cpu_baseline": cpu,
         "e2e": {"value": units / e2e_t, "unit": "token·head/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -499,9 +547,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--part", choices=["all", "speculative"], default="all",
-                    help="'speculative' times only the verify + fold pair (about 3 GB on the device; "
-                         "for profiling) and prints its object")
+    ap.add_argument("--part", choices=["all", "speculative", "fused"], default="all",
+                    help="'speculative' times only the verify + fold pair, 'fused' only the fused decode "
+                         "(each about 3 GB on the device; for profiling) and prints its object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -511,10 +559,11 @@ def main():
         return
     rank, world, local = dist_setup(args.gpus)
     try:
-        if args.part == "speculative":
-            spec = run_speculative(args.steps, args.warmup, world, seed=1000 * rank)
+        if args.part != "all":
+            run = run_speculative if args.part == "speculative" else run_fused_decode
+            res = run(args.steps, args.warmup, world, seed=1000 * rank)
             if rank == 0:
-                print(json.dumps({"speculative": spec}), flush=True)
+                print(json.dumps({args.part: res}), flush=True)
             return
         main_ours(args, rank, world, local)
     finally:

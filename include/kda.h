@@ -261,6 +261,43 @@ int kda_replay_fold(const uint16_t *k, const uint16_t *v, const float *gk_log, c
                     int32_t num_seqs, int32_t num_heads, int32_t num_tokens,
                     int32_t d_k, int32_t d_v, void *stream);
 
+/*
+ * kda_fused_decode - one decode token of the whole KDA layer step between the
+ * projections: causal conv -> recurrent update -> gated RMSNorm in one launch ('Kimi K3
+ * attention deep dive', §6.3), with the activations of the same page's §2.3:
+ *
+ *   q = L2Norm(Swish(ShortConv(x_q))),  k = L2Norm(Swish(ShortConv(x_k))),
+ *   v = Swish(ShortConv(x_v))
+ *   then the update of kda_recurrent_decode() on state[n, h] (in place), o = S^T q
+ *   y = o / sqrt(mean(o^2) + eps_rms) * norm_w * sigmoid(g)
+ *
+ * ShortConv is depthwise and causal with 4 taps: output channel c is
+ *   conv_w[s, h, c, 0] x_{t-3} + conv_w[s, h, c, 1] x_{t-2} + conv_w[s, h, c, 2] x_{t-1}
+ *   + conv_w[s, h, c, 3] x_t,
+ * with x_{t-3..t-1} read from the conv state, which afterwards holds x_{t-2}, x_{t-1}, x_t
+ * (a new sequence starts from zeros). L2Norm(x) = x / sqrt(sum(x^2) + eps_l2) over the
+ * head's 128 channels; Swish(x) = x sigmoid(x). There is no 1/sqrt(d) scale on q.
+ *
+ * Arguments (N = num_seqs, H = num_heads; all device pointers, caller-owned):
+ *   x_q, x_k, x_v  bf16 [N, H, 128]      the projections before the convolution
+ *   conv_state     bf16 [N, 3, 3, H, 128] per stream (q, k, v) the last three inputs,
+ *                  oldest first; read and updated in place
+ *   conv_w         fp32 [3, H, 128, 4]    taps per stream, head, channel, oldest first
+ *   z, A, b        as kda_recurrent_decode()
+ *   g              fp32 [N, H, 128]       output-gate pre-activation
+ *   norm_w         fp32 [128]             RMSNorm weight (shared by the heads)
+ *   eps_l2, eps_rms  >= 0 (negative or NaN: KDA_ERR_UNSUPPORTED)
+ *   state          fp32 [N, H, 128, 128]  read and overwritten in place
+ *   y              fp32 [N, H, 128]       written
+ * Alignment: 16 bytes (A, b: 4). All arithmetic is fp32. Stream-ordered, asynchronous.
+ */
+int kda_fused_decode(const uint16_t *x_q, const uint16_t *x_k, const uint16_t *x_v,
+                     uint16_t *conv_state, const float *conv_w,
+                     const float *z, const float *A, const float *b,
+                     const float *g, const float *norm_w, float eps_l2, float eps_rms,
+                     float *state, float *y,
+                     int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,6 +34,10 @@ cudaError_t launch_verify(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const 
 cudaError_t launch_fold(const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *gk_log, const float *beta_log,
                         const int32_t *accepted, float *state, int32_t N, int32_t H, int32_t m, int num_sms,
                         cudaStream_t st);
+cudaError_t launch_fused_decode(const __nv_bfloat16 *xq, const __nv_bfloat16 *xk, const __nv_bfloat16 *xv,
+                                __nv_bfloat16 *conv_state, const float *conv_w, const float *z, const float *A,
+                                const float *b, const float *g, const float *norm_w, float eps_l2, float eps_rms,
+                                float *state, float *y, int32_t N, int32_t H, int num_sms, cudaStream_t st);
 size_t intra_smem_bytes();
 }  // namespace kda
 
@@ -287,6 +291,32 @@ int kda_replay_fold(const uint16_t *k, const uint16_t *v, const float *gk_log, c
     if (kda::launch_fold(reinterpret_cast<const __nv_bfloat16 *>(k), reinterpret_cast<const __nv_bfloat16 *>(v),
                          gk_log, beta_log, num_accepted, state, num_seqs, num_heads, num_tokens, dev.sms,
                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+int kda_fused_decode(const uint16_t *x_q, const uint16_t *x_k, const uint16_t *x_v, uint16_t *conv_state,
+                     const float *conv_w, const float *z, const float *A, const float *b, const float *g,
+                     const float *norm_w, float eps_l2, float eps_rms, float *state, float *y, int32_t num_seqs,
+                     int32_t num_heads, int32_t d_k, int32_t d_v, void *stream) {
+    if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
+    if (!(eps_l2 >= 0.0f) || !(eps_rms >= 0.0f)) return KDA_ERR_UNSUPPORTED;  // NaN fails both
+    if (num_seqs < 0 || num_heads <= 0) return KDA_ERR_SHAPE;
+    if (num_seqs == 0) return KDA_OK;
+    if (!x_q || !x_k || !x_v || !conv_state || !conv_w || !z || !A || !b || !g || !norm_w || !state || !y)
+        return KDA_ERR_NULL;
+    if (!aligned(x_q, 16) || !aligned(x_k, 16) || !aligned(x_v, 16) || !aligned(conv_state, 16) ||
+        !aligned(conv_w, 16) || !aligned(z, 16) || !aligned(g, 16) || !aligned(norm_w, 16) || !aligned(state, 16) ||
+        !aligned(y, 16) || !aligned(A, 4) || !aligned(b, 4))
+        return KDA_ERR_ALIGN;
+    DeviceInfo dev;
+    int rc = device_info(dev);
+    if (rc != KDA_OK) return rc;
+    if (kda::launch_fused_decode(
+            reinterpret_cast<const __nv_bfloat16 *>(x_q), reinterpret_cast<const __nv_bfloat16 *>(x_k),
+            reinterpret_cast<const __nv_bfloat16 *>(x_v), reinterpret_cast<__nv_bfloat16 *>(conv_state), conv_w, z,
+            A, b, g, norm_w, eps_l2, eps_rms, state, y, num_seqs, num_heads, dev.sms,
+            static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -22,67 +22,17 @@
 // draft token, the verify kernel logs each token's gate values (log a, beta) next to the
 // caller's k and v, about 1 KB per token and head; once the sampler has accepted a prefix,
 // the fold kernel replays just that prefix on the checkpoint. The three kernels share
-// the per-element arithmetic below, written with explicitly rounded intrinsics, the same
+// the per-element arithmetic of kda_decode_step.cuh (explicitly rounded intrinsics), the same
 // column slice for the same (sequence, head) count, and the same reduction order, so a
 // fold of a tokens leaves exactly the bits that a calls of the decode kernel leave, and
 // verify's outputs are exactly the decode kernel's.
 
 #include "kda.h"
-#include "kda_common.cuh"
+#include "kda_decode_step.cuh"
 
 namespace kda {
 
-constexpr int kDecodeThreads = 256;
 constexpr int kMaxReplay = KDA_MAX_REPLAY_TOKENS;  // draft tokens per verify / fold call
-
-template <int CWD>
-struct DecodeGeom {
-    static constexpr int LPR = CWD / 4;              // threads per row (one float4 each)
-    static constexpr int RG = kDecodeThreads / LPR;  // row groups
-    static constexpr int RPT = kD / RG;              // rows per thread
-    static_assert(RG * LPR == kDecodeThreads && RPT * RG == kD, "decode layout");
-};
-
-// ---- the per-element arithmetic every kernel here shares ----
-
-// S' = a S on one row of this thread, and its term of the projection p += k_r S'_r
-__device__ __forceinline__ void decay_project(float4 &s, float a, float kr, float4 &p) {
-    s.x = __fmul_rn(s.x, a); s.y = __fmul_rn(s.y, a); s.z = __fmul_rn(s.z, a); s.w = __fmul_rn(s.w, a);
-    p.x = __fmaf_rn(kr, s.x, p.x); p.y = __fmaf_rn(kr, s.y, p.y);
-    p.z = __fmaf_rn(kr, s.z, p.z); p.w = __fmaf_rn(kr, s.w, p.w);
-}
-// e = beta (v - p)
-__device__ __forceinline__ float4 delta_error(float beta, float4 v, float4 p) {
-    return make_float4(__fmul_rn(beta, __fsub_rn(v.x, p.x)), __fmul_rn(beta, __fsub_rn(v.y, p.y)),
-                       __fmul_rn(beta, __fsub_rn(v.z, p.z)), __fmul_rn(beta, __fsub_rn(v.w, p.w)));
-}
-// S = S' + k_r e on one row
-__device__ __forceinline__ void rank1(float4 &s, float kr, float4 e) {
-    s.x = __fmaf_rn(kr, e.x, s.x); s.y = __fmaf_rn(kr, e.y, s.y);
-    s.z = __fmaf_rn(kr, e.z, s.z); s.w = __fmaf_rn(kr, e.w, s.w);
-}
-// o += q_r S_r
-__device__ __forceinline__ void readout(const float4 &s, float qr, float4 &o) {
-    o.x = __fmaf_rn(qr, s.x, o.x); o.y = __fmaf_rn(qr, s.y, o.y);
-    o.z = __fmaf_rn(qr, s.z, o.z); o.w = __fmaf_rn(qr, s.w, o.w);
-}
-// sum of the RG row-group partials of this thread's four columns, in row-group order
-template <int CWD>
-__device__ __forceinline__ float4 sum_partials(const float (*red)[CWD], int cq) {
-    constexpr int RG = DecodeGeom<CWD>::RG;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int r = 0; r < RG; ++r) {
-        const float4 x = *reinterpret_cast<const float4 *>(&red[r][4 * cq]);
-        acc.x = __fadd_rn(acc.x, x.x); acc.y = __fadd_rn(acc.y, x.y);
-        acc.z = __fadd_rn(acc.z, x.z); acc.w = __fadd_rn(acc.w, x.w);
-    }
-    return acc;
-}
-// the gate of one key channel, as every kernel here computes it
-__device__ __forceinline__ float decode_log_decay(const float *A, int h, float z) {
-    return gate_log_decay(expf(A[h]), z);
-}
 
 // Three CTAs per SM (registers capped accordingly, a few spilled): each CTA has its
 // 64 KB of state in flight, and the third CTA keeps loads outstanding while the others
@@ -296,11 +246,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(S + (rg + i * RG) * kD + col), sv[i]);
 }
 
-// Column slice per CTA: whole rows when there are enough (sequence, head) pairs to
-// fill the GPU, otherwise quarter rows so that small batches still spread over SMs.
-// Verify and fold take the same choice for the same pair count, which keeps them
-// bit-identical to the decode kernel.
-static bool whole_rows(int64_t pairs, int num_sms) { return pairs >= 4ll * num_sms; }
+// Verify and fold take the decode kernel's column slice for the same pair count
+// (whole_rows), which keeps them bit-identical to it.
 
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                           const float *A, const float *b, float *state, float *o, int32_t N, int32_t H,

@@ -92,3 +92,29 @@ def decode_step_inputs(N, H, seed=0, step=0, d_k=D, d_v=D, device="cpu", A=None)
         ga = _gen(seed * 1000003 + 1, device)
         A = torch.log(1.0 + 15.0 * torch.rand((H,), generator=ga, device=device, dtype=f32))
     return dict(q=q, k=k, v=v, z=z, A=A, b=b)
+
+
+def fused_decode_params(H, seed=0, d=D, device="cpu"):
+    """Synthetic stand-ins for the layer weights around the fused decode: conv taps
+    fp32 [3, H, d, 4] ~ N(0, 0.5^2) and the RMSNorm weight fp32 [d] ~ 1 + N(0, 0.1^2)."""
+    g = _gen(seed * 1000003 + 2, device)
+    f32 = torch.float32
+    conv_w = 0.5 * torch.randn((3, H, d, 4), generator=g, device=device, dtype=f32)
+    norm_w = 1.0 + 0.1 * torch.randn((d,), generator=g, device=device, dtype=f32)
+    return dict(conv_w=conv_w, norm_w=norm_w)
+
+
+def fused_decode_step_inputs(N, H, seed=0, step=0, d=D, device="cpu"):
+    """One fused decode token: the pre-conv projections x_q, x_k, x_v ~ N(0, 1) bf16
+    [N, H, d], z ~ N(0, 1) fp32, b ~ N(0, 1) fp32 [N, H], the output-gate pre-activation
+    g ~ N(0, 1) fp32 [N, H, d], and A [H] drawn once per seed as for decode."""
+    gen = _gen(seed * 1000003 + 7919 * (step + 1) + 3, device)
+    f32 = torch.float32
+    xq, xk, xv = (torch.randn((N, H, d), generator=gen, device=device, dtype=f32).to(torch.bfloat16)
+                  for _ in range(3))
+    z = torch.randn((N, H, d), generator=gen, device=device, dtype=f32)
+    b = torch.randn((N, H), generator=gen, device=device, dtype=f32)
+    g = torch.randn((N, H, d), generator=gen, device=device, dtype=f32)
+    ga = _gen(seed * 1000003 + 1, device)
+    A = torch.log(1.0 + 15.0 * torch.rand((H,), generator=ga, device=device, dtype=f32))
+    return dict(x_q=xq, x_k=xk, x_v=xv, z=z, A=A, b=b, g=g)

@@ -52,6 +52,10 @@ def library():
         lib.kda_recurrent_verify.restype = ctypes.c_int
         lib.kda_replay_fold.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
         lib.kda_replay_fold.restype = ctypes.c_int
+        f32 = ctypes.c_float
+        lib.kda_fused_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, vp, i32, i32, i32, i32,
+                                         vp]
+        lib.kda_fused_decode.restype = ctypes.c_int
         _LIB = lib
     return _LIB
 
@@ -230,6 +234,28 @@ def kda_replay_fold(k, v, gk_log, beta_log, num_accepted, state, num_tokens, str
     if rc != 0:
         raise KdaError("kda_replay_fold", rc)
     return state
+
+
+def kda_fused_decode(x_q, x_k, x_v, conv_state, conv_w, z, A, b, g, norm_w, state, y=None, eps_l2=1e-6,
+                     eps_rms=1e-6, stream=None):
+    """Fused decode layer step (conv -> recurrent update -> gated RMSNorm) for one token per
+    sequence. conv_state bf16 [N, 3, 3, H, 128] and state fp32 [N, H, 128, 128] are updated
+    in place. Returns y fp32 [N, H, 128]."""
+    for name, t in (("x_q", x_q), ("x_k", x_k), ("x_v", x_v), ("conv_state", conv_state)):
+        _need(t, name, torch.bfloat16)
+    for name, t in (("conv_w", conv_w), ("z", z), ("A", A), ("b", b), ("g", g), ("norm_w", norm_w),
+                    ("state", state)):
+        _need(t, name, torch.float32)
+    N, H = x_q.shape[0], x_q.shape[1]
+    if y is None:
+        y = torch.empty((N, H, D), dtype=torch.float32, device=x_q.device)
+    _need(y, "y", torch.float32)
+    rc = library().kda_fused_decode(_ptr(x_q), _ptr(x_k), _ptr(x_v), _ptr(conv_state), _ptr(conv_w), _ptr(z),
+                                    _ptr(A), _ptr(b), _ptr(g), _ptr(norm_w), float(eps_l2), float(eps_rms),
+                                    _ptr(state), _ptr(y), N, H, D, D, _stream(stream))
+    if rc != 0:
+        raise KdaError("kda_fused_decode", rc)
+    return y
 
 
 def kda_chunk_prefill_noalloc(q, k, v, z, A, b, initial_state=None, cu_seqlens=None, cu_seqlens_host=None,

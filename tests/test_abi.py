@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_chunk_prefill_workspace_size",
                      "kda_status_string", "kda_workspace_status", "kda_version",
-                     "kda_chunk_prefill_launch_count", "kda_recurrent_verify", "kda_replay_fold"):
+                     "kda_chunk_prefill_launch_count", "kda_recurrent_verify", "kda_replay_fold", "kda_fused_decode"):
         assert required in names
 
 
@@ -205,3 +205,28 @@ def test_max_replay_constant_matches_header():
     text = open(os.path.join(ROOT, "include", "kda.h")).read()
     m = re.search(r"#define KDA_MAX_REPLAY_TOKENS (\d+)", text)
     assert m and int(m.group(1)) == KDA_MAX_REPLAY == kda.MAX_REPLAY_TOKENS
+
+
+def _fused(**over):
+    args = dict(xq=FAKE, xk=FAKE, xv=FAKE, cs=FAKE, cw=FAKE, z=FAKE, A=FAKE, b=FAKE, g=FAKE, nw=FAKE, e1=1e-6,
+                e2=1e-6, state=FAKE, y=FAKE, num_seqs=4, num_heads=2, d_k=128, d_v=128, stream=None)
+    args.update(over)
+    return kda.library().kda_fused_decode(
+        args["xq"], args["xk"], args["xv"], args["cs"], args["cw"], args["z"], args["A"], args["b"], args["g"],
+        args["nw"], args["e1"], args["e2"], args["state"], args["y"], args["num_seqs"], args["num_heads"],
+        args["d_k"], args["d_v"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d_k=64), KDA_ERR_UNSUPPORTED),
+    (dict(e1=-1.0), KDA_ERR_UNSUPPORTED),
+    (dict(e2=float("nan")), KDA_ERR_UNSUPPORTED),
+    (dict(num_heads=0), KDA_ERR_SHAPE),
+    (dict(cs=None), KDA_ERR_NULL),
+    (dict(nw=None), KDA_ERR_NULL),
+    (dict(cw=FAKE + 4), KDA_ERR_ALIGN),
+    (dict(g=FAKE + 8), KDA_ERR_ALIGN),
+    (dict(num_seqs=0), KDA_OK),
+])
+def test_fused_decode_argument_checks(over, code):
+    assert _fused(**over) == code
