@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     using G = DecodeGeom<CWD>;
     constexpr int LPR = G::LPR, RG = G::RG, RPT = G::RPT;
 
-    __shared__ float s_alpha[kMaxReplay][kD], s_k[kMaxReplay][kD], s_v[kMaxReplay][kD];
+    __shared__ float s_alpha[kMaxReplay][kD], s_k[kMaxReplay][kD];
+    __shared__ __align__(16) float s_v[kMaxReplay][kD];  // read as float4
     __shared__ float s_beta[kMaxReplay];
     __shared__ __align__(16) float s_redp[2][RG][CWD];
 

@@ -51,7 +51,8 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     constexpr int LPR = G::LPR, RG = G::RG, RPT = G::RPT;
     constexpr int NCTA = kD / CWD;  // CTAs per (sequence, head)
 
-    __shared__ float s_alpha[kD], s_k[kD], s_q[kD], s_v[kD];
+    __shared__ float s_alpha[kD], s_k[kD], s_q[kD];
+    __shared__ __align__(16) float s_v[kD];  // read as float4
     __shared__ __align__(16) float s_red[RG][CWD];
     __shared__ float s_sq[2][kD / 32];  // per-warp sums of q^2 and k^2
     __shared__ float s_oo[NCTA];        // per-CTA sums of o^2 (one slot per cluster rank)
