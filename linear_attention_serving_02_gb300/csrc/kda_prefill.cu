@@ -220,46 +220,81 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
 // Phase B: Sin[g + 1] = M[g] Sin[g] + R[g] along each sequence's segments, in fp32 on the
 // CUDA cores (exact accumulation, a short serial chain). One CTA per (sequence, head,
 // 16 value columns); thread t computes row t / 2, columns 8 (t % 2) .. +7 of its slice.
+// M and R do not depend on the chain, so the next step's M (64 KB) and R slice are
+// copied into shared memory (cp.async) while the current step multiplies; the chained
+// slice itself stays in shared memory from one step to the next.
+struct CombineSmem {
+    float m[2][kD][kD + 4];  // rows padded: the 16 rows a warp reads hit distinct banks
+    float r[2][kD][16];
+    float x[kD][16];
+};
+
 __global__ void __launch_bounds__(256)
     kda_combine_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ chains, int32_t H,
                        float *__restrict__ Sin, const float *__restrict__ Mseg, const float *__restrict__ Rseg) {
-    __shared__ __align__(16) float xs[kD][16];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    CombineSmem &s = *reinterpret_cast<CombineSmem *>(smem_raw);
     if (*status != 0) return;
     const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * 16;
     const int g0 = chains[2 * n], S = chains[2 * n + 1];
+    if (S < 3) return;  // no step: segment 1's input state is phase A's R of segment 0
     const int tid = threadIdx.x, row = tid >> 1, cpart = (tid & 1) * 8;
     const size_t seg_stride = (size_t)H * kStateFloats, hoff = (size_t)h * kStateFloats;
-    for (int sg = 1; sg <= S - 2; ++sg) {
-        const float *X = Sin + (size_t)(g0 + sg) * seg_stride + hoff;
+
+    auto stage = [&](int sg, int buf) {
         const float *M = Mseg + (size_t)(g0 + sg) * seg_stride + hoff;
         const float *R = Rseg + (size_t)(g0 + sg) * seg_stride + hoff;
-        float *Y = Sin + (size_t)(g0 + sg + 1) * seg_stride + hoff;
-        *reinterpret_cast<float4 *>(&xs[row][cpart]) = *reinterpret_cast<const float4 *>(X + row * kD + col0 + cpart);
-        *reinterpret_cast<float4 *>(&xs[row][cpart + 4]) =
-            *reinterpret_cast<const float4 *>(X + row * kD + col0 + cpart + 4);
-        __syncthreads();
+        for (int e = tid; e < kD * (kD / 4); e += 256) {
+            const int rr = e / (kD / 4), c4 = (e % (kD / 4)) * 4;
+            cp_async16(&s.m[buf][rr][c4], M + rr * kD + c4);
+        }
+        for (int e = tid; e < kD * 4; e += 256) {
+            const int rr = e / 4, c4 = (e % 4) * 4;
+            cp_async16(&s.r[buf][rr][c4], R + rr * kD + col0 + c4);
+        }
+        cp_async_commit();
+    };
+
+    stage(1, 0);
+    {
+        const float *X = Sin + (size_t)(g0 + 1) * seg_stride + hoff + row * kD + col0 + cpart;
+        *reinterpret_cast<float4 *>(&s.x[row][cpart]) = *reinterpret_cast<const float4 *>(X);
+        *reinterpret_cast<float4 *>(&s.x[row][cpart + 4]) = *reinterpret_cast<const float4 *>(X + 4);
+    }
+    for (int sg = 1; sg <= S - 2; ++sg) {
+        const int buf = (sg - 1) & 1;
+        if (sg + 1 <= S - 2) {
+            stage(sg + 1, buf ^ 1);  // buffer buf ^ 1 was last read before the previous barrier
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // this step's M, R and x are visible
         float acc[8];
-        const float4 r0 = *reinterpret_cast<const float4 *>(R + row * kD + col0 + cpart);
-        const float4 r1 = *reinterpret_cast<const float4 *>(R + row * kD + col0 + cpart + 4);
+        const float4 r0 = *reinterpret_cast<const float4 *>(&s.r[buf][row][cpart]);
+        const float4 r1 = *reinterpret_cast<const float4 *>(&s.r[buf][row][cpart + 4]);
         acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
         acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
-        const float4 *mrow = reinterpret_cast<const float4 *>(M + row * kD);
 #pragma unroll 4
         for (int k4 = 0; k4 < kD / 4; ++k4) {
-            const float4 m = mrow[k4];
+            const float4 m = *reinterpret_cast<const float4 *>(&s.m[buf][row][4 * k4]);
             const float mk[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 x0 = *reinterpret_cast<const float4 *>(&xs[4 * k4 + q][cpart]);
-                const float4 x1 = *reinterpret_cast<const float4 *>(&xs[4 * k4 + q][cpart + 4]);
+                const float4 x0 = *reinterpret_cast<const float4 *>(&s.x[4 * k4 + q][cpart]);
+                const float4 x1 = *reinterpret_cast<const float4 *>(&s.x[4 * k4 + q][cpart + 4]);
                 acc[0] += mk[q] * x0.x; acc[1] += mk[q] * x0.y; acc[2] += mk[q] * x0.z; acc[3] += mk[q] * x0.w;
                 acc[4] += mk[q] * x1.x; acc[5] += mk[q] * x1.y; acc[6] += mk[q] * x1.z; acc[7] += mk[q] * x1.w;
             }
         }
-        *reinterpret_cast<float4 *>(Y + row * kD + col0 + cpart) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4 *>(Y + row * kD + col0 + cpart + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        __threadfence_block();
-        __syncthreads();  // this slice of Y is the next step's X, written by this CTA alone
+        __syncthreads();  // every thread is done with x and with buffer buf
+        const float4 y0 = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        const float4 y1 = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        *reinterpret_cast<float4 *>(&s.x[row][cpart]) = y0;
+        *reinterpret_cast<float4 *>(&s.x[row][cpart + 4]) = y1;
+        float *Y = Sin + (size_t)(g0 + sg + 1) * seg_stride + hoff + row * kD + col0 + cpart;
+        *reinterpret_cast<float4 *>(Y) = y0;
+        *reinterpret_cast<float4 *>(Y + 4) = y1;
     }
 }
 
@@ -964,8 +999,15 @@ cudaError_t launch_segment_plan(const int32_t *status, const int32_t *seq_cu, co
 
 cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
                            const float *Mseg, const float *Rseg, cudaStream_t st) {
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(kda_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)sizeof(CombineSmem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
     dim3 grid((unsigned)N, (unsigned)H, kD / 16);
-    kda_combine_kernel<<<grid, 256, 0, st>>>(status, chains, H, Sin, Mseg, Rseg);
+    kda_combine_kernel<<<grid, 256, sizeof(CombineSmem), st>>>(status, chains, H, Sin, Mseg, Rseg);
     return cudaGetLastError();
 }
 
