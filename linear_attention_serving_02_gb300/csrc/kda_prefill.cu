@@ -301,6 +301,12 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------------
 // intra-chunk kernel
 // ---------------------------------------------------------------------------------
+// named barriers (bar.sync / bar.arrive) over a subset of a CTA's warps
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n));
+}
+
 struct IntraSmem {
     float G[kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay
     float beta[kC];
@@ -366,6 +372,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         else
             *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    cp_async_commit();  // group: z
     for (int e = tid; e < 3 * kC * (kD / 8); e += kIntraThreads) {  // q, k, v: 16 x 16 B per row
         const int which = e / (kC * (kD / 8));
         const int r = e % (kC * (kD / 8));
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         else
             *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
-    cp_async_commit();
+    cp_async_commit();  // group: q, k, v (waited for before the Gram matrices)
     if (tid >= kD && tid < kD + kC) {
         const int i = tid - kD;
         s.beta[i] = (i < L) ? sigmoid_f(bgate[(t0 + i) * H + h]) : 0.f;
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int plane = e / (int)(kPlaneCC / 16), off = e % (int)(kPlaneCC / 16);
         *reinterpret_cast<uint4 *>(rec + kRecAqk + plane * kStackAK + (size_t)off * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    cp_async_wait<0>();
+    cp_async_wait<1>();
     __syncthreads();
 
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
@@ -419,6 +426,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
         __syncthreads();
     }
+
+    cp_async_wait<0>();
+    __syncthreads();  // q, k, v in place
 
     // ---- decayed Gram matrices, one 16-token tile row at a time -----------------
     for (int a = 0; a < kC / kTile; ++a) {
@@ -495,70 +505,101 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         __syncthreads();
     }
 
-    // ---- UT transform: T = (I + A_kk)^-1, unit lower triangular -----------------
-    // diagonal 16x16 blocks by forward substitution: warp a solves block a, lane j (and
-    // j + 16, a duplicate) its column j, in registers; row i reads A[i][*] as a broadcast
-    if (warp < 4) {
-        const int base = warp * kTile, j = lane & 15;
-        float x[kTile];
+    // ---- UT transform on warps 0-7: T = (I + A_kk)^-1, unit lower triangular. -----
+    // ---- Meanwhile warps 8-15 write Qhat, Kend^T and gamma to the record and build -
+    // ---- the Khat operand planes: they need only q, k and G. -----------------------
+    if (warp < 8) {
+        // diagonal 16x16 blocks by forward substitution: warp a solves block a, lane j
+        // (and j + 16, a duplicate) its column j, in registers; row i reads A[i][*] as a
+        // broadcast. Warps 4-7 zero the blocks above the diagonal.
+        if (warp < 4) {
+            const int base = warp * kTile, j = lane & 15;
+            float x[kTile];
 #pragma unroll
-        for (int i = 0; i < kTile; ++i) {
-            float acc = 0.f;
+            for (int i = 0; i < kTile; ++i) {
+                float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < i; ++m) acc += s.Akk[base + i][base + m] * x[m];  // x[m] = 0 for m < j
-            x[i] = (i < j) ? 0.f : ((i == j) ? 1.f : -acc);
+                for (int m = 0; m < i; ++m) acc += s.Akk[base + i][base + m] * x[m];  // x[m] = 0 for m < j
+                x[i] = (i < j) ? 0.f : ((i == j) ? 1.f : -acc);
+            }
+            if (lane < kTile) {
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) s.T[base + i][base + j] = x[i];
+            }
+        } else {
+            for (int e = tid - 128; e < kC * kC; e += 128) {
+                const int i = e / kC, j = e % kC;
+                if ((j >> 4) > (i >> 4)) s.T[i][j] = 0.f;
+            }
         }
-        if (lane < kTile) {
+        named_sync(1, 256);
+        // off-diagonal blocks by distance l: T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb
+        for (int l = 1; l < kC / kTile; ++l) {
+            const int nblk = kC / kTile - l;
+            for (int e = tid; e < nblk * kTile * kTile; e += 256) {
+                const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                const int b = blk, a = b + l;
+                float acc = 0.f;
+                for (int m = b; m < a; ++m)
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) s.T[base + i][base + j] = x[i];
+                    for (int x = 0; x < kTile; ++x)
+                        acc += s.Akk[a * kTile + rr][m * kTile + x] * s.T[m * kTile + x][b * kTile + cc];
+                s.X[blk][rr][cc] = acc;
+            }
+            named_sync(1, 256);
+            for (int e = tid; e < nblk * kTile * kTile; e += 256) {
+                const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                const int b = blk, a = b + l;
+                float acc = 0.f;
+#pragma unroll
+                for (int x = 0; x < kTile; ++x) acc += s.T[a * kTile + rr][a * kTile + x] * s.X[blk][x][cc];
+                s.T[a * kTile + rr][b * kTile + cc] = -acc;
+            }
+            named_sync(1, 256);
         }
     } else {
-        // zero the blocks above the diagonal
-        for (int e = tid - 128; e < kC * kC; e += kIntraThreads - 128) {
-            const int i = e / kC, j = e % kC;
-            if ((j >> 4) > (i >> 4)) s.T[i][j] = 0.f;
+        const int t2 = tid - 256;
+        // Khat = k * exp(G), split: the B operand of W (the Gram operands are dead)
+        for (int e = t2; e < kC * (kD / 2); e += 256) {
+            const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
+            const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
+            uint32_t hi, lo;
+            split_bf16x2(kk.x * __expf(s.G[i][c]), kk.y * __expf(s.G[i][c + 1]), hi, lo);
+            *reinterpret_cast<uint32_t *>(&s.u.w.kh[0][i][c]) = hi;
+            *reinterpret_cast<uint32_t *>(&s.u.w.kh[1][i][c]) = lo;
         }
+        uint8_t *Qh = rec + kRecQh;
+        for (int e = t2; e < kC * (kD / 2); e += 256) {
+            const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
+            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
+            uint32_t hi, lo;
+            split_bf16x2(qq.x * __expf(s.G[i][c]), qq.y * __expf(s.G[i][c + 1]), hi, lo);
+            *reinterpret_cast<uint32_t *>(Qh + il_off(i, c, kD)) = hi;
+            *reinterpret_cast<uint32_t *>(Qh + kStackWQ + il_off(i, c, kD)) = lo;
+        }
+        uint8_t *KeT = rec + kRecKeT;
+        for (int e = t2; e < kD * (kC / 2); e += 256) {
+            const int c = e % kD, j = (e / kD) * 2;  // consecutive threads: consecutive channels
+            const float k0 = __bfloat162float(s.ks[j][c]);
+            const float k1 = __bfloat162float(s.ks[j + 1][c]);
+            const float gl = s.G[kC - 1][c];
+            uint32_t hi, lo;
+            split_bf16x2(k0 * __expf(gl - s.G[j][c]), k1 * __expf(gl - s.G[j + 1][c]), hi, lo);
+            *reinterpret_cast<uint32_t *>(KeT + il_off(c, j, kC)) = hi;
+            *reinterpret_cast<uint32_t *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
+        }
+        float *gam = reinterpret_cast<float *>(rec + kRecGam);
+        if (t2 < kD) gam[t2] = expf(s.G[kC - 1][t2]);
     }
     __syncthreads();
-    // off-diagonal blocks by distance l: T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb
-    for (int l = 1; l < kC / kTile; ++l) {
-        const int nblk = kC / kTile - l;
-        for (int e = tid; e < nblk * kTile * kTile; e += kIntraThreads) {
-            const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            const int b = blk, a = b + l;
-            float acc = 0.f;
-            for (int m = b; m < a; ++m)
-#pragma unroll
-                for (int x = 0; x < kTile; ++x) acc += s.Akk[a * kTile + rr][m * kTile + x] * s.T[m * kTile + x][b * kTile + cc];
-            s.X[blk][rr][cc] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < nblk * kTile * kTile; e += kIntraThreads) {
-            const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            const int b = blk, a = b + l;
-            float acc = 0.f;
-#pragma unroll
-            for (int x = 0; x < kTile; ++x) acc += s.T[a * kTile + rr][a * kTile + x] * s.X[blk][x][cc];
-            s.T[a * kTile + rr][b * kTile + cc] = -acc;
-        }
-        __syncthreads();
-    }
 
-    // ---- operands of W and U': T' = T Diag(beta), Khat = k * exp(G), V ------------
+    // ---- the other W / U' operand: T' = T Diag(beta), split -----------------------
     for (int e = tid; e < kC * (kC / 2); e += kIntraThreads) {
         const int i = e / (kC / 2), j = (e % (kC / 2)) * 2;
         uint32_t hi, lo;
         split_bf16x2(s.T[i][j] * s.beta[j], s.T[i][j + 1] * s.beta[j + 1], hi, lo);
         *reinterpret_cast<uint32_t *>(&s.u.w.t[0][i][j]) = hi;
         *reinterpret_cast<uint32_t *>(&s.u.w.t[1][i][j]) = lo;
-    }
-    for (int e = tid; e < kC * (kD / 2); e += kIntraThreads) {
-        const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
-        const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
-        uint32_t hi, lo;
-        split_bf16x2(kk.x * __expf(s.G[i][c]), kk.y * __expf(s.G[i][c + 1]), hi, lo);
-        *reinterpret_cast<uint32_t *>(&s.u.w.kh[0][i][c]) = hi;
-        *reinterpret_cast<uint32_t *>(&s.u.w.kh[1][i][c]) = lo;
     }
     __syncthreads();
 
@@ -620,32 +661,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 }
         }
     }
-
-    // ---- Qhat, Kend^T, A_qk, gamma (elementwise) --------------------------------
-    {
-        uint8_t *Qh = rec + kRecQh;
-        for (int e = tid; e < kC * (kD / 2); e += kIntraThreads) {
-            const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
-            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
-            uint32_t hi, lo;
-            split_bf16x2(qq.x * __expf(s.G[i][c]), qq.y * __expf(s.G[i][c + 1]), hi, lo);
-            *reinterpret_cast<uint32_t *>(Qh + il_off(i, c, kD)) = hi;
-            *reinterpret_cast<uint32_t *>(Qh + kStackWQ + il_off(i, c, kD)) = lo;
-        }
-        uint8_t *KeT = rec + kRecKeT;
-        for (int e = tid; e < kD * (kC / 2); e += kIntraThreads) {
-            const int c = e % kD, j = (e / kD) * 2;  // consecutive threads: consecutive channels
-            const float k0 = __bfloat162float(s.ks[j][c]);
-            const float k1 = __bfloat162float(s.ks[j + 1][c]);
-            const float gl = s.G[kC - 1][c];
-            uint32_t hi, lo;
-            split_bf16x2(k0 * __expf(gl - s.G[j][c]), k1 * __expf(gl - s.G[j + 1][c]), hi, lo);
-            *reinterpret_cast<uint32_t *>(KeT + il_off(c, j, kC)) = hi;
-            *reinterpret_cast<uint32_t *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
-        }
-        float *gam = reinterpret_cast<float *>(rec + kRecGam);
-        if (tid < kD) gam[tid] = expf(s.G[kC - 1][tid]);
-    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -690,10 +705,6 @@ constexpr int kWalkThreads = 256;
 constexpr uint32_t kWalkTmemCols = 512;  // D_U [0,64) D_O1 [64,128) D_O2 [128,192) D_S [192,320)
 constexpr int kBarOR = 2, kBarU = 3;
 
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
-__device__ __forceinline__ void named_arrive(int id, int n) {
-    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n));
-}
 
 // 8 consecutive fp32 values -> one 16-byte chunk of the hi plane and one of the lo plane
 __device__ __forceinline__ void split8_store(const float *x, unsigned char *hi_plane, unsigned char *lo_plane,
@@ -912,11 +923,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
+            // the next [ -W ; Qhat ] copy starts as soon as group 1 of this chunk is done
+            // with the buffer, before the U epilogue
+            if (issuer && c + 1 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_wq(c + 1);
+            __syncwarp();
             named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
-            if (issuer) {
-                if (c + 1 < c_end && !fail) issue_wq(c + 1);  // group 1 is done with [ -W ; Qhat ]
-                issue_g2(c);
-            }
+            if (issuer) issue_g2(c);
             __syncwarp();
             const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
             if (issuer && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
