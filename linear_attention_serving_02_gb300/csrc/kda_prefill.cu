@@ -568,25 +568,39 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             *reinterpret_cast<uint32_t *>(&s.u.w.kh[0][i][c]) = hi;
             *reinterpret_cast<uint32_t *>(&s.u.w.kh[1][i][c]) = lo;
         }
+        // Qhat and Kend^T: each thread makes one 16-byte row of a core matrix (8 values
+        // along K) for the hi and the lo plane, and consecutive threads fill consecutive
+        // 16-byte chunks of the record, so every warp store covers 512 contiguous bytes
         uint8_t *Qh = rec + kRecQh;
-        for (int e = t2; e < kC * (kD / 2); e += 256) {
-            const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
-            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
-            uint32_t hi, lo;
-            split_bf16x2(qq.x * __expf(s.G[i][c]), qq.y * __expf(s.G[i][c + 1]), hi, lo);
-            *reinterpret_cast<uint32_t *>(Qh + il_off(i, c, kD)) = hi;
-            *reinterpret_cast<uint32_t *>(Qh + kStackWQ + il_off(i, c, kD)) = lo;
+        for (int e = t2; e < kC * (kD / 8); e += 256) {
+            const int c8 = (e >> 3) & 15, i = (e >> 7) * 8 + (e & 7), c = c8 * 8;
+            const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[i][c]);
+            const float4 g0 = *reinterpret_cast<const float4 *>(&s.G[i][c]);
+            const float4 g1 = *reinterpret_cast<const float4 *>(&s.G[i][c + 4]);
+            const float2 q01 = bf16x2_to_float2(qraw.x), q23 = bf16x2_to_float2(qraw.y);
+            const float2 q45 = bf16x2_to_float2(qraw.z), q67 = bf16x2_to_float2(qraw.w);
+            uint4 hi, lo;
+            split_bf16x2(q01.x * __expf(g0.x), q01.y * __expf(g0.y), hi.x, lo.x);
+            split_bf16x2(q23.x * __expf(g0.z), q23.y * __expf(g0.w), hi.y, lo.y);
+            split_bf16x2(q45.x * __expf(g1.x), q45.y * __expf(g1.y), hi.z, lo.z);
+            split_bf16x2(q67.x * __expf(g1.z), q67.y * __expf(g1.w), hi.w, lo.w);
+            *reinterpret_cast<uint4 *>(Qh + il_off(i, c, kD)) = hi;
+            *reinterpret_cast<uint4 *>(Qh + kStackWQ + il_off(i, c, kD)) = lo;
         }
         uint8_t *KeT = rec + kRecKeT;
-        for (int e = t2; e < kD * (kC / 2); e += 256) {
-            const int c = e % kD, j = (e / kD) * 2;  // consecutive threads: consecutive channels
-            const float k0 = __bfloat162float(s.ks[j][c]);
-            const float k1 = __bfloat162float(s.ks[j + 1][c]);
+        for (int e = t2; e < kD * (kC / 8); e += 256) {
+            const int j8 = (e >> 3) & 7, c = (e >> 6) * 8 + (e & 7), j = j8 * 8;
             const float gl = s.G[kC - 1][c];
-            uint32_t hi, lo;
-            split_bf16x2(k0 * __expf(gl - s.G[j][c]), k1 * __expf(gl - s.G[j + 1][c]), hi, lo);
-            *reinterpret_cast<uint32_t *>(KeT + il_off(c, j, kC)) = hi;
-            *reinterpret_cast<uint32_t *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
+            float x[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) x[m] = __bfloat162float(s.ks[j + m][c]) * __expf(gl - s.G[j + m][c]);
+            uint4 hi, lo;
+            split_bf16x2(x[0], x[1], hi.x, lo.x);
+            split_bf16x2(x[2], x[3], hi.y, lo.y);
+            split_bf16x2(x[4], x[5], hi.z, lo.z);
+            split_bf16x2(x[6], x[7], hi.w, lo.w);
+            *reinterpret_cast<uint4 *>(KeT + il_off(c, j, kC)) = hi;
+            *reinterpret_cast<uint4 *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
         }
         float *gam = reinterpret_cast<float *>(rec + kRecGam);
         if (t2 < kD) gam[t2] = expf(s.G[kC - 1][t2]);
