@@ -30,6 +30,8 @@
 // factor is <= 1; the second is <= 1 for j <= r and at most e^75 (15 tokens of at most
 // -5 each, §5.4 of the blog) inside the diagonal tile, within bf16/fp32 range.
 
+#include <algorithm>
+
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
 
@@ -308,7 +310,8 @@ __device__ __forceinline__ void named_arrive(int id, int n) {
 }
 
 struct IntraSmem {
-    float G[kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay
+    float G[2][kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay; the
+                             // other buffer receives the next chunk's z meanwhile
     float beta[kC];
     float Akk[kC][kC + 1];
     float T[kC][kC + 1];
@@ -353,26 +356,51 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int slot = blockIdx.x, h = blockIdx.y;
     if (*status != 0 || N <= 0) return;
-    if (slot >= chunk_off[N]) return;
-    const int n = find_seq(chunk_off, N, slot);
-    const int64_t t0 = (int64_t)seq_cu[n] + (int64_t)(slot - chunk_off[n]) * kC;
-    const int L = (int)min((int64_t)kC, (int64_t)seq_cu[n + 1] - t0);
+    // persistent: CTA b takes items b, b + gridDim.x, ...; item = slot * H + h
+    const int n_items = chunk_off[N] * H;
+    int item = blockIdx.x;
+    if (item >= n_items) return;
     const int64_t rowstride = (int64_t)H * kD;  // elements between consecutive tokens
-    const int64_t hoff = (int64_t)h * kD;
-    uint8_t *rec = records + ((int64_t)slot * H + h) * (int64_t)kRecBytes;
 
-    // ---- stage z, q, k, v of the chunk in shared memory (all requests in flight at once) ----
-    for (int e = tid; e < kC * (kD / 4); e += kIntraThreads) {  // z: 32 x 16 B per row
-        const int i = e / (kD / 4), c = (e % (kD / 4)) * 4;
-        float *dst = &s.G[i][c];
-        if (i < L)
-            cp_async16(dst, z + (t0 + i) * rowstride + hoff + c);
-        else
-            *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    cp_async_commit();  // group: z
+    struct Item {
+        int slot, h;
+        int64_t t0;
+        int L;
+    };
+    auto item_of = [&](int it) {
+        Item r;
+        r.slot = it / H;
+        r.h = it % H;
+        const int n = find_seq(chunk_off, N, r.slot);
+        r.t0 = (int64_t)seq_cu[n] + (int64_t)(r.slot - chunk_off[n]) * kC;
+        r.L = (int)min((int64_t)kC, (int64_t)seq_cu[n + 1] - r.t0);
+        return r;
+    };
+    // z of an item into a G buffer (rows past the sequence end are zero), as one copy group
+    auto stage_z = [&](const Item &it, float (*Gd)[kD + 4]) {
+        for (int e = tid; e < kC * (kD / 4); e += kIntraThreads) {  // 32 x 16 B per row
+            const int i = e / (kD / 4), c = (e % (kD / 4)) * 4;
+            float *dst = &Gd[i][c];
+            if (i < it.L)
+                cp_async16(dst, z + (it.t0 + i) * rowstride + (int64_t)it.h * kD + c);
+            else
+                *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        cp_async_commit();
+    };
+
+    Item cur = item_of(item);
+    stage_z(cur, s.G[0]);
+    for (int iter = 0; item < n_items; ++iter, item += gridDim.x) {
+    float(*G)[kD + 4] = s.G[iter & 1];
+    const int h = cur.h;
+    const int64_t t0 = cur.t0;
+    const int L = cur.L;
+    const int64_t hoff = (int64_t)h * kD;
+    uint8_t *rec = records + ((int64_t)cur.slot * H + h) * (int64_t)kRecBytes;
+
+    // ---- stage q, k, v of this chunk, and z of the next one (its buffer is free) ----
     for (int e = tid; e < 3 * kC * (kD / 8); e += kIntraThreads) {  // q, k, v: 16 x 16 B per row
         const int which = e / (kC * (kD / 8));
         const int r = e % (kC * (kD / 8));
@@ -385,6 +413,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
     cp_async_commit();  // group: q, k, v (waited for before the Gram matrices)
+    Item nxt = cur;
+    if (item + (int)gridDim.x < n_items) {
+        nxt = item_of(item + gridDim.x);
+        stage_z(nxt, s.G[(iter + 1) & 1]);
+    } else {
+        cp_async_commit();  // an empty group keeps the group arithmetic below uniform
+    }
     if (tid >= kD && tid < kD + kC) {
         const int i = tid - kD;
         s.beta[i] = (i < L) ? sigmoid_f(bgate[(t0 + i) * H + h]) : 0.f;
@@ -396,7 +431,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int plane = e / (int)(kPlaneCC / 16), off = e % (int)(kPlaneCC / 16);
         *reinterpret_cast<uint4 *>(rec + kRecAqk + plane * kStackAK + (size_t)off * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    cp_async_wait<1>();
+    cp_async_wait<2>();  // this chunk's z (q, k, v and the next z may still be in flight)
     __syncthreads();
 
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
@@ -404,7 +439,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const float eA = expf(A[h]);
         for (int e = tid; e < kC * kD; e += kIntraThreads) {
             const int i = e / kD, c = e % kD;
-            s.G[i][c] = (i < L) ? gate_log_decay(eA, s.G[i][c]) : 0.f;
+            G[i][c] = (i < L) ? gate_log_decay(eA, G[i][c]) : 0.f;
         }
         __syncthreads();
         // column scan: thread (c, quarter) sums its 16 rows, then adds the totals of the
@@ -413,22 +448,22 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         float acc = 0.f;
 #pragma unroll
         for (int i = qt * 16; i < qt * 16 + 16; ++i) {
-            acc += s.G[i][c];
-            s.G[i][c] = acc;
+            acc += G[i][c];
+            G[i][c] = acc;
         }
         __syncthreads();
         float below = 0.f;
-        for (int p = 0; p < qt; ++p) below += s.G[p * 16 + 15][c];
+        for (int p = 0; p < qt; ++p) below += G[p * 16 + 15][c];
         __syncthreads();
         if (qt > 0) {
 #pragma unroll
-            for (int i = qt * 16; i < qt * 16 + 16; ++i) s.G[i][c] += below;
+            for (int i = qt * 16; i < qt * 16 + 16; ++i) G[i][c] += below;
         }
         __syncthreads();
     }
 
-    cp_async_wait<0>();
-    __syncthreads();  // q, k, v in place
+    cp_async_wait<1>();
+    __syncthreads();  // q, k, v in place (the next chunk's z may still be in flight)
 
     // ---- decayed Gram matrices, one 16-token tile row at a time -----------------
     for (int a = 0; a < kC / kTile; ++a) {
@@ -437,8 +472,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // A operands: q and k of the tile row share the factor exp(G_i - G_r)
         for (int e = tid; e < kTile * (kD / 2); e += kIntraThreads) {
             const int row = e / (kD / 2), c = (e % (kD / 2)) * 2, i = r + row;
-            const float2 g = *reinterpret_cast<const float2 *>(&s.G[i][c]);
-            const float2 gr = *reinterpret_cast<const float2 *>(&s.G[r][c]);
+            const float2 g = *reinterpret_cast<const float2 *>(&G[i][c]);
+            const float2 gr = *reinterpret_cast<const float2 *>(&G[r][c]);
             const float f0 = __expf(g.x - gr.x), f1 = __expf(g.y - gr.y);
             const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
             const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
@@ -453,8 +488,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // B operand: keys j = 0 .. r+15 with the factor exp(G_r - G_j)
         for (int e = tid; e < nb * (kD / 2); e += kIntraThreads) {
             const int j = e / (kD / 2), c = (e % (kD / 2)) * 2;
-            const float2 g = *reinterpret_cast<const float2 *>(&s.G[j][c]);
-            const float2 gr = *reinterpret_cast<const float2 *>(&s.G[r][c]);
+            const float2 g = *reinterpret_cast<const float2 *>(&G[j][c]);
+            const float2 gr = *reinterpret_cast<const float2 *>(&G[r][c]);
             const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[j][c]));
             uint32_t hi, lo;
             split_bf16x2(kk.x * __expf(gr.x - g.x), kk.y * __expf(gr.y - g.y), hi, lo);
@@ -564,7 +599,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
             const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
             uint32_t hi, lo;
-            split_bf16x2(kk.x * __expf(s.G[i][c]), kk.y * __expf(s.G[i][c + 1]), hi, lo);
+            split_bf16x2(kk.x * __expf(G[i][c]), kk.y * __expf(G[i][c + 1]), hi, lo);
             *reinterpret_cast<uint32_t *>(&s.u.w.kh[0][i][c]) = hi;
             *reinterpret_cast<uint32_t *>(&s.u.w.kh[1][i][c]) = lo;
         }
@@ -575,8 +610,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         for (int e = t2; e < kC * (kD / 8); e += 256) {
             const int c8 = (e >> 3) & 15, i = (e >> 7) * 8 + (e & 7), c = c8 * 8;
             const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[i][c]);
-            const float4 g0 = *reinterpret_cast<const float4 *>(&s.G[i][c]);
-            const float4 g1 = *reinterpret_cast<const float4 *>(&s.G[i][c + 4]);
+            const float4 g0 = *reinterpret_cast<const float4 *>(&G[i][c]);
+            const float4 g1 = *reinterpret_cast<const float4 *>(&G[i][c + 4]);
             const float2 q01 = bf16x2_to_float2(qraw.x), q23 = bf16x2_to_float2(qraw.y);
             const float2 q45 = bf16x2_to_float2(qraw.z), q67 = bf16x2_to_float2(qraw.w);
             uint4 hi, lo;
@@ -590,10 +625,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         uint8_t *KeT = rec + kRecKeT;
         for (int e = t2; e < kD * (kC / 8); e += 256) {
             const int j8 = (e >> 3) & 7, c = (e >> 6) * 8 + (e & 7), j = j8 * 8;
-            const float gl = s.G[kC - 1][c];
+            const float gl = G[kC - 1][c];
             float x[8];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) x[m] = __bfloat162float(s.ks[j + m][c]) * __expf(gl - s.G[j + m][c]);
+            for (int m = 0; m < 8; ++m) x[m] = __bfloat162float(s.ks[j + m][c]) * __expf(gl - G[j + m][c]);
             uint4 hi, lo;
             split_bf16x2(x[0], x[1], hi.x, lo.x);
             split_bf16x2(x[2], x[3], hi.y, lo.y);
@@ -603,7 +638,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             *reinterpret_cast<uint4 *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
         }
         float *gam = reinterpret_cast<float *>(rec + kRecGam);
-        if (t2 < kD) gam[t2] = expf(s.G[kC - 1][t2]);
+        if (t2 < kD) gam[t2] = expf(G[kC - 1][t2]);
     }
     __syncthreads();
 
@@ -675,6 +710,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 }
         }
     }
+    __syncthreads();  // this chunk's shared memory is free for the next one
+    cur = nxt;
+    }
+    cp_async_wait<0>();  // nothing left in flight (the last group is empty)
 }
 
 // ---------------------------------------------------------------------------------
@@ -1040,7 +1079,7 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                          const float *A, const float *b, const int32_t *status, const int32_t *seq_cu,
                          const int32_t *chunk_off, int32_t N, int32_t H, int64_t nslots, uint8_t *records,
-                         cudaStream_t st) {
+                         int num_sms, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kda_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1049,7 +1088,9 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
         configured = true;
     }
     if (nslots <= 0) return cudaSuccess;
-    dim3 grid((unsigned)nslots, (unsigned)H);
+    // persistent: one CTA per SM (the shared memory allows no more) walks the items
+    const int64_t items = nslots * H;
+    const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)num_sms);
     kda_intra_kernel<<<grid, kIntraThreads, sizeof(IntraSmem), st>>>(q, k, v, z, A, b, status, seq_cu, chunk_off, N,
                                                                      H, records);
     return cudaGetLastError();
