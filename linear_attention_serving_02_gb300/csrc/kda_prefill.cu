@@ -390,36 +390,42 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         cp_async_commit();
     };
 
+    // q and k (one copy group) and v (another) of an item; rows past the end are zero
+    auto stage_rows = [&](const Item &it, int first, int count) {
+        for (int e = tid; e < count * kC * (kD / 8); e += kIntraThreads) {  // 16 x 16 B per row
+            const int which = first + e / (kC * (kD / 8));
+            const int r = e % (kC * (kD / 8));
+            const int i = r / (kD / 8), c = (r % (kD / 8)) * 8;
+            const __nv_bfloat16 *src = which == 0 ? q : (which == 1 ? k : v);
+            __nv_bfloat16 *dst = which == 0 ? &s.qs[i][c] : (which == 1 ? &s.ks[i][c] : &s.vs[i][c]);
+            if (i < it.L)
+                cp_async16(dst, src + (it.t0 + i) * rowstride + (int64_t)it.h * kD + c);
+            else
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        cp_async_commit();
+    };
+
+    // Copy groups in flight at the top of every iteration, oldest first: this chunk's z,
+    // its q and k, its v; then the next chunk's z is added. The next chunk's q and k are
+    // issued once this chunk no longer reads them (after the UT phase), its v at the end.
     Item cur = item_of(item);
     stage_z(cur, s.G[0]);
+    stage_rows(cur, 0, 2);
+    stage_rows(cur, 2, 1);
     for (int iter = 0; item < n_items; ++iter, item += gridDim.x) {
     float(*G)[kD + 4] = s.G[iter & 1];
     const int h = cur.h;
     const int64_t t0 = cur.t0;
     const int L = cur.L;
-    const int64_t hoff = (int64_t)h * kD;
     uint8_t *rec = records + ((int64_t)cur.slot * H + h) * (int64_t)kRecBytes;
+    const bool has_next = item + (int)gridDim.x < n_items;
+    const Item nxt = has_next ? item_of(item + gridDim.x) : cur;
+    if (has_next)
+        stage_z(nxt, s.G[(iter + 1) & 1]);  // its buffer was last read by the previous chunk
+    else
+        cp_async_commit();  // an empty group keeps the group arithmetic uniform
 
-    // ---- stage q, k, v of this chunk, and z of the next one (its buffer is free) ----
-    for (int e = tid; e < 3 * kC * (kD / 8); e += kIntraThreads) {  // q, k, v: 16 x 16 B per row
-        const int which = e / (kC * (kD / 8));
-        const int r = e % (kC * (kD / 8));
-        const int i = r / (kD / 8), c = (r % (kD / 8)) * 8;
-        const __nv_bfloat16 *src = which == 0 ? q : (which == 1 ? k : v);
-        __nv_bfloat16 *dst = which == 0 ? &s.qs[i][c] : (which == 1 ? &s.ks[i][c] : &s.vs[i][c]);
-        if (i < L)
-            cp_async16(dst, src + (t0 + i) * rowstride + hoff + c);
-        else
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    cp_async_commit();  // group: q, k, v (waited for before the Gram matrices)
-    Item nxt = cur;
-    if (item + (int)gridDim.x < n_items) {
-        nxt = item_of(item + gridDim.x);
-        stage_z(nxt, s.G[(iter + 1) & 1]);
-    } else {
-        cp_async_commit();  // an empty group keeps the group arithmetic below uniform
-    }
     if (tid >= kD && tid < kD + kC) {
         const int i = tid - kD;
         s.beta[i] = (i < L) ? sigmoid_f(bgate[(t0 + i) * H + h]) : 0.f;
@@ -431,7 +437,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int plane = e / (int)(kPlaneCC / 16), off = e % (int)(kPlaneCC / 16);
         *reinterpret_cast<uint4 *>(rec + kRecAqk + plane * kStackAK + (size_t)off * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    cp_async_wait<2>();  // this chunk's z (q, k, v and the next z may still be in flight)
+    cp_async_wait<3>();  // this chunk's z
     __syncthreads();
 
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
@@ -641,6 +647,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         if (t2 < kD) gam[t2] = expf(G[kC - 1][t2]);
     }
     __syncthreads();
+    // q and k are read no more: the next chunk's come in behind the remaining phases
+    if (has_next)
+        stage_rows(nxt, 0, 2);
+    else
+        cp_async_commit();
 
     // ---- the other W / U' operand: T' = T Diag(beta), split -----------------------
     for (int e = tid; e < kC * (kC / 2); e += kIntraThreads) {
@@ -711,6 +722,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
     }
     __syncthreads();  // this chunk's shared memory is free for the next one
+    if (has_next)
+        stage_rows(nxt, 2, 1);  // v
+    else
+        cp_async_commit();
     cur = nxt;
     }
     cp_async_wait<0>();  // nothing left in flight (the last group is empty)
