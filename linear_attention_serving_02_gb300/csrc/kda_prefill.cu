@@ -313,9 +313,9 @@ struct IntraSmem {
     float G[2][kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay; the
                              // other buffer receives the next chunk's z meanwhile
     float beta[kC];
-    float Akk[kC][kC + 1];
-    float T[kC][kC + 1];
-    float X[3][kTile][kTile + 1];  // off-diagonal block products of the solve
+    float Akk[kC][kC + 4];         // rows 16-byte aligned for float4 reads; the 4-float pad
+    float T[kC][kC + 4];           // puts 8 consecutive rows on distinct banks
+    float X[3][kTile][kTile];      // off-diagonal block products of the solve
     __nv_bfloat16 qs[kC][kLd128];  // the chunk's q, k, v (rows past the sequence end are zero)
     __nv_bfloat16 ks[kC][kLd128];
     __nv_bfloat16 vs[kC][kLd128];
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int i = tid - kD;
         s.beta[i] = (i < L) ? sigmoid_f(bgate[(t0 + i) * H + h]) : 0.f;
     }
-    for (int e = tid; e < kC * (kC + 1); e += kIntraThreads) (&s.Akk[0][0])[e] = 0.f;
+    for (int e = tid; e < kC * (kC + 4); e += kIntraThreads) (&s.Akk[0][0])[e] = 0.f;
     // A_qk goes to the record straight from the MMA fragments; the blocks above the
     // diagonal stay zero (ordered before those stores by the barriers in between)
     for (int e = tid; e < (int)(2 * kPlaneCC / 16); e += kIntraThreads) {  // the hi and the lo plane
@@ -574,27 +574,44 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             }
         }
         named_sync(1, 256);
-        // off-diagonal blocks by distance l: T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb
+        // off-diagonal blocks by distance l: T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb.
+        // Thread (block, row rr, column quad cq) makes four outputs, reading a float4 of
+        // A along k and a float4 of T per k: about one shared load per three FMAs.
         for (int l = 1; l < kC / kTile; ++l) {
             const int nblk = kC / kTile - l;
-            for (int e = tid; e < nblk * kTile * kTile; e += 256) {
-                const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int b = blk, a = b + l;
-                float acc = 0.f;
-                for (int m = b; m < a; ++m)
+            const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = (tid & 3) * 4;
+            const int b = blk, a = b + l;
+            if (tid < nblk * 64) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int m = b; m < a; ++m) {
 #pragma unroll
-                    for (int x = 0; x < kTile; ++x)
-                        acc += s.Akk[a * kTile + rr][m * kTile + x] * s.T[m * kTile + x][b * kTile + cc];
-                s.X[blk][rr][cc] = acc;
+                    for (int x4 = 0; x4 < kTile; x4 += 4) {
+                        const float4 av = *reinterpret_cast<const float4 *>(&s.Akk[a * kTile + rr][m * kTile + x4]);
+                        const float am[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float4 tv = *reinterpret_cast<const float4 *>(&s.T[m * kTile + x4 + u][b * kTile + cq]);
+                            acc.x += am[u] * tv.x; acc.y += am[u] * tv.y; acc.z += am[u] * tv.z; acc.w += am[u] * tv.w;
+                        }
+                    }
+                }
+                *reinterpret_cast<float4 *>(&s.X[blk][rr][cq]) = acc;
             }
             named_sync(1, 256);
-            for (int e = tid; e < nblk * kTile * kTile; e += 256) {
-                const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int b = blk, a = b + l;
-                float acc = 0.f;
+            if (tid < nblk * 64) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int x = 0; x < kTile; ++x) acc += s.T[a * kTile + rr][a * kTile + x] * s.X[blk][x][cc];
-                s.T[a * kTile + rr][b * kTile + cc] = -acc;
+                for (int x4 = 0; x4 < kTile; x4 += 4) {
+                    const float4 tv = *reinterpret_cast<const float4 *>(&s.T[a * kTile + rr][a * kTile + x4]);
+                    const float tm[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 xv = *reinterpret_cast<const float4 *>(&s.X[blk][x4 + u][cq]);
+                        acc.x += tm[u] * xv.x; acc.y += tm[u] * xv.y; acc.z += tm[u] * xv.z; acc.w += tm[u] * xv.w;
+                    }
+                }
+                *reinterpret_cast<float4 *>(&s.T[a * kTile + rr][b * kTile + cq]) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
             }
             named_sync(1, 256);
         }
