@@ -468,8 +468,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         __syncthreads();
     }
 
-    cp_async_wait<1>();
-    __syncthreads();  // q, k, v in place (the next chunk's z may still be in flight)
+    cp_async_wait<2>();
+    __syncthreads();  // q and k in place (v and the next chunk's z may still be in flight)
 
     // ---- decayed Gram matrices, one 16-token tile row at a time -----------------
     for (int a = 0; a < kC / kTile; ++a) {
@@ -678,7 +678,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         *reinterpret_cast<uint32_t *>(&s.u.w.t[0][i][j]) = hi;
         *reinterpret_cast<uint32_t *>(&s.u.w.t[1][i][j]) = lo;
     }
-    __syncthreads();
+    // groups in flight: this chunk's v, the next chunk's z, its q and k
+    cp_async_wait<2>();
+    __syncthreads();  // v in place too
 
     // ---- W = T' Khat (split x split), U' = T' V (split x exact bf16) ------------
     // warp w owns output columns 16 (w % 8) .. +15; the two halves of the warps split the
