@@ -132,13 +132,14 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
 // ---------------------------------------------------------------------------------
 // segmented walk: tables of the three phases (one thread; used only when there are few
 // sequences). Segment g of the batch is segment sigma of sequence n, g = seg_base[n] + sigma.
-//   phase A  segment 0 from the initial state, writing o -> Sin[g0 + 1] (the next input,
-//            or the final state when the sequence has one segment)
+//   phase A  segment 0 from the initial state -> Sin[g0 + 1] (the next input); with one
+//            segment, the whole walk with o and the final state instead
 //            segment sigma (1 .. S-2) from zero     -> R[g],  with U'
 //            segment sigma (1 .. S-2) from identity -> M[g],  without U'
+//            (walks without outputs read only -W and Kend^T of the records)
 //   phase B  Sin[g + 1] = M[g] Sin[g] + R[g]  for sigma = 1 .. S-2 (kda_combine_kernel)
-//   phase C  segments 1 .. S-1 from their input states Sin[g], writing o; the last one
-//            writes the final state
+//   phase C  segments 0 .. S-1 from their input states, writing o; the last one writes
+//            the final state
 // ---------------------------------------------------------------------------------
 __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
                                         const int32_t *__restrict__ chunk_off, int32_t N, int32_t H, int32_t P,
@@ -190,11 +191,22 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
             u.t_begin = t0 + sg * P * kC;
             u.t_end = min(t1, t0 + (sg + 1) * P * kC);
             u.pad = 0;
-            if (sg == 0) {  // phase A, with outputs: the only walk of segment 0
+            if (sg == 0) {
                 u.in = init;
-                u.out = S == 1 ? Sout + (size_t)n * seg_stride : Sin + (size_t)(g + 1) * seg_stride;
-                u.flags = kUnitWriteO | kUnitAddUp;
+                if (S == 1) {  // phase A: the sequence's only walk, with outputs
+                    u.out = Sout + (size_t)n * seg_stride;
+                    u.flags = kUnitWriteO | kUnitAddUp;
+                    unitsA[a++] = u;
+                    continue;
+                }
+                // phase A: the end state only (a walk without outputs is cheaper) ...
+                u.out = Sin + (size_t)(g + 1) * seg_stride;
+                u.flags = kUnitAddUp;
                 unitsA[a++] = u;
+                // ... phase C: again with outputs, alongside the other segments
+                u.out = nullptr;
+                u.flags = kUnitWriteO | kUnitAddUp;
+                unitsC[cc++] = u;
                 continue;
             }
             // phase C
@@ -442,10 +454,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
     {
+        // log a = g_min sigmoid(e^A z), with the division by __fdividef (2 ulp; for an
+        // infinite denominator, z = -inf, it gives 0, i.e. a = 1 exactly, as it should)
         const float eA = expf(A[h]);
         for (int e = tid; e < kC * kD; e += kIntraThreads) {
             const int i = e / kD, c = e % kD;
-            G[i][c] = (i < L) ? gate_log_decay(eA, G[i][c]) : 0.f;
+            G[i][c] = (i < L) ? __fdividef(kGMin, 1.0f + expf(-eA * G[i][c])) : 0.f;
         }
         __syncthreads();
         // column scan: thread (c, quarter) sums its 16 rows, then adds the totals of the
@@ -758,6 +772,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // and every accumulator row is one TMEM lane. Per chunk, two MMA groups:
 //   group 1   [D_U | D_O1] = S^T [ -W ; Qhat ]^T          N = 128, K = 128
 //   group 2   [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T      N = 192, K = 64
+// A walk that writes no outputs (a segment map) drops Qhat and A_qk: N = 64 and 128.
 // with U^T = U'^T + D_U, o = (D_O1 + D_O2)^T and S^T <- S^T Diag(gamma) + D_S.
 // Every product is split-bf16 (hi*hi + hi*lo + lo*hi); S^T and U^T are written to
 // shared memory as split planes (A operands), the record tiles are the B operands.
@@ -911,6 +926,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             named_arrive(kBarOR, 256);  // output accumulators read: the next group 1 may overwrite them
             // stage o as [token][channel] in the U^T buffer (free until the next U epilogue)
             // and write it out in 16-byte row chunks while the next group 1 runs
+            if (write_o) {  // uniform over the CTA: the named barriers below stay matched
             float *stage = reinterpret_cast<float *>(s.ut);
 #pragma unroll
             for (int i = 0; i < kC; ++i) {
@@ -934,28 +950,61 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 }
             }
             named_sync(5, 128);  // staged tile read out before the next U^T planes land here
+            }
             if (c + 1 < c_end) load_up(c + 1);
         }
     } else {
         // ----------------- state warps (thread 128 issues the MMAs) -----------------
         const bool issuer = (tid == 128);
-        constexpr uint32_t kId128 = tc::idesc_bf16_m128(128), kId192 = tc::idesc_bf16_m128(192);
+        // A walk without outputs (segment maps) needs only -W and Kend^T: it copies those
+        // parts of the record and runs group 1 with N = 64, group 2 with N = 128.
+        const bool maps = !write_o;
+        const uint32_t kIdG1 = tc::idesc_bf16_m128(maps ? 64 : 128);
+        const uint32_t kIdG2 = tc::idesc_bf16_m128(maps ? 128 : 192);
+        const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
+        const uint32_t ds_col = maps ? 0u : 64u;                  // TMEM column of D_S within D_AK
         int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (issuer)
         auto issue_wq = [&](int c) {
-            tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
-            tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
+            if (maps) {  // the -W rows of the hi and the lo plane
+                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kPlaneQK));
+                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)kPlaneQK, &s.bar_wq);
+                tc::bulk_g2s(s.wq + kStackWQ, rec_of(c) + kRecWQ + kStackWQ, (uint32_t)kPlaneQK, &s.bar_wq);
+            } else {
+                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
+                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
+            }
             ++n_wq;
         };
         auto issue_ak = [&](int c) {
-            tc::mbar_arrive_expect_tx(&s.bar_ak, (uint32_t)(2 * kStackAK));
-            tc::bulk_g2s(s.ak, rec_of(c) + kRecAK, (uint32_t)(2 * kStackAK), &s.bar_ak);
+            if (maps) {  // the Kend^T rows of the hi and the lo plane
+                tc::mbar_arrive_expect_tx(&s.bar_ak, (uint32_t)(2 * kPlaneKT));
+                tc::bulk_g2s(s.ak + kPlaneCC, rec_of(c) + kRecAK + kPlaneCC, (uint32_t)kPlaneKT, &s.bar_ak);
+                tc::bulk_g2s(s.ak + kStackAK + kPlaneCC, rec_of(c) + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT,
+                             &s.bar_ak);
+            } else {
+                tc::mbar_arrive_expect_tx(&s.bar_ak, (uint32_t)(2 * kStackAK));
+                tc::bulk_g2s(s.ak, rec_of(c) + kRecAK, (uint32_t)(2 * kStackAK), &s.bar_ak);
+            }
             ++n_ak;
+        };
+        // L2 prefetch of what a later chunk's walk will read
+        auto prefetch = [&](int c) {
+            const uint8_t *r = rec_of(c);
+            if (!maps) {
+                tc::prefetch_l2(r, (uint32_t)kRecBytes);
+                return;
+            }
+            tc::prefetch_l2(r + kRecWQ, (uint32_t)kPlaneQK);
+            tc::prefetch_l2(r + kRecWQ + kStackWQ, (uint32_t)kPlaneQK);
+            tc::prefetch_l2(r + kRecAK + kPlaneCC, (uint32_t)kPlaneKT);
+            tc::prefetch_l2(r + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT);
+            tc::prefetch_l2(r + kRecGam, (uint32_t)(kRecBytes - kRecGam));  // gamma and U'
         };
         // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
         auto issue_g1 = [&](int c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
-            if (c + 2 < c_end) tc::prefetch_l2(rec_of(c + 2), (uint32_t)kRecBytes);
+            if (c + 2 < c_end) prefetch(c + 2);
             if (!wait_or_fail(&s.bar_wq, ph, fail)) return;
             ++w_wq;
             const uint32_t a0s = tc::smem_addr(s.st), a1s = a0s + 128 * kD * 2;
@@ -964,9 +1013,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             for (int ks = 0; ks < kD / 16; ++ks) {
                 const uint64_t a0 = tc::desc_k(a0s, kD, ks), a1 = tc::desc_k(a1s, kD, ks);
                 const uint64_t b0 = tc::desc_k(b0s, kD, ks), b1 = tc::desc_k(b1s, kD, ks);
-                tc::mma(D_UO, a0, b0, kId128, ks > 0);
-                tc::mma(D_UO, a0, b1, kId128, 1);
-                tc::mma(D_UO, a1, b0, kId128, 1);
+                tc::mma(D_UO, a0, b0, kIdG1, ks > 0);
+                tc::mma(D_UO, a0, b1, kIdG1, 1);
+                tc::mma(D_UO, a1, b0, kIdG1, 1);
             }
             tc::commit(&s.bar_m1);
             ++n_m1;
@@ -978,14 +1027,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             if (!wait_or_fail(&s.bar_ak, ph, fail)) return;
             ++w_ak;
             const uint32_t a0s = tc::smem_addr(s.ut), a1s = a0s + 128 * kC * 2;
-            const uint32_t b0s = tc::smem_addr(s.ak), b1s = b0s + (uint32_t)kStackAK;
+            const uint32_t b0s = tc::smem_addr(s.ak) + ak_off, b1s = b0s + (uint32_t)kStackAK;
 #pragma unroll 1
             for (int ks = 0; ks < kC / 16; ++ks) {
                 const uint64_t a0 = tc::desc_k(a0s, kC, ks), a1 = tc::desc_k(a1s, kC, ks);
                 const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
-                tc::mma(D_AK, a0, b0, kId192, ks > 0);
-                tc::mma(D_AK, a0, b1, kId192, 1);
-                tc::mma(D_AK, a1, b0, kId192, 1);
+                tc::mma(D_AK, a0, b0, kIdG2, ks > 0);
+                tc::mma(D_AK, a0, b1, kIdG2, 1);
+                tc::mma(D_AK, a1, b0, kIdG2, 1);
             }
             tc::commit(&s.bar_m2);
             ++n_m2;
@@ -1002,7 +1051,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         if (issuer && c_begin < c_end) {
             issue_wq(c_begin);
             issue_ak(c_begin);
-            if (c_begin + 1 < c_end) tc::prefetch_l2(rec_of(c_begin + 1), (uint32_t)kRecBytes);
+            if (c_begin + 1 < c_end) prefetch(c_begin + 1);
         }
         named_sync(kBarOR, 256);
         if (issuer && c_begin < c_end) issue_g1(c_begin);
@@ -1026,8 +1075,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 #pragma unroll
                 for (int part = 0; part < 4; part += 2) {
                     uint32_t d0[32], d1[32];
-                    tc::tmem_ld32_nowait(D_AK + lanes + 64 + 32 * part, d0);
-                    tc::tmem_ld32_nowait(D_AK + lanes + 64 + 32 * part + 32, d1);
+                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * part, d0);
+                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * part + 32, d1);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
