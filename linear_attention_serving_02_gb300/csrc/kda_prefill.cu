@@ -325,6 +325,7 @@ struct IntraSmem {
     float G[2][kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay; the
                              // other buffer receives the next chunk's z meanwhile
     float beta[kC];
+    float colsum[4][kD];           // per-quarter column totals of the cumulative sum
     float Akk[kC][kC + 4];         // rows 16-byte aligned for float4 reads; the 4-float pad
     float T[kC][kC + 4];           // puts 8 consecutive rows on distinct banks
     float X[3][kTile][kTile];      // off-diagonal block products of the solve
@@ -454,31 +455,26 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
     {
-        // log a = g_min sigmoid(e^A z), with the division by __fdividef (2 ulp; for an
-        // infinite denominator, z = -inf, it gives 0, i.e. a = 1 exactly, as it should)
+        // thread (column c, quarter qt) takes 16 consecutive rows of its column: the gate
+        // log a = g_min sigmoid(e^A z) (the division by __fdividef: 2 ulp; an infinite
+        // denominator, z = -inf, gives 0, i.e. a = 1 exactly), then its running sum in
+        // registers; the totals of the quarters below are added after one barrier
         const float eA = expf(A[h]);
-        for (int e = tid; e < kC * kD; e += kIntraThreads) {
-            const int i = e / kD, c = e % kD;
-            G[i][c] = (i < L) ? __fdividef(kGMin, 1.0f + expf(-eA * G[i][c])) : 0.f;
-        }
-        __syncthreads();
-        // column scan: thread (c, quarter) sums its 16 rows, then adds the totals of the
-        // quarters below it
         const int c = tid % kD, qt = tid / kD;
-        float acc = 0.f;
+        float g[16];
 #pragma unroll
-        for (int i = qt * 16; i < qt * 16 + 16; ++i) {
-            acc += G[i][c];
-            G[i][c] = acc;
+        for (int m = 0; m < 16; ++m) {
+            const int i = qt * 16 + m;
+            g[m] = (i < L) ? __fdividef(kGMin, 1.0f + expf(-eA * G[i][c])) : 0.f;
         }
+#pragma unroll
+        for (int m = 1; m < 16; ++m) g[m] += g[m - 1];
+        s.colsum[qt][c] = g[15];
         __syncthreads();
         float below = 0.f;
-        for (int p = 0; p < qt; ++p) below += G[p * 16 + 15][c];
-        __syncthreads();
-        if (qt > 0) {
+        for (int p = 0; p < qt; ++p) below += s.colsum[p][c];
 #pragma unroll
-            for (int i = qt * 16; i < qt * 16 + 16; ++i) G[i][c] += below;
-        }
+        for (int m = 0; m < 16; ++m) G[qt * 16 + m][c] = (qt > 0) ? g[m] + below : g[m];
         __syncthreads();
     }
 
