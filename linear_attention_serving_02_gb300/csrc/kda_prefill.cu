@@ -420,8 +420,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     };
 
     // Copy groups in flight at the top of every iteration, oldest first: this chunk's z,
-    // its q and k, its v; then the next chunk's z is added. The next chunk's q and k are
-    // issued once this chunk no longer reads them (after the UT phase), its v at the end.
+    // its q and k, its v. The next chunk's z is added after the gate, its q and k once
+    // this chunk no longer reads them (after the UT phase), its v at the end.
     Item cur = item_of(item);
     stage_z(cur, s.G[0]);
     stage_rows(cur, 0, 2);
@@ -434,10 +434,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     uint8_t *rec = records + ((int64_t)cur.slot * H + h) * (int64_t)kRecBytes;
     const bool has_next = item + (int)gridDim.x < n_items;
     const Item nxt = has_next ? item_of(item + gridDim.x) : cur;
-    if (has_next)
-        stage_z(nxt, s.G[(iter + 1) & 1]);  // its buffer was last read by the previous chunk
-    else
-        cp_async_commit();  // an empty group keeps the group arithmetic uniform
+    const float eA = expf(A[h]);  // loaded here, off the gate's critical path
 
     if (tid >= kD && tid < kD + kC) {
         const int i = tid - kD;
@@ -450,7 +447,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const int plane = e / (int)(kPlaneCC / 16), off = e % (int)(kPlaneCC / 16);
         *reinterpret_cast<uint4 *>(rec + kRecAqk + plane * kStackAK + (size_t)off * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    cp_async_wait<3>();  // this chunk's z
+    cp_async_wait<2>();  // this chunk's z (its q, k and v may still be in flight)
     __syncthreads();
 
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
@@ -459,7 +456,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // log a = g_min sigmoid(e^A z) (the division by __fdividef: 2 ulp; an infinite
         // denominator, z = -inf, gives 0, i.e. a = 1 exactly), then its running sum in
         // registers; the totals of the quarters below are added after one barrier
-        const float eA = expf(A[h]);
         const int c = tid % kD, qt = tid / kD;
         float g[16];
 #pragma unroll
@@ -475,8 +471,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         for (int p = 0; p < qt; ++p) below += s.colsum[p][c];
 #pragma unroll
         for (int m = 0; m < 16; ++m) G[qt * 16 + m][c] = (qt > 0) ? g[m] + below : g[m];
-        __syncthreads();
     }
+    // the next chunk's z goes to the other buffer (last read by the previous chunk); it is
+    // issued after the gate so that its landing does not compete with the gate's reads
+    if (has_next)
+        stage_z(nxt, s.G[(iter + 1) & 1]);
+    else
+        cp_async_commit();  // an empty group keeps the group arithmetic uniform
+    __syncthreads();
 
     cp_async_wait<2>();
     __syncthreads();  // q and k in place (v and the next chunk's z may still be in flight)
