@@ -629,33 +629,31 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
     } else {
         const int t2 = tid - 256;
-        // Khat = k * exp(G), split: the B operand of W (the Gram operands are dead)
-        for (int e = t2; e < kC * (kD / 2); e += 256) {
-            const int i = e / (kD / 2), c = (e % (kD / 2)) * 2;
-            const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
-            uint32_t hi, lo;
-            split_bf16x2(kk.x * __expf(G[i][c]), kk.y * __expf(G[i][c + 1]), hi, lo);
-            *reinterpret_cast<uint32_t *>(&s.u.w.kh[0][i][c]) = hi;
-            *reinterpret_cast<uint32_t *>(&s.u.w.kh[1][i][c]) = lo;
-        }
-        // Qhat and Kend^T: each thread makes one 16-byte row of a core matrix (8 values
-        // along K) for the hi and the lo plane, and consecutive threads fill consecutive
-        // 16-byte chunks of the record, so every warp store covers 512 contiguous bytes
+        // Khat = k * exp(G) (the B operand of W, into the dead Gram operand space) and
+        // Qhat = q * exp(G) (into the record) share their factors: one thread makes 8
+        // channels of one row of both, as 16-byte chunks; consecutive threads fill
+        // consecutive 16-byte chunks of the record tile
         uint8_t *Qh = rec + kRecQh;
         for (int e = t2; e < kC * (kD / 8); e += 256) {
             const int c8 = (e >> 3) & 15, i = (e >> 7) * 8 + (e & 7), c = c8 * 8;
-            const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[i][c]);
             const float4 g0 = *reinterpret_cast<const float4 *>(&G[i][c]);
             const float4 g1 = *reinterpret_cast<const float4 *>(&G[i][c + 4]);
-            const float2 q01 = bf16x2_to_float2(qraw.x), q23 = bf16x2_to_float2(qraw.y);
-            const float2 q45 = bf16x2_to_float2(qraw.z), q67 = bf16x2_to_float2(qraw.w);
-            uint4 hi, lo;
-            split_bf16x2(q01.x * __expf(g0.x), q01.y * __expf(g0.y), hi.x, lo.x);
-            split_bf16x2(q23.x * __expf(g0.z), q23.y * __expf(g0.w), hi.y, lo.y);
-            split_bf16x2(q45.x * __expf(g1.x), q45.y * __expf(g1.y), hi.z, lo.z);
-            split_bf16x2(q67.x * __expf(g1.z), q67.y * __expf(g1.w), hi.w, lo.w);
-            *reinterpret_cast<uint4 *>(Qh + il_off(i, c, kD)) = hi;
-            *reinterpret_cast<uint4 *>(Qh + kStackWQ + il_off(i, c, kD)) = lo;
+            const float f[8] = {__expf(g0.x), __expf(g0.y), __expf(g0.z), __expf(g0.w),
+                                __expf(g1.x), __expf(g1.y), __expf(g1.z), __expf(g1.w)};
+            const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[i][c]);
+            const uint4 kraw = *reinterpret_cast<const uint4 *>(&s.ks[i][c]);
+            const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w}, kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
+            uint32_t qh[4], ql[4], kh[4], kl[4];
+#pragma unroll
+            for (int p2 = 0; p2 < 4; ++p2) {
+                const float2 qq = bf16x2_to_float2(qw[p2]), kk = bf16x2_to_float2(kw[p2]);
+                split_bf16x2(qq.x * f[2 * p2], qq.y * f[2 * p2 + 1], qh[p2], ql[p2]);
+                split_bf16x2(kk.x * f[2 * p2], kk.y * f[2 * p2 + 1], kh[p2], kl[p2]);
+            }
+            *reinterpret_cast<uint4 *>(Qh + il_off(i, c, kD)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+            *reinterpret_cast<uint4 *>(Qh + kStackWQ + il_off(i, c, kD)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+            *reinterpret_cast<uint4 *>(&s.u.w.kh[0][i][c]) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+            *reinterpret_cast<uint4 *>(&s.u.w.kh[1][i][c]) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
         }
         uint8_t *KeT = rec + kRecKeT;
         for (int e = t2; e < kD * (kC / 8); e += 256) {
