@@ -562,22 +562,34 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // ---- Meanwhile warps 8-15 write Qhat, Kend^T and gamma to the record and build -
     // ---- the Khat operand planes: they need only q, k and G. -----------------------
     if (warp < 8) {
-        // diagonal 16x16 blocks by forward substitution: warp a solves block a, lane j
-        // (and j + 16, a duplicate) its column j, in registers; row i reads A[i][*] as a
-        // broadcast. Warps 4-7 zero the blocks above the diagonal.
+        // diagonal 16x16 blocks, warp a solving block a: lane i holds row i of A_aa and
+        // of T_aa in registers (lanes 16-31 mirror lanes 0-15 and store nothing); T
+        // starts as I and, for m = 0 .. 14 in order, every row i > m subtracts
+        // A[i][m] * (row m, now final), broadcast by shuffles. No shared-memory reads in
+        // the loop, and the terms of each entry add in the order of forward substitution.
         if (warp < 4) {
-            const int base = warp * kTile, j = lane & 15;
-            float x[kTile];
+            const int base = warp * kTile, i = lane & 15;
+            float a[kTile], t[kTile];
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
-                float acc = 0.f;
+            for (int q4 = 0; q4 < kTile; q4 += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(&s.Akk[base + i][base + q4]);
+                a[q4] = v.x; a[q4 + 1] = v.y; a[q4 + 2] = v.z; a[q4 + 3] = v.w;
+            }
 #pragma unroll
-                for (int m = 0; m < i; ++m) acc += s.Akk[base + i][base + m] * x[m];  // x[m] = 0 for m < j
-                x[i] = (i < j) ? 0.f : ((i == j) ? 1.f : -acc);
+            for (int j = 0; j < kTile; ++j) t[j] = (j == i) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < kTile - 1; ++m) {
+#pragma unroll
+                for (int j = 0; j <= m; ++j) {  // row m is zero beyond its diagonal
+                    const float tm = __shfl_sync(0xffffffffu, t[j], m, 16);
+                    if (i > m) t[j] = __fmaf_rn(-a[m], tm, t[j]);
+                }
             }
             if (lane < kTile) {
 #pragma unroll
-                for (int i = 0; i < kTile; ++i) s.T[base + i][base + j] = x[i];
+                for (int q4 = 0; q4 < kTile; q4 += 4)
+                    *reinterpret_cast<float4 *>(&s.T[base + i][base + q4]) =
+                        make_float4(t[q4], t[q4 + 1], t[q4 + 2], t[q4 + 3]);
             }
         } else {
             for (int e = tid - 128; e < kC * kC; e += 128) {
