@@ -812,8 +812,6 @@ struct WalkSmem {
 static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
 
 constexpr int kWalkThreads = 256;
-constexpr uint32_t kCopyPiece = 16384;  // bulk copies and L2 prefetches of records go in pieces this large
-static_assert((2 * kStackWQ) % kCopyPiece == 0 && (2 * kStackAK) % kCopyPiece == 0, "copy pieces");
 constexpr uint32_t kWalkTmemCols = 512;  // D_U [0,64) D_O1 [64,128) D_O2 [128,192) D_S [192,320)
 constexpr int kBarOR = 2, kBarU = 3;
 
@@ -979,11 +977,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kPlaneQK));
                 tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)kPlaneQK, &s.bar_wq);
                 tc::bulk_g2s(s.wq + kStackWQ, rec_of(c) + kRecWQ + kStackWQ, (uint32_t)kPlaneQK, &s.bar_wq);
-            } else {  // in 16 KB pieces: more requests in flight than one 64 KB copy
+            } else {
                 tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
-#pragma unroll
-                for (uint32_t off = 0; off < 2 * kStackWQ; off += kCopyPiece)
-                    tc::bulk_g2s(s.wq + off, rec_of(c) + kRecWQ + off, kCopyPiece, &s.bar_wq);
+                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
             }
             ++n_wq;
         };
@@ -995,9 +991,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                              &s.bar_ak);
             } else {
                 tc::mbar_arrive_expect_tx(&s.bar_ak, (uint32_t)(2 * kStackAK));
-#pragma unroll
-                for (uint32_t off = 0; off < 2 * kStackAK; off += kCopyPiece)
-                    tc::bulk_g2s(s.ak + off, rec_of(c) + kRecAK + off, kCopyPiece, &s.bar_ak);
+                tc::bulk_g2s(s.ak, rec_of(c) + kRecAK, (uint32_t)(2 * kStackAK), &s.bar_ak);
             }
             ++n_ak;
         };
@@ -1005,17 +999,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         auto prefetch = [&](int c) {
             const uint8_t *r = rec_of(c);
             if (!maps) {
-                for (uint32_t off = 0; off < (uint32_t)kRecBytes; off += kCopyPiece)
-                    tc::prefetch_l2(r + off, min(kCopyPiece, (uint32_t)kRecBytes - off));
+                tc::prefetch_l2(r, (uint32_t)kRecBytes);
                 return;
             }
             tc::prefetch_l2(r + kRecWQ, (uint32_t)kPlaneQK);
             tc::prefetch_l2(r + kRecWQ + kStackWQ, (uint32_t)kPlaneQK);
             tc::prefetch_l2(r + kRecAK + kPlaneCC, (uint32_t)kPlaneKT);
             tc::prefetch_l2(r + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT);
-            tc::prefetch_l2(r + kRecGam, (uint32_t)(kRecUp - kRecGam));  // gamma
-            tc::prefetch_l2(r + kRecUp, (uint32_t)(kRecBytes - kRecUp) / 2);  // U'
-            tc::prefetch_l2(r + kRecUp + (kRecBytes - kRecUp) / 2, (uint32_t)(kRecBytes - kRecUp) / 2);
+            tc::prefetch_l2(r + kRecGam, (uint32_t)(kRecBytes - kRecGam));  // gamma and U'
         };
         // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
         auto issue_g1 = [&](int c) {
