@@ -782,8 +782,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 //   group 2   [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T      N = 192, K = 64
 // A walk that writes no outputs (a segment map) drops Qhat and A_qk: N = 64 and 128.
 // with U^T = U'^T + D_U, o = (D_O1 + D_O2)^T and S^T <- S^T Diag(gamma) + D_S.
-// Every product is split-bf16 (hi*hi + hi*lo + lo*hi); S^T and U^T are written to
-// shared memory as split planes (A operands), the record tiles are the B operands.
+// Every product is split-bf16 (hi*hi + hi*lo + lo*hi). S^T and U^T, the A operands, are
+// written as split planes straight into tensor memory by the threads that own their rows
+// (tcgen05.st); the record tiles in shared memory are the B operands.
 //
 // Eight warps with fixed roles:
 //   warps 0-3  U and O: thread = value channel dv (TMEM lane dv). After group 1 they
@@ -803,8 +804,7 @@ struct WalkSmem {
     unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
     unsigned char ak[2 * kStackAK];      // [ A_qk ; Kend^T ] hi | lo
     alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1)
-    unsigned char st[2 * 128 * kD * 2];  // S^T hi | lo   (M 128 x K 128)
-    unsigned char ut[2 * 128 * kC * 2];  // U^T hi | lo   (M 128 x K 64)
+    unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
     uint64_t bar_wq, bar_ak, bar_m1, bar_m2;
     uint32_t tmem_base;
     int fail;
@@ -812,18 +812,21 @@ struct WalkSmem {
 static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
 
 constexpr int kWalkThreads = 256;
-constexpr uint32_t kWalkTmemCols = 512;  // D_U [0,64) D_O1 [64,128) D_O2 [128,192) D_S [192,320)
+// TMEM columns: accumulators D_U [0,64) D_O1 [64,128) D_O2 [128,192) D_S [192,320); the
+// A operands of the two MMA groups as split bf16 (two per column): S^T hi [320,384),
+// S^T lo [384,448), U^T hi [448,480), U^T lo [480,512)
+constexpr uint32_t kWalkTmemCols = 512;
+constexpr uint32_t kColSHi = 320, kColSLo = 384, kColUHi = 448, kColULo = 480;
 constexpr int kBarOR = 2, kBarU = 3;
 
 
-// 8 consecutive fp32 values -> one 16-byte chunk of the hi plane and one of the lo plane
-__device__ __forceinline__ void split8_store(const float *x, unsigned char *hi_plane, unsigned char *lo_plane,
-                                             uint32_t off) {
-    uint32_t h[4], l[4];
+// 32 fp32 values of this thread's lane -> 16 columns of the hi plane and 16 of the lo plane
+__device__ __forceinline__ void split32_tmem(const float *x, uint32_t t_hi, uint32_t t_lo) {
+    uint32_t h[16], l[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) split_bf16x2(x[2 * j], x[2 * j + 1], h[j], l[j]);
-    *reinterpret_cast<uint4 *>(hi_plane + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4 *>(lo_plane + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    for (int j = 0; j < 16; ++j) split_bf16x2(x[2 * j], x[2 * j + 1], h[j], l[j]);
+    tc::tmem_st16(t_hi, h);
+    tc::tmem_st16(t_lo, l);
 }
 
 // bounded wait that gives up at once when the CTA has already failed
@@ -907,10 +910,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     Upr[j] += __uint_as_float(d0[j]);
                     Upr[32 + j] += __uint_as_float(d1[j]);
                 }
-#pragma unroll
-                for (int j = 0; j < 64; j += 8) split8_store(&Upr[j], s.ut, s.ut + 128 * kC * 2, il_off(dv, j, kC));
+                split32_tmem(&Upr[0], tmem + lanes + kColUHi, tmem + lanes + kColULo);
+                split32_tmem(&Upr[32], tmem + lanes + kColUHi + 16, tmem + lanes + kColULo + 16);
+                tc::tmem_wait_st();
             }
-            tc::fence_proxy_async();
             tc::fence_before_sync();
             named_arrive(kBarU, 256);  // U^T planes complete; group 1 is done with [ -W ; Qhat ]
             // o = (D_O1 + D_O2)^T for this thread's value channel
@@ -1015,15 +1018,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             if (c + 2 < c_end) prefetch(c + 2);
             if (!wait_or_fail(&s.bar_wq, ph, fail)) return;
             ++w_wq;
-            const uint32_t a0s = tc::smem_addr(s.st), a1s = a0s + 128 * kD * 2;
             const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
 #pragma unroll 1
             for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint64_t a0 = tc::desc_k(a0s, kD, ks), a1 = tc::desc_k(a1s, kD, ks);
+                const uint32_t a0 = tmem + kColSHi + 8 * ks, a1 = tmem + kColSLo + 8 * ks;
                 const uint64_t b0 = tc::desc_k(b0s, kD, ks), b1 = tc::desc_k(b1s, kD, ks);
-                tc::mma(D_UO, a0, b0, kIdG1, ks > 0);
-                tc::mma(D_UO, a0, b1, kIdG1, 1);
-                tc::mma(D_UO, a1, b0, kIdG1, 1);
+                tc::mma_ts(D_UO, a0, b0, kIdG1, ks > 0);
+                tc::mma_ts(D_UO, a0, b1, kIdG1, 1);
+                tc::mma_ts(D_UO, a1, b0, kIdG1, 1);
             }
             tc::commit(&s.bar_m1);
             ++n_m1;
@@ -1034,15 +1036,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             tc::fence_after_sync();
             if (!wait_or_fail(&s.bar_ak, ph, fail)) return;
             ++w_ak;
-            const uint32_t a0s = tc::smem_addr(s.ut), a1s = a0s + 128 * kC * 2;
             const uint32_t b0s = tc::smem_addr(s.ak) + ak_off, b1s = b0s + (uint32_t)kStackAK;
 #pragma unroll 1
             for (int ks = 0; ks < kC / 16; ++ks) {
-                const uint64_t a0 = tc::desc_k(a0s, kC, ks), a1 = tc::desc_k(a1s, kC, ks);
+                const uint32_t a0 = tmem + kColUHi + 8 * ks, a1 = tmem + kColULo + 8 * ks;
                 const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
-                tc::mma(D_AK, a0, b0, kIdG2, ks > 0);
-                tc::mma(D_AK, a0, b1, kIdG2, 1);
-                tc::mma(D_AK, a1, b0, kIdG2, 1);
+                tc::mma_ts(D_AK, a0, b0, kIdG2, ks > 0);
+                tc::mma_ts(D_AK, a0, b1, kIdG2, 1);
+                tc::mma_ts(D_AK, a1, b0, kIdG2, 1);
             }
             tc::commit(&s.bar_m2);
             ++n_m2;
@@ -1052,8 +1053,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 #pragma unroll
         for (int j = 0; j < kD; ++j) Sr[j] = S0 ? S0[(int64_t)j * kD + dv] : ((identity && j == dv) ? 1.f : 0.f);
 #pragma unroll
-        for (int j = 0; j < kD; j += 8) split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, j, kD));
-        tc::fence_proxy_async();
+        for (int j = 0; j < kD; j += 32)
+            split32_tmem(&Sr[j], tmem + lanes + kColSHi + j / 2, tmem + lanes + kColSLo + j / 2);
+        tc::tmem_wait_st();
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes complete
         if (issuer && c_begin < c_end) {
@@ -1103,8 +1105,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 }
             }
 #pragma unroll
-            for (int j = 0; j < kD; j += 8) split8_store(&Sr[j], s.st, s.st + 128 * kD * 2, il_off(dv, j, kD));
-            tc::fence_proxy_async();
+            for (int j = 0; j < kD; j += 32)
+                split32_tmem(&Sr[j], tmem + lanes + kColSHi + j / 2, tmem + lanes + kColSLo + j / 2);
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             named_sync(4, 128);       // next S^T planes complete, D_S read
             named_sync(kBarOR, 256);  // the U and O warps have read this chunk's output accumulators
