@@ -801,11 +801,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // the rest of the walk skips its work but keeps the sequence.
 // ---------------------------------------------------------------------------------
 struct WalkSmem {
-    unsigned char wq[2][2 * kStackWQ];   // [ -W ; Qhat ] hi | lo, two chunks in flight
+    unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
     unsigned char ak[2 * kStackAK];      // [ A_qk ; Kend^T ] hi | lo
     alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1)
     unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
-    uint64_t bar_wq[2], bar_ak, bar_m1, bar_m2;
+    uint64_t bar_wq, bar_ak, bar_m1, bar_m2;
     uint32_t tmem_base;
     int fail;
 };
@@ -865,8 +865,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            tc::mbar_init(&s.bar_wq[0], 1);
-            tc::mbar_init(&s.bar_wq[1], 1);
+            tc::mbar_init(&s.bar_wq, 1);
             tc::mbar_init(&s.bar_ak, 1);
             tc::mbar_init(&s.bar_m1, 1);
             tc::mbar_init(&s.bar_m2, 1);
@@ -975,19 +974,17 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const uint32_t kIdG2 = tc::idesc_bf16_m128(maps ? 128 : 192);
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
         const uint32_t ds_col = maps ? 0u : 64u;                  // TMEM column of D_S within D_AK
-        // phase bookkeeping (issuer); chunk c's [ -W ; Qhat ] uses slot (c - c_begin) & 1
-        int n_wq[2] = {0, 0}, w_wq[2] = {0, 0}, n_ak = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;
+        int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (issuer)
         auto issue_wq = [&](int c) {
-            const int sl = (c - c_begin) & 1;
             if (maps) {  // the -W rows of the hi and the lo plane
-                tc::mbar_arrive_expect_tx(&s.bar_wq[sl], (uint32_t)(2 * kPlaneQK));
-                tc::bulk_g2s(s.wq[sl], rec_of(c) + kRecWQ, (uint32_t)kPlaneQK, &s.bar_wq[sl]);
-                tc::bulk_g2s(s.wq[sl] + kStackWQ, rec_of(c) + kRecWQ + kStackWQ, (uint32_t)kPlaneQK, &s.bar_wq[sl]);
+                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kPlaneQK));
+                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)kPlaneQK, &s.bar_wq);
+                tc::bulk_g2s(s.wq + kStackWQ, rec_of(c) + kRecWQ + kStackWQ, (uint32_t)kPlaneQK, &s.bar_wq);
             } else {
-                tc::mbar_arrive_expect_tx(&s.bar_wq[sl], (uint32_t)(2 * kStackWQ));
-                tc::bulk_g2s(s.wq[sl], rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq[sl]);
+                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
+                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
             }
-            ++n_wq[sl];
+            ++n_wq;
         };
         auto issue_ak = [&](int c) {
             if (maps) {  // the Kend^T rows of the hi and the lo plane
@@ -1016,12 +1013,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         };
         // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
         auto issue_g1 = [&](int c) {
+            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
-            if (c + 3 < c_end) prefetch(c + 3);
-            const int sl = (c - c_begin) & 1;
-            if (!wait_or_fail(&s.bar_wq[sl], (uint32_t)(((c - c_begin) >> 1) & 1), fail)) return;
-            ++w_wq[sl];
-            const uint32_t b0s = tc::smem_addr(s.wq[sl]), b1s = b0s + (uint32_t)kStackWQ;
+            if (c + 2 < c_end) prefetch(c + 2);
+            if (!wait_or_fail(&s.bar_wq, ph, fail)) return;
+            ++w_wq;
+            const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
 #pragma unroll 1
             for (int ks = 0; ks < kD / 16; ++ks) {
                 const uint32_t a0 = tmem + kColSHi + 8 * ks, a1 = tmem + kColSLo + 8 * ks;
@@ -1064,9 +1061,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         if (issuer && c_begin < c_end) {
             issue_wq(c_begin);
             issue_ak(c_begin);
-            if (c_begin + 1 < c_end) issue_wq(c_begin + 1);
             if (c_begin + 1 < c_end) prefetch(c_begin + 1);
-            if (c_begin + 2 < c_end) prefetch(c_begin + 2);
         }
         named_sync(kBarOR, 256);
         if (issuer && c_begin < c_end) issue_g1(c_begin);
@@ -1074,9 +1069,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
-            // the [ -W ; Qhat ] copy of chunk c + 2 starts as soon as group 1 of this chunk
-            // is done with their shared slot
-            if (issuer && c + 2 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_wq(c + 2);
+            // the next [ -W ; Qhat ] copy starts as soon as group 1 of this chunk is done
+            // with the buffer, before the U epilogue
+            if (issuer && c + 1 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_wq(c + 1);
             __syncwarp();
             named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
             if (issuer) issue_g2(c);
@@ -1122,8 +1117,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         if (issuer && fail) {
             // a wait gave up: let copies and MMAs still in flight land (bounded) before
             // shared memory and TMEM are released, and report through the status word
-            for (int sl = 0; sl < 2; ++sl)
-                if (n_wq[sl] > w_wq[sl]) tc::mbar_wait(&s.bar_wq[sl], (uint32_t)(w_wq[sl] & 1));
+            if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
             if (n_ak > w_ak) tc::mbar_wait(&s.bar_ak, (uint32_t)(w_ak & 1));
             if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
             if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
