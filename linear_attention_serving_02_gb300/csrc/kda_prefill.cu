@@ -1080,33 +1080,35 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             if (issuer && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
             s.gam[ph][dv] = gnext;
             named_sync(4, 128);  // gamma of this chunk in place
-            if (ok) {
-                tc::fence_after_sync();
+            // S <- Diag(gamma) S + D_S and its split planes, in blocks of 32 key channels:
+            // the TMEM load of the next block is in flight while this one is updated,
+            // split and stored
+            {
+                uint32_t dA[32], dB[32];
+                if (ok) {
+                    tc::fence_after_sync();
+                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col, dA);
+                }
 #pragma unroll
-                for (int part = 0; part < 4; part += 2) {
-                    uint32_t d0[32], d1[32];
-                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * part, d0);
-                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * part + 32, d1);
-                    tc::tmem_wait_ld();
+                for (int b = 0; b < 4; ++b) {
+                    uint32_t(&cur)[32] = (b & 1) ? dB : dA;
+                    uint32_t(&nxt)[32] = (b & 1) ? dA : dB;
+                    if (ok) {
+                        tc::tmem_wait_ld();
+                        if (b + 1 < 4) tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * (b + 1), nxt);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const int cc = 32 * part + j;
-                        const float4 g0 = *reinterpret_cast<const float4 *>(&s.gam[ph][cc]);
-                        const float4 g1 = *reinterpret_cast<const float4 *>(&s.gam[ph][cc + 32]);
-                        Sr[cc] = g0.x * Sr[cc] + __uint_as_float(d0[j]);
-                        Sr[cc + 1] = g0.y * Sr[cc + 1] + __uint_as_float(d0[j + 1]);
-                        Sr[cc + 2] = g0.z * Sr[cc + 2] + __uint_as_float(d0[j + 2]);
-                        Sr[cc + 3] = g0.w * Sr[cc + 3] + __uint_as_float(d0[j + 3]);
-                        Sr[cc + 32] = g1.x * Sr[cc + 32] + __uint_as_float(d1[j]);
-                        Sr[cc + 33] = g1.y * Sr[cc + 33] + __uint_as_float(d1[j + 1]);
-                        Sr[cc + 34] = g1.z * Sr[cc + 34] + __uint_as_float(d1[j + 2]);
-                        Sr[cc + 35] = g1.w * Sr[cc + 35] + __uint_as_float(d1[j + 3]);
+                        for (int j = 0; j < 32; j += 4) {
+                            const int cc = 32 * b + j;
+                            const float4 g = *reinterpret_cast<const float4 *>(&s.gam[ph][cc]);
+                            Sr[cc] = g.x * Sr[cc] + __uint_as_float(cur[j]);
+                            Sr[cc + 1] = g.y * Sr[cc + 1] + __uint_as_float(cur[j + 1]);
+                            Sr[cc + 2] = g.z * Sr[cc + 2] + __uint_as_float(cur[j + 2]);
+                            Sr[cc + 3] = g.w * Sr[cc + 3] + __uint_as_float(cur[j + 3]);
+                        }
                     }
+                    split32_tmem(&Sr[32 * b], tmem + lanes + kColSHi + 16 * b, tmem + lanes + kColSLo + 16 * b);
                 }
             }
-#pragma unroll
-            for (int j = 0; j < kD; j += 32)
-                split32_tmem(&Sr[j], tmem + lanes + kColSHi + j / 2, tmem + lanes + kColSLo + j / 2);
             tc::tmem_wait_st();
             tc::fence_before_sync();
             named_sync(4, 128);       // next S^T planes complete, D_S read
