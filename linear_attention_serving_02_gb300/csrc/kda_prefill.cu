@@ -805,7 +805,7 @@ struct WalkSmem {
     unsigned char ak[2 * kStackAK];      // [ A_qk ; Kend^T ] hi | lo
     alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1)
     unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
-    uint64_t bar_w, bar_q, bar_ak, bar_m1, bar_m2, bar_mo;
+    uint64_t bar_wq, bar_ak, bar_m1, bar_m2;
     uint32_t tmem_base;
     int fail;
 };
@@ -836,14 +836,6 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
     fail = 1;
     return false;
 }
-// bounded wait that also waits after a failure: the issuer commits every group's barrier
-// even when it skips the MMAs, so this returns promptly and keeps the U and O warps'
-// BAR_U / BAR_OR arrivals behind the state warps' matching syncs. True when the data
-// behind the barrier is valid.
-__device__ __forceinline__ bool wait_in_order(uint64_t *bar, uint32_t parity, volatile int &fail) {
-    if (!tc::mbar_wait(bar, parity)) fail = 1;
-    return !fail;
-}
 
 __global__ void __launch_bounds__(kWalkThreads, 1)
     kda_walk_kernel(int32_t *__restrict__ status, const WalkUnit *__restrict__ units,
@@ -873,12 +865,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            tc::mbar_init(&s.bar_w, 1);
-            tc::mbar_init(&s.bar_q, 1);
+            tc::mbar_init(&s.bar_wq, 1);
             tc::mbar_init(&s.bar_ak, 1);
             tc::mbar_init(&s.bar_m1, 1);
             tc::mbar_init(&s.bar_m2, 1);
-            tc::mbar_init(&s.bar_mo, 1);
             tc::mbar_init_fence();
             s.fail = 0;
         }
@@ -903,13 +893,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         };
         if (c_begin < c_end) load_up(c_begin);
         tc::fence_before_sync();
-        named_arrive(kBarOR, 256);  // nothing to read yet: group 1b of the first chunk may start
+        named_arrive(kBarOR, 256);  // nothing to read yet: group 1 of the first chunk may start
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
             const int L = (int)min((int64_t)kC, t_end - t0);
             // U^T = U'^T + D_U, written as split planes for group 2
-            if (wait_in_order(&s.bar_m1, ph, fail)) {
+            if (wait_or_fail(&s.bar_m1, ph, fail)) {
                 tc::fence_after_sync();
                 uint32_t d0[32], d1[32];
                 tc::tmem_ld32_nowait(D_UO + lanes, d0);
@@ -930,10 +920,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             float ov[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) ov[j] = 0.f;
-            // group 1b (Qhat S) follows group 2 in the pipe: its commit covers both output
-            // accumulators. Waited for in every mode, so that this warp group never reaches
-            // the next BAR_OR before the state warps have passed the current one.
-            const bool ok = wait_in_order(&s.bar_mo, ph, fail) && write_o;
+            const bool ok = wait_or_fail(&s.bar_m2, ph, fail) && write_o;
             if (ok) {
                 tc::fence_after_sync();
 #pragma unroll
@@ -947,7 +934,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 }
             }
             tc::fence_before_sync();
-            named_arrive(kBarOR, 256);  // output accumulators read: the next groups may overwrite them
+            named_arrive(kBarOR, 256);  // output accumulators read: the next group 1 may overwrite them
             // stage o as [token][channel] in the U^T buffer (free until the next U epilogue)
             // and write it out in 16-byte row chunks while the next group 1 runs
             if (write_o) {  // uniform over the CTA: the named barriers below stay matched
@@ -981,28 +968,23 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // ----------------- state warps (thread 128 issues the MMAs) -----------------
         const bool issuer = (tid == 128);
         // A walk without outputs (segment maps) needs only -W and Kend^T: it copies those
-        // parts of the record, skips group 1b and runs group 2 with N = 128.
+        // parts of the record and runs group 1 with N = 64, group 2 with N = 128.
         const bool maps = !write_o;
-        constexpr uint32_t kIdG1 = tc::idesc_bf16_m128(64);
+        const uint32_t kIdG1 = tc::idesc_bf16_m128(maps ? 64 : 128);
         const uint32_t kIdG2 = tc::idesc_bf16_m128(maps ? 128 : 192);
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
         const uint32_t ds_col = maps ? 0u : 64u;                  // TMEM column of D_S within D_AK
-        // phase bookkeeping (issuer): copies issued / waited for, commits
-        int n_w = 0, w_w = 0, n_q = 0, w_q = 0, n_ak = 0, w_ak = 0, n_m1 = 0, n_m2 = 0, n_mo = 0;
-        // -W (rows 0-63 of the [ -W ; Qhat ] stack) and Qhat (rows 64-127) of the hi and the
-        // lo plane, each copied as soon as its own group is done with the previous chunk's
-        auto issue_w = [&](int c) {
-            tc::mbar_arrive_expect_tx(&s.bar_w, (uint32_t)(2 * kPlaneQK));
-            tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)kPlaneQK, &s.bar_w);
-            tc::bulk_g2s(s.wq + kStackWQ, rec_of(c) + kRecWQ + kStackWQ, (uint32_t)kPlaneQK, &s.bar_w);
-            ++n_w;
-        };
-        auto issue_q = [&](int c) {
-            tc::mbar_arrive_expect_tx(&s.bar_q, (uint32_t)(2 * kPlaneQK));
-            tc::bulk_g2s(s.wq + kPlaneQK, rec_of(c) + kRecWQ + kPlaneQK, (uint32_t)kPlaneQK, &s.bar_q);
-            tc::bulk_g2s(s.wq + kStackWQ + kPlaneQK, rec_of(c) + kRecWQ + kStackWQ + kPlaneQK, (uint32_t)kPlaneQK,
-                         &s.bar_q);
-            ++n_q;
+        int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (issuer)
+        auto issue_wq = [&](int c) {
+            if (maps) {  // the -W rows of the hi and the lo plane
+                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kPlaneQK));
+                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)kPlaneQK, &s.bar_wq);
+                tc::bulk_g2s(s.wq + kStackWQ, rec_of(c) + kRecWQ + kStackWQ, (uint32_t)kPlaneQK, &s.bar_wq);
+            } else {
+                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
+                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
+            }
+            ++n_wq;
         };
         auto issue_ak = [&](int c) {
             if (maps) {  // the Kend^T rows of the hi and the lo plane
@@ -1029,58 +1011,42 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             tc::prefetch_l2(r + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT);
             tc::prefetch_l2(r + kRecGam, (uint32_t)(kRecBytes - kRecGam));  // gamma and U'
         };
-        // split products of one group: D (+)= A_tmem-planes x B-planes, K in steps of 16
-        auto mma_group = [&](uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b0s, uint32_t b1s, int K,
-                             uint32_t idesc) {
-#pragma unroll 1
-            for (int ks = 0; ks < K / 16; ++ks) {
-                const uint32_t a0 = a_hi + 8 * ks, a1 = a_lo + 8 * ks;
-                const uint64_t b0 = tc::desc_k(b0s, K, ks), b1 = tc::desc_k(b1s, K, ks);
-                tc::mma_ts(d, a0, b0, idesc, ks > 0);
-                tc::mma_ts(d, a0, b1, idesc, 1);
-                tc::mma_ts(d, a1, b0, idesc, 1);
-            }
-        };
-        // group 1a of chunk c: D_U = S^T (-W)^T   (N = 64, K = 128); commit -> bar_m1
-        auto issue_g1a = [&](int c) {
+        // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
+        auto issue_g1 = [&](int c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
             if (c + 2 < c_end) prefetch(c + 2);
-            if (wait_or_fail(&s.bar_w, ph, fail)) {
-                ++w_w;
-                const uint32_t b0s = tc::smem_addr(s.wq);
-                mma_group(D_UO, tmem + kColSHi, tmem + kColSLo, b0s, b0s + (uint32_t)kStackWQ, kD, kIdG1);
+            if (!wait_or_fail(&s.bar_wq, ph, fail)) return;
+            ++w_wq;
+            const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
+#pragma unroll 1
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t a0 = tmem + kColSHi + 8 * ks, a1 = tmem + kColSLo + 8 * ks;
+                const uint64_t b0 = tc::desc_k(b0s, kD, ks), b1 = tc::desc_k(b1s, kD, ks);
+                tc::mma_ts(D_UO, a0, b0, kIdG1, ks > 0);
+                tc::mma_ts(D_UO, a0, b1, kIdG1, 1);
+                tc::mma_ts(D_UO, a1, b0, kIdG1, 1);
             }
-            tc::commit(&s.bar_m1);  // also after a failure: the U and O warps wait for it in order
+            tc::commit(&s.bar_m1);
             ++n_m1;
         };
-        // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T; commit -> bar_m2
+        // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T
         auto issue_g2 = [&](int c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
-            if (wait_or_fail(&s.bar_ak, ph, fail)) {
-                ++w_ak;
-                const uint32_t b0s = tc::smem_addr(s.ak) + ak_off;
-                mma_group(D_AK, tmem + kColUHi, tmem + kColULo, b0s, b0s + (uint32_t)kStackAK, kC, kIdG2);
+            if (!wait_or_fail(&s.bar_ak, ph, fail)) return;
+            ++w_ak;
+            const uint32_t b0s = tc::smem_addr(s.ak) + ak_off, b1s = b0s + (uint32_t)kStackAK;
+#pragma unroll 1
+            for (int ks = 0; ks < kC / 16; ++ks) {
+                const uint32_t a0 = tmem + kColUHi + 8 * ks, a1 = tmem + kColULo + 8 * ks;
+                const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
+                tc::mma_ts(D_AK, a0, b0, kIdG2, ks > 0);
+                tc::mma_ts(D_AK, a0, b1, kIdG2, 1);
+                tc::mma_ts(D_AK, a1, b0, kIdG2, 1);
             }
-            tc::commit(&s.bar_m2);  // also after a failure (see group 1a)
+            tc::commit(&s.bar_m2);
             ++n_m2;
-        };
-        // group 1b of chunk c: D_O1 = S^T Qhat^T (N = 64, K = 128), after group 2 in the pipe,
-        // off the chain from one state to the next; commit -> bar_mo (with no outputs the
-        // commit alone, which then tracks group 2)
-        auto issue_g1b = [&](int c) {
-            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
-            tc::fence_after_sync();
-            if (!maps && !fail) {
-                if (wait_or_fail(&s.bar_q, ph, fail)) {
-                    ++w_q;
-                    const uint32_t b0s = tc::smem_addr(s.wq) + (uint32_t)kPlaneQK;
-                    mma_group(D_UO + 64, tmem + kColSHi, tmem + kColSLo, b0s, b0s + (uint32_t)kStackWQ, kD, kIdG1);
-                }
-            }
-            tc::commit(&s.bar_mo);
-            ++n_mo;
         };
 
         float Sr[128];
@@ -1093,75 +1059,70 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes complete
         if (issuer && c_begin < c_end) {
-            issue_w(c_begin);
-            if (!maps) issue_q(c_begin);
+            issue_wq(c_begin);
             issue_ak(c_begin);
             if (c_begin + 1 < c_end) prefetch(c_begin + 1);
-            issue_g1a(c_begin);
         }
+        named_sync(kBarOR, 256);
+        if (issuer && c_begin < c_end) issue_g1(c_begin);
         __syncwarp();
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
-            // the next -W copy starts as soon as group 1a of this chunk is done with it
-            if (issuer && c + 1 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_w(c + 1);
+            // the next [ -W ; Qhat ] copy starts as soon as group 1 of this chunk is done
+            // with the buffer, before the U epilogue
+            if (issuer && c + 1 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_wq(c + 1);
             __syncwarp();
-            named_sync(kBarU, 256);  // U^T planes of this chunk written
+            named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
             if (issuer) issue_g2(c);
-            __syncwarp();
-            named_sync(kBarOR, 256);  // the previous chunk's output accumulators have been read
-            if (issuer) issue_g1b(c);
             __syncwarp();
             const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
             if (issuer && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
             s.gam[ph][dv] = gnext;
             named_sync(4, 128);  // gamma of this chunk in place
-            // S <- Diag(gamma) S + D_S in registers, in blocks of 32 key channels with the
-            // next block's TMEM load in flight
-            if (ok) {
+            // S <- Diag(gamma) S + D_S and its split planes, in blocks of 32 key channels:
+            // the TMEM load of the next block is in flight while this one is updated,
+            // split and stored
+            {
                 uint32_t dA[32], dB[32];
-                tc::fence_after_sync();
-                tc::tmem_ld32_nowait(D_AK + lanes + ds_col, dA);
+                if (ok) {
+                    tc::fence_after_sync();
+                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col, dA);
+                }
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     uint32_t(&cur)[32] = (b & 1) ? dB : dA;
                     uint32_t(&nxt)[32] = (b & 1) ? dA : dB;
-                    tc::tmem_wait_ld();
-                    if (b + 1 < 4) tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * (b + 1), nxt);
+                    if (ok) {
+                        tc::tmem_wait_ld();
+                        if (b + 1 < 4) tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * (b + 1), nxt);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const int cc = 32 * b + j;
-                        const float4 g = *reinterpret_cast<const float4 *>(&s.gam[ph][cc]);
-                        Sr[cc] = g.x * Sr[cc] + __uint_as_float(cur[j]);
-                        Sr[cc + 1] = g.y * Sr[cc + 1] + __uint_as_float(cur[j + 1]);
-                        Sr[cc + 2] = g.z * Sr[cc + 2] + __uint_as_float(cur[j + 2]);
-                        Sr[cc + 3] = g.w * Sr[cc + 3] + __uint_as_float(cur[j + 3]);
+                        for (int j = 0; j < 32; j += 4) {
+                            const int cc = 32 * b + j;
+                            const float4 g = *reinterpret_cast<const float4 *>(&s.gam[ph][cc]);
+                            Sr[cc] = g.x * Sr[cc] + __uint_as_float(cur[j]);
+                            Sr[cc + 1] = g.y * Sr[cc + 1] + __uint_as_float(cur[j + 1]);
+                            Sr[cc + 2] = g.z * Sr[cc + 2] + __uint_as_float(cur[j + 2]);
+                            Sr[cc + 3] = g.w * Sr[cc + 3] + __uint_as_float(cur[j + 3]);
+                        }
                     }
+                    split32_tmem(&Sr[32 * b], tmem + lanes + kColSHi + 16 * b, tmem + lanes + kColSLo + 16 * b);
                 }
             }
-            // group 1b still reads the current S^T planes and Qhat: wait for it, then
-            // refill Qhat and write the next planes
-            const bool ok_o = wait_or_fail(&s.bar_mo, ph, fail);
-            if (issuer && ok_o && !maps && c + 1 < c_end) issue_q(c + 1);
-#pragma unroll
-            for (int j = 0; j < kD; j += 32)
-                split32_tmem(&Sr[j], tmem + lanes + kColSHi + j / 2, tmem + lanes + kColSLo + j / 2);
             tc::tmem_wait_st();
             tc::fence_before_sync();
-            named_sync(4, 128);  // next S^T planes complete, D_S read
-            if (issuer && c + 1 < c_end) issue_g1a(c + 1);
+            named_sync(4, 128);       // next S^T planes complete, D_S read
+            named_sync(kBarOR, 256);  // the U and O warps have read this chunk's output accumulators
+            if (issuer && c + 1 < c_end) issue_g1(c + 1);
             __syncwarp();
         }
-        named_sync(kBarOR, 256);  // the last chunk's output accumulators have been read
         if (issuer && fail) {
             // a wait gave up: let copies and MMAs still in flight land (bounded) before
             // shared memory and TMEM are released, and report through the status word
-            if (n_w > w_w) tc::mbar_wait(&s.bar_w, (uint32_t)(w_w & 1));
-            if (n_q > w_q) tc::mbar_wait(&s.bar_q, (uint32_t)(w_q & 1));
+            if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
             if (n_ak > w_ak) tc::mbar_wait(&s.bar_ak, (uint32_t)(w_ak & 1));
             if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
             if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
-            if (n_mo > 0) tc::mbar_wait(&s.bar_mo, (uint32_t)((n_mo - 1) & 1));
             atomicExch(status, -7);
         }
         const bool failed = fail;
