@@ -836,6 +836,15 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
     fail = 1;
     return false;
 }
+// bounded wait that also waits after a failure: the issuer commits every group's barrier
+// even when it skips the MMAs, so this returns promptly and keeps the U and O warps'
+// BAR_U / BAR_OR arrivals behind the state warps' matching syncs (a named barrier counts
+// arrivals, so one side may never arrive twice before the other has synced). True when
+// the data behind the barrier is valid.
+__device__ __forceinline__ bool wait_in_order(uint64_t *bar, uint32_t parity, volatile int &fail) {
+    if (!tc::mbar_wait(bar, parity)) fail = 1;
+    return !fail;
+}
 
 __global__ void __launch_bounds__(kWalkThreads, 1)
     kda_walk_kernel(int32_t *__restrict__ status, const WalkUnit *__restrict__ units,
@@ -899,7 +908,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
             const int L = (int)min((int64_t)kC, t_end - t0);
             // U^T = U'^T + D_U, written as split planes for group 2
-            if (wait_or_fail(&s.bar_m1, ph, fail)) {
+            if (wait_in_order(&s.bar_m1, ph, fail)) {
                 tc::fence_after_sync();
                 uint32_t d0[32], d1[32];
                 tc::tmem_ld32_nowait(D_UO + lanes, d0);
@@ -920,7 +929,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             float ov[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) ov[j] = 0.f;
-            const bool ok = wait_or_fail(&s.bar_m2, ph, fail) && write_o;
+            const bool ok = wait_in_order(&s.bar_m2, ph, fail) && write_o;
             if (ok) {
                 tc::fence_after_sync();
 #pragma unroll
@@ -1016,36 +1025,38 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
             if (c + 2 < c_end) prefetch(c + 2);
-            if (!wait_or_fail(&s.bar_wq, ph, fail)) return;
-            ++w_wq;
-            const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
+            if (wait_or_fail(&s.bar_wq, ph, fail)) {
+                ++w_wq;
+                const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
 #pragma unroll 1
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint32_t a0 = tmem + kColSHi + 8 * ks, a1 = tmem + kColSLo + 8 * ks;
-                const uint64_t b0 = tc::desc_k(b0s, kD, ks), b1 = tc::desc_k(b1s, kD, ks);
-                tc::mma_ts(D_UO, a0, b0, kIdG1, ks > 0);
-                tc::mma_ts(D_UO, a0, b1, kIdG1, 1);
-                tc::mma_ts(D_UO, a1, b0, kIdG1, 1);
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t a0 = tmem + kColSHi + 8 * ks, a1 = tmem + kColSLo + 8 * ks;
+                    const uint64_t b0 = tc::desc_k(b0s, kD, ks), b1 = tc::desc_k(b1s, kD, ks);
+                    tc::mma_ts(D_UO, a0, b0, kIdG1, ks > 0);
+                    tc::mma_ts(D_UO, a0, b1, kIdG1, 1);
+                    tc::mma_ts(D_UO, a1, b0, kIdG1, 1);
+                }
             }
-            tc::commit(&s.bar_m1);
+            tc::commit(&s.bar_m1);  // also after a failure: the U and O warps wait for it in order
             ++n_m1;
         };
         // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T
         auto issue_g2 = [&](int c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
-            if (!wait_or_fail(&s.bar_ak, ph, fail)) return;
-            ++w_ak;
-            const uint32_t b0s = tc::smem_addr(s.ak) + ak_off, b1s = b0s + (uint32_t)kStackAK;
+            if (wait_or_fail(&s.bar_ak, ph, fail)) {
+                ++w_ak;
+                const uint32_t b0s = tc::smem_addr(s.ak) + ak_off, b1s = b0s + (uint32_t)kStackAK;
 #pragma unroll 1
-            for (int ks = 0; ks < kC / 16; ++ks) {
-                const uint32_t a0 = tmem + kColUHi + 8 * ks, a1 = tmem + kColULo + 8 * ks;
-                const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
-                tc::mma_ts(D_AK, a0, b0, kIdG2, ks > 0);
-                tc::mma_ts(D_AK, a0, b1, kIdG2, 1);
-                tc::mma_ts(D_AK, a1, b0, kIdG2, 1);
+                for (int ks = 0; ks < kC / 16; ++ks) {
+                    const uint32_t a0 = tmem + kColUHi + 8 * ks, a1 = tmem + kColULo + 8 * ks;
+                    const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
+                    tc::mma_ts(D_AK, a0, b0, kIdG2, ks > 0);
+                    tc::mma_ts(D_AK, a0, b1, kIdG2, 1);
+                    tc::mma_ts(D_AK, a1, b0, kIdG2, 1);
+                }
             }
-            tc::commit(&s.bar_m2);
+            tc::commit(&s.bar_m2);  // also after a failure (see group 1)
             ++n_m2;
         };
 
