@@ -487,32 +487,55 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     for (int a = 0; a < kC / kTile; ++a) {
         const int r = a * kTile;  // reference token of this tile row
         const int nb = r + kTile; // key rows j = 0 .. r+15
-        // A operands: q and k of the tile row share the factor exp(G_i - G_r)
-        for (int e = tid; e < kTile * (kD / 2); e += kIntraThreads) {
-            const int row = e / (kD / 2), c = (e % (kD / 2)) * 2, i = r + row;
-            const float2 g = *reinterpret_cast<const float2 *>(&G[i][c]);
-            const float2 gr = *reinterpret_cast<const float2 *>(&G[r][c]);
-            const float f0 = __expf(g.x - gr.x), f1 = __expf(g.y - gr.y);
-            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.qs[i][c]));
-            const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[i][c]));
-            uint32_t hi, lo;
-            split_bf16x2(qq.x * f0, qq.y * f1, hi, lo);
-            *reinterpret_cast<uint32_t *>(&s.u.g.aq[0][row][c]) = hi;
-            *reinterpret_cast<uint32_t *>(&s.u.g.aq[1][row][c]) = lo;
-            split_bf16x2(kk.x * f0, kk.y * f1, hi, lo);
-            *reinterpret_cast<uint32_t *>(&s.u.g.ak[0][row][c]) = hi;
-            *reinterpret_cast<uint32_t *>(&s.u.g.ak[1][row][c]) = lo;
-        }
-        // B operand: keys j = 0 .. r+15 with the factor exp(G_r - G_j)
-        for (int e = tid; e < nb * (kD / 2); e += kIntraThreads) {
-            const int j = e / (kD / 2), c = (e % (kD / 2)) * 2;
-            const float2 g = *reinterpret_cast<const float2 *>(&G[j][c]);
-            const float2 gr = *reinterpret_cast<const float2 *>(&G[r][c]);
-            const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&s.ks[j][c]));
-            uint32_t hi, lo;
-            split_bf16x2(kk.x * __expf(gr.x - g.x), kk.y * __expf(gr.y - g.y), hi, lo);
-            *reinterpret_cast<uint32_t *>(&s.u.g.bk[0][j][c]) = hi;
-            *reinterpret_cast<uint32_t *>(&s.u.g.bk[1][j][c]) = lo;
+        // Operands, 8 channels per item (16-byte loads and stores): the A operands (q and
+        // k of the tile row, sharing the factor exp(G_i - G_r)) are items 0 .. 255, the B
+        // operand (keys j = 0 .. r+15 with the factor exp(G_r - G_j)) the rest. A thread's
+        // channel slice, tid % 16, is the same for all its items, so G_r is read once.
+        {
+            const int c = (tid & 15) * 8;
+            float gr[8];
+            {
+                const float4 r0 = *reinterpret_cast<const float4 *>(&G[r][c]);
+                const float4 r1 = *reinterpret_cast<const float4 *>(&G[r][c + 4]);
+                gr[0] = r0.x; gr[1] = r0.y; gr[2] = r0.z; gr[3] = r0.w;
+                gr[4] = r1.x; gr[5] = r1.y; gr[6] = r1.z; gr[7] = r1.w;
+            }
+            for (int e = tid; e < (kTile + nb) * 16; e += kIntraThreads) {
+                const bool aside = e < kTile * 16;
+                const int row = aside ? r + (e >> 4) : (e >> 4) - kTile;  // token i (A side) or j (B side)
+                const float4 g0 = *reinterpret_cast<const float4 *>(&G[row][c]);
+                const float4 g1 = *reinterpret_cast<const float4 *>(&G[row][c + 4]);
+                const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                float f[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) f[m] = __expf(aside ? g[m] - gr[m] : gr[m] - g[m]);
+                const uint4 kraw = *reinterpret_cast<const uint4 *>(&s.ks[row][c]);
+                const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
+                uint32_t kh[4], kl[4];
+#pragma unroll
+                for (int p2 = 0; p2 < 4; ++p2) {
+                    const float2 kk = bf16x2_to_float2(kw[p2]);
+                    split_bf16x2(kk.x * f[2 * p2], kk.y * f[2 * p2 + 1], kh[p2], kl[p2]);
+                }
+                if (aside) {
+                    const int ar = e >> 4;
+                    const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[row][c]);
+                    const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+                    uint32_t qh[4], ql[4];
+#pragma unroll
+                    for (int p2 = 0; p2 < 4; ++p2) {
+                        const float2 qq = bf16x2_to_float2(qw[p2]);
+                        split_bf16x2(qq.x * f[2 * p2], qq.y * f[2 * p2 + 1], qh[p2], ql[p2]);
+                    }
+                    *reinterpret_cast<uint4 *>(&s.u.g.aq[0][ar][c]) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+                    *reinterpret_cast<uint4 *>(&s.u.g.aq[1][ar][c]) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+                    *reinterpret_cast<uint4 *>(&s.u.g.ak[0][ar][c]) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                    *reinterpret_cast<uint4 *>(&s.u.g.ak[1][ar][c]) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+                } else {
+                    *reinterpret_cast<uint4 *>(&s.u.g.bk[0][row][c]) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                    *reinterpret_cast<uint4 *>(&s.u.g.bk[1][row][c]) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+                }
+            }
         }
         __syncthreads();
         const int ntiles = nb / 8;  // n8 tiles of key rows
