@@ -193,7 +193,7 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     }
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 3) kda_fused_decode_kernel(FusedArgs p) {
+__global__ void __launch_bounds__(kDecodeThreads, 2) kda_fused_decode_kernel(FusedArgs p) {
     fused_decode_body<128>(p);
 }
 
