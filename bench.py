@@ -418,6 +418,66 @@ def run_fused_decode(steps, warmup, world, seed):
             "finite": bool(torch.isfinite(state).all() and torch.isfinite(y).all())}
 
 
+def run_prefill_workload(which, steps, warmup, world, seed):
+    """Prefill alone on the pages' other prefill workloads, device-timed with CUDA events
+    (bf16 o; inputs drawn on the device, so nothing here is oracle-checked: the parity
+    tests cover these shapes):
+      varlen  8 packed sequences of U[1024, 32768] tokens (from seed 0), 32 heads, zero
+              initial states;
+      long    one 1,048,576-token sequence, 12 heads, then 128 recurrent decode steps on its
+              final state."""
+    from linear_attention_serving_02_gb300 import kda
+
+    if which == "varlen":
+        H = 32
+        lens = inputs.varlen_lengths(8, 1024, 32768, seed=0)
+        cu_host = inputs.cu_seqlens_from_lengths(lens)
+        T = int(cu_host[-1])
+        inp = inputs.prefill_inputs(T, H, len(lens), seed=seed, device="cuda")
+        cu = cu_host.cuda()
+        n_seqs = len(lens)
+    else:
+        H, T = 12, 1 << 20
+        inp = inputs.prefill_inputs(T, H, 1, seed=seed, device="cuda")
+        cu = cu_host = None
+        n_seqs = 1
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(T, n_seqs, H), dtype=torch.uint8, device="cuda")
+    o = torch.empty(inp["q"].shape, dtype=torch.bfloat16, device="cuda")
+    S = torch.empty((n_seqs, H, D, D), dtype=torch.float32, device="cuda")
+    main = torch.cuda.current_stream()
+
+    def prefill():
+        kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], cu_seqlens=cu,
+                              cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws)
+
+    for _ in range(warmup):
+        prefill()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for _ in range(steps):
+        prefill()  # inputs of several GB: larger than L2, no flush needed
+    e1.record(main)
+    e1.synchronize()
+    t = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / steps, world)
+    res = {"workload": which, "tokens": T, "heads": H, "sequences": n_seqs, "prefill_ms": 1e3 * t,
+           "token_heads_per_s": world * T * H / t, "hbm_frac_of_io": PREFILL_BYTES_PER_TH * T * H / t / 1e9}
+    if which == "long":
+        # the decode that follows: 128 steps of one token per head on the prefilled state
+        dec = [inputs.decode_step_inputs(1, H, seed=seed + 5, step=i, device="cuda", A=inp["A"]) for i in range(8)]
+        o_dec = torch.empty((1, H, D), dtype=torch.float32, device="cuda")
+        e0.record(main)
+        for i in range(128):
+            d = dec[i % len(dec)]
+            kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["z"], d["A"], d["b"], S, o=o_dec)
+        e1.record(main)
+        e1.synchronize()
+        res["decode_128_steps_ms"] = e0.elapsed_time(e1)
+    res["finite"] = bool(torch.isfinite(S).all())
+    return res
+
+
 # ------------------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ------------------------------------------------------------------------------------
@@ -583,9 +643,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--part", choices=["all", "speculative", "fused"], default="all",
+    ap.add_argument("--part", choices=["all", "speculative", "fused", "varlen", "long"], default="all",
                     help="'speculative' times only the verify + fold pair, 'fused' only the fused decode "
-                         "(each about 3 GB on the device; for profiling) and prints its object")
+                         "(each about 3 GB on the device; for profiling); 'varlen' and 'long' time the "
+                         "prefill of the packed 8 x U[1024, 32768] x 32-head batch and of the 1M-token "
+                         "sequence; each prints its object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -596,8 +658,11 @@ def main():
     rank, world, local = dist_setup(args.gpus)
     try:
         if args.part != "all":
-            run = run_speculative if args.part == "speculative" else run_fused_decode
-            res = run(args.steps, args.warmup, world, seed=1000 * rank)
+            if args.part in ("varlen", "long"):
+                res = run_prefill_workload(args.part, args.steps, args.warmup, world, seed=1000 * rank)
+            else:
+                run = run_speculative if args.part == "speculative" else run_fused_decode
+                res = run(args.steps, args.warmup, world, seed=1000 * rank)
             if rank == 0:
                 print(json.dumps({args.part: res}), flush=True)
             return
