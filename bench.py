@@ -462,7 +462,7 @@ def run_prefill_workload(which, steps, warmup, world, seed):
     e1.synchronize()
     t = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / steps, world)
     res = {"workload": which, "tokens": T, "heads": H, "sequences": n_seqs, "prefill_ms": 1e3 * t,
-           "token_heads_per_s": world * T * H / t, "hbm_frac_of_io": PREFILL_BYTES_PER_TH * T * H / t / 1e9}
+           "token_heads_per_s": world * T * H / t, "io_gbs": PREFILL_BYTES_PER_TH * T * H / t / 1e9}
     if which == "long":
         # the decode that follows: 128 steps of one token per head on the prefilled state
         dec = [inputs.decode_step_inputs(1, H, seed=seed + 5, step=i, device="cuda", A=inp["A"]) for i in range(8)]
