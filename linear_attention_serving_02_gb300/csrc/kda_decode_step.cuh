@@ -1,8 +1,9 @@
 // The per-token decode step that every decode-family kernel shares: the thread layout
 // over a CTA's slice of value columns, and the per-element arithmetic of the update
 // S' = Diag(a) S, p = S'^T k, S = S' + beta k (v - p)^T, o = S^T q ('Kimi K3 attention
-// deep dive', §2.2). Every operation is an explicitly rounded intrinsic, so the kernels
-// that include this file produce the same bits for the same inputs and layout.
+// deep dive', §2.2). Every operation is an explicitly rounded IEEE operation (packed two
+// lanes at a time), so the kernels that include this file produce the same bits for the
+// same inputs and layout.
 #pragma once
 
 #include "kda.h"
@@ -21,27 +22,67 @@ struct DecodeGeom {
 };
 
 // ---- the per-element arithmetic every kernel here shares ----
+// Two fp32 lanes per instruction (the packed .f32x2 forms of sm_100 and later): each lane
+// is the same IEEE round-to-nearest multiply, add or fused multiply-add as its scalar
+// form, so the results are those of the scalar code, with half the instructions.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ void set4(float4 &v, uint64_t lo, uint64_t hi) {
+    const float2 a = upk2(lo), b = upk2(hi);
+    v = make_float4(a.x, a.y, b.x, b.y);
+}
 
 // S' = a S on one row of this thread, and its term of the projection p += k_r S'_r
 __device__ __forceinline__ void decay_project(float4 &s, float a, float kr, float4 &p) {
-    s.x = __fmul_rn(s.x, a); s.y = __fmul_rn(s.y, a); s.z = __fmul_rn(s.z, a); s.w = __fmul_rn(s.w, a);
-    p.x = __fmaf_rn(kr, s.x, p.x); p.y = __fmaf_rn(kr, s.y, p.y);
-    p.z = __fmaf_rn(kr, s.z, p.z); p.w = __fmaf_rn(kr, s.w, p.w);
+    const uint64_t a2 = pk2(a, a), k2 = pk2(kr, kr);
+    const uint64_t s01 = mul2(pk2(s.x, s.y), a2), s23 = mul2(pk2(s.z, s.w), a2);
+    set4(s, s01, s23);
+    set4(p, fma2(k2, s01, pk2(p.x, p.y)), fma2(k2, s23, pk2(p.z, p.w)));
 }
 // e = beta (v - p)
 __device__ __forceinline__ float4 delta_error(float beta, float4 v, float4 p) {
-    return make_float4(__fmul_rn(beta, __fsub_rn(v.x, p.x)), __fmul_rn(beta, __fsub_rn(v.y, p.y)),
-                       __fmul_rn(beta, __fsub_rn(v.z, p.z)), __fmul_rn(beta, __fsub_rn(v.w, p.w)));
+    const uint64_t b2 = pk2(beta, beta);
+    float4 e;
+    set4(e, mul2(b2, sub2(pk2(v.x, v.y), pk2(p.x, p.y))), mul2(b2, sub2(pk2(v.z, v.w), pk2(p.z, p.w))));
+    return e;
 }
 // S = S' + k_r e on one row
 __device__ __forceinline__ void rank1(float4 &s, float kr, float4 e) {
-    s.x = __fmaf_rn(kr, e.x, s.x); s.y = __fmaf_rn(kr, e.y, s.y);
-    s.z = __fmaf_rn(kr, e.z, s.z); s.w = __fmaf_rn(kr, e.w, s.w);
+    const uint64_t k2 = pk2(kr, kr);
+    set4(s, fma2(k2, pk2(e.x, e.y), pk2(s.x, s.y)), fma2(k2, pk2(e.z, e.w), pk2(s.z, s.w)));
 }
 // o += q_r S_r
 __device__ __forceinline__ void readout(const float4 &s, float qr, float4 &o) {
-    o.x = __fmaf_rn(qr, s.x, o.x); o.y = __fmaf_rn(qr, s.y, o.y);
-    o.z = __fmaf_rn(qr, s.z, o.z); o.w = __fmaf_rn(qr, s.w, o.w);
+    const uint64_t q2 = pk2(qr, qr);
+    set4(o, fma2(q2, pk2(s.x, s.y), pk2(o.x, o.y)), fma2(q2, pk2(s.z, s.w), pk2(o.z, o.w)));
 }
 // sum of the RG row-group partials of this thread's four columns, in row-group order
 template <int CWD>
@@ -51,8 +92,7 @@ __device__ __forceinline__ float4 sum_partials(const float (*red)[CWD], int cq) 
 #pragma unroll 8
     for (int r = 0; r < RG; ++r) {
         const float4 x = *reinterpret_cast<const float4 *>(&red[r][4 * cq]);
-        acc.x = __fadd_rn(acc.x, x.x); acc.y = __fadd_rn(acc.y, x.y);
-        acc.z = __fadd_rn(acc.z, x.z); acc.w = __fadd_rn(acc.w, x.w);
+        set4(acc, add2(pk2(acc.x, acc.y), pk2(x.x, x.y)), add2(pk2(acc.z, acc.w), pk2(x.z, x.w)));
     }
     return acc;
 }
