@@ -58,19 +58,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int col = blockIdx.y * CWD + 4 * cq;
     float *S = state + nh * (kD * kD);
 
-    // issue the state loads first; the gate math below overlaps their latency
+    // the token's small loads first, so that they do not queue behind the state's 64 KB;
+    // the gate math then overlaps the state loads' latency
+    float zc = 0.f;
+    __nv_bfloat16 kc = __float2bfloat16(0.f), qc = kc;
+    if (tid < kD) {
+        zc = z[nh * kD + tid];
+        kc = k[nh * kD + tid];
+        qc = q[nh * kD + tid];
+    } else if (tid == kD) {
+        zc = bgate[nh];
+    }
+    const uint2 vraw = *reinterpret_cast<const uint2 *>(v + nh * kD + col);
     float4 sv[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
 
     if (tid < kD) {
-        s_alpha[tid] = expf(decode_log_decay(A, h, z[nh * kD + tid]));
-        s_k[tid] = __bfloat162float(k[nh * kD + tid]);
-        s_q[tid] = __bfloat162float(q[nh * kD + tid]);
+        s_alpha[tid] = expf(decode_log_decay(A, h, zc));
+        s_k[tid] = __bfloat162float(kc);
+        s_q[tid] = __bfloat162float(qc);
     } else if (tid == kD) {
-        s_beta = sigmoid_f(bgate[nh]);
+        s_beta = sigmoid_f(zc);
     }
-    const uint2 vraw = *reinterpret_cast<const uint2 *>(v + nh * kD + col);
     const float2 v01 = bf16x2_to_float2(vraw.x), v23 = bf16x2_to_float2(vraw.y);
     __syncthreads();
 

@@ -67,22 +67,32 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     const int col = rank * CWD + 4 * cq;
     float *S = p.state + nh * (kD * kD);
 
-    float4 sv[RPT];
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
-
-    // ---- prologue: conv, Swish, squares for the L2 norms, gate ----
-    float hist[3][3], xin[3], act[3];
+    // ---- the prologue's small loads first, so that they do not queue behind the state ----
+    float hist[3][3], xin[3], act[3], zc = 0.f;
+    float4 wv[3];
+    const __nv_bfloat16 *xs[3] = {p.xq, p.xk, p.xv};
     if (tid < kD) {
         const int c = tid;
-        const __nv_bfloat16 *xs[3] = {p.xq, p.xk, p.xv};
 #pragma unroll
         for (int s = 0; s < 3; ++s) {
             xin[s] = __bfloat162float(xs[s][nh * kD + c]);
 #pragma unroll
             for (int j = 0; j < 3; ++j)
                 hist[s][j] = __bfloat162float(p.conv_state[(((n * 3 + s) * 3 + j) * p.H + h) * kD + c]);
-            const float4 w = *reinterpret_cast<const float4 *>(p.conv_w + (((int64_t)s * p.H + h) * kD + c) * 4);
+            wv[s] = *reinterpret_cast<const float4 *>(p.conv_w + (((int64_t)s * p.H + h) * kD + c) * 4);
+        }
+        zc = p.z[nh * kD + c];
+    }
+    float4 sv[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+
+    // ---- prologue: conv, Swish, squares for the L2 norms, gate ----
+    if (tid < kD) {
+        const int c = tid;
+#pragma unroll
+        for (int s = 0; s < 3; ++s) {
+            const float4 w = wv[s];
             float acc = __fmul_rn(w.x, hist[s][0]);
             acc = __fmaf_rn(w.y, hist[s][1], acc);
             acc = __fmaf_rn(w.z, hist[s][2], acc);
@@ -95,7 +105,7 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
             s_sq[0][tid >> 5] = sq;
             s_sq[1][tid >> 5] = sk;
         }
-        s_alpha[c] = expf(decode_log_decay(p.A, h, p.z[nh * kD + c]));
+        s_alpha[c] = expf(decode_log_decay(p.A, h, zc));
         if constexpr (NCTA == 1) {
             // one CTA per (sequence, head): the thread that read channel c's window writes it
 #pragma unroll
