@@ -141,12 +141,46 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     const int col = blockIdx.y * CWD + 4 * cq;
     const float *S = state + nh * (kD * kD);
 
+    // the first two staging items of this thread are loaded before the state, so that
+    // they do not queue behind its 64 KB; the rest after it
+    constexpr int kPre = 2;
+    float pre_z[kPre], pre_b = 0.f;
+    __nv_bfloat16 pre_k[kPre], pre_q[kPre], pre_v[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int idx = tid + u * kDecodeThreads;
+        pre_z[u] = 0.f;
+        pre_k[u] = pre_q[u] = pre_v[u] = __float2bfloat16(0.f);
+        if (idx < m * kD) {
+            const int64_t row = ((n * m + idx / kD) * H + h) * kD + idx % kD;
+            pre_z[u] = z[row];
+            pre_k[u] = k[row];
+            pre_q[u] = q[row];
+            pre_v[u] = v[row];
+        }
+    }
+    if (tid < m) pre_b = bgate[(n * m + tid) * H + h];
+
     float4 sv[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
 
     // stage every token's gate, k, q, v (and write the log while at it)
-    for (int idx = tid; idx < m * kD; idx += kDecodeThreads) {
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int idx = tid + u * kDecodeThreads;
+        if (idx < m * kD) {
+            const int t = idx / kD, c = idx % kD;
+            const int64_t row = ((n * m + t) * H + h) * kD + c;
+            const float la = decode_log_decay(A, h, pre_z[u]);
+            s_alpha[t][c] = expf(la);
+            s_k[t][c] = __bfloat162float(pre_k[u]);
+            s_q[t][c] = __bfloat162float(pre_q[u]);
+            s_v[t][c] = pre_v[u];
+            if (gk_log) gk_log[row] = la;
+        }
+    }
+    for (int idx = tid + kPre * kDecodeThreads; idx < m * kD; idx += kDecodeThreads) {
         const int t = idx / kD, c = idx % kD;
         const int64_t row = ((n * m + t) * H + h) * kD + c;
         const float la = decode_log_decay(A, h, z[row]);
@@ -158,7 +192,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     }
     if (tid < m) {
         const int64_t tok = (n * m + tid) * H + h;
-        const float beta = sigmoid_f(bgate[tok]);
+        const float beta = sigmoid_f(pre_b);
         s_beta[tid] = beta;
         if (beta_log) beta_log[tok] = beta;
     }
@@ -227,18 +261,47 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int col = blockIdx.y * CWD + 4 * cq;
     float *S = state + nh * (kD * kD);
 
+    // the first two staging items of this thread (four tokens) are loaded before the
+    // state, so that they do not queue behind its 64 KB; any further tokens after it
+    constexpr int kPre = 2;
+    float pre_g[kPre], pre_b = 0.f;
+    __nv_bfloat16 pre_k[kPre], pre_v[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int idx = tid + u * kDecodeThreads;
+        pre_g[u] = 0.f;
+        pre_k[u] = pre_v[u] = __float2bfloat16(0.f);
+        if (idx < a * kD) {
+            const int64_t row = ((n * m + idx / kD) * H + h) * kD + idx % kD;
+            pre_g[u] = gk_log[row];
+            pre_k[u] = k[row];
+            pre_v[u] = v[row];
+        }
+    }
+    if (tid < a) pre_b = beta_log[(n * m + tid) * H + h];
+
     float4 sv[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
 
-    for (int idx = tid; idx < a * kD; idx += kDecodeThreads) {
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int idx = tid + u * kDecodeThreads;
+        if (idx < a * kD) {
+            const int t = idx / kD, c = idx % kD;
+            s_alpha[t][c] = expf(pre_g[u]);
+            s_k[t][c] = __bfloat162float(pre_k[u]);
+            s_v[t][c] = __bfloat162float(pre_v[u]);
+        }
+    }
+    for (int idx = tid + kPre * kDecodeThreads; idx < a * kD; idx += kDecodeThreads) {
         const int t = idx / kD, c = idx % kD;
         const int64_t row = ((n * m + t) * H + h) * kD + c;
         s_alpha[t][c] = expf(gk_log[row]);
         s_k[t][c] = __bfloat162float(k[row]);
         s_v[t][c] = __bfloat162float(v[row]);
     }
-    if (tid < a) s_beta[tid] = beta_log[(n * m + tid) * H + h];
+    if (tid < a) s_beta[tid] = pre_b;
     __syncthreads();
 
     for (int t = 0; t < a; ++t) {
