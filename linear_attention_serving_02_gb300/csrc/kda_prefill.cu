@@ -948,6 +948,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             }
             tc::fence_before_sync();
             named_arrive(kBarU, 256);  // U^T planes complete; group 1 is done with [ -W ; Qhat ]
+            // U' of the next chunk: issued now, ahead of this chunk's output stores, so that
+            // it does not queue behind them (the registers are free once the planes are out)
+            if (c + 1 < c_end) load_up(c + 1);
             // o = (D_O1 + D_O2)^T for this thread's value channel
             float ov[64];
 #pragma unroll
@@ -992,9 +995,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                             reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(stage) + i * kD)[ch];
                 }
             }
-            named_sync(5, 128);  // staged tile read out before the next U^T planes land here
+            named_sync(5, 128);  // staged tile read out before the next output lands here
             }
-            if (c + 1 < c_end) load_up(c + 1);
         }
     } else {
         // ----------------- state warps (thread 128 issues the MMAs) -----------------
