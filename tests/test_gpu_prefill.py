@@ -172,12 +172,15 @@ def test_prefill_then_decode_equals_longer_prefill():
     assert_prefill_close(o_split.cpu(), state.cpu(), np64(o_long[0]), np64(S_long), "prefill + decode vs long")
 
 
-@pytest.mark.parametrize("lens,H", [([4000, 2000, 0, 900], 2), ([2000], 1), ([1700, 3000], 3)])
+@pytest.mark.parametrize("lens,H", [([4000, 2000, 0, 900], 2), ([2000], 1), ([1700, 3000], 3),
+                                    ([8000, 150, 0, 256, 257], 2)])
 def test_segmented_walk(lens, H):
     """Few long sequences take the segmented walk: per-segment affine state maps from
     walks started at zero and at the identity, chained per sequence, then every segment
-    walked again from its true input state. Ragged segment tails, an empty sequence and
-    a one-segment sequence included."""
+    walked again from its true input state. Ragged segment tails and an empty sequence
+    included; in the last case the segments are 4 chunks long, so the 150- and 256-token
+    sequences are one segment each (their whole walk runs in the first phase) and the
+    257-token one ends in a one-chunk segment."""
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
     inp = inputs.prefill_inputs(cu[-1], H, len(lens), seed=13, init_state=True)
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
