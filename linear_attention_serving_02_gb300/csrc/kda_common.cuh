@@ -1,6 +1,6 @@
 // Device helpers shared by the KDA kernels: the gate, tile geometry, the layout of
-// the per-chunk record that the intra-chunk kernel writes and the inter-chunk kernel
-// reads, and thin wrappers over the PTX used (mma.sync, ldmatrix, cp.async).
+// the per-chunk record that the intra-chunk kernel writes and the state walk reads, and
+// thin wrappers over the PTX used (mma.sync, ldmatrix, cp.async).
 #pragma once
 
 #include <cuda_bf16.h>

@@ -803,25 +803,26 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // and every accumulator row is one TMEM lane. Per chunk, two MMA groups:
 //   group 1   [D_U | D_O1] = S^T [ -W ; Qhat ]^T          N = 128, K = 128
 //   group 2   [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T      N = 192, K = 64
-// A walk that writes no outputs (a segment map) drops Qhat and A_qk: N = 64 and 128.
-// with U^T = U'^T + D_U, o = (D_O1 + D_O2)^T and S^T <- S^T Diag(gamma) + D_S.
+// with U^T = U'^T + D_U, o = (D_O1 + D_O2)^T and S^T <- S^T Diag(gamma) + D_S. A walk
+// that writes no outputs (a segment map) drops Qhat and A_qk: N = 64 and 128.
 // Every product is split-bf16 (hi*hi + hi*lo + lo*hi). S^T and U^T, the A operands, are
 // written as split planes straight into tensor memory by the threads that own their rows
 // (tcgen05.st); the record tiles in shared memory are the B operands.
 //
 // Eight warps with fixed roles:
 //   warps 0-3  U and O: thread = value channel dv (TMEM lane dv). After group 1 they
-//              build U^T; after group 2 they read the output accumulators, then stage
-//              o through shared memory and store it in 16-byte row chunks while the
-//              next chunk's group 1 runs.
+//              build U^T (and start loading the next chunk's U'); after group 2 they
+//              read the output accumulators, then stage o through shared memory and
+//              store it in 16-byte row chunks while the next chunk's group 1 runs.
 //   warps 4-7  state: thread = value channel dv, its 128 state entries in fp32
 //              registers. After group 2 they update S and write the next S^T planes.
 //              Thread 128 also issues the bulk copies (one chunk ahead, with an L2
 //              prefetch two chunks ahead) and the MMAs.
 // Named barriers hand the steps over: BAR_U (U^T planes ready), BAR_OR (output
 // accumulators read), and a state-warp barrier (S^T planes ready). Every role runs the
-// same barrier sequence whatever happens: a wait that gives up marks the CTA failed and
-// the rest of the walk skips its work but keeps the sequence.
+// same barrier sequence whatever happens: a wait that gives up marks the CTA failed, the
+// rest of the walk skips its work but keeps the sequence, and the issuer still commits
+// every MMA group so that the U and O warps' waits keep their arrivals in order.
 // ---------------------------------------------------------------------------------
 struct WalkSmem {
     unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
@@ -970,8 +971,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             }
             tc::fence_before_sync();
             named_arrive(kBarOR, 256);  // output accumulators read: the next group 1 may overwrite them
-            // stage o as [token][channel] in the U^T buffer (free until the next U epilogue)
-            // and write it out in 16-byte row chunks while the next group 1 runs
+            // stage o as [token][channel] in shared memory and write it out in 16-byte row
+            // chunks while the next group 1 runs
             if (write_o) {  // uniform over the CTA: the named barriers below stay matched
             float *stage = reinterpret_cast<float *>(s.ut);
 #pragma unroll
