@@ -1,12 +1,17 @@
-// KDA chunkwise prefill: three kernels on one stream.
+// KDA chunkwise prefill: kernels on one stream.
 //
-//   kda_plan_kernel   validate cu_seqlens, tabulate sequence starts and chunk offsets
-//   kda_intra_kernel  one CTA per (chunk, head), all chunks in parallel: gate and
-//                     cumulative decay, decayed K K^T / Q K^T per 16-token tile row,
-//                     UT transform T = (I + A_kk)^-1, W = T' Khat and U' = T' V
-//   kda_walk_kernel   one CTA per (sequence, head): walks the chunks in order with the
-//                     full state on chip, on tcgen05 tensor cores (TMEM accumulators),
+//   kda_plan_kernel   validate cu_seqlens, tabulate sequence starts and chunk offsets,
+//                     and the walk units of a plain walk
+//   kda_intra_kernel  persistent, one CTA per SM over the (chunk, head) items, all chunks
+//                     independent: gate and cumulative decay, decayed K K^T / Q K^T per
+//                     16-token tile row, UT transform T = (I + A_kk)^-1, W = T' Khat and
+//                     U' = T' V, written as a chunk record
+//   kda_walk_kernel   one CTA per walk unit (a run of chunks of one (sequence, head)):
+//                     walks the chunks in order with the full state on chip, on tcgen05
+//                     tensor cores (TMEM accumulators),
 //                     U = U' - W S;  O = Qhat S + A_qk U;  S = Diag(gamma) S + Kend^T U
+//   with few long sequences the walk is segmented (kda_segment_plan_kernel, two walk
+//   launches and kda_combine_kernel between them; see below)
 //
 // The algebra is the chunkwise form of 'From Linear Attention to KDA' (blog), §7.1-7.3
 // with the per-channel decay of §7.2 folded into the UT system, and the 16-token
