@@ -338,10 +338,11 @@ struct IntraSmem {
     __nv_bfloat16 ks[kC][kLd128];
     __nv_bfloat16 vs[kC][kLd128];
     union {
-        struct {  // operands of the decayed Gram products of one tile row
-            __nv_bfloat16 aq[2][kTile][kLd128];
-            __nv_bfloat16 ak[2][kTile][kLd128];
-            __nv_bfloat16 bk[2][kC][kLd128];
+        struct {  // operands of the decayed Gram products of one 32-token tile row,
+                  // 256-byte rows with the 16-byte chunks XOR-swizzled by row (gram_off)
+            __nv_bfloat16 aq[2][2 * kTile][kD];
+            __nv_bfloat16 ak[2][2 * kTile][kD];
+            __nv_bfloat16 bk[2][kC][kD];
         } g;
         struct {  // operands of W = T' Khat and U' = T' V
             __nv_bfloat16 kh[2][kC][kLd128];
@@ -351,6 +352,25 @@ struct IntraSmem {
 };
 
 constexpr int kIntraThreads = 512;
+
+// Byte offset of element (row, col) in a 256-byte-row bf16 Gram operand tile: the 16-byte
+// chunk index is XORed with row % 8, so that the eight rows one ldmatrix phase reads and
+// the rows a warp's 16-byte stores write fall on distinct banks without padding.
+__device__ __forceinline__ uint32_t gram_off(int row, int col) {
+    return (uint32_t)(row * (kD * 2) + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2);
+}
+// A fragment (16 x 16) at (row0, col0) of a swizzled Gram tile
+__device__ __forceinline__ void load_a_sw(uint32_t (&r)[4], const __nv_bfloat16 *base, int row0, int col0,
+                                          int lane) {
+    ldsm_x4(r, reinterpret_cast<const unsigned char *>(base) +
+                   gram_off(row0 + (lane & 15), col0 + ((lane >> 4) << 3)));
+}
+// B fragment of one n8 tile (rows n0..n0+7, stored [n][k]) of a swizzled Gram tile, k0..k0+15
+__device__ __forceinline__ void load_b_nk_sw(uint32_t &r0, uint32_t &r1, const __nv_bfloat16 *base, int n0,
+                                             int k0, int lane) {
+    ldsm_x2(r0, r1, reinterpret_cast<const unsigned char *>(base) +
+                        gram_off(n0 + (lane & 7), k0 + (((lane >> 3) & 1) << 3)));
+}
 
 __device__ __forceinline__ int find_seq(const int32_t *chunk_off, int32_t N, int32_t slot) {
     // largest n with chunk_off[n] <= slot (empty sequences share an offset and are skipped)
@@ -488,32 +508,45 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     cp_async_wait<2>();
     __syncthreads();  // q and k in place (v and the next chunk's z may still be in flight)
 
-    // ---- decayed Gram matrices, one 16-token tile row at a time -----------------
-    for (int a = 0; a < kC / kTile; ++a) {
-        const int r = a * kTile;  // reference token of this tile row
-        const int nb = r + kTile; // key rows j = 0 .. r+15
+    // ---- decayed Gram matrices, one 32-token tile row at a time -----------------
+    // Tile row a (tokens 32a .. 32a+31) takes the reference token m = 32a + 16, so that
+    // exp(G_i - G_j) = exp(G_i - G_m) * exp(G_m - G_j) with neither factor beyond e^80
+    // (at most 16 tokens of log decay >= -5 between i or j and m on the side where the
+    // factor exceeds 1), inside the range of fp32 and bf16; a factor that underflows
+    // belongs to a product below e^-20, negligible next to the O(1) entries.
+    for (int a = 0; a < kC / (2 * kTile); ++a) {
+        const int r0 = a * 2 * kTile;  // first token of the tile row
+        const int m = r0 + kTile;      // reference token
+        const int nb = r0 + 2 * kTile; // key rows j = 0 .. r0+31
         // Operands, 8 channels per item (16-byte loads and stores): the A operands (q and
-        // k of the tile row, sharing the factor exp(G_i - G_r)) are items 0 .. 255, the B
-        // operand (keys j = 0 .. r+15 with the factor exp(G_r - G_j)) the rest. A thread's
-        // channel slice, tid % 16, is the same for all its items, so G_r is read once.
+        // k of the tile row, sharing the factor exp(G_i - G_m)) are items 0 .. 511, the B
+        // operand (keys j with the factor exp(G_m - G_j)) the rest. A thread's channel
+        // slice, tid % 16, is the same for all its items, so G_m is read once.
         {
             const int c = (tid & 15) * 8;
-            float gr[8];
+            float gm[8];
             {
-                const float4 r0 = *reinterpret_cast<const float4 *>(&G[r][c]);
-                const float4 r1 = *reinterpret_cast<const float4 *>(&G[r][c + 4]);
-                gr[0] = r0.x; gr[1] = r0.y; gr[2] = r0.z; gr[3] = r0.w;
-                gr[4] = r1.x; gr[5] = r1.y; gr[6] = r1.z; gr[7] = r1.w;
+                const float4 m0 = *reinterpret_cast<const float4 *>(&G[m][c]);
+                const float4 m1 = *reinterpret_cast<const float4 *>(&G[m][c + 4]);
+                gm[0] = m0.x; gm[1] = m0.y; gm[2] = m0.z; gm[3] = m0.w;
+                gm[4] = m1.x; gm[5] = m1.y; gm[6] = m1.z; gm[7] = m1.w;
             }
-            for (int e = tid; e < (kTile + nb) * 16; e += kIntraThreads) {
-                const bool aside = e < kTile * 16;
-                const int row = aside ? r + (e >> 4) : (e >> 4) - kTile;  // token i (A side) or j (B side)
+            unsigned char *aqb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.aq[0][0][0]),
+                                     reinterpret_cast<unsigned char *>(&s.u.g.aq[1][0][0])};
+            unsigned char *akb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.ak[0][0][0]),
+                                     reinterpret_cast<unsigned char *>(&s.u.g.ak[1][0][0])};
+            unsigned char *bkb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.bk[0][0][0]),
+                                     reinterpret_cast<unsigned char *>(&s.u.g.bk[1][0][0])};
+            for (int e = tid; e < (2 * kTile + nb) * 16; e += kIntraThreads) {
+                const bool aside = e < 2 * kTile * 16;
+                const int ar = e >> 4;                                   // A-side row in the tile row
+                const int row = aside ? r0 + ar : ar - 2 * kTile;         // token i (A side) or j (B side)
                 const float4 g0 = *reinterpret_cast<const float4 *>(&G[row][c]);
                 const float4 g1 = *reinterpret_cast<const float4 *>(&G[row][c + 4]);
                 const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
                 float f[8];
 #pragma unroll
-                for (int m = 0; m < 8; ++m) f[m] = __expf(aside ? g[m] - gr[m] : gr[m] - g[m]);
+                for (int mm = 0; mm < 8; ++mm) f[mm] = __expf(aside ? g[mm] - gm[mm] : gm[mm] - g[mm]);
                 const uint4 kraw = *reinterpret_cast<const uint4 *>(&s.ks[row][c]);
                 const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
                 uint32_t kh[4], kl[4];
@@ -523,7 +556,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                     split_bf16x2(kk.x * f[2 * p2], kk.y * f[2 * p2 + 1], kh[p2], kl[p2]);
                 }
                 if (aside) {
-                    const int ar = e >> 4;
                     const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[row][c]);
                     const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
                     uint32_t qh[4], ql[4];
@@ -532,31 +564,38 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                         const float2 qq = bf16x2_to_float2(qw[p2]);
                         split_bf16x2(qq.x * f[2 * p2], qq.y * f[2 * p2 + 1], qh[p2], ql[p2]);
                     }
-                    *reinterpret_cast<uint4 *>(&s.u.g.aq[0][ar][c]) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-                    *reinterpret_cast<uint4 *>(&s.u.g.aq[1][ar][c]) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
-                    *reinterpret_cast<uint4 *>(&s.u.g.ak[0][ar][c]) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-                    *reinterpret_cast<uint4 *>(&s.u.g.ak[1][ar][c]) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+                    const uint32_t off = gram_off(ar, c);
+                    *reinterpret_cast<uint4 *>(aqb[0] + off) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+                    *reinterpret_cast<uint4 *>(aqb[1] + off) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+                    *reinterpret_cast<uint4 *>(akb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                    *reinterpret_cast<uint4 *>(akb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
                 } else {
-                    *reinterpret_cast<uint4 *>(&s.u.g.bk[0][row][c]) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-                    *reinterpret_cast<uint4 *>(&s.u.g.bk[1][row][c]) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+                    const uint32_t off = gram_off(row, c);
+                    *reinterpret_cast<uint4 *>(bkb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                    *reinterpret_cast<uint4 *>(bkb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
                 }
             }
         }
         __syncthreads();
-        const int ntiles = nb / 8;  // n8 tiles of key rows
-        for (int p = warp; p < 2 * ntiles; p += kIntraThreads / 32) {
-            const int mat = p / ntiles;  // 0: A_qk, 1: A_kk
-            const int nt = p % ntiles;
+        // MMA tasks: (matrix, 16-row m tile, 8-key n tile), skipping n tiles wholly above
+        // the diagonal: m tile 0 (rows r0..r0+15) takes keys below r0+16, m tile 1 all
+        const int nt0 = (r0 + kTile) / 8, nt1 = nb / 8;  // n tiles of m tile 0 and of m tile 1
+        const int per_mat = nt0 + nt1;
+        for (int p = warp; p < 2 * per_mat; p += kIntraThreads / 32) {
+            const int mat = p / per_mat;  // 0: A_qk, 1: A_kk
+            const int q = p % per_mat;
+            const int mt = q < nt0 ? 0 : 1;
+            const int nt = mt == 0 ? q : q - nt0;
             const __nv_bfloat16 *ah_base = mat ? &s.u.g.ak[0][0][0] : &s.u.g.aq[0][0][0];
             const __nv_bfloat16 *al_base = mat ? &s.u.g.ak[1][0][0] : &s.u.g.aq[1][0][0];
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
                 uint32_t ah[4], al[4], bh0, bh1, bl0, bl1;
-                load_a(ah, ah_base, kLd128, 0, ks * 16, lane);
-                load_a(al, al_base, kLd128, 0, ks * 16, lane);
-                load_b_nk(bh0, bh1, &s.u.g.bk[0][0][0], kLd128, nt * 8, ks * 16, lane);
-                load_b_nk(bl0, bl1, &s.u.g.bk[1][0][0], kLd128, nt * 8, ks * 16, lane);
+                load_a_sw(ah, ah_base, mt * kTile, ks * 16, lane);
+                load_a_sw(al, al_base, mt * kTile, ks * 16, lane);
+                load_b_nk_sw(bh0, bh1, &s.u.g.bk[0][0][0], nt * 8, ks * 16, lane);
+                load_b_nk_sw(bl0, bl1, &s.u.g.bk[1][0][0], nt * 8, ks * 16, lane);
                 mma_bf16(a0, ah, bh0, bh1);  // the three split products in separate chains
                 mma_bf16(a1, ah, bl0, bl1);
                 mma_bf16(a2, al, bh0, bh1);
@@ -565,10 +604,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[e] = a0[e] + (a1[e] + a2[e]);
             const int g = lane >> 2, t4 = lane & 3;
+            const int ib = r0 + mt * kTile + g;
             if (mat == 0) {  // A_qk (diagonal included), split, into the record
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int i = r + g + hr * 8, j = nt * 8 + 2 * t4;
+                    const int i = ib + hr * 8, j = nt * 8 + 2 * t4;
                     uint32_t hi, lo;
                     split_bf16x2(j <= i ? acc[2 * hr] : 0.f, j + 1 <= i ? acc[2 * hr + 1] : 0.f, hi, lo);
                     *reinterpret_cast<uint32_t *>(rec + kRecAqk + il_off(i, j, kC)) = hi;
@@ -577,7 +617,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int i = r + g + ((e >> 1) << 3);
+                    const int i = ib + ((e >> 1) << 3);
                     const int j = nt * 8 + 2 * t4 + (e & 1);
                     s.Akk[i][j] = (j < i) ? s.beta[i] * acc[e] : 0.f;
                 }
