@@ -4,7 +4,7 @@
 //                     and the walk units of a plain walk
 //   kda_intra_kernel  persistent, one CTA per SM over the (chunk, head) items, all chunks
 //                     independent: gate and cumulative decay, decayed K K^T / Q K^T per
-//                     16-token tile row, UT transform T = (I + A_kk)^-1, W = T' Khat and
+//                     32-token tile row, UT transform T = (I + A_kk)^-1, W = T' Khat and
 //                     U' = T' V, written as a chunk record
 //   kda_walk_kernel   one CTA per walk unit (a run of chunks of one (sequence, head)):
 //                     walks the chunks in order with the full state on chip, on tcgen05
@@ -14,8 +14,8 @@
 //   launches and kda_combine_kernel between them; see below)
 //
 // The algebra is the chunkwise form of 'From Linear Attention to KDA' (blog), §7.1-7.3
-// with the per-channel decay of §7.2 folded into the UT system, and the 16-token
-// tiles of §8 for the decayed Gram matrices. Inside one chunk (positions i, j):
+// with the per-channel decay of §7.2 folded into the UT system, and tiles as in §8 for
+// the decayed Gram matrices. Inside one chunk (positions i, j):
 //   G_i        = sum_{m<=i} log a_m                (fp32, per key channel)
 //   A_kk[i,j]  = beta_i sum_c k_i k_j exp(G_i - G_j)    j <  i
 //   A_qk[i,j]  =        sum_c q_i k_j exp(G_i - G_j)    j <= i
@@ -30,10 +30,11 @@
 // prediction-error cancellation in U = U' - W S amplifies beyond the accuracy the
 // outputs are held to; the split keeps about 16 mantissa bits.
 //
-// Decay factors never overflow: for tile row a (tokens 16a..16a+15) the reference
-// point is r = 16a, and exp(G_i - G_j) = exp(G_i - G_r) * exp(G_r - G_j). The first
-// factor is <= 1; the second is <= 1 for j <= r and at most e^75 (15 tokens of at most
-// -5 each, §5.4 of the blog) inside the diagonal tile, within bf16/fp32 range.
+// Decay factors never overflow: for the 32-token tile row a (tokens 32a..32a+31) the
+// reference point is m = 32a + 16, and exp(G_i - G_j) = exp(G_i - G_m) * exp(G_m - G_j).
+// A factor exceeds 1 only across the at most 16 tokens between m and a row of the tile
+// row (log decay >= -5 per token, §5.4 of the blog), so neither exceeds e^80, within
+// bf16/fp32 range (the blog's §8 uses 16-token sub-chunks; the middle reference allows 32).
 
 #include <algorithm>
 
