@@ -366,6 +366,13 @@ __device__ __forceinline__ void load_a_sw(uint32_t (&r)[4], const __nv_bfloat16 
     ldsm_x4(r, reinterpret_cast<const unsigned char *>(base) +
                    gram_off(row0 + (lane & 15), col0 + ((lane >> 4) << 3)));
 }
+// B fragments of two n8 tiles (rows n0..n0+15, stored [n][k]) of a swizzled Gram tile,
+// k0..k0+15: r[0], r[1] = tile n0; r[2], r[3] = tile n0 + 8
+__device__ __forceinline__ void load_b_nk16_sw(uint32_t (&r)[4], const __nv_bfloat16 *base, int n0, int k0,
+                                               int lane) {
+    ldsm_x4(r, reinterpret_cast<const unsigned char *>(base) +
+                   gram_off(n0 + (lane & 7) + ((lane >> 4) << 3), k0 + (((lane >> 3) & 1) << 3)));
+}
 // B fragment of one n8 tile (rows n0..n0+7, stored [n][k]) of a swizzled Gram tile, k0..k0+15
 __device__ __forceinline__ void load_b_nk_sw(uint32_t &r0, uint32_t &r1, const __nv_bfloat16 *base, int n0,
                                              int k0, int lane) {
@@ -578,49 +585,61 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             }
         }
         __syncthreads();
-        // MMA tasks: (matrix, 16-row m tile, 8-key n tile), skipping n tiles wholly above
-        // the diagonal: m tile 0 (rows r0..r0+15) takes keys below r0+16, m tile 1 all
-        const int nt0 = (r0 + kTile) / 8, nt1 = nb / 8;  // n tiles of m tile 0 and of m tile 1
-        const int per_mat = nt0 + nt1;
+        // MMA tasks: (matrix, 16-row m tile, 16-key n tile: two n8 tiles sharing the A
+        // fragments), skipping n tiles wholly above the diagonal: m tile 0 (rows r0..r0+15)
+        // takes keys below r0+16, m tile 1 all keys below r0+32
+        const int n16_0 = (r0 + kTile) / 16, n16_1 = nb / 16;
+        const int per_mat = n16_0 + n16_1;
         for (int p = warp; p < 2 * per_mat; p += kIntraThreads / 32) {
             const int mat = p / per_mat;  // 0: A_qk, 1: A_kk
             const int q = p % per_mat;
-            const int mt = q < nt0 ? 0 : 1;
-            const int nt = mt == 0 ? q : q - nt0;
+            const int mt = q < n16_0 ? 0 : 1;
+            const int n0 = (mt == 0 ? q : q - n16_0) * 16;
             const __nv_bfloat16 *ah_base = mat ? &s.u.g.ak[0][0][0] : &s.u.g.aq[0][0][0];
             const __nv_bfloat16 *al_base = mat ? &s.u.g.ak[1][0][0] : &s.u.g.aq[1][0][0];
-            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+            float a0[2][4], a1[2][4], a2[2][4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a0[h2][e] = a1[h2][e] = a2[h2][e] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
-                uint32_t ah[4], al[4], bh0, bh1, bl0, bl1;
+                uint32_t ah[4], al[4], bh[4], bl[4];
                 load_a_sw(ah, ah_base, mt * kTile, ks * 16, lane);
                 load_a_sw(al, al_base, mt * kTile, ks * 16, lane);
-                load_b_nk_sw(bh0, bh1, &s.u.g.bk[0][0][0], nt * 8, ks * 16, lane);
-                load_b_nk_sw(bl0, bl1, &s.u.g.bk[1][0][0], nt * 8, ks * 16, lane);
-                mma_bf16(a0, ah, bh0, bh1);  // the three split products in separate chains
-                mma_bf16(a1, ah, bl0, bl1);
-                mma_bf16(a2, al, bh0, bh1);
-            }
-            float acc[4];
+                load_b_nk16_sw(bh, &s.u.g.bk[0][0][0], n0, ks * 16, lane);
+                load_b_nk16_sw(bl, &s.u.g.bk[1][0][0], n0, ks * 16, lane);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = a0[e] + (a1[e] + a2[e]);
+                for (int h2 = 0; h2 < 2; ++h2) {  // the three split products in separate chains
+                    mma_bf16(a0[h2], ah, bh[2 * h2], bh[2 * h2 + 1]);
+                    mma_bf16(a1[h2], ah, bl[2 * h2], bl[2 * h2 + 1]);
+                    mma_bf16(a2[h2], al, bh[2 * h2], bh[2 * h2 + 1]);
+                }
+            }
             const int g = lane >> 2, t4 = lane & 3;
             const int ib = r0 + mt * kTile + g;
-            if (mat == 0) {  // A_qk (diagonal included), split, into the record
 #pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int i = ib + hr * 8, j = nt * 8 + 2 * t4;
-                    uint32_t hi, lo;
-                    split_bf16x2(j <= i ? acc[2 * hr] : 0.f, j + 1 <= i ? acc[2 * hr + 1] : 0.f, hi, lo);
-                    *reinterpret_cast<uint32_t *>(rec + kRecAqk + il_off(i, j, kC)) = hi;
-                    *reinterpret_cast<uint32_t *>(rec + kRecAqk + kStackAK + il_off(i, j, kC)) = lo;
-                }
-            } else {
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float acc[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = ib + ((e >> 1) << 3);
-                    const int j = nt * 8 + 2 * t4 + (e & 1);
-                    s.Akk[i][j] = (j < i) ? s.beta[i] * acc[e] : 0.f;
+                for (int e = 0; e < 4; ++e) acc[e] = a0[h2][e] + (a1[h2][e] + a2[h2][e]);
+                const int jb = n0 + h2 * 8 + 2 * t4;
+                if (mat == 0) {  // A_qk (diagonal included), split, into the record
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int i = ib + hr * 8, j = jb;
+                        uint32_t hi, lo;
+                        split_bf16x2(j <= i ? acc[2 * hr] : 0.f, j + 1 <= i ? acc[2 * hr + 1] : 0.f, hi, lo);
+                        *reinterpret_cast<uint32_t *>(rec + kRecAqk + il_off(i, j, kC)) = hi;
+                        *reinterpret_cast<uint32_t *>(rec + kRecAqk + kStackAK + il_off(i, j, kC)) = lo;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = ib + ((e >> 1) << 3);
+                        const int j = jb + (e & 1);
+                        s.Akk[i][j] = (j < i) ? s.beta[i] * acc[e] : 0.f;
+                    }
                 }
             }
         }
