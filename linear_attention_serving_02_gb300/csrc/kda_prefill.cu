@@ -353,6 +353,7 @@ struct IntraSmem {
 };
 
 constexpr int kIntraThreads = 512;
+constexpr int kSolveWarps = 8;  // the UT solve's warps; the other eight write the record's elementwise parts
 
 // Byte offset of element (row, col) in a 256-byte-row bf16 Gram operand tile: the 16-byte
 // chunk index is XORed with row % 8, so that the eight rows one ldmatrix phase reads and
@@ -486,15 +487,18 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
     {
         // thread (column c, quarter qt) takes 16 consecutive rows of its column: the gate
-        // log a = g_min sigmoid(e^A z) (the division by __fdividef: 2 ulp; an infinite
-        // denominator, z = -inf, gives 0, i.e. a = 1 exactly), then its running sum in
-        // registers; the totals of the quarters below are added after one barrier
+        // log a = g_min sigmoid(e^A z), then its running sum in registers; the totals of
+        // the quarters below are added after one barrier. The exponential is __expf: its
+        // error grows with |e^A z|, but where that is large the sigmoid saturates, and
+        // where the sigmoid is sensitive (|e^A z| < ~5) the relative error is ~3e-7, so
+        // log a moves by < 1e-6. The division is __fdividef (2 ulp; an infinite
+        // denominator, z = -inf, gives 0, i.e. a = 1 exactly).
         const int c = tid % kD, qt = tid / kD;
         float g[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
             const int i = qt * 16 + m;
-            g[m] = (i < L) ? __fdividef(kGMin, 1.0f + expf(-eA * G[i][c])) : 0.f;
+            g[m] = (i < L) ? __fdividef(kGMin, 1.0f + __expf(-eA * G[i][c])) : 0.f;
         }
 #pragma unroll
         for (int m = 1; m < 16; ++m) g[m] += g[m - 1];
@@ -649,7 +653,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // ---- UT transform on warps 0-7: T = (I + A_kk)^-1, unit lower triangular. -----
     // ---- Meanwhile warps 8-15 write Qhat, Kend^T and gamma to the record and build -
     // ---- the Khat operand planes: they need only q, k and G. -----------------------
-    if (warp < 8) {
+    if (warp < kSolveWarps) {
         // diagonal 16x16 blocks, warp a solving block a: lane i holds row i of A_aa and
         // of T_aa in registers (lanes 16-31 mirror lanes 0-15 and store nothing); T
         // starts as I and, for m = 0 .. 14 in order, every row i > m subtracts
@@ -680,12 +684,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                         make_float4(t[q4], t[q4 + 1], t[q4 + 2], t[q4 + 3]);
             }
         } else {
-            for (int e = tid - 128; e < kC * kC; e += 128) {
+            for (int e = tid - 128; e < kC * kC; e += kSolveWarps * 32 - 128) {
                 const int i = e / kC, j = e % kC;
                 if ((j >> 4) > (i >> 4)) s.T[i][j] = 0.f;
             }
         }
-        named_sync(1, 256);
+        named_sync(1, kSolveWarps * 32);
         // off-diagonal blocks by distance l: T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb.
         // Thread (block, row rr, column quad cq) makes four outputs, reading a float4 of
         // A along k and a float4 of T per k: about one shared load per three FMAs.
@@ -709,7 +713,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 }
                 *reinterpret_cast<float4 *>(&s.X[blk][rr][cq]) = acc;
             }
-            named_sync(1, 256);
+            named_sync(1, kSolveWarps * 32);
             if (tid < nblk * 64) {
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -725,16 +729,17 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 *reinterpret_cast<float4 *>(&s.T[a * kTile + rr][b * kTile + cq]) =
                     make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
             }
-            named_sync(1, 256);
+            named_sync(1, kSolveWarps * 32);
         }
     } else {
-        const int t2 = tid - 256;
+        const int t2 = tid - kSolveWarps * 32;
+        constexpr int kElemThreads = kIntraThreads - kSolveWarps * 32;
         // Khat = k * exp(G) (the B operand of W, into the dead Gram operand space) and
         // Qhat = q * exp(G) (into the record) share their factors: one thread makes 8
         // channels of one row of both, as 16-byte chunks; consecutive threads fill
         // consecutive 16-byte chunks of the record tile
         uint8_t *Qh = rec + kRecQh;
-        for (int e = t2; e < kC * (kD / 8); e += 256) {
+        for (int e = t2; e < kC * (kD / 8); e += kElemThreads) {
             const int c8 = (e >> 3) & 15, i = (e >> 7) * 8 + (e & 7), c = c8 * 8;
             const float4 g0 = *reinterpret_cast<const float4 *>(&G[i][c]);
             const float4 g1 = *reinterpret_cast<const float4 *>(&G[i][c + 4]);
@@ -756,7 +761,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             *reinterpret_cast<uint4 *>(&s.u.w.kh[1][i][c]) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
         }
         uint8_t *KeT = rec + kRecKeT;
-        for (int e = t2; e < kD * (kC / 8); e += 256) {
+        for (int e = t2; e < kD * (kC / 8); e += kElemThreads) {
             const int j8 = (e >> 3) & 7, c = (e >> 6) * 8 + (e & 7), j = j8 * 8;
             const float gl = G[kC - 1][c];
             float x[8];
