@@ -132,11 +132,13 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest x over all ranks (on the device with NCCL, on the host with gloo)."""
     if world <= 1:
         return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
