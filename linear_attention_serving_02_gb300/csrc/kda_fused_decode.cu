@@ -16,6 +16,11 @@
 // shares the output's sum of squares through distributed shared memory, and each CTA
 // writes back its own quarter of the conv state once the cluster barrier shows that
 // every CTA has read the old one.
+//
+// The step's small inputs (x, the conv state, the taps, z, g and w_norm: 10.5 KB) are
+// copied into shared memory with cp.async before the state's 64 KB are requested, so they
+// are not queued behind the state and hold no registers while it is in flight. That keeps
+// the kernel within 80 registers, three CTAs per SM, as the plain decode.
 
 #include <cooperative_groups.h>
 
@@ -37,6 +42,55 @@ struct FusedArgs {
     int32_t H;
 };
 
+// Shared-memory image of one (sequence, head)'s small inputs; every array is a whole
+// number of 16-byte chunks.
+struct FusedStage {
+    __nv_bfloat16 x[3][kD];        // x_q, x_k, x_v of this token
+    __nv_bfloat16 hist[3][3][kD];  // the three previous inputs of each stream, oldest first
+    float4 w[3][kD];               // the four taps of each stream and channel
+    float z[kD], g[kD], nw[kD];
+};
+constexpr int kRowChunks = kD * 2 / 16;                          // 16-byte chunks in a bf16 row of 128
+constexpr int kStageChunks = 12 * kRowChunks + 3 * kD + 3 * 32;  // x, hist, taps, z / g / w_norm
+
+// Issue the cp.async of chunk i of the stage (i < kStageChunks).
+__device__ __forceinline__ void stage_chunk(FusedStage &st, const FusedArgs &p, int64_t n, int h, int64_t nh,
+                                            int i) {
+    if (i < 3 * kRowChunks) {  // x_q, x_k, x_v
+        const int s = i / kRowChunks, j = i % kRowChunks;
+        const __nv_bfloat16 *xs = s == 0 ? p.xq : (s == 1 ? p.xk : p.xv);
+        cp_async16(&st.x[s][8 * j], xs + nh * kD + 8 * j);
+        return;
+    }
+    i -= 3 * kRowChunks;
+    if (i < 9 * kRowChunks) {  // conv state rows (stream s, age r)
+        const int sr = i / kRowChunks, j = i % kRowChunks;
+        cp_async16(&st.hist[sr / 3][sr % 3][8 * j], p.conv_state + ((n * 9 + sr) * p.H + h) * kD + 8 * j);
+        return;
+    }
+    i -= 9 * kRowChunks;
+    if (i < 3 * kD) {  // taps: one chunk per (stream, channel)
+        const int s = i / kD, c = i % kD;
+        cp_async16(&st.w[s][c], p.conv_w + (((int64_t)s * p.H + h) * kD + c) * 4);
+        return;
+    }
+    i -= 3 * kD;
+    const int a = i / 32, j = i % 32;  // z, g, w_norm: 32 chunks of four floats each
+    float *dst = a == 0 ? st.z : (a == 1 ? st.g : st.nw);
+    const float *src = a == 0 ? p.z + nh * kD : (a == 1 ? p.g + nh * kD : p.norm_w);
+    cp_async16(dst + 4 * j, src + 4 * j);
+}
+
+// Write chunk i of the shifted conv state: age 0 <- age 1, age 1 <- age 2, age 2 <- x.
+// Chunk i covers 8 channels of one (stream, age) row; bf16 bits are copied unchanged.
+__device__ __forceinline__ void write_conv_chunk(const FusedStage &st, const FusedArgs &p, int64_t n, int h,
+                                                 int sr, int j) {
+    const int s = sr / 3, r = sr % 3;
+    const __nv_bfloat16 *src = r < 2 ? &st.hist[s][r + 1][8 * j] : &st.x[s][8 * j];
+    *reinterpret_cast<uint4 *>(p.conv_state + ((n * 9 + sr) * p.H + h) * kD + 8 * j) =
+        *reinterpret_cast<const uint4 *>(src);
+}
+
 __device__ __forceinline__ float swish_f(float x) { return x / (1.0f + expf(-x)); }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -51,6 +105,7 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     constexpr int LPR = G::LPR, RG = G::RG, RPT = G::RPT;
     constexpr int NCTA = kD / CWD;  // CTAs per (sequence, head)
 
+    __shared__ __align__(16) FusedStage st;
     __shared__ float s_alpha[kD], s_k[kD], s_q[kD];
     __shared__ __align__(16) float s_v[kD];  // read as float4
     __shared__ __align__(16) float s_red[RG][CWD];
@@ -67,66 +122,64 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     const int col = rank * CWD + 4 * cq;
     float *S = p.state + nh * (kD * kD);
 
-    // ---- the prologue's small loads first, so that they do not queue behind the state ----
-    float hist[3][3], xin[3], act[3], zc = 0.f;
-    float4 wv[3];
-    const __nv_bfloat16 *xs[3] = {p.xq, p.xk, p.xv};
-    if (tid < kD) {
-        const int c = tid;
-#pragma unroll
-        for (int s = 0; s < 3; ++s) {
-            xin[s] = __bfloat162float(xs[s][nh * kD + c]);
-#pragma unroll
-            for (int j = 0; j < 3; ++j)
-                hist[s][j] = __bfloat162float(p.conv_state[(((n * 3 + s) * 3 + j) * p.H + h) * kD + c]);
-            wv[s] = *reinterpret_cast<const float4 *>(p.conv_w + (((int64_t)s * p.H + h) * kD + c) * 4);
-        }
-        zc = p.z[nh * kD + c];
-    }
+    // ---- the small inputs first, into shared memory; then the state, into registers ----
+    for (int i = tid; i < kStageChunks; i += kDecodeThreads) stage_chunk(st, p, n, h, nh, i);
+    cp_async_commit();
+    const float Ah = p.A[h];
+    const float bv = tid == kD ? p.b[nh] : 0.f;
     float4 sv[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+    cp_async_wait<0>();
+    __syncthreads();
 
     // ---- prologue: conv, Swish, squares for the L2 norms, gate ----
     if (tid < kD) {
         const int c = tid;
+        float act[3];
 #pragma unroll
         for (int s = 0; s < 3; ++s) {
-            const float4 w = wv[s];
-            float acc = __fmul_rn(w.x, hist[s][0]);
-            acc = __fmaf_rn(w.y, hist[s][1], acc);
-            acc = __fmaf_rn(w.z, hist[s][2], acc);
-            acc = __fmaf_rn(w.w, xin[s], acc);
+            const float4 w = st.w[s][c];
+            float acc = __fmul_rn(w.x, __bfloat162float(st.hist[s][0][c]));
+            acc = __fmaf_rn(w.y, __bfloat162float(st.hist[s][1][c]), acc);
+            acc = __fmaf_rn(w.z, __bfloat162float(st.hist[s][2][c]), acc);
+            acc = __fmaf_rn(w.w, __bfloat162float(st.x[s][c]), acc);
             act[s] = swish_f(acc);
         }
+        s_q[c] = act[0];  // normalised below, once the sums of squares are in
+        s_k[c] = act[1];
         s_v[c] = act[2];
         const float sq = warp_sum(act[0] * act[0]), sk = warp_sum(act[1] * act[1]);
         if ((tid & 31) == 0) {
             s_sq[0][tid >> 5] = sq;
             s_sq[1][tid >> 5] = sk;
         }
-        s_alpha[c] = expf(decode_log_decay(p.A, h, zc));
+        s_alpha[c] = expf(gate_log_decay(expf(Ah), st.z[c]));
+    } else {
+        if (tid == kD) s_beta = sigmoid_f(bv);
         if constexpr (NCTA == 1) {
-            // one CTA per (sequence, head): the thread that read channel c's window writes it
-#pragma unroll
-            for (int s = 0; s < 3; ++s) {
-                __nv_bfloat16 *cs = p.conv_state + ((n * 3 + s) * 3) * p.H * kD + h * kD + c;
-                cs[0] = __float2bfloat16_rn(hist[s][1]);
-                cs[(int64_t)p.H * kD] = __float2bfloat16_rn(hist[s][2]);
-                cs[(int64_t)2 * p.H * kD] = xs[s][nh * kD + c];
-            }
+            // the only reader of this (sequence, head)'s conv state has staged it: shift it
+            for (int i = tid - kD; i < 9 * kRowChunks; i += kDecodeThreads - kD)
+                write_conv_chunk(st, p, n, h, i / kRowChunks, i % kRowChunks);
         }
-    } else if (tid == kD) {
-        s_beta = sigmoid_f(p.b[nh]);
     }
     __syncthreads();
     if (tid < kD) {
         const float nq = (s_sq[0][0] + s_sq[0][1]) + (s_sq[0][2] + s_sq[0][3]);
         const float nk = (s_sq[1][0] + s_sq[1][1]) + (s_sq[1][2] + s_sq[1][3]);
-        s_q[tid] = act[0] / sqrtf(nq + p.eps_l2);
-        s_k[tid] = act[1] / sqrtf(nk + p.eps_l2);
+        s_q[tid] = s_q[tid] / sqrtf(nq + p.eps_l2);
+        s_k[tid] = s_k[tid] / sqrtf(nk + p.eps_l2);
     }
-    if constexpr (NCTA > 1) cg::this_cluster().sync();  // every CTA of the cluster runs before any DSMEM write
+    if constexpr (NCTA > 1) {
+        // every CTA of the cluster has staged the old conv state (and runs) before any
+        // conv-state or DSMEM write; each CTA then shifts its own quarter of the channels
+        cg::this_cluster().sync();
+        constexpr int QC = kRowChunks / NCTA;  // chunks of a row in one quarter
+        if (tid >= kD && tid - kD < 9 * QC) {
+            const int i = tid - kD;
+            write_conv_chunk(st, p, n, h, i / QC, rank * QC + i % QC);
+        }
+    }
     __syncthreads();
 
     // ---- the recurrent update ----
@@ -172,7 +225,7 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
         }
     }
     if constexpr (NCTA > 1) {
-        cg::this_cluster().sync();  // partials delivered; every CTA has read the old conv state
+        cg::this_cluster().sync();  // every CTA's partial delivered
     } else {
         __syncthreads();
     }
@@ -181,8 +234,8 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
 #pragma unroll
         for (int r = 0; r < NCTA; ++r) tot += s_oo[r];
         const float inv = 1.0f / sqrtf(tot * (1.0f / kD) + p.eps_rms);
-        const float4 w = *reinterpret_cast<const float4 *>(p.norm_w + col);
-        const float4 gg = *reinterpret_cast<const float4 *>(p.g + nh * kD + col);
+        const float4 w = *reinterpret_cast<const float4 *>(&st.nw[col]);
+        const float4 gg = *reinterpret_cast<const float4 *>(&st.g[col]);
         float4 yv;
         yv.x = O.x * inv * w.x * sigmoid_f(gg.x);
         yv.y = O.y * inv * w.y * sigmoid_f(gg.y);
@@ -190,24 +243,13 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
         yv.w = O.w * inv * w.w * sigmoid_f(gg.w);
         *reinterpret_cast<float4 *>(p.y + nh * kD + col) = yv;
     }
-    if (NCTA > 1 && tid < kD && (tid / CWD) == rank) {
-        // this CTA's quarter of the conv state, after the cluster barrier above
-        const int c = tid;
-#pragma unroll
-        for (int s = 0; s < 3; ++s) {
-            __nv_bfloat16 *cs = p.conv_state + ((n * 3 + s) * 3) * p.H * kD + h * kD + c;
-            cs[0] = __float2bfloat16_rn(hist[s][1]);
-            cs[(int64_t)p.H * kD] = __float2bfloat16_rn(hist[s][2]);
-            cs[(int64_t)2 * p.H * kD] = __float2bfloat16_rn(xin[s]);
-        }
-    }
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 2) kda_fused_decode_kernel(FusedArgs p) {
+__global__ void __launch_bounds__(kDecodeThreads, 3) kda_fused_decode_kernel(FusedArgs p) {
     fused_decode_body<128>(p);
 }
 
-__global__ void __cluster_dims__(1, 4, 1) __launch_bounds__(kDecodeThreads, 2)
+__global__ void __cluster_dims__(1, 4, 1) __launch_bounds__(kDecodeThreads, 3)
     kda_fused_decode_cluster_kernel(FusedArgs p) {
     fused_decode_body<32>(p);
 }
