@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const uint2 vraw = *reinterpret_cast<const uint2 *>(v + nh * kD + col);
     float4 sv[RPT];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + row_of<CWD>(rg, i) * kD + col));
 
     if (tid < kD) {
         s_alpha[tid] = expf(decode_log_decay(A, h, zc));
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const int row = rg + i * RG;
+        const int row = row_of<CWD>(rg, i);
         decay_project(sv[i], s_alpha[row], s_k[row], p);
     }
     *reinterpret_cast<float4 *>(&s_red[rg][4 * cq]) = p;
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     float4 oq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const int row = rg + i * RG;
+        const int row = row_of<CWD>(rg, i);
         rank1(sv[i], s_k[row], e);
         __stcs(reinterpret_cast<float4 *>(S + row * kD + col), sv[i]);
         readout(sv[i], s_q[row], oq);
@@ -127,7 +127,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 
     // v stays bf16 in shared memory (each thread converts only its own four columns),
     // which keeps the static total under 48 KB
-    __shared__ float s_alpha[kMaxReplay][kD], s_k[kMaxReplay][kD], s_q[kMaxReplay][kD];
+    __shared__ __align__(16) float s_alpha[kMaxReplay][kD];  // read four rows at a time
+    __shared__ __align__(16) float s_k[kMaxReplay][kD];
+    __shared__ __align__(16) float s_q[kMaxReplay][kD];
     __shared__ __align__(16) __nv_bfloat16 s_v[kMaxReplay][kD];
     __shared__ float s_beta[kMaxReplay];
     __shared__ __align__(16) float s_redp[2][RG][CWD];
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 
     float4 sv[RPT];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + row_of<CWD>(rg, i) * kD + col));
 
     // stage every token's gate, k, q, v (and write the log while at it)
 #pragma unroll
@@ -202,10 +204,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     // token t is summed after the barrier of token t + 1.
     for (int t = 0; t < m; ++t) {
         float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 a4, k4, q4;
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
-            const int row = rg + i * RG;
-            decay_project(sv[i], s_alpha[t][row], s_k[t][row], p);
+            if ((i & 3) == 0) a4 = rows4<CWD>(s_alpha[t], rg, i), k4 = rows4<CWD>(s_k[t], rg, i);
+            decay_project(sv[i], lane4(a4, i & 3), lane4(k4, i & 3), p);
         }
         *reinterpret_cast<float4 *>(&s_redp[t & 1][rg][4 * cq]) = p;
         __syncthreads();
@@ -219,9 +222,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
         float4 oq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
-            const int row = rg + i * RG;
-            rank1(sv[i], s_k[t][row], e);
-            readout(sv[i], s_q[t][row], oq);
+            if ((i & 3) == 0) k4 = rows4<CWD>(s_k[t], rg, i), q4 = rows4<CWD>(s_q[t], rg, i);
+            rank1(sv[i], lane4(k4, i & 3), e);
+            readout(sv[i], lane4(q4, i & 3), oq);
         }
         *reinterpret_cast<float4 *>(&s_redo[t & 1][rg][4 * cq]) = oq;
     }
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     if (state_out) {
         float *So = state_out + nh * (kD * kD);
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(So + (rg + i * RG) * kD + col), sv[i]);
+        for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(So + row_of<CWD>(rg, i) * kD + col), sv[i]);
     }
 }
 
@@ -246,8 +249,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     using G = DecodeGeom<CWD>;
     constexpr int LPR = G::LPR, RG = G::RG, RPT = G::RPT;
 
-    __shared__ float s_alpha[kMaxReplay][kD], s_k[kMaxReplay][kD];
+    __shared__ __align__(16) float s_alpha[kMaxReplay][kD];  // staged log a, then a
+    __shared__ float s_k[kMaxReplay][kD];
     __shared__ __align__(16) float s_v[kMaxReplay][kD];  // read as float4
+    __shared__ __align__(16) __nv_bfloat16 s_kb[kMaxReplay][kD], s_vb[kMaxReplay][kD];
     __shared__ float s_beta[kMaxReplay];
     __shared__ __align__(16) float s_redp[2][RG][CWD];
 
@@ -261,54 +266,42 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int col = blockIdx.y * CWD + 4 * cq;
     float *S = state + nh * (kD * kD);
 
-    // the first two staging items of this thread (four tokens) are loaded before the
-    // state, so that they do not queue behind its 64 KB; any further tokens after it
-    constexpr int kPre = 2;
-    float pre_g[kPre], pre_b = 0.f;
-    __nv_bfloat16 pre_k[kPre], pre_v[kPre];
-#pragma unroll
-    for (int u = 0; u < kPre; ++u) {
-        const int idx = tid + u * kDecodeThreads;
-        pre_g[u] = 0.f;
-        pre_k[u] = pre_v[u] = __float2bfloat16(0.f);
-        if (idx < a * kD) {
-            const int64_t row = ((n * m + idx / kD) * H + h) * kD + idx % kD;
-            pre_g[u] = gk_log[row];
-            pre_k[u] = k[row];
-            pre_v[u] = v[row];
+    // every accepted token's log goes first, into shared memory by cp.async, so that none
+    // of it queues behind the state's 64 KB or holds registers while the state is in flight
+    constexpr int kTokenChunks = 64;  // 16-byte pieces of one token's log: a 32, k 16, v 16
+    for (int i = tid; i < a * kTokenChunks; i += kDecodeThreads) {
+        const int t = i / kTokenChunks, j = i % kTokenChunks;
+        const int64_t row = ((n * m + t) * H + h) * kD;
+        if (j < 32) {
+            cp_async16(&s_alpha[t][4 * j], gk_log + row + 4 * j);
+        } else if (j < 48) {
+            cp_async16(&s_kb[t][8 * (j - 32)], k + row + 8 * (j - 32));
+        } else {
+            cp_async16(&s_vb[t][8 * (j - 48)], v + row + 8 * (j - 48));
         }
     }
-    if (tid < a) pre_b = beta_log[(n * m + tid) * H + h];
+    if (tid < a) cp_async4(&s_beta[tid], beta_log + (n * m + tid) * H + h);
+    cp_async_commit();
 
     float4 sv[RPT];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + row_of<CWD>(rg, i) * kD + col));
 
-#pragma unroll
-    for (int u = 0; u < kPre; ++u) {
-        const int idx = tid + u * kDecodeThreads;
-        if (idx < a * kD) {
-            const int t = idx / kD, c = idx % kD;
-            s_alpha[t][c] = expf(pre_g[u]);
-            s_k[t][c] = __bfloat162float(pre_k[u]);
-            s_v[t][c] = __bfloat162float(pre_v[u]);
-        }
-    }
-    for (int idx = tid + kPre * kDecodeThreads; idx < a * kD; idx += kDecodeThreads) {
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int idx = tid; idx < a * kD; idx += kDecodeThreads) {
         const int t = idx / kD, c = idx % kD;
-        const int64_t row = ((n * m + t) * H + h) * kD + c;
-        s_alpha[t][c] = expf(gk_log[row]);
-        s_k[t][c] = __bfloat162float(k[row]);
-        s_v[t][c] = __bfloat162float(v[row]);
+        s_alpha[t][c] = expf(s_alpha[t][c]);
+        s_k[t][c] = __bfloat162float(s_kb[t][c]);
+        s_v[t][c] = __bfloat162float(s_vb[t][c]);
     }
-    if (tid < a) s_beta[tid] = pre_b;
     __syncthreads();
 
     for (int t = 0; t < a; ++t) {
         float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
-            const int row = rg + i * RG;
+            const int row = row_of<CWD>(rg, i);
             decay_project_scalar(sv[i], s_alpha[t][row], s_k[t][row], p);
         }
         *reinterpret_cast<float4 *>(&s_redp[t & 1][rg][4 * cq]) = p;
@@ -316,10 +309,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
         const float4 P = sum_partials_scalar<CWD>(s_redp[t & 1], cq);
         const float4 e = delta_error_scalar(s_beta[t], *reinterpret_cast<const float4 *>(&s_v[t][col]), P);
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) rank1_scalar(sv[i], s_k[t][rg + i * RG], e);
+        for (int i = 0; i < RPT; ++i) rank1_scalar(sv[i], s_k[t][row_of<CWD>(rg, i)], e);
     }
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(S + (rg + i * RG) * kD + col), sv[i]);
+    for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(S + row_of<CWD>(rg, i) * kD + col), sv[i]);
 }
 
 // Verify and fold take the decode kernel's column slice for the same pair count

@@ -18,8 +18,25 @@ struct DecodeGeom {
     static constexpr int LPR = CWD / 4;              // threads per row (one float4 each)
     static constexpr int RG = kDecodeThreads / LPR;  // row groups
     static constexpr int RPT = kD / RG;              // rows per thread
-    static_assert(RG * LPR == kDecodeThreads && RPT * RG == kD, "decode layout");
+    static_assert(RG * LPR == kDecodeThreads && RPT * RG == kD && RPT % 4 == 0, "decode layout");
 };
+
+// Thread group rg owns the RPT consecutive key rows rg * RPT ... rg * RPT + RPT - 1 (of
+// its CTA's value columns), so a token's per-row values (a, k, q) are read from shared
+// memory four rows at a time. A warp's load of one of its rows is still whole 128-byte
+// lines of the state.
+template <int CWD>
+__device__ __forceinline__ int row_of(int rg, int i) {
+    return rg * DecodeGeom<CWD>::RPT + i;
+}
+// rows row_of(rg, i) ... row_of(rg, i + 3) of a 16-byte aligned shared row vector
+template <int CWD>
+__device__ __forceinline__ float4 rows4(const float *vec, int rg, int i) {
+    return *reinterpret_cast<const float4 *>(vec + row_of<CWD>(rg, i));
+}
+__device__ __forceinline__ float lane4(const float4 &v, int j) {
+    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+}
 
 // ---- the per-element arithmetic every kernel here shares ----
 // Two fp32 lanes per instruction (the packed .f32x2 forms of sm_100 and later): each lane

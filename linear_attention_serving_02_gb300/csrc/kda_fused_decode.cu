@@ -129,7 +129,7 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     const float bv = tid == kD ? p.b[nh] : 0.f;
     float4 sv[RPT];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + (rg + i * RG) * kD + col));
+    for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + row_of<CWD>(rg, i) * kD + col));
     cp_async_wait<0>();
     __syncthreads();
 
@@ -186,7 +186,7 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     float4 pp = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const int row = rg + i * RG;
+        const int row = row_of<CWD>(rg, i);
         decay_project(sv[i], s_alpha[row], s_k[row], pp);
     }
     *reinterpret_cast<float4 *>(&s_red[rg][4 * cq]) = pp;
@@ -197,7 +197,7 @@ __device__ __forceinline__ void fused_decode_body(const FusedArgs &p) {
     float4 oq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const int row = rg + i * RG;
+        const int row = row_of<CWD>(rg, i);
         rank1(sv[i], s_k[row], e);
         __stcs(reinterpret_cast<float4 *>(S + row * kD + col), sv[i]);
         readout(sv[i], s_q[row], oq);
