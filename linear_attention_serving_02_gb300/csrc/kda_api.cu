@@ -11,11 +11,7 @@ namespace kda {
 struct WalkUnit;
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
-                        int32_t *n_units, cudaStream_t st);
-cudaError_t launch_segment_plan(const int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N,
-                                int32_t H, int32_t P, const float *S0, float *Sout, float *Sin, float *Mseg,
-                                float *Rseg, WalkUnit *unitsA, int32_t *nA, WalkUnit *unitsC, int32_t *nC,
-                                int32_t *chains, cudaStream_t st);
+                        int32_t *n_units, const SegPlan &sp, cudaStream_t st);
 cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
                            const float *Mseg, const float *Rseg, cudaStream_t st);
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
@@ -141,7 +137,7 @@ size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, 
 int32_t kda_chunk_prefill_launch_count(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
     if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return -1;
     if (num_seqs == 0) return 0;
-    return kda::walk_segment_chunks(total_tokens, num_seqs, num_heads) ? 6 : 3;
+    return kda::walk_segment_chunks(total_tokens, num_seqs, num_heads) ? 5 : 3;
 }
 
 int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
@@ -188,8 +184,21 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
     kda::WalkUnit *units = reinterpret_cast<kda::WalkUnit *>(ws + w.units);
     const int o_f32 = (o_dtype == KDA_OUT_F32) ? 1 : 0;
 
+    // the segmented walk's tables (when w.P > 0) are written by the plan kernel too
+    kda::SegPlan sp{};
+    sp.P = w.P;
+    if (w.P > 0) {
+        sp.Sin = reinterpret_cast<float *>(ws + w.sin);
+        sp.Mseg = reinterpret_cast<float *>(ws + w.mseg);
+        sp.Rseg = reinterpret_cast<float *>(ws + w.rseg);
+        sp.unitsA = reinterpret_cast<kda::WalkUnit *>(ws + w.unitsA);
+        sp.unitsC = reinterpret_cast<kda::WalkUnit *>(ws + w.unitsC);
+        sp.nA = counts + 1;
+        sp.nC = counts + 2;
+        sp.chains = reinterpret_cast<int32_t *>(ws + w.chains);
+    }
     if (kda::launch_plan(cu_seqlens, num_seqs, seq_len, total, status, seq_cu, chunk_off, num_heads, initial_state,
-                         final_state, units, counts, st) != cudaSuccess)
+                         final_state, units, counts, sp, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (kda::launch_intra(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k),
                           reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, status, seq_cu, chunk_off, num_seqs,
@@ -201,21 +210,12 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
         return KDA_OK;
     }
     // segmented walk: phase A (segment maps), phase B (chain them), phase C (outputs)
-    kda::WalkUnit *unitsA = reinterpret_cast<kda::WalkUnit *>(ws + w.unitsA);
-    kda::WalkUnit *unitsC = reinterpret_cast<kda::WalkUnit *>(ws + w.unitsC);
-    int32_t *chains = reinterpret_cast<int32_t *>(ws + w.chains);
-    float *sin = reinterpret_cast<float *>(ws + w.sin);
-    float *mseg = reinterpret_cast<float *>(ws + w.mseg);
-    float *rseg = reinterpret_cast<float *>(ws + w.rseg);
-    if (kda::launch_segment_plan(status, seq_cu, chunk_off, num_seqs, num_heads, w.P, initial_state, final_state, sin,
-                                 mseg, rseg, unitsA, counts + 1, unitsC, counts + 2, chains, st) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    if (kda::launch_walk(status, unitsA, counts + 1, 3 * w.seg_bound, num_heads, records, o, o_f32, st) !=
+    if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, st) !=
         cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_combine(status, chains, num_seqs, num_heads, sin, mseg, rseg, st) != cudaSuccess)
+    if (kda::launch_combine(status, sp.chains, num_seqs, num_heads, sp.Sin, sp.Mseg, sp.Rseg, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_walk(status, unitsC, counts + 2, w.seg_bound, num_heads, records, o, o_f32, st) != cudaSuccess)
+    if (kda::launch_walk(status, sp.unitsC, sp.nC, w.seg_bound, num_heads, records, o, o_f32, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
 }

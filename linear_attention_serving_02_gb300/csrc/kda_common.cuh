@@ -92,6 +92,16 @@ constexpr int kUnitAddUp = 2;     // U = U' - W S (else U = -W S: the homogeneou
 constexpr int kUnitIdentity = 4;  // start from the identity when in == nullptr
 constexpr size_t kStateFloats = (size_t)kD * kD;
 
+// Tables of the segmented walk, built by the plan kernel when P > 0 (segment length in
+// chunks; P == 0: a plain walk, nothing else is read).
+struct SegPlan {
+    int32_t P;
+    float *Sin, *Mseg, *Rseg;  // per (segment, head): input state, map M, offset R
+    WalkUnit *unitsA, *unitsC;
+    int32_t *nA, *nC;
+    int32_t *chains;  // per sequence: first segment, number of segments
+};
+
 // Segment length (in chunks) of the segmented walk, or 0 for a plain walk. A pure
 // function of the batch size, so that the workspace size can be computed without a
 // device: segments pay when there are fewer (sequence, head) chains than about a wave

@@ -143,60 +143,50 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     const int col = blockIdx.y * CWD + 4 * cq;
     const float *S = state + nh * (kD * kD);
 
-    // the first two staging items of this thread are loaded before the state, so that
-    // they do not queue behind its 64 KB; the rest after it
-    constexpr int kPre = 2;
-    float pre_z[kPre], pre_b = 0.f;
-    __nv_bfloat16 pre_k[kPre], pre_q[kPre], pre_v[kPre];
-#pragma unroll
-    for (int u = 0; u < kPre; ++u) {
-        const int idx = tid + u * kDecodeThreads;
-        pre_z[u] = 0.f;
-        pre_k[u] = pre_q[u] = pre_v[u] = __float2bfloat16(0.f);
-        if (idx < m * kD) {
-            const int64_t row = ((n * m + idx / kD) * H + h) * kD + idx % kD;
-            pre_z[u] = z[row];
-            pre_k[u] = k[row];
-            pre_q[u] = q[row];
-            pre_v[u] = v[row];
+    // every token's inputs go first, into shared memory by cp.async, so that none of them
+    // queue behind the state's 64 KB or hold registers while it is in flight: z lands in
+    // s_alpha, v in s_v, b in s_beta, and k and q (bf16) in the reduction buffers, which
+    // the token loop only uses after they have been converted
+    __nv_bfloat16(*raw)[kMaxReplay][kD] = reinterpret_cast<__nv_bfloat16(*)[kMaxReplay][kD]>(&s_redp[0][0][0]);
+    static_assert(sizeof(s_redp) >= 2 * kMaxReplay * kD * sizeof(__nv_bfloat16), "k and q staging");
+    constexpr int kTokenChunks = 80;  // 16-byte pieces of one token's inputs: z 32, k, q and v 16 each
+    for (int i = tid; i < m * kTokenChunks; i += kDecodeThreads) {
+        const int t = i / kTokenChunks, j = i % kTokenChunks;
+        const int64_t row = ((n * m + t) * H + h) * kD;
+        if (j < 32) {
+            cp_async16(&s_alpha[t][4 * j], z + row + 4 * j);
+        } else if (j < 48) {
+            cp_async16(&raw[0][t][8 * (j - 32)], k + row + 8 * (j - 32));
+        } else if (j < 64) {
+            cp_async16(&raw[1][t][8 * (j - 48)], q + row + 8 * (j - 48));
+        } else {
+            cp_async16(&s_v[t][8 * (j - 64)], v + row + 8 * (j - 64));
         }
     }
-    if (tid < m) pre_b = bgate[(n * m + tid) * H + h];
+    if (tid < m) cp_async4(&s_beta[tid], bgate + (n * m + tid) * H + h);
+    cp_async_commit();
+    const float Ah = A[h];
 
     float4 sv[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) sv[i] = __ldcs(reinterpret_cast<const float4 *>(S + row_of<CWD>(rg, i) * kD + col));
 
-    // stage every token's gate, k, q, v (and write the log while at it)
-#pragma unroll
-    for (int u = 0; u < kPre; ++u) {
-        const int idx = tid + u * kDecodeThreads;
-        if (idx < m * kD) {
-            const int t = idx / kD, c = idx % kD;
-            const int64_t row = ((n * m + t) * H + h) * kD + c;
-            const float la = decode_log_decay(A, h, pre_z[u]);
-            s_alpha[t][c] = expf(la);
-            s_k[t][c] = __bfloat162float(pre_k[u]);
-            s_q[t][c] = __bfloat162float(pre_q[u]);
-            s_v[t][c] = pre_v[u];
-            if (gk_log) gk_log[row] = la;
-        }
-    }
-    for (int idx = tid + kPre * kDecodeThreads; idx < m * kD; idx += kDecodeThreads) {
+    // the gate of every token (and the log, while at it), k and q to fp32
+    cp_async_wait<0>();
+    __syncthreads();
+    const float eA = expf(Ah);
+    for (int idx = tid; idx < m * kD; idx += kDecodeThreads) {
         const int t = idx / kD, c = idx % kD;
-        const int64_t row = ((n * m + t) * H + h) * kD + c;
-        const float la = decode_log_decay(A, h, z[row]);
+        const float la = gate_log_decay(eA, s_alpha[t][c]);
         s_alpha[t][c] = expf(la);
-        s_k[t][c] = __bfloat162float(k[row]);
-        s_q[t][c] = __bfloat162float(q[row]);
-        s_v[t][c] = v[row];
-        if (gk_log) gk_log[row] = la;
+        s_k[t][c] = __bfloat162float(raw[0][t][c]);
+        s_q[t][c] = __bfloat162float(raw[1][t][c]);
+        if (gk_log) gk_log[((n * m + t) * H + h) * kD + c] = la;
     }
     if (tid < m) {
-        const int64_t tok = (n * m + tid) * H + h;
-        const float beta = sigmoid_f(pre_b);
+        const float beta = sigmoid_f(s_beta[tid]);
         s_beta[tid] = beta;
-        if (beta_log) beta_log[tok] = beta;
+        if (beta_log) beta_log[(n * m + tid) * H + h] = beta;
     }
     __syncthreads();
 

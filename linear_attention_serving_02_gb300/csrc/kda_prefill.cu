@@ -1,7 +1,7 @@
 // KDA chunkwise prefill: kernels on one stream.
 //
 //   kda_plan_kernel   validate cu_seqlens, tabulate sequence starts and chunk offsets,
-//                     and the walk units of a plain walk
+//                     and the walk units of a plain walk (or the segmented walk's tables)
 //   kda_intra_kernel  persistent, one CTA per SM over the (chunk, head) items, all chunks
 //                     independent: gate and cumulative decay, decayed K K^T / Q K^T per
 //                     32-token tile row, UT transform T = (I + A_kk)^-1, W = T' Khat and
@@ -10,8 +10,8 @@
 //                     walks the chunks in order with the full state on chip, on tcgen05
 //                     tensor cores (TMEM accumulators),
 //                     U = U' - W S;  O = Qhat S + A_qk U;  S = Diag(gamma) S + Kend^T U
-//   with few long sequences the walk is segmented (kda_segment_plan_kernel, two walk
-//   launches and kda_combine_kernel between them; see below)
+//   with few long sequences the walk is segmented (two walk launches and
+//   kda_combine_kernel between them; see below)
 //
 // The algebra is the chunkwise form of 'From Linear Attention to KDA' (blog), §7.1-7.3
 // with the per-channel decay of §7.2 folded into the UT system, and tiles as in §8 for
@@ -46,98 +46,9 @@ namespace kda {
 // ---------------------------------------------------------------------------------
 // plan: seq_cu[N+1] and chunk_off[N+1] (prefix sums of ceil(len / C)) in the workspace
 // ---------------------------------------------------------------------------------
-__global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t N, int64_t seq_len,
-                                int64_t total_tokens, int32_t *__restrict__ status, int32_t *__restrict__ seq_cu,
-                                int32_t *__restrict__ chunk_off, int32_t H, const float *S0, float *Sout,
-                                WalkUnit *__restrict__ units, int32_t *__restrict__ n_units) {
-    __shared__ int32_t carry;
-    __shared__ int32_t bad;
-    __shared__ int32_t scan[256];
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        carry = 0;
-        bad = 0;
-    }
-    __syncthreads();
-    // validation: cu[0] == 0, cu[N] == total, non-decreasing
-    if (cu_seqlens != nullptr) {
-        for (int64_t n = tid; n <= N; n += blockDim.x) {
-            int32_t c = cu_seqlens[n];
-            if (n == 0 && c != 0) atomicOr(&bad, 1);
-            if (n == N && (int64_t)c != total_tokens) atomicOr(&bad, 1);
-            if (n > 0 && c < cu_seqlens[n - 1]) atomicOr(&bad, 1);
-        }
-    }
-    __syncthreads();
-    if (bad) {
-        // empty walks whose only job is to mark each final state invalid (NaN)
-        for (int64_t n = tid; n <= N; n += blockDim.x) {
-            seq_cu[n] = 0;
-            chunk_off[n] = 0;
-            if (n < N) {
-                WalkUnit u;
-                u.in = nullptr;
-                u.out = Sout + (size_t)n * H * kStateFloats;
-                u.c_begin = u.c_end = u.t_begin = u.t_end = 0;
-                u.flags = 0;
-                u.pad = 0;
-                units[n] = u;
-            }
-        }
-        if (tid == 0) {
-            *status = -4;  // KDA_ERR_SEQLENS
-            *n_units = N;
-        }
-        return;
-    }
-    if (tid == 0) {
-        *status = 0;
-        *n_units = N;
-    }
-    for (int64_t base = 0; base <= N; base += 256) {
-        const int64_t n = base + tid;
-        int32_t start = 0, len = 0;
-        if (n <= N) {
-            start = cu_seqlens ? cu_seqlens[n] : (int32_t)(n * seq_len);
-            seq_cu[n] = start;
-            if (n < N) {
-                int32_t end = cu_seqlens ? cu_seqlens[n + 1] : (int32_t)((n + 1) * seq_len);
-                len = (end - start + kC - 1) / kC;
-            }
-        }
-        scan[tid] = len;
-        __syncthreads();
-        for (int off = 1; off < 256; off <<= 1) {  // inclusive Hillis-Steele scan
-            int32_t x = tid >= off ? scan[tid - off] : 0;
-            __syncthreads();
-            scan[tid] += x;
-            __syncthreads();
-        }
-        // exclusive offset of sequence n = carry + inclusive(n) - len(n)
-        if (n <= N) chunk_off[n] = carry + scan[tid] - len;
-        __syncthreads();
-        // the plain walk: one unit per sequence (read after this kernel, so the table
-        // entries of n + 1 written in the same pass are complete by then)
-        if (n < N) {
-            WalkUnit u;
-            u.in = S0 ? S0 + (size_t)n * H * kStateFloats : nullptr;
-            u.out = Sout + (size_t)n * H * kStateFloats;
-            u.c_begin = chunk_off[n];
-            u.c_end = chunk_off[n] + len;
-            u.t_begin = start;
-            u.t_end = cu_seqlens ? cu_seqlens[n + 1] : (int32_t)((n + 1) * seq_len);
-            u.flags = kUnitWriteO | kUnitAddUp;
-            u.pad = 0;
-            units[n] = u;
-        }
-        if (tid == 255) carry += scan[255];
-        __syncthreads();
-    }
-}
-
 // ---------------------------------------------------------------------------------
-// segmented walk: tables of the three phases (one thread; used only when there are few
-// sequences). Segment g of the batch is segment sigma of sequence n, g = seg_base[n] + sigma.
+// segmented walk: tables of the three phases, written by one thread of the plan kernel
+// (used only when there are few sequences). Segment g of the batch is segment sigma of sequence n, g = seg_base[n] + sigma.
 //   phase A  segment 0 from the initial state -> Sin[g0 + 1] (the next input); with one
 //            segment, the whole walk with o and the final state instead
 //            segment sigma (1 .. S-2) from zero     -> R[g],  with U'
@@ -147,14 +58,13 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
 //   phase C  segments 0 .. S-1 from their input states, writing o; the last one writes
 //            the final state
 // ---------------------------------------------------------------------------------
-__global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ seq_cu,
-                                        const int32_t *__restrict__ chunk_off, int32_t N, int32_t H, int32_t P,
-                                        const float *S0, float *Sout, float *Sin, float *Mseg, float *Rseg,
-                                        WalkUnit *__restrict__ unitsA, int32_t *__restrict__ nA,
-                                        WalkUnit *__restrict__ unitsC, int32_t *__restrict__ nC,
-                                        int32_t *__restrict__ chains) {
-    if (threadIdx.x != 0) return;
-    if (*status != 0) {
+__device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, const int32_t *__restrict__ chunk_off,
+                              int32_t N, int32_t H, const float *S0, float *Sout, const SegPlan &sp) {
+    const int32_t P = sp.P;
+    float *Sin = sp.Sin, *Mseg = sp.Mseg, *Rseg = sp.Rseg;
+    WalkUnit *unitsA = sp.unitsA, *unitsC = sp.unitsC;
+    int32_t *chains = sp.chains;
+    if (bad) {
         // no maps to build; phase C only marks each final state invalid (NaN)
         for (int32_t n = 0; n < N; ++n) {
             chains[2 * n] = 0;
@@ -167,8 +77,8 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
             u.pad = 0;
             unitsC[n] = u;
         }
-        *nA = 0;
-        *nC = N;
+        *sp.nA = 0;
+        *sp.nC = N;
         return;
     }
     const size_t seg_stride = (size_t)H * kStateFloats;  // one segment's states for all heads
@@ -233,8 +143,100 @@ __global__ void kda_segment_plan_kernel(const int32_t *__restrict__ status, cons
         }
         g += S;
     }
-    *nA = a;
-    *nC = cc;
+    *sp.nA = a;
+    *sp.nC = cc;
+}
+
+__global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t N, int64_t seq_len,
+                                int64_t total_tokens, int32_t *__restrict__ status, int32_t *__restrict__ seq_cu,
+                                int32_t *__restrict__ chunk_off, int32_t H, const float *S0, float *Sout,
+                                WalkUnit *__restrict__ units, int32_t *__restrict__ n_units, SegPlan sp) {
+    __shared__ int32_t carry;
+    __shared__ int32_t bad;
+    __shared__ int32_t scan[256];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        carry = 0;
+        bad = 0;
+    }
+    __syncthreads();
+    // validation: cu[0] == 0, cu[N] == total, non-decreasing
+    if (cu_seqlens != nullptr) {
+        for (int64_t n = tid; n <= N; n += blockDim.x) {
+            int32_t c = cu_seqlens[n];
+            if (n == 0 && c != 0) atomicOr(&bad, 1);
+            if (n == N && (int64_t)c != total_tokens) atomicOr(&bad, 1);
+            if (n > 0 && c < cu_seqlens[n - 1]) atomicOr(&bad, 1);
+        }
+    }
+    __syncthreads();
+    if (bad) {
+        // empty walks whose only job is to mark each final state invalid (NaN)
+        for (int64_t n = tid; n <= N; n += blockDim.x) {
+            seq_cu[n] = 0;
+            chunk_off[n] = 0;
+            if (n < N) {
+                WalkUnit u;
+                u.in = nullptr;
+                u.out = Sout + (size_t)n * H * kStateFloats;
+                u.c_begin = u.c_end = u.t_begin = u.t_end = 0;
+                u.flags = 0;
+                u.pad = 0;
+                units[n] = u;
+            }
+        }
+        if (tid == 0) {
+            *status = -4;  // KDA_ERR_SEQLENS
+            *n_units = N;
+            if (sp.P > 0) plan_segments(true, seq_cu, chunk_off, N, H, S0, Sout, sp);
+        }
+        return;
+    }
+    if (tid == 0) {
+        *status = 0;
+        *n_units = N;
+    }
+    for (int64_t base = 0; base <= N; base += 256) {
+        const int64_t n = base + tid;
+        int32_t start = 0, len = 0;
+        if (n <= N) {
+            start = cu_seqlens ? cu_seqlens[n] : (int32_t)(n * seq_len);
+            seq_cu[n] = start;
+            if (n < N) {
+                int32_t end = cu_seqlens ? cu_seqlens[n + 1] : (int32_t)((n + 1) * seq_len);
+                len = (end - start + kC - 1) / kC;
+            }
+        }
+        scan[tid] = len;
+        __syncthreads();
+        for (int off = 1; off < 256; off <<= 1) {  // inclusive Hillis-Steele scan
+            int32_t x = tid >= off ? scan[tid - off] : 0;
+            __syncthreads();
+            scan[tid] += x;
+            __syncthreads();
+        }
+        // exclusive offset of sequence n = carry + inclusive(n) - len(n)
+        if (n <= N) chunk_off[n] = carry + scan[tid] - len;
+        __syncthreads();
+        // the plain walk: one unit per sequence (read after this kernel, so the table
+        // entries of n + 1 written in the same pass are complete by then)
+        if (n < N) {
+            WalkUnit u;
+            u.in = S0 ? S0 + (size_t)n * H * kStateFloats : nullptr;
+            u.out = Sout + (size_t)n * H * kStateFloats;
+            u.c_begin = chunk_off[n];
+            u.c_end = chunk_off[n] + len;
+            u.t_begin = start;
+            u.t_end = cu_seqlens ? cu_seqlens[n + 1] : (int32_t)((n + 1) * seq_len);
+            u.flags = kUnitWriteO | kUnitAddUp;
+            u.pad = 0;
+            units[n] = u;
+        }
+        if (tid == 255) carry += scan[255];
+        __syncthreads();
+    }
+    // the segmented walk's tables, from the offsets that the barrier above made visible
+    if (sp.P > 0 && tid == 0) plan_segments(false, seq_cu, chunk_off, N, H, S0, Sout, sp);
 }
 
 // Phase B: Sin[g + 1] = M[g] Sin[g] + R[g] along each sequence's segments, in fp32 on the
@@ -1250,18 +1252,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 size_t intra_smem_bytes() { return sizeof(IntraSmem); }
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
-                        int32_t *n_units, cudaStream_t st) {
+                        int32_t *n_units, const SegPlan &sp, cudaStream_t st) {
     kda_plan_kernel<<<1, 256, 0, st>>>(cu, N, seq_len, total, status, seq_cu, chunk_off, H, S0, Sout, units,
-                                       n_units);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_segment_plan(const int32_t *status, const int32_t *seq_cu, const int32_t *chunk_off, int32_t N,
-                                int32_t H, int32_t P, const float *S0, float *Sout, float *Sin, float *Mseg,
-                                float *Rseg, WalkUnit *unitsA, int32_t *nA, WalkUnit *unitsC, int32_t *nC,
-                                int32_t *chains, cudaStream_t st) {
-    kda_segment_plan_kernel<<<1, 32, 0, st>>>(status, seq_cu, chunk_off, N, H, P, S0, Sout, Sin, Mseg, Rseg, unitsA,
-                                              nA, unitsC, nC, chains);
+                                       n_units, sp);
     return cudaGetLastError();
 }
 

@@ -72,8 +72,8 @@ def test_launch_count():
     # short chains are not worth splitting
     assert lc(256, 1, 2) == 3
     # one long sequence over few heads: segmented walk
-    assert lc(8192, 1, 12) == 6
-    assert lc(1 << 20, 1, 12) == 6
+    assert lc(8192, 1, 12) == 5
+    assert lc(1 << 20, 1, 12) == 5
 
 
 def _prefill(**over):
