@@ -899,7 +899,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 struct WalkSmem {
     unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
     unsigned char ak[2 * kStackAK];      // [ A_qk ; Kend^T ] hi | lo
-    alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1)
+    alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1), the state warps' copy
+    alignas(16) float gam_uo[2][kD];     // the same, the U and O warps' copy
     unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
     uint64_t bar_wq, bar_ak, bar_m1, bar_m2;
     uint32_t tmem_base;
@@ -988,21 +989,38 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     const uint32_t D_UO = tmem, D_AK = tmem + 128;
     volatile int &fail = s.fail;
 
+    // A walk without outputs (segment maps) needs only -W and Kend^T: it copies those
+    // parts of the record and runs group 1 with N = 64, group 2 with N = 128.
+    const bool maps = !write_o;
+    const uint32_t ds_col = maps ? 0u : 64u;  // TMEM column of D_S within D_AK
+    // this thread's half of its value column of S: key rows 0 .. 63 in the state warps,
+    // 64 .. 127 in the U and O warps, so that both halves are updated at the same time
+    float Sh[64];
     if (warp < 4) {
-        // ----------------------------- U and O warps -----------------------------
+        // ------------- U and O warps; they also hold key rows 64 .. 127 of S -------------
         float Upr[64];
         auto load_up = [&](int c) {
             const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
 #pragma unroll
             for (int j = 0; j < 64; ++j) Upr[j] = add_up ? up[j * kD + dv] : 0.f;
         };
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            const int r = 64 + j;
+            Sh[j] = S0 ? S0[(int64_t)r * kD + dv] : ((identity && r == dv) ? 1.f : 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 64; j += 32)
+            split32_tmem(&Sh[j], tmem + lanes + kColSHi + 32 + j / 2, tmem + lanes + kColSLo + 32 + j / 2);
+        tc::tmem_wait_st();
         if (c_begin < c_end) load_up(c_begin);
         tc::fence_before_sync();
-        named_arrive(kBarOR, 256);  // nothing to read yet: group 1 of the first chunk may start
+        named_arrive(kBarOR, 256);  // initial planes of rows 64 .. 127 written; nothing to read yet
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
             const int L = (int)min((int64_t)kC, t_end - t0);
+            const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
             // U^T = U'^T + D_U, written as split planes for group 2
             if (wait_in_order(&s.bar_m1, ph, fail)) {
                 tc::fence_after_sync();
@@ -1021,16 +1039,43 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             }
             tc::fence_before_sync();
             named_arrive(kBarU, 256);  // U^T planes complete; group 1 is done with [ -W ; Qhat ]
+            s.gam_uo[ph][dv] = gnext;
             // U' of the next chunk: issued now, ahead of this chunk's output stores, so that
             // it does not queue behind them (the registers are free once the planes are out)
             if (c + 1 < c_end) load_up(c + 1);
-            // o = (D_O1 + D_O2)^T for this thread's value channel
-            float ov[64];
+            named_sync(5, 128);  // gamma of this chunk in place (this group's copy)
+            const bool m2ok = wait_in_order(&s.bar_m2, ph, fail);
+            // S <- Diag(gamma) S + D_S on key rows 64 .. 127, and their split planes
+            {
+                uint32_t dA[32], dB[32];
+                if (m2ok) {
+                    tc::fence_after_sync();
+                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 64, dA);
+                    tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 96, dB);
+                    tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 64; ++j) ov[j] = 0.f;
-            const bool ok = wait_in_order(&s.bar_m2, ph, fail) && write_o;
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 ga = *reinterpret_cast<const float4 *>(&s.gam_uo[ph][64 + j]);
+                        const float4 gb = *reinterpret_cast<const float4 *>(&s.gam_uo[ph][96 + j]);
+                        Sh[j] = ga.x * Sh[j] + __uint_as_float(dA[j]);
+                        Sh[j + 1] = ga.y * Sh[j + 1] + __uint_as_float(dA[j + 1]);
+                        Sh[j + 2] = ga.z * Sh[j + 2] + __uint_as_float(dA[j + 2]);
+                        Sh[j + 3] = ga.w * Sh[j + 3] + __uint_as_float(dA[j + 3]);
+                        Sh[32 + j] = gb.x * Sh[32 + j] + __uint_as_float(dB[j]);
+                        Sh[33 + j] = gb.y * Sh[33 + j] + __uint_as_float(dB[j + 1]);
+                        Sh[34 + j] = gb.z * Sh[34 + j] + __uint_as_float(dB[j + 2]);
+                        Sh[35 + j] = gb.w * Sh[35 + j] + __uint_as_float(dB[j + 3]);
+                    }
+                }
+                split32_tmem(&Sh[0], tmem + lanes + kColSHi + 32, tmem + lanes + kColSLo + 32);
+                split32_tmem(&Sh[32], tmem + lanes + kColSHi + 48, tmem + lanes + kColSLo + 48);
+                tc::tmem_wait_st();
+            }
+            // o = (D_O1 + D_O2)^T for this thread's value channel, staged as [token][channel]
+            // in shared memory (the previous chunk's tile has been written out)
+            const bool ok = m2ok && write_o;
             if (ok) {
-                tc::fence_after_sync();
+                float *stage = reinterpret_cast<float *>(s.ut);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t d1[32], d2[32];
@@ -1038,49 +1083,46 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     tc::tmem_ld32_nowait(D_AK + lanes + 32 * half, d2);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) ov[32 * half + j] = __uint_as_float(d1[j]) + __uint_as_float(d2[j]);
+                    for (int j = 0; j < 32; ++j) {
+                        const int i = 32 * half + j;
+                        const float ov = __uint_as_float(d1[j]) + __uint_as_float(d2[j]);
+                        if (o_f32)
+                            stage[i * kD + dv] = ov;
+                        else
+                            reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov);
+                    }
                 }
             }
             tc::fence_before_sync();
-            named_arrive(kBarOR, 256);  // output accumulators read: the next group 1 may overwrite them
-            // stage o as [token][channel] in shared memory and write it out in 16-byte row
-            // chunks while the next group 1 runs
+            named_arrive(kBarOR, 256);  // rows 64 .. 127 of the next S^T planes written, D_S and
+                                        // the output accumulators read: the next group 1 may start
+            // write the staged tile out in 16-byte row chunks while the next group 1 runs
             if (write_o) {  // uniform over the CTA: the named barriers below stay matched
-            float *stage = reinterpret_cast<float *>(s.ut);
-#pragma unroll
-            for (int i = 0; i < kC; ++i) {
-                if (o_f32)
-                    stage[i * kD + dv] = ov[i];
-                else
-                    reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov[i]);
-            }
-            named_sync(5, 128);
-            if (ok) {
-                const int chunks_per_row = o_f32 ? kD / 4 : kD / 8;  // 16-byte chunks
-                for (int e = tid; e < L * chunks_per_row; e += 128) {
-                    const int i = e / chunks_per_row, ch = e % chunks_per_row;
-                    const int64_t row = ((t0 + i) * H + h) * (int64_t)kD;
-                    if (o_f32)
-                        reinterpret_cast<uint4 *>(static_cast<float *>(o) + row)[ch] =
-                            reinterpret_cast<const uint4 *>(stage + i * kD)[ch];
-                    else
-                        reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + row)[ch] =
-                            reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(stage) + i * kD)[ch];
+                named_sync(5, 128);
+                if (ok) {
+                    const float *stage = reinterpret_cast<const float *>(s.ut);
+                    const int chunks_per_row = o_f32 ? kD / 4 : kD / 8;  // 16-byte chunks
+                    for (int e = tid; e < L * chunks_per_row; e += 128) {
+                        const int i = e / chunks_per_row, ch = e % chunks_per_row;
+                        const int64_t row = ((t0 + i) * H + h) * (int64_t)kD;
+                        if (o_f32)
+                            reinterpret_cast<uint4 *>(static_cast<float *>(o) + row)[ch] =
+                                reinterpret_cast<const uint4 *>(stage + i * kD)[ch];
+                        else
+                            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + row)[ch] =
+                                reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(stage) +
+                                                                i * kD)[ch];
+                    }
                 }
-            }
-            named_sync(5, 128);  // staged tile read out before the next output lands here
+                named_sync(5, 128);  // staged tile read out before the next output lands here
             }
         }
     } else {
         // ----------------- state warps (thread 128 issues the MMAs) -----------------
         const bool issuer = (tid == 128);
-        // A walk without outputs (segment maps) needs only -W and Kend^T: it copies those
-        // parts of the record and runs group 1 with N = 64, group 2 with N = 128.
-        const bool maps = !write_o;
         const uint32_t kIdG1 = tc::idesc_bf16_m128(maps ? 64 : 128);
         const uint32_t kIdG2 = tc::idesc_bf16_m128(maps ? 128 : 192);
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
-        const uint32_t ds_col = maps ? 0u : 64u;                  // TMEM column of D_S within D_AK
         int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (issuer)
         auto issue_wq = [&](int c) {
             if (maps) {  // the -W rows of the hi and the lo plane
@@ -1158,15 +1200,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++n_m2;
         };
 
-        float Sr[128];
+        // key rows 0 .. 63 of this thread's value column (the U and O warps hold the rest)
 #pragma unroll
-        for (int j = 0; j < kD; ++j) Sr[j] = S0 ? S0[(int64_t)j * kD + dv] : ((identity && j == dv) ? 1.f : 0.f);
+        for (int j = 0; j < 64; ++j) Sh[j] = S0 ? S0[(int64_t)j * kD + dv] : ((identity && j == dv) ? 1.f : 0.f);
 #pragma unroll
-        for (int j = 0; j < kD; j += 32)
-            split32_tmem(&Sr[j], tmem + lanes + kColSHi + j / 2, tmem + lanes + kColSLo + j / 2);
+        for (int j = 0; j < 64; j += 32)
+            split32_tmem(&Sh[j], tmem + lanes + kColSHi + j / 2, tmem + lanes + kColSLo + j / 2);
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        named_sync(4, 128);  // initial S^T planes complete
+        named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
         if (issuer && c_begin < c_end) {
             issue_wq(c_begin);
             issue_ak(c_begin);
@@ -1189,9 +1231,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             if (issuer && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
             s.gam[ph][dv] = gnext;
             named_sync(4, 128);  // gamma of this chunk in place
-            // S <- Diag(gamma) S + D_S and its split planes, in blocks of 32 key channels:
-            // the TMEM load of the next block is in flight while this one is updated,
-            // split and stored
+            // S <- Diag(gamma) S + D_S on key rows 0 .. 63 and their split planes, in blocks
+            // of 32 key channels: the TMEM load of the second block is in flight while the
+            // first is updated, split and stored
             {
                 uint32_t dA[32], dB[32];
                 if (ok) {
@@ -1199,29 +1241,30 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     tc::tmem_ld32_nowait(D_AK + lanes + ds_col, dA);
                 }
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
+                for (int b = 0; b < 2; ++b) {
                     uint32_t(&cur)[32] = (b & 1) ? dB : dA;
                     uint32_t(&nxt)[32] = (b & 1) ? dA : dB;
                     if (ok) {
                         tc::tmem_wait_ld();
-                        if (b + 1 < 4) tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * (b + 1), nxt);
+                        if (b + 1 < 2) tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * (b + 1), nxt);
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
                             const int cc = 32 * b + j;
                             const float4 g = *reinterpret_cast<const float4 *>(&s.gam[ph][cc]);
-                            Sr[cc] = g.x * Sr[cc] + __uint_as_float(cur[j]);
-                            Sr[cc + 1] = g.y * Sr[cc + 1] + __uint_as_float(cur[j + 1]);
-                            Sr[cc + 2] = g.z * Sr[cc + 2] + __uint_as_float(cur[j + 2]);
-                            Sr[cc + 3] = g.w * Sr[cc + 3] + __uint_as_float(cur[j + 3]);
+                            Sh[cc] = g.x * Sh[cc] + __uint_as_float(cur[j]);
+                            Sh[cc + 1] = g.y * Sh[cc + 1] + __uint_as_float(cur[j + 1]);
+                            Sh[cc + 2] = g.z * Sh[cc + 2] + __uint_as_float(cur[j + 2]);
+                            Sh[cc + 3] = g.w * Sh[cc + 3] + __uint_as_float(cur[j + 3]);
                         }
                     }
-                    split32_tmem(&Sr[32 * b], tmem + lanes + kColSHi + 16 * b, tmem + lanes + kColSLo + 16 * b);
+                    split32_tmem(&Sh[32 * b], tmem + lanes + kColSHi + 16 * b, tmem + lanes + kColSLo + 16 * b);
                 }
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
-            named_sync(4, 128);       // next S^T planes complete, D_S read
-            named_sync(kBarOR, 256);  // the U and O warps have read this chunk's output accumulators
+            named_sync(4, 128);       // rows 0 .. 63 of the next S^T planes complete
+            named_sync(kBarOR, 256);  // the U and O warps have written rows 64 .. 127 and read
+                                      // this chunk's D_S and output accumulators
             if (issuer && c + 1 < c_end) issue_g1(c + 1);
             __syncwarp();
         }
@@ -1234,15 +1277,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
             atomicExch(status, -7);
         }
-        const bool failed = fail;
-        if (Sout) {
-#pragma unroll
-            for (int j = 0; j < kD; ++j) Sout[(int64_t)j * kD + dv] = failed ? __int_as_float(0x7fc00000) : Sr[j];
-        }
     }
 
     tc::fence_before_sync();
     __syncthreads();
+    // the final state: rows 0 .. 63 from the state warps, 64 .. 127 from the U and O warps
+    // (every wait has ended: the failure flag is final)
+    if (Sout) {
+        const bool failed = fail;
+        float *dst = Sout + (warp >= 4 ? 0 : (int64_t)64 * kD) + dv;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) dst[(int64_t)j * kD] = failed ? __int_as_float(0x7fc00000) : Sh[j];
+    }
     if (warp == 0) tc::tmem_dealloc(tmem, kWalkTmemCols);
 }
 
