@@ -528,6 +528,56 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // (at most 16 tokens of log decay >= -5 between i or j and m on the side where the
     // factor exceeds 1), inside the range of fp32 and bf16; a factor that underflows
     // belongs to a product below e^-20, negligible next to the O(1) entries.
+    unsigned char *const aqb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.aq[0][0][0]),
+                                   reinterpret_cast<unsigned char *>(&s.u.g.aq[1][0][0])};
+    unsigned char *const akb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.ak[0][0][0]),
+                                   reinterpret_cast<unsigned char *>(&s.u.g.ak[1][0][0])};
+    unsigned char *const bkb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.bk[0][0][0]),
+                                   reinterpret_cast<unsigned char *>(&s.u.g.bk[1][0][0])};
+    // G of the reference token m on channels c .. c+7
+    auto ref8 = [&](int m, int c, float (&gm)[8]) {
+        const float4 m0 = *reinterpret_cast<const float4 *>(&G[m][c]);
+        const float4 m1 = *reinterpret_cast<const float4 *>(&G[m][c + 4]);
+        gm[0] = m0.x; gm[1] = m0.y; gm[2] = m0.z; gm[3] = m0.w;
+        gm[4] = m1.x; gm[5] = m1.y; gm[6] = m1.z; gm[7] = m1.w;
+    };
+    // one 8-channel item of an operand row: the A side (q and k of token i, factor
+    // exp(G_i - G_m)) or the B side (k of key j, factor exp(G_m - G_j)), split into planes
+    auto prep_item = [&](bool aside, int row, int ar, int c, const float (&gm)[8]) {
+        const float4 g0 = *reinterpret_cast<const float4 *>(&G[row][c]);
+        const float4 g1 = *reinterpret_cast<const float4 *>(&G[row][c + 4]);
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        float f[8];
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) f[mm] = __expf(aside ? g[mm] - gm[mm] : gm[mm] - g[mm]);
+        const uint4 kraw = *reinterpret_cast<const uint4 *>(&s.ks[row][c]);
+        const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
+        uint32_t kh[4], kl[4];
+#pragma unroll
+        for (int p2 = 0; p2 < 4; ++p2) {
+            const float2 kk = bf16x2_to_float2(kw[p2]);
+            split_bf16x2(kk.x * f[2 * p2], kk.y * f[2 * p2 + 1], kh[p2], kl[p2]);
+        }
+        if (aside) {
+            const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[row][c]);
+            const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+            uint32_t qh[4], ql[4];
+#pragma unroll
+            for (int p2 = 0; p2 < 4; ++p2) {
+                const float2 qq = bf16x2_to_float2(qw[p2]);
+                split_bf16x2(qq.x * f[2 * p2], qq.y * f[2 * p2 + 1], qh[p2], ql[p2]);
+            }
+            const uint32_t off = gram_off(ar, c);
+            *reinterpret_cast<uint4 *>(aqb[0] + off) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+            *reinterpret_cast<uint4 *>(aqb[1] + off) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+            *reinterpret_cast<uint4 *>(akb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+            *reinterpret_cast<uint4 *>(akb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+        } else {
+            const uint32_t off = gram_off(row, c);
+            *reinterpret_cast<uint4 *>(bkb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+            *reinterpret_cast<uint4 *>(bkb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+        }
+    };
     for (int a = 0; a < kC / (2 * kTile); ++a) {
         const int r0 = a * 2 * kTile;  // first token of the tile row
         const int m = r0 + kTile;      // reference token
@@ -535,59 +585,18 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // Operands, 8 channels per item (16-byte loads and stores): the A operands (q and
         // k of the tile row, sharing the factor exp(G_i - G_m)) are items 0 .. 511, the B
         // operand (keys j with the factor exp(G_m - G_j)) the rest. A thread's channel
-        // slice, tid % 16, is the same for all its items, so G_m is read once.
+        // slice, tid % 16, is the same for all its items, so G_m is read once. Keys 32 ..
+        // 63 of the second tile row, which the first does not use, were built by the warps
+        // that had no MMA task in the first round; so each round builds keys 0 .. 31 here.
         {
             const int c = (tid & 15) * 8;
             float gm[8];
-            {
-                const float4 m0 = *reinterpret_cast<const float4 *>(&G[m][c]);
-                const float4 m1 = *reinterpret_cast<const float4 *>(&G[m][c + 4]);
-                gm[0] = m0.x; gm[1] = m0.y; gm[2] = m0.z; gm[3] = m0.w;
-                gm[4] = m1.x; gm[5] = m1.y; gm[6] = m1.z; gm[7] = m1.w;
-            }
-            unsigned char *aqb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.aq[0][0][0]),
-                                     reinterpret_cast<unsigned char *>(&s.u.g.aq[1][0][0])};
-            unsigned char *akb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.ak[0][0][0]),
-                                     reinterpret_cast<unsigned char *>(&s.u.g.ak[1][0][0])};
-            unsigned char *bkb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.bk[0][0][0]),
-                                     reinterpret_cast<unsigned char *>(&s.u.g.bk[1][0][0])};
-            for (int e = tid; e < (2 * kTile + nb) * 16; e += kIntraThreads) {
+            ref8(m, c, gm);
+            for (int e = tid; e < 4 * kTile * 16; e += kIntraThreads) {
                 const bool aside = e < 2 * kTile * 16;
-                const int ar = e >> 4;                                   // A-side row in the tile row
-                const int row = aside ? r0 + ar : ar - 2 * kTile;         // token i (A side) or j (B side)
-                const float4 g0 = *reinterpret_cast<const float4 *>(&G[row][c]);
-                const float4 g1 = *reinterpret_cast<const float4 *>(&G[row][c + 4]);
-                const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                float f[8];
-#pragma unroll
-                for (int mm = 0; mm < 8; ++mm) f[mm] = __expf(aside ? g[mm] - gm[mm] : gm[mm] - g[mm]);
-                const uint4 kraw = *reinterpret_cast<const uint4 *>(&s.ks[row][c]);
-                const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
-                uint32_t kh[4], kl[4];
-#pragma unroll
-                for (int p2 = 0; p2 < 4; ++p2) {
-                    const float2 kk = bf16x2_to_float2(kw[p2]);
-                    split_bf16x2(kk.x * f[2 * p2], kk.y * f[2 * p2 + 1], kh[p2], kl[p2]);
-                }
-                if (aside) {
-                    const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[row][c]);
-                    const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
-                    uint32_t qh[4], ql[4];
-#pragma unroll
-                    for (int p2 = 0; p2 < 4; ++p2) {
-                        const float2 qq = bf16x2_to_float2(qw[p2]);
-                        split_bf16x2(qq.x * f[2 * p2], qq.y * f[2 * p2 + 1], qh[p2], ql[p2]);
-                    }
-                    const uint32_t off = gram_off(ar, c);
-                    *reinterpret_cast<uint4 *>(aqb[0] + off) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-                    *reinterpret_cast<uint4 *>(aqb[1] + off) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
-                    *reinterpret_cast<uint4 *>(akb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-                    *reinterpret_cast<uint4 *>(akb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
-                } else {
-                    const uint32_t off = gram_off(row, c);
-                    *reinterpret_cast<uint4 *>(bkb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-                    *reinterpret_cast<uint4 *>(bkb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
-                }
+                const int ar = e >> 4;                            // A-side row in the tile row
+                const int row = aside ? r0 + ar : ar - 2 * kTile;  // token i (A side) or j (B side)
+                prep_item(aside, row, ar, c, gm);
             }
         }
         __syncthreads();
@@ -596,6 +605,15 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // takes keys below r0+16, m tile 1 all keys below r0+32
         const int n16_0 = (r0 + kTile) / 16, n16_1 = nb / 16;
         const int per_mat = n16_0 + n16_1;
+        if (a == 0 && warp >= 2 * per_mat) {
+            // no MMA task in this round: keys 32 .. 63 of the next tile row (reference 48),
+            // rows of the B buffer that this round's products do not read
+            const int t2 = tid - 2 * per_mat * 32, nthr = kIntraThreads - 2 * per_mat * 32;
+            const int c = (t2 & 15) * 8;  // nthr is a multiple of 16: the slice stays fixed
+            float gm[8];
+            ref8(3 * kTile, c, gm);
+            for (int e = t2; e < 2 * kTile * 16; e += nthr) prep_item(false, 2 * kTile + (e >> 4), 0, c, gm);
+        }
         for (int p = warp; p < 2 * per_mat; p += kIntraThreads / 32) {
             const int mat = p / per_mat;  // 0: A_qk, 1: A_kk
             const int q = p % per_mat;
@@ -1200,6 +1218,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++n_m2;
         };
 
+        // the first chunk's record is copied while the initial state is read
+        if (issuer && c_begin < c_end) {
+            issue_wq(c_begin);
+            issue_ak(c_begin);
+            if (c_begin + 1 < c_end) prefetch(c_begin + 1);
+        }
         // key rows 0 .. 63 of this thread's value column (the U and O warps hold the rest)
 #pragma unroll
         for (int j = 0; j < 64; ++j) Sh[j] = S0 ? S0[(int64_t)j * kD + dv] : ((identity && j == dv) ? 1.f : 0.f);
@@ -1209,11 +1233,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         tc::tmem_wait_st();
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
-        if (issuer && c_begin < c_end) {
-            issue_wq(c_begin);
-            issue_ak(c_begin);
-            if (c_begin + 1 < c_end) prefetch(c_begin + 1);
-        }
         named_sync(kBarOR, 256);
         if (issuer && c_begin < c_end) issue_g1(c_begin);
         __syncwarp();
