@@ -8,6 +8,7 @@
 
 #include "kda.h"
 #include "kda_common.cuh"
+#include "kda_f32x2.cuh"
 
 namespace kda {
 
@@ -38,45 +39,7 @@ __device__ __forceinline__ float lane4(const float4 &v, int j) {
     return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-// ---- the per-element arithmetic every kernel here shares ----
-// Two fp32 lanes per instruction (the packed .f32x2 forms of sm_100 and later): each lane
-// is the same IEEE round-to-nearest multiply, add or fused multiply-add as its scalar
-// form, so the results are those of the scalar code, with half the instructions.
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float2 upk2(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ void set4(float4 &v, uint64_t lo, uint64_t hi) {
-    const float2 a = upk2(lo), b = upk2(hi);
-    v = make_float4(a.x, a.y, b.x, b.y);
-}
-
+// ---- the per-element arithmetic every kernel here shares (packed forms in kda_f32x2.cuh) ----
 // S' = a S on one row of this thread, and its term of the projection p += k_r S'_r
 __device__ __forceinline__ void decay_project(float4 &s, float a, float kr, float4 &p) {
     const uint64_t a2 = pk2(a, a), k2 = pk2(kr, kr);

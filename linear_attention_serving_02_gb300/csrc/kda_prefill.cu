@@ -39,6 +39,7 @@
 #include <algorithm>
 
 #include "kda_common.cuh"
+#include "kda_f32x2.cuh"
 #include "kda_tc.cuh"
 
 namespace kda {
@@ -241,7 +242,9 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
 
 // Phase B: Sin[g + 1] = M[g] Sin[g] + R[g] along each sequence's segments, in fp32 on the
 // CUDA cores (exact accumulation, a short serial chain). One CTA per (sequence, head,
-// 16 value columns); thread t computes row t / 2, columns 8 (t % 2) .. +7 of its slice.
+// 16 value columns); thread t computes rows t / 4 and t / 4 + 64, columns 4 (t % 4) .. +3
+// of its slice, two columns per packed FMA (each lane the IEEE fma of the scalar form,
+// the terms added in k order).
 // M and R do not depend on the chain, so the next step's M (64 KB) and R slice are
 // copied into shared memory (cp.async) while the current step multiplies; the chained
 // slice itself stays in shared memory from one step to the next.
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(256)
     const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * 16;
     const int g0 = chains[2 * n], S = chains[2 * n + 1];
     if (S < 3) return;  // no step: segment 1's input state is phase A's R of segment 0
-    const int tid = threadIdx.x, row = tid >> 1, cpart = (tid & 1) * 8;
+    const int tid = threadIdx.x, row = tid >> 2, cpart = (tid & 3) * 4;  // rows row and row + 64
     const size_t seg_stride = (size_t)H * kStateFloats, hoff = (size_t)h * kStateFloats;
 
     auto stage = [&](int sg, int buf) {
@@ -278,10 +281,11 @@ __global__ void __launch_bounds__(256)
     };
 
     stage(1, 0);
-    {
-        const float *X = Sin + (size_t)(g0 + 1) * seg_stride + hoff + row * kD + col0 + cpart;
-        *reinterpret_cast<float4 *>(&s.x[row][cpart]) = *reinterpret_cast<const float4 *>(X);
-        *reinterpret_cast<float4 *>(&s.x[row][cpart + 4]) = *reinterpret_cast<const float4 *>(X + 4);
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int r = row + 64 * hr;
+        *reinterpret_cast<float4 *>(&s.x[r][cpart]) =
+            *reinterpret_cast<const float4 *>(Sin + (size_t)(g0 + 1) * seg_stride + hoff + r * kD + col0 + cpart);
     }
     for (int sg = 1; sg <= S - 2; ++sg) {
         const int buf = (sg - 1) & 1;
@@ -292,31 +296,40 @@ __global__ void __launch_bounds__(256)
             cp_async_wait<0>();
         }
         __syncthreads();  // this step's M, R and x are visible
-        float acc[8];
-        const float4 r0 = *reinterpret_cast<const float4 *>(&s.r[buf][row][cpart]);
-        const float4 r1 = *reinterpret_cast<const float4 *>(&s.r[buf][row][cpart + 4]);
-        acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
-        acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
+        // acc[hr][0] holds columns cpart, cpart + 1 of row + 64 hr; acc[hr][1] the next two
+        uint64_t acc[2][2];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const float4 r0 = *reinterpret_cast<const float4 *>(&s.r[buf][row + 64 * hr][cpart]);
+            acc[hr][0] = pk2(r0.x, r0.y);
+            acc[hr][1] = pk2(r0.z, r0.w);
+        }
 #pragma unroll 4
         for (int k4 = 0; k4 < kD / 4; ++k4) {
-            const float4 m = *reinterpret_cast<const float4 *>(&s.m[buf][row][4 * k4]);
-            const float mk[4] = {m.x, m.y, m.z, m.w};
+            const float4 ma = *reinterpret_cast<const float4 *>(&s.m[buf][row][4 * k4]);
+            const float4 mb = *reinterpret_cast<const float4 *>(&s.m[buf][row + 64][4 * k4]);
+            const float mk[2][4] = {{ma.x, ma.y, ma.z, ma.w}, {mb.x, mb.y, mb.z, mb.w}};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 x0 = *reinterpret_cast<const float4 *>(&s.x[4 * k4 + q][cpart]);
-                const float4 x1 = *reinterpret_cast<const float4 *>(&s.x[4 * k4 + q][cpart + 4]);
-                acc[0] += mk[q] * x0.x; acc[1] += mk[q] * x0.y; acc[2] += mk[q] * x0.z; acc[3] += mk[q] * x0.w;
-                acc[4] += mk[q] * x1.x; acc[5] += mk[q] * x1.y; acc[6] += mk[q] * x1.z; acc[7] += mk[q] * x1.w;
+                const float4 x = *reinterpret_cast<const float4 *>(&s.x[4 * k4 + q][cpart]);
+                const uint64_t x01 = pk2(x.x, x.y), x23 = pk2(x.z, x.w);
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const uint64_t m2 = pk2(mk[hr][q], mk[hr][q]);
+                    acc[hr][0] = fma2(m2, x01, acc[hr][0]);
+                    acc[hr][1] = fma2(m2, x23, acc[hr][1]);
+                }
             }
         }
         __syncthreads();  // every thread is done with x and with buffer buf
-        const float4 y0 = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        const float4 y1 = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        *reinterpret_cast<float4 *>(&s.x[row][cpart]) = y0;
-        *reinterpret_cast<float4 *>(&s.x[row][cpart + 4]) = y1;
-        float *Y = Sin + (size_t)(g0 + sg + 1) * seg_stride + hoff + row * kD + col0 + cpart;
-        *reinterpret_cast<float4 *>(Y) = y0;
-        *reinterpret_cast<float4 *>(Y + 4) = y1;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int r = row + 64 * hr;
+            const float2 a = upk2(acc[hr][0]), b = upk2(acc[hr][1]);
+            const float4 y = make_float4(a.x, a.y, b.x, b.y);
+            *reinterpret_cast<float4 *>(&s.x[r][cpart]) = y;
+            *reinterpret_cast<float4 *>(Sin + (size_t)(g0 + sg + 1) * seg_stride + hoff + r * kD + col0 + cpart) = y;
+        }
     }
 }
 
