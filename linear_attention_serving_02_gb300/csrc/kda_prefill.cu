@@ -241,10 +241,11 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
 }
 
 // Phase B: Sin[g + 1] = M[g] Sin[g] + R[g] along each sequence's segments, in fp32 on the
-// CUDA cores (exact accumulation, a short serial chain). One CTA per (sequence, head,
-// 16 value columns); thread t computes rows t / 4 and t / 4 + 64, columns 4 (t % 4) .. +3
-// of its slice, two columns per packed FMA (each lane the IEEE fma of the scalar form,
-// the terms added in k order).
+// CUDA cores (exact accumulation, a short serial chain). One CTA of 128 threads per
+// (sequence, head, 16 value columns); thread t computes rows t / 4 + 32 i (i = 0 .. 3),
+// columns 4 (t % 4) .. +3 of its slice, two columns per packed FMA (each lane the IEEE
+// fma of the scalar form, the terms added in k order). The step is bound by the shared
+// loads of M and x, so each thread reuses every value it loads four times.
 // M and R do not depend on the chain, so the next step's M (64 KB) and R slice are
 // copied into shared memory (cp.async) while the current step multiplies; the chained
 // slice itself stays in shared memory from one step to the next.
@@ -254,7 +255,9 @@ struct CombineSmem {
     float x[kD][16];
 };
 
-__global__ void __launch_bounds__(256)
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads)
     kda_combine_kernel(const int32_t *__restrict__ status, const int32_t *__restrict__ chains, int32_t H,
                        float *__restrict__ Sin, const float *__restrict__ Mseg, const float *__restrict__ Rseg) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -263,17 +266,17 @@ __global__ void __launch_bounds__(256)
     const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * 16;
     const int g0 = chains[2 * n], S = chains[2 * n + 1];
     if (S < 3) return;  // no step: segment 1's input state is phase A's R of segment 0
-    const int tid = threadIdx.x, row = tid >> 2, cpart = (tid & 3) * 4;  // rows row and row + 64
+    const int tid = threadIdx.x, row = tid >> 2, cpart = (tid & 3) * 4;  // rows row + 32 i
     const size_t seg_stride = (size_t)H * kStateFloats, hoff = (size_t)h * kStateFloats;
 
     auto stage = [&](int sg, int buf) {
         const float *M = Mseg + (size_t)(g0 + sg) * seg_stride + hoff;
         const float *R = Rseg + (size_t)(g0 + sg) * seg_stride + hoff;
-        for (int e = tid; e < kD * (kD / 4); e += 256) {
+        for (int e = tid; e < kD * (kD / 4); e += kCombineThreads) {
             const int rr = e / (kD / 4), c4 = (e % (kD / 4)) * 4;
             cp_async16(&s.m[buf][rr][c4], M + rr * kD + c4);
         }
-        for (int e = tid; e < kD * 4; e += 256) {
+        for (int e = tid; e < kD * 4; e += kCombineThreads) {
             const int rr = e / 4, c4 = (e % 4) * 4;
             cp_async16(&s.r[buf][rr][c4], R + rr * kD + col0 + c4);
         }
@@ -282,8 +285,8 @@ __global__ void __launch_bounds__(256)
 
     stage(1, 0);
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        const int r = row + 64 * hr;
+    for (int i = 0; i < 4; ++i) {
+        const int r = row + 32 * i;
         *reinterpret_cast<float4 *>(&s.x[r][cpart]) =
             *reinterpret_cast<const float4 *>(Sin + (size_t)(g0 + 1) * seg_stride + hoff + r * kD + col0 + cpart);
     }
@@ -296,36 +299,39 @@ __global__ void __launch_bounds__(256)
             cp_async_wait<0>();
         }
         __syncthreads();  // this step's M, R and x are visible
-        // acc[hr][0] holds columns cpart, cpart + 1 of row + 64 hr; acc[hr][1] the next two
-        uint64_t acc[2][2];
+        // acc[i][0] holds columns cpart, cpart + 1 of row + 32 i; acc[i][1] the next two
+        uint64_t acc[4][2];
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const float4 r0 = *reinterpret_cast<const float4 *>(&s.r[buf][row + 64 * hr][cpart]);
-            acc[hr][0] = pk2(r0.x, r0.y);
-            acc[hr][1] = pk2(r0.z, r0.w);
+        for (int i = 0; i < 4; ++i) {
+            const float4 r0 = *reinterpret_cast<const float4 *>(&s.r[buf][row + 32 * i][cpart]);
+            acc[i][0] = pk2(r0.x, r0.y);
+            acc[i][1] = pk2(r0.z, r0.w);
         }
-#pragma unroll 4
+#pragma unroll 2
         for (int k4 = 0; k4 < kD / 4; ++k4) {
-            const float4 ma = *reinterpret_cast<const float4 *>(&s.m[buf][row][4 * k4]);
-            const float4 mb = *reinterpret_cast<const float4 *>(&s.m[buf][row + 64][4 * k4]);
-            const float mk[2][4] = {{ma.x, ma.y, ma.z, ma.w}, {mb.x, mb.y, mb.z, mb.w}};
+            float mk[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 m = *reinterpret_cast<const float4 *>(&s.m[buf][row + 32 * i][4 * k4]);
+                mk[i][0] = m.x; mk[i][1] = m.y; mk[i][2] = m.z; mk[i][3] = m.w;
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float4 x = *reinterpret_cast<const float4 *>(&s.x[4 * k4 + q][cpart]);
                 const uint64_t x01 = pk2(x.x, x.y), x23 = pk2(x.z, x.w);
 #pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const uint64_t m2 = pk2(mk[hr][q], mk[hr][q]);
-                    acc[hr][0] = fma2(m2, x01, acc[hr][0]);
-                    acc[hr][1] = fma2(m2, x23, acc[hr][1]);
+                for (int i = 0; i < 4; ++i) {
+                    const uint64_t m2 = pk2(mk[i][q], mk[i][q]);
+                    acc[i][0] = fma2(m2, x01, acc[i][0]);
+                    acc[i][1] = fma2(m2, x23, acc[i][1]);
                 }
             }
         }
         __syncthreads();  // every thread is done with x and with buffer buf
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int r = row + 64 * hr;
-            const float2 a = upk2(acc[hr][0]), b = upk2(acc[hr][1]);
+        for (int i = 0; i < 4; ++i) {
+            const int r = row + 32 * i;
+            const float2 a = upk2(acc[i][0]), b = upk2(acc[i][1]);
             const float4 y = make_float4(a.x, a.y, b.x, b.y);
             *reinterpret_cast<float4 *>(&s.x[r][cpart]) = y;
             *reinterpret_cast<float4 *>(Sin + (size_t)(g0 + sg + 1) * seg_stride + hoff + r * kD + col0 + cpart) = y;
@@ -1346,7 +1352,7 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
         configured = true;
     }
     dim3 grid((unsigned)N, (unsigned)H, kD / 16);
-    kda_combine_kernel<<<grid, 256, sizeof(CombineSmem), st>>>(status, chains, H, Sin, Mseg, Rseg);
+    kda_combine_kernel<<<grid, kCombineThreads, sizeof(CombineSmem), st>>>(status, chains, H, Sin, Mseg, Rseg);
     return cudaGetLastError();
 }
 
