@@ -921,12 +921,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // Eight warps with fixed roles:
 //   warps 0-3  U and O: thread = value channel dv (TMEM lane dv). After group 1 they
 //              build U^T (and start loading the next chunk's U'); after group 2 they
-//              read the output accumulators, then stage o through shared memory and
+//              update key rows 64-127 of S (in fp32 registers) and write their S^T
+//              planes, stage o in shared memory from the output accumulators, and
 //              store it in 16-byte row chunks while the next chunk's group 1 runs.
-//   warps 4-7  state: thread = value channel dv, its 128 state entries in fp32
-//              registers. After group 2 they update S and write the next S^T planes.
-//              Thread 128 also issues the bulk copies (one chunk ahead, with an L2
-//              prefetch two chunks ahead) and the MMAs.
+//   warps 4-7  state: thread = value channel dv, key rows 0-63 of S in fp32 registers.
+//              After group 2 they update those rows and write their S^T planes.
+//              Thread 128 also issues the MMAs and the bulk copies: [ -W ; Qhat ] one
+//              chunk ahead, [ A_qk ; Kend^T ] two chunks ahead into two slots. (An L2
+//              prefetch of later records measured slower: it holds the copy engine.)
 // Named barriers hand the steps over: BAR_U (U^T planes ready), BAR_OR (output
 // accumulators read), and a state-warp barrier (S^T planes ready). Every role runs the
 // same barrier sequence whatever happens: a wait that gives up marks the CTA failed, the
@@ -935,11 +937,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // ---------------------------------------------------------------------------------
 struct WalkSmem {
     unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
-    unsigned char ak[2 * kStackAK];      // [ A_qk ; Kend^T ] hi | lo
+    unsigned char ak[2][2 * kStackAK];   // [ A_qk ; Kend^T ] hi | lo, of chunks c (slot c & 1)
     alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1), the state warps' copy
     alignas(16) float gam_uo[2][kD];     // the same, the U and O warps' copy
     unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
-    uint64_t bar_wq, bar_ak, bar_m1, bar_m2;
+    uint64_t bar_wq, bar_ak[2], bar_m1, bar_m2;
     uint32_t tmem_base;
     int fail;
 };
@@ -1009,7 +1011,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             tc::mbar_init(&s.bar_wq, 1);
-            tc::mbar_init(&s.bar_ak, 1);
+            tc::mbar_init(&s.bar_ak[0], 1);
+            tc::mbar_init(&s.bar_ak[1], 1);
             tc::mbar_init(&s.bar_m1, 1);
             tc::mbar_init(&s.bar_m2, 1);
             tc::mbar_init_fence();
@@ -1160,7 +1163,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const uint32_t kIdG1 = tc::idesc_bf16_m128(maps ? 64 : 128);
         const uint32_t kIdG2 = tc::idesc_bf16_m128(maps ? 128 : 192);
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
-        int n_wq = 0, n_ak = 0, w_wq = 0, w_ak = 0, n_m1 = 0, n_m2 = 0;  // phase bookkeeping (issuer)
+        // phase bookkeeping (issuer); the [ A_qk ; Kend^T ] slot of chunk c is (c - c_begin) & 1
+        int n_wq = 0, w_wq = 0, n_m1 = 0, n_m2 = 0, n_ak0 = 0, n_ak1 = 0, w_ak0 = 0, w_ak1 = 0;
         auto issue_wq = [&](int c) {
             if (maps) {  // the -W rows of the hi and the lo plane
                 tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kPlaneQK));
@@ -1173,35 +1177,24 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++n_wq;
         };
         auto issue_ak = [&](int c) {
+            const int slot = (c - c_begin) & 1;
+            unsigned char *dst = s.ak[slot];
+            uint64_t *bar = &s.bar_ak[slot];
             if (maps) {  // the Kend^T rows of the hi and the lo plane
-                tc::mbar_arrive_expect_tx(&s.bar_ak, (uint32_t)(2 * kPlaneKT));
-                tc::bulk_g2s(s.ak + kPlaneCC, rec_of(c) + kRecAK + kPlaneCC, (uint32_t)kPlaneKT, &s.bar_ak);
-                tc::bulk_g2s(s.ak + kStackAK + kPlaneCC, rec_of(c) + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT,
-                             &s.bar_ak);
+                tc::mbar_arrive_expect_tx(bar, (uint32_t)(2 * kPlaneKT));
+                tc::bulk_g2s(dst + kPlaneCC, rec_of(c) + kRecAK + kPlaneCC, (uint32_t)kPlaneKT, bar);
+                tc::bulk_g2s(dst + kStackAK + kPlaneCC, rec_of(c) + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT,
+                             bar);
             } else {
-                tc::mbar_arrive_expect_tx(&s.bar_ak, (uint32_t)(2 * kStackAK));
-                tc::bulk_g2s(s.ak, rec_of(c) + kRecAK, (uint32_t)(2 * kStackAK), &s.bar_ak);
+                tc::mbar_arrive_expect_tx(bar, (uint32_t)(2 * kStackAK));
+                tc::bulk_g2s(dst, rec_of(c) + kRecAK, (uint32_t)(2 * kStackAK), bar);
             }
-            ++n_ak;
-        };
-        // L2 prefetch of what a later chunk's walk will read
-        auto prefetch = [&](int c) {
-            const uint8_t *r = rec_of(c);
-            if (!maps) {
-                tc::prefetch_l2(r, (uint32_t)kRecBytes);
-                return;
-            }
-            tc::prefetch_l2(r + kRecWQ, (uint32_t)kPlaneQK);
-            tc::prefetch_l2(r + kRecWQ + kStackWQ, (uint32_t)kPlaneQK);
-            tc::prefetch_l2(r + kRecAK + kPlaneCC, (uint32_t)kPlaneKT);
-            tc::prefetch_l2(r + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT);
-            tc::prefetch_l2(r + kRecGam, (uint32_t)(kRecBytes - kRecGam));  // gamma and U'
+            ++(slot ? n_ak1 : n_ak0);
         };
         // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
         auto issue_g1 = [&](int c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
-            if (c + 2 < c_end) prefetch(c + 2);
             if (wait_or_fail(&s.bar_wq, ph, fail)) {
                 ++w_wq;
                 const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
@@ -1221,9 +1214,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         auto issue_g2 = [&](int c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             tc::fence_after_sync();
-            if (wait_or_fail(&s.bar_ak, ph, fail)) {
-                ++w_ak;
-                const uint32_t b0s = tc::smem_addr(s.ak) + ak_off, b1s = b0s + (uint32_t)kStackAK;
+            const int slot = (c - c_begin) & 1;
+            if (wait_or_fail(&s.bar_ak[slot], (uint32_t)(((c - c_begin) >> 1) & 1), fail)) {
+                ++(slot ? w_ak1 : w_ak0);
+                const uint32_t b0s = tc::smem_addr(s.ak[slot]) + ak_off, b1s = b0s + (uint32_t)kStackAK;
 #pragma unroll 1
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint32_t a0 = tmem + kColUHi + 8 * ks, a1 = tmem + kColULo + 8 * ks;
@@ -1237,11 +1231,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++n_m2;
         };
 
-        // the first chunk's record is copied while the initial state is read
+        // the first chunk's record (and the second's [ A_qk ; Kend^T ]) are copied while
+        // the initial state is read
         if (issuer && c_begin < c_end) {
             issue_wq(c_begin);
             issue_ak(c_begin);
-            if (c_begin + 1 < c_end) prefetch(c_begin + 1);
+            if (c_begin + 1 < c_end) issue_ak(c_begin + 1);
         }
         // key rows 0 .. 63 of this thread's value column (the U and O warps hold the rest)
 #pragma unroll
@@ -1266,7 +1261,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             if (issuer) issue_g2(c);
             __syncwarp();
             const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
-            if (issuer && ok && c + 1 < c_end) issue_ak(c + 1);  // group 2 is done with [ A_qk ; Kend^T ]
+            // group 2 is done with this slot of [ A_qk ; Kend^T ]: the chunk after next lands there
+            if (issuer && ok && c + 2 < c_end) issue_ak(c + 2);
             s.gam[ph][dv] = gnext;
             named_sync(4, 128);  // gamma of this chunk in place
             // S <- Diag(gamma) S + D_S on key rows 0 .. 63 and their split planes, in blocks
@@ -1310,7 +1306,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             // a wait gave up: let copies and MMAs still in flight land (bounded) before
             // shared memory and TMEM are released, and report through the status word
             if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
-            if (n_ak > w_ak) tc::mbar_wait(&s.bar_ak, (uint32_t)(w_ak & 1));
+            if (n_ak0 > w_ak0) tc::mbar_wait(&s.bar_ak[0], (uint32_t)(w_ak0 & 1));
+            if (n_ak1 > w_ak1) tc::mbar_wait(&s.bar_ak[1], (uint32_t)(w_ak1 & 1));
             if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
             if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
             atomicExch(status, -7);
