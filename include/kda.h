@@ -42,7 +42,9 @@ extern "C" {
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_NULL = -1,        /* a required pointer is NULL */
-    KDA_ERR_SHAPE = -2,       /* a size is negative or inconsistent */
+    KDA_ERR_SHAPE = -2,       /* a size is negative or inconsistent, or beyond the launch
+                                 limits: num_seqs x num_heads >= 2^31, num_heads > 65535, or
+                                 (prefill) chunk slots x num_heads >= 2^31 */
     KDA_ERR_UNSUPPORTED = -3, /* d_k or d_v other than 128, or an unknown output dtype */
     KDA_ERR_SEQLENS = -4,     /* cu_seqlens not rising from 0 to the token count */
     KDA_ERR_ALIGN = -5,       /* a pointer is not 16-byte (workspace: 256-byte) aligned */

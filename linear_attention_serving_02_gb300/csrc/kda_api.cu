@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <climits>
+
 #include "kda.h"
 #include "kda_common.cuh"
 
@@ -147,7 +149,7 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                       void *workspace, size_t workspace_bytes, void *stream) {
     if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
     if (o_dtype != KDA_OUT_BF16 && o_dtype != KDA_OUT_F32) return KDA_ERR_UNSUPPORTED;
-    if (batch < 0 || seq_len < 0 || num_seqs < 0 || num_heads <= 0) return KDA_ERR_SHAPE;
+    if (batch < 0 || seq_len < 0 || num_seqs < 0 || num_heads <= 0 || num_heads > 65535) return KDA_ERR_SHAPE;
     const int64_t total = (int64_t)batch * seq_len;
     if (total >= (int64_t)1 << 31) return KDA_ERR_SHAPE;  // token offsets are int32
     if (cu_seqlens) {
@@ -162,6 +164,8 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
         !aligned(final_state, 16) || !aligned(initial_state, 16) || !aligned(A, 4) || !aligned(b, 4))
         return KDA_ERR_ALIGN;
     if (!aligned(workspace, 256)) return KDA_ERR_ALIGN;
+    // (chunk slot, head) items are counted in int32 by the intra-chunk kernel
+    if (ws_layout(total, num_seqs, num_heads).nslots * num_heads > INT32_MAX) return KDA_ERR_SHAPE;
     if (workspace_bytes < kda_chunk_prefill_workspace_size(total, num_seqs, num_heads)) return KDA_ERR_WORKSPACE;
     if (cu_seqlens_host) {
         if (cu_seqlens_host[0] != 0 || (int64_t)cu_seqlens_host[num_seqs] != total) return KDA_ERR_SEQLENS;
@@ -230,11 +234,17 @@ int kda_workspace_status(const void *workspace, void *stream) {
     return st_host;
 }
 
+// (sequence, head) pairs are grid x of the decode-family launches; heads are grid y of
+// the walk and the combine
+static bool pairs_fit(int32_t num_seqs, int32_t num_heads) {
+    return (int64_t)num_seqs * num_heads <= INT32_MAX && num_heads <= 65535;
+}
+
 int kda_recurrent_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
                          const float *b, float *state, float *o, int32_t num_seqs, int32_t num_heads, int32_t d_k,
                          int32_t d_v, void *stream) {
     if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
-    if (num_seqs < 0 || num_heads <= 0) return KDA_ERR_SHAPE;
+    if (num_seqs < 0 || num_heads <= 0 || !pairs_fit(num_seqs, num_heads)) return KDA_ERR_SHAPE;
     if (num_seqs == 0) return KDA_OK;
     if (!q || !k || !v || !z || !A || !b || !state || !o) return KDA_ERR_NULL;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) || !aligned(state, 16) ||
@@ -255,7 +265,7 @@ int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          float *beta_log, int32_t num_seqs, int32_t num_heads, int32_t num_tokens, int32_t d_k,
                          int32_t d_v, void *stream) {
     if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
-    if (num_seqs < 0 || num_heads <= 0 || num_tokens < 0) return KDA_ERR_SHAPE;
+    if (num_seqs < 0 || num_heads <= 0 || num_tokens < 0 || !pairs_fit(num_seqs, num_heads)) return KDA_ERR_SHAPE;
     if (num_tokens > KDA_MAX_REPLAY_TOKENS) return KDA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || num_tokens == 0) return KDA_OK;
     if (!q || !k || !v || !z || !A || !b || !state || !o) return KDA_ERR_NULL;
@@ -278,7 +288,7 @@ int kda_replay_fold(const uint16_t *k, const uint16_t *v, const float *gk_log, c
                     const int32_t *num_accepted, float *state, int32_t num_seqs, int32_t num_heads,
                     int32_t num_tokens, int32_t d_k, int32_t d_v, void *stream) {
     if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
-    if (num_seqs < 0 || num_heads <= 0 || num_tokens < 0) return KDA_ERR_SHAPE;
+    if (num_seqs < 0 || num_heads <= 0 || num_tokens < 0 || !pairs_fit(num_seqs, num_heads)) return KDA_ERR_SHAPE;
     if (num_tokens > KDA_MAX_REPLAY_TOKENS) return KDA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || num_tokens == 0) return KDA_OK;
     if (!k || !v || !gk_log || !beta_log || !num_accepted || !state) return KDA_ERR_NULL;
@@ -301,7 +311,7 @@ int kda_fused_decode(const uint16_t *x_q, const uint16_t *x_k, const uint16_t *x
                      int32_t num_heads, int32_t d_k, int32_t d_v, void *stream) {
     if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
     if (!(eps_l2 >= 0.0f) || !(eps_rms >= 0.0f)) return KDA_ERR_UNSUPPORTED;  // NaN fails both
-    if (num_seqs < 0 || num_heads <= 0) return KDA_ERR_SHAPE;
+    if (num_seqs < 0 || num_heads <= 0 || !pairs_fit(num_seqs, num_heads)) return KDA_ERR_SHAPE;
     if (num_seqs == 0) return KDA_OK;
     if (!x_q || !x_k || !x_v || !conv_state || !conv_w || !z || !A || !b || !g || !norm_w || !state || !y)
         return KDA_ERR_NULL;

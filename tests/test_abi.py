@@ -102,6 +102,8 @@ def _host_cu(vals):
     (dict(batch=2, num_seqs=1), KDA_ERR_SHAPE),
     (dict(batch=2, num_seqs=2, cu=FAKE), KDA_ERR_SHAPE),
     (dict(seq_len=1 << 31), KDA_ERR_SHAPE),
+    (dict(num_heads=65536), KDA_ERR_SHAPE),                       # heads are grid y
+    (dict(seq_len=1 << 30, num_heads=4096), KDA_ERR_SHAPE),        # chunk slots x heads >= 2^31
     (dict(q=None), KDA_ERR_NULL),
     (dict(final_state=None), KDA_ERR_NULL),
     (dict(workspace=None), KDA_ERR_NULL),
@@ -141,6 +143,8 @@ def _decode(**over):
     (dict(d_k=96), KDA_ERR_UNSUPPORTED),
     (dict(num_heads=0), KDA_ERR_SHAPE),
     (dict(num_seqs=-3), KDA_ERR_SHAPE),
+    (dict(num_seqs=1 << 30, num_heads=4), KDA_ERR_SHAPE),          # pairs >= 2^31
+    (dict(num_seqs=1, num_heads=65536), KDA_ERR_SHAPE),
     (dict(state=None), KDA_ERR_NULL),
     (dict(o=None), KDA_ERR_NULL),
     (dict(v=FAKE + 2), KDA_ERR_ALIGN),
@@ -165,6 +169,7 @@ def _verify(**over):
     (dict(d_v=64), KDA_ERR_UNSUPPORTED),
     (dict(m=17), KDA_ERR_UNSUPPORTED),
     (dict(m=-1), KDA_ERR_SHAPE),
+    (dict(num_seqs=1 << 30, num_heads=4), KDA_ERR_SHAPE),
     (dict(num_heads=0), KDA_ERR_SHAPE),
     (dict(state=None), KDA_ERR_NULL),
     (dict(z=None), KDA_ERR_NULL),
@@ -191,6 +196,7 @@ def _fold(**over):
     (dict(d_k=256), KDA_ERR_UNSUPPORTED),
     (dict(m=KDA_MAX_REPLAY + 1), KDA_ERR_UNSUPPORTED),
     (dict(num_seqs=-1), KDA_ERR_SHAPE),
+    (dict(num_seqs=1 << 30, num_heads=4), KDA_ERR_SHAPE),
     (dict(acc=None), KDA_ERR_NULL),
     (dict(gk=None), KDA_ERR_NULL),
     (dict(acc=FAKE + 2), KDA_ERR_ALIGN),
@@ -222,6 +228,7 @@ def _fused(**over):
     (dict(e1=-1.0), KDA_ERR_UNSUPPORTED),
     (dict(e2=float("nan")), KDA_ERR_UNSUPPORTED),
     (dict(num_heads=0), KDA_ERR_SHAPE),
+    (dict(num_seqs=1 << 30, num_heads=4), KDA_ERR_SHAPE),
     (dict(cs=None), KDA_ERR_NULL),
     (dict(nw=None), KDA_ERR_NULL),
     (dict(cw=FAKE + 4), KDA_ERR_ALIGN),
