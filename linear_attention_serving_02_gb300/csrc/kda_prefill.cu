@@ -1192,11 +1192,23 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++(slot ? n_ak1 : n_ak0);
         };
         // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
-        auto issue_g1 = [&](int c) {
-            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
+        // The copy waits run before the barrier that precedes each group, off the chain:
+        // a wait right after the barrier cost its issue about 400 cycles even when the
+        // data had long landed.
+        auto wait_wq = [&](int c) {
+            if (!wait_or_fail(&s.bar_wq, (uint32_t)((c - c_begin) & 1), fail)) return false;
+            ++w_wq;
+            return true;
+        };
+        auto wait_ak = [&](int c) {
+            const int slot = (c - c_begin) & 1;
+            if (!wait_or_fail(&s.bar_ak[slot], (uint32_t)(((c - c_begin) >> 1) & 1), fail)) return false;
+            ++(slot ? w_ak1 : w_ak0);
+            return true;
+        };
+        auto issue_g1 = [&](int c, bool ready) {
             tc::fence_after_sync();
-            if (wait_or_fail(&s.bar_wq, ph, fail)) {
-                ++w_wq;
+            if (ready) {
                 const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
 #pragma unroll 1
                 for (int ks = 0; ks < kD / 16; ++ks) {
@@ -1211,12 +1223,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++n_m1;
         };
         // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T
-        auto issue_g2 = [&](int c) {
-            const uint32_t ph = (uint32_t)((c - c_begin) & 1);
+        auto issue_g2 = [&](int c, bool ready) {
             tc::fence_after_sync();
             const int slot = (c - c_begin) & 1;
-            if (wait_or_fail(&s.bar_ak[slot], (uint32_t)(((c - c_begin) >> 1) & 1), fail)) {
-                ++(slot ? w_ak1 : w_ak0);
+            if (ready) {
                 const uint32_t b0s = tc::smem_addr(s.ak[slot]) + ak_off, b1s = b0s + (uint32_t)kStackAK;
 #pragma unroll 1
                 for (int ks = 0; ks < kC / 16; ++ks) {
@@ -1247,8 +1257,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         tc::tmem_wait_st();
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
+        bool wq_ok = false;
+        if (issuer && c_begin < c_end) wq_ok = wait_wq(c_begin);
+        __syncwarp();
         named_sync(kBarOR, 256);
-        if (issuer && c_begin < c_end) issue_g1(c_begin);
+        if (issuer && c_begin < c_end) issue_g1(c_begin, wq_ok);
         __syncwarp();
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
@@ -1256,9 +1269,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             // the next [ -W ; Qhat ] copy starts as soon as group 1 of this chunk is done
             // with the buffer, before the U epilogue
             if (issuer && c + 1 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_wq(c + 1);
+            bool ak_ok = false;
+            if (issuer) ak_ok = wait_ak(c);
             __syncwarp();
             named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
-            if (issuer) issue_g2(c);
+            if (issuer) issue_g2(c, ak_ok);
             __syncwarp();
             const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
             // group 2 is done with this slot of [ A_qk ; Kend^T ]: the chunk after next lands there
@@ -1296,10 +1311,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
+            wq_ok = false;
+            if (issuer && c + 1 < c_end) wq_ok = wait_wq(c + 1);
+            __syncwarp();
             named_sync(4, 128);       // rows 0 .. 63 of the next S^T planes complete
             named_sync(kBarOR, 256);  // the U and O warps have written rows 64 .. 127 and read
                                       // this chunk's D_S and output accumulators
-            if (issuer && c + 1 < c_end) issue_g1(c + 1);
+            if (issuer && c + 1 < c_end) issue_g1(c + 1, wq_ok);
             __syncwarp();
         }
         if (issuer && fail) {
