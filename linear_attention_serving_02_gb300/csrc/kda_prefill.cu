@@ -1192,9 +1192,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++(slot ? n_ak1 : n_ak0);
         };
         // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
-        // The copy waits run before the barrier that precedes each group, off the chain:
-        // a wait right after the barrier cost its issue about 400 cycles even when the
-        // data had long landed.
+        // The copy waits run off the chain (an mbarrier wait costs a few hundred cycles
+        // even when the data has long landed; right after a barrier it held the group's
+        // issue that long): chunk c + 1's [ A_qk ; Kend^T ] while chunk c's group 2 runs,
+        // its [ -W ; Qhat ] at the end of chunk c's state update.
         auto wait_wq = [&](int c) {
             if (!wait_or_fail(&s.bar_wq, (uint32_t)((c - c_begin) & 1), fail)) return false;
             ++w_wq;
@@ -1257,8 +1258,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         tc::tmem_wait_st();
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
-        bool wq_ok = false;
-        if (issuer && c_begin < c_end) wq_ok = wait_wq(c_begin);
+        bool wq_ok = false, ak_ok = false;
+        if (issuer && c_begin < c_end) {
+            wq_ok = wait_wq(c_begin);
+            ak_ok = wait_ak(c_begin);
+        }
         __syncwarp();
         named_sync(kBarOR, 256);
         if (issuer && c_begin < c_end) issue_g1(c_begin, wq_ok);
@@ -1269,11 +1273,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             // the next [ -W ; Qhat ] copy starts as soon as group 1 of this chunk is done
             // with the buffer, before the U epilogue
             if (issuer && c + 1 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_wq(c + 1);
-            bool ak_ok = false;
-            if (issuer) ak_ok = wait_ak(c);
             __syncwarp();
             named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
             if (issuer) issue_g2(c, ak_ok);
+            // while group 2 runs: the next chunk's [ A_qk ; Kend^T ] (issued a chunk ago)
+            if (issuer) ak_ok = c + 1 < c_end && wait_ak(c + 1);
             __syncwarp();
             const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
             // group 2 is done with this slot of [ A_qk ; Kend^T ]: the chunk after next lands there
@@ -1311,7 +1315,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
-            wq_ok = false;
+            wq_ok = false;  // the next chunk's [ -W ; Qhat ], issued after this chunk's group 1
             if (issuer && c + 1 < c_end) wq_ok = wait_wq(c + 1);
             __syncwarp();
             named_sync(4, 128);       // rows 0 .. 63 of the next S^T planes complete
