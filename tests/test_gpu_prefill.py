@@ -187,3 +187,35 @@ def test_segmented_walk(lens, H):
                                       cu_seqlens=cu)
     o, S = gpu_prefill(inp, cu=cu)
     assert_prefill_close(o, S, o_ref, S_ref, "segmented %s" % lens)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_segmented_walk_random(seed):
+    """Random batches that take the segmented walk (checked through the launch count):
+    one to four sequences, lengths chunk-aligned or ragged, with an occasional empty or
+    short one, against the oracle."""
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 5))
+    H = int(rng.integers(1, 4))
+    lens = []
+    for _ in range(n):
+        kind = rng.integers(0, 4)
+        if kind == 0:
+            lens.append(int(rng.integers(24, 80)) * 64)          # whole chunks
+        elif kind == 1:
+            lens.append(int(rng.integers(1600, 5000)))          # ragged tail
+        elif kind == 2 and n > 1:
+            lens.append(int(rng.integers(0, 3)) * int(rng.integers(1, 70)))  # empty or short
+        else:
+            lens.append(int(rng.integers(2000, 4000)))
+    total = int(sum(lens))
+    if kda.kda_chunk_prefill_launch_count(total, n, H) != 5:
+        lens[0] += 64 * 24 * n  # long enough on average for the segmented walk
+        total = int(sum(lens))
+    assert kda.kda_chunk_prefill_launch_count(total, n, H) == 5, (lens, H)
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    inp = inputs.prefill_inputs(total, H, n, seed=200 + seed, init_state=True)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu)
+    assert_prefill_close(o, S, o_ref, S_ref, "segmented random %s x %d" % (lens, H))
