@@ -98,3 +98,38 @@ def test_decode_batched_config_sampled():
     torch.cuda.synchronize()
     assert rel_frob(state[ns, hs], S_s[0]) <= DECODE_TOL
     assert torch.isfinite(state).all()
+
+
+@pytest.mark.parametrize("extra", [-1, 0])
+def test_decode_at_the_column_split_boundary(extra):
+    """Just below and at the pair count where decode switches from quarter-row CTAs to
+    whole-row CTAs (four per SM of this device): both against the oracle, and verify and
+    fold (which must take the same split) bit for bit against it."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = 4 * sms + extra
+    N, H = pairs, 1
+    steps = [inputs.decode_step_inputs(N, H, seed=31, step=t) for t in range(2)]
+    S0 = inputs.decode_state(N, H, seed=31)
+    state = S0.cuda()
+    outs = []
+    for st in steps:
+        g = _to(st, "cuda")
+        outs.append(kda.kda_recurrent_decode(g["q"], g["k"], g["v"], g["z"], g["A"], g["b"], state))
+    torch.cuda.synchronize()
+    o_ref, S_ref = _oracle_steps(steps, S0)
+    for t in range(2):
+        assert max_over_rms(outs[t], o_ref[t]) <= DECODE_TOL, t
+    assert rel_frob(state, S_ref) <= DECODE_TOL
+    # verify over the same two tokens from the checkpoint, then fold both: identical bits
+    win = {key: torch.stack([st[key] for st in steps], 1).reshape((N * 2,) + tuple(steps[0][key].shape[1:]))
+           for key in ("q", "k", "v", "z", "b")}
+    g = _to(win, "cuda")
+    S0c = S0.cuda()
+    o_v, gk, beta = kda.kda_recurrent_verify(g["q"], g["k"], g["v"], g["z"], steps[0]["A"].cuda(), g["b"], S0c, 2)
+    o_v = o_v.reshape(N, 2, H, 128)
+    for t in range(2):
+        assert torch.equal(o_v[:, t], outs[t]), t
+    acc = torch.full((N,), 2, dtype=torch.int32, device="cuda")
+    folded = S0c.clone()
+    kda.kda_replay_fold(g["k"], g["v"], gk, beta, acc, folded, 2)
+    assert torch.equal(folded, state)

@@ -219,3 +219,23 @@ def test_segmented_walk_random(seed):
                                       cu_seqlens=cu)
     o, S = gpu_prefill(inp, cu=cu)
     assert_prefill_close(o, S, o_ref, S_ref, "segmented random %s x %d" % (lens, H))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plain_walk_random(seed):
+    """Random batches of many short sequences (one plain walk unit per chain, checked
+    through the launch count), lengths drawn from the edge values 0, 1, 63, 64, 65 and
+    from 1 .. 700, against the oracle."""
+    rng = np.random.default_rng(300 + seed)
+    n = int(rng.integers(8, 41))
+    H = int(rng.integers(1, 5))
+    edges = [0, 1, 63, 64, 65]
+    lens = [int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(1, 701)) for _ in range(n)]
+    total = int(sum(lens))
+    assert kda.kda_chunk_prefill_launch_count(total, n, H) == 3, (lens, H)
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    inp = inputs.prefill_inputs(total, H, n, seed=400 + seed, init_state=True)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu)
+    assert_prefill_close(o, S, o_ref, S_ref, "plain random %d sequences x %d" % (n, H))
