@@ -44,6 +44,13 @@
 
 namespace kda {
 
+// Programmatic dependent launch: the kernels after the plan kernel are launched while
+// their predecessor runs. Each waits for the predecessor to finish (and its memory to be
+// visible) before anything else; each lets its successor launch once all its own CTAs
+// are resident, so a waiting successor never holds an SM a predecessor CTA still needs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // ---------------------------------------------------------------------------------
 // plan: seq_cu[N+1] and chunk_off[N+1] (prefix sums of ceil(len / C)) in the workspace
 // ---------------------------------------------------------------------------------
@@ -155,6 +162,7 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
     __shared__ int32_t carry;
     __shared__ int32_t bad;
     __shared__ int32_t scan[256];
+    pdl_trigger();
     const int tid = threadIdx.x;
     if (tid == 0) {
         carry = 0;
@@ -262,6 +270,8 @@ __global__ void __launch_bounds__(kCombineThreads)
                        float *__restrict__ Sin, const float *__restrict__ Mseg, const float *__restrict__ Rseg) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     CombineSmem &s = *reinterpret_cast<CombineSmem *>(smem_raw);
+    pdl_wait();
+    pdl_trigger();
     if (*status != 0) return;
     const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * 16;
     const int g0 = chains[2 * n], S = chains[2 * n + 1];
@@ -424,6 +434,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
     if (*status != 0 || N <= 0) return;
     // persistent: CTA b takes items b, b + gridDim.x, ...; item = slot * H + h
     const int n_items = chunk_off[N] * H;
@@ -990,6 +1002,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y;
+    pdl_wait();
+    pdl_trigger();
     if ((int)blockIdx.x >= *n_units) return;
     const WalkUnit unit = units[blockIdx.x];
     const float *S0 = unit.in ? unit.in + (size_t)h * kStateFloats : nullptr;
@@ -1353,6 +1367,24 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 // host-side launchers (called from kda_api.cu)
 // ---------------------------------------------------------------------------------
 size_t intra_smem_bytes() { return sizeof(IntraSmem); }
+
+// a launch that may start while the previous kernel on the stream runs (the kernel
+// waits for it with griddepcontrol.wait before touching its results)
+template <typename... Params, typename... Args>
+static cudaError_t launch_after(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
                         int32_t *n_units, const SegPlan &sp, cudaStream_t st) {
@@ -1371,8 +1403,8 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
         configured = true;
     }
     dim3 grid((unsigned)N, (unsigned)H, kD / 16);
-    kda_combine_kernel<<<grid, kCombineThreads, sizeof(CombineSmem), st>>>(status, chains, H, Sin, Mseg, Rseg);
-    return cudaGetLastError();
+    return launch_after(kda_combine_kernel, grid, dim3(kCombineThreads), sizeof(CombineSmem), st, status, chains, H,
+                        Sin, Mseg, Rseg);
 }
 
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
@@ -1390,9 +1422,8 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
     // persistent: one CTA per SM (the shared memory allows no more) walks the items
     const int64_t items = nslots * H;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)num_sms);
-    kda_intra_kernel<<<grid, kIntraThreads, sizeof(IntraSmem), st>>>(q, k, v, z, A, b, status, seq_cu, chunk_off, N,
-                                                                     H, records);
-    return cudaGetLastError();
+    return launch_after(kda_intra_kernel, dim3(grid), dim3(kIntraThreads), sizeof(IntraSmem), st, q, k, v, z, A, b,
+                        status, seq_cu, chunk_off, N, H, records);
 }
 
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
@@ -1406,8 +1437,8 @@ cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n
     }
     if (max_units <= 0) return cudaSuccess;
     dim3 grid((unsigned)max_units, (unsigned)H);
-    kda_walk_kernel<<<grid, kWalkThreads, sizeof(WalkSmem), st>>>(status, units, n_units, H, records, o, o_f32);
-    return cudaGetLastError();
+    return launch_after(kda_walk_kernel, grid, dim3(kWalkThreads), sizeof(WalkSmem), st, status, units, n_units, H,
+                        records, o, o_f32);
 }
 
 }  // namespace kda
