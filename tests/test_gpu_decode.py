@@ -133,3 +133,14 @@ def test_decode_at_the_column_split_boundary(extra):
     folded = S0c.clone()
     kda.kda_replay_fold(g["k"], g["v"], gk, beta, acc, folded, 2)
     assert torch.equal(folded, state)
+
+
+def test_decode_writes_every_output_over_poison():
+    """o starts as NaN: every (sequence, head, channel) is written."""
+    for N, H in ((3, 2), (80, 8)):  # quarter-row and whole-row launches
+        st = _to(inputs.decode_step_inputs(N, H, seed=41, step=0), "cuda")
+        state = inputs.decode_state(N, H, seed=41).cuda()
+        o = torch.full((N, H, 128), float("nan"), dtype=torch.float32, device="cuda")
+        kda.kda_recurrent_decode(st["q"], st["k"], st["v"], st["z"], st["A"], st["b"], state, o=o)
+        torch.cuda.synchronize()
+        assert torch.isfinite(o).all() and torch.isfinite(state).all()

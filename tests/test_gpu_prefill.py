@@ -239,3 +239,27 @@ def test_plain_walk_random(seed):
                                       cu_seqlens=cu)
     o, S = gpu_prefill(inp, cu=cu)
     assert_prefill_close(o, S, o_ref, S_ref, "plain random %d sequences x %d" % (n, H))
+
+
+@pytest.mark.parametrize("lens,H,o_dtype", [([300, 0, 1, 64, 129], 3, torch.bfloat16),   # plain walk
+                                            ([5000, 0, 1700], 2, torch.float32)])      # segmented walk
+def test_every_output_written_over_poison(lens, H, o_dtype):
+    """o, final_state and the workspace start filled with NaN bytes: every output must be
+    written (finite) and right, and nothing may read workspace that was not written."""
+    total = int(sum(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    inp = inputs.prefill_inputs(total, H, len(lens), seed=500, init_state=True)
+    g = _cuda(inp)
+    o = torch.full((1, total, H, 128), float("nan"), dtype=o_dtype, device="cuda")
+    S = torch.full((len(lens), H, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.full((kda.kda_chunk_prefill_workspace_size(total, len(lens), H),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    kda.kda_chunk_prefill(g["q"], g["k"], g["v"], g["z"], g["A"], g["b"], initial_state=g["S0"],
+                          cu_seqlens=torch.tensor(cu, dtype=torch.int32, device="cuda"),
+                          cu_seqlens_host=torch.tensor(cu, dtype=torch.int32), o=o, final_state=S, workspace=ws,
+                          o_dtype=o_dtype)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    assert_prefill_close(o.cpu(), S.cpu(), o_ref, S_ref, "poisoned %s" % lens)
