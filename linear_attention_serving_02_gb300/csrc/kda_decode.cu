@@ -15,16 +15,15 @@
 // L2) and keep it in registers between the reductions over key channels.
 //
 // Thread layout: a CTA of 256 threads covers a slice of CWD value columns. Each thread
-// owns 4 consecutive columns (one float4) of RPT key rows; the rows of the 256 threads
-// interleave so that every warp-wide access is one contiguous run of a row.
+// owns 4 consecutive columns (one float4) of RPT consecutive key rows; a warp-wide access
+// to one of its rows is one contiguous run of that row.
 //
 // ReplaySSM ('Kimi K3 attention deep dive', §6.2): instead of a 64 KB state snapshot per
 // draft token, the verify kernel logs each token's gate values (log a, beta) next to the
 // caller's k and v, about 1 KB per token and head; once the sampler has accepted a prefix,
 // the fold kernel replays just that prefix on the checkpoint. The three kernels share
-// the per-element arithmetic of kda_decode_step.cuh (explicitly rounded IEEE operations;
-// the fold issues them one lane at a time, the others two lanes per instruction, which
-// gives the same results), the same
+// the per-element arithmetic of kda_decode_step.cuh (explicitly rounded IEEE operations,
+// two lanes per instruction), the same
 // column slice for the same (sequence, head) count, and the same reduction order, so a
 // fold of a tokens leaves exactly the bits that a calls of the decode kernel leave, and
 // verify's outputs are exactly the decode kernel's.
@@ -292,14 +291,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
             const int row = row_of<CWD>(rg, i);
-            decay_project_scalar(sv[i], s_alpha[t][row], s_k[t][row], p);
+            decay_project(sv[i], s_alpha[t][row], s_k[t][row], p);
         }
         *reinterpret_cast<float4 *>(&s_redp[t & 1][rg][4 * cq]) = p;
         __syncthreads();
-        const float4 P = sum_partials_scalar<CWD>(s_redp[t & 1], cq);
-        const float4 e = delta_error_scalar(s_beta[t], *reinterpret_cast<const float4 *>(&s_v[t][col]), P);
+        const float4 P = sum_partials<CWD>(s_redp[t & 1], cq);
+        const float4 e = delta_error(s_beta[t], *reinterpret_cast<const float4 *>(&s_v[t][col]), P);
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) rank1_scalar(sv[i], s_k[t][row_of<CWD>(rg, i)], e);
+        for (int i = 0; i < RPT; ++i) rank1(sv[i], s_k[t][row_of<CWD>(rg, i)], e);
     }
 #pragma unroll
     for (int i = 0; i < RPT; ++i) __stcs(reinterpret_cast<float4 *>(S + row_of<CWD>(rg, i) * kD + col), sv[i]);

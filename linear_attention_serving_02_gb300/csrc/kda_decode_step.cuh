@@ -64,25 +64,6 @@ __device__ __forceinline__ void readout(const float4 &s, float qr, float4 &o) {
     const uint64_t q2 = pk2(qr, qr);
     set4(o, fma2(q2, pk2(s.x, s.y), pk2(o.x, o.y)), fma2(q2, pk2(s.z, s.w), pk2(o.z, o.w)));
 }
-// The same operations one lane at a time. Identical results (each packed lane is the same
-// IEEE operation); for the fold kernel, whose register budget at three CTAs per SM
-// suits the unpacked form better.
-__device__ __forceinline__ void decay_project_scalar(float4 &s, float a, float kr, float4 &p) {
-    s.x = __fmul_rn(s.x, a); s.y = __fmul_rn(s.y, a); s.z = __fmul_rn(s.z, a); s.w = __fmul_rn(s.w, a);
-    p.x = __fmaf_rn(kr, s.x, p.x); p.y = __fmaf_rn(kr, s.y, p.y);
-    p.z = __fmaf_rn(kr, s.z, p.z); p.w = __fmaf_rn(kr, s.w, p.w);
-}
-__device__ __forceinline__ float4 delta_error_scalar(float beta, float4 v, float4 p) {
-    return make_float4(__fmul_rn(beta, __fsub_rn(v.x, p.x)), __fmul_rn(beta, __fsub_rn(v.y, p.y)),
-                       __fmul_rn(beta, __fsub_rn(v.z, p.z)), __fmul_rn(beta, __fsub_rn(v.w, p.w)));
-}
-__device__ __forceinline__ void rank1_scalar(float4 &s, float kr, float4 e) {
-    s.x = __fmaf_rn(kr, e.x, s.x); s.y = __fmaf_rn(kr, e.y, s.y);
-    s.z = __fmaf_rn(kr, e.z, s.z); s.w = __fmaf_rn(kr, e.w, s.w);
-}
-template <int CWD>
-__device__ __forceinline__ float4 sum_partials_scalar(const float (*red)[CWD], int cq);
-
 // sum of the RG row-group partials of this thread's four columns, in row-group order
 template <int CWD>
 __device__ __forceinline__ float4 sum_partials(const float (*red)[CWD], int cq) {
@@ -92,18 +73,6 @@ __device__ __forceinline__ float4 sum_partials(const float (*red)[CWD], int cq) 
     for (int r = 0; r < RG; ++r) {
         const float4 x = *reinterpret_cast<const float4 *>(&red[r][4 * cq]);
         set4(acc, add2(pk2(acc.x, acc.y), pk2(x.x, x.y)), add2(pk2(acc.z, acc.w), pk2(x.z, x.w)));
-    }
-    return acc;
-}
-template <int CWD>
-__device__ __forceinline__ float4 sum_partials_scalar(const float (*red)[CWD], int cq) {
-    constexpr int RG = DecodeGeom<CWD>::RG;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int r = 0; r < RG; ++r) {
-        const float4 x = *reinterpret_cast<const float4 *>(&red[r][4 * cq]);
-        acc.x = __fadd_rn(acc.x, x.x); acc.y = __fadd_rn(acc.y, x.y);
-        acc.z = __fadd_rn(acc.z, x.z); acc.w = __fadd_rn(acc.w, x.w);
     }
     return acc;
 }
