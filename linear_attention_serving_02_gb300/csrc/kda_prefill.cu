@@ -976,6 +976,20 @@ __device__ __forceinline__ void split32_tmem(const float *x, uint32_t t_hi, uint
     tc::tmem_st16(t_hi, h);
     tc::tmem_st16(t_lo, l);
 }
+// the same for 16 pairs (x0, x1) held as packed registers: hi = bf16 pair, lo = bf16 of
+// the pair minus hi (one packed subtraction; the same values as split_bf16x2)
+__device__ __forceinline__ void split32_tmem_pk(const uint64_t *x, uint32_t t_hi, uint32_t t_lo) {
+    uint32_t h[16], l[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float2 v = upk2(x[j]);
+        h[j] = pack_bf16x2(__floats2bfloat162_rn(v.x, v.y));
+        const float2 d = upk2(sub2(x[j], pk2(__uint_as_float(h[j] << 16), __uint_as_float(h[j] & 0xffff0000u))));
+        l[j] = pack_bf16x2(__floats2bfloat162_rn(d.x, d.y));
+    }
+    tc::tmem_st16(t_hi, h);
+    tc::tmem_st16(t_lo, l);
+}
 
 // bounded wait that gives up at once when the CTA has already failed
 __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int &fail) {
@@ -1049,7 +1063,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     const uint32_t ds_col = maps ? 0u : 64u;  // TMEM column of D_S within D_AK
     // this thread's half of its value column of S: key rows 0 .. 63 in the state warps,
     // 64 .. 127 in the U and O warps, so that both halves are updated at the same time
-    float Sh[64];
+    uint64_t Sh[32];  // key rows 2j, 2j + 1 of this half as one packed pair
     if (warp < 4) {
         // ------------- U and O warps; they also hold key rows 64 .. 127 of S -------------
         float Upr[64];
@@ -1059,13 +1073,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             for (int j = 0; j < 64; ++j) Upr[j] = add_up ? up[j * kD + dv] : 0.f;
         };
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            const int r = 64 + j;
-            Sh[j] = S0 ? S0[(int64_t)r * kD + dv] : ((identity && r == dv) ? 1.f : 0.f);
+        for (int j = 0; j < 32; ++j) {
+            const int r = 64 + 2 * j;
+            Sh[j] = S0 ? pk2(S0[(int64_t)r * kD + dv], S0[(int64_t)(r + 1) * kD + dv])
+                       : pk2((identity && r == dv) ? 1.f : 0.f, (identity && r + 1 == dv) ? 1.f : 0.f);
         }
 #pragma unroll
-        for (int j = 0; j < 64; j += 32)
-            split32_tmem(&Sh[j], tmem + lanes + kColSHi + 32 + j / 2, tmem + lanes + kColSLo + 32 + j / 2);
+        for (int j = 0; j < 32; j += 16)
+            split32_tmem_pk(&Sh[j], tmem + lanes + kColSHi + 32 + j, tmem + lanes + kColSLo + 32 + j);
         tc::tmem_wait_st();
         if (c_begin < c_end) load_up(c_begin);
         tc::fence_before_sync();
@@ -1108,21 +1123,21 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 96, dB);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
+                    for (int j = 0; j < 32; j += 4) {  // S = gamma S + D_S, two rows per packed FMA
                         const float4 ga = *reinterpret_cast<const float4 *>(&s.gam_uo[ph][64 + j]);
                         const float4 gb = *reinterpret_cast<const float4 *>(&s.gam_uo[ph][96 + j]);
-                        Sh[j] = ga.x * Sh[j] + __uint_as_float(dA[j]);
-                        Sh[j + 1] = ga.y * Sh[j + 1] + __uint_as_float(dA[j + 1]);
-                        Sh[j + 2] = ga.z * Sh[j + 2] + __uint_as_float(dA[j + 2]);
-                        Sh[j + 3] = ga.w * Sh[j + 3] + __uint_as_float(dA[j + 3]);
-                        Sh[32 + j] = gb.x * Sh[32 + j] + __uint_as_float(dB[j]);
-                        Sh[33 + j] = gb.y * Sh[33 + j] + __uint_as_float(dB[j + 1]);
-                        Sh[34 + j] = gb.z * Sh[34 + j] + __uint_as_float(dB[j + 2]);
-                        Sh[35 + j] = gb.w * Sh[35 + j] + __uint_as_float(dB[j + 3]);
+                        const int p = j / 2;
+                        Sh[p] = fma2(pk2(ga.x, ga.y), Sh[p], pk2(__uint_as_float(dA[j]), __uint_as_float(dA[j + 1])));
+                        Sh[p + 1] = fma2(pk2(ga.z, ga.w), Sh[p + 1],
+                                         pk2(__uint_as_float(dA[j + 2]), __uint_as_float(dA[j + 3])));
+                        Sh[16 + p] = fma2(pk2(gb.x, gb.y), Sh[16 + p],
+                                          pk2(__uint_as_float(dB[j]), __uint_as_float(dB[j + 1])));
+                        Sh[17 + p] = fma2(pk2(gb.z, gb.w), Sh[17 + p],
+                                          pk2(__uint_as_float(dB[j + 2]), __uint_as_float(dB[j + 3])));
                     }
                 }
-                split32_tmem(&Sh[0], tmem + lanes + kColSHi + 32, tmem + lanes + kColSLo + 32);
-                split32_tmem(&Sh[32], tmem + lanes + kColSHi + 48, tmem + lanes + kColSLo + 48);
+                split32_tmem_pk(&Sh[0], tmem + lanes + kColSHi + 32, tmem + lanes + kColSLo + 32);
+                split32_tmem_pk(&Sh[16], tmem + lanes + kColSHi + 48, tmem + lanes + kColSLo + 48);
                 tc::tmem_wait_st();
             }
             // o = (D_O1 + D_O2)^T for this thread's value channel, staged as [token][channel]
@@ -1265,10 +1280,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         }
         // key rows 0 .. 63 of this thread's value column (the U and O warps hold the rest)
 #pragma unroll
-        for (int j = 0; j < 64; ++j) Sh[j] = S0 ? S0[(int64_t)j * kD + dv] : ((identity && j == dv) ? 1.f : 0.f);
+        for (int j = 0; j < 32; ++j) {
+            const int r = 2 * j;
+            Sh[j] = S0 ? pk2(S0[(int64_t)r * kD + dv], S0[(int64_t)(r + 1) * kD + dv])
+                       : pk2((identity && r == dv) ? 1.f : 0.f, (identity && r + 1 == dv) ? 1.f : 0.f);
+        }
 #pragma unroll
-        for (int j = 0; j < 64; j += 32)
-            split32_tmem(&Sh[j], tmem + lanes + kColSHi + j / 2, tmem + lanes + kColSLo + j / 2);
+        for (int j = 0; j < 32; j += 16)
+            split32_tmem_pk(&Sh[j], tmem + lanes + kColSHi + j, tmem + lanes + kColSLo + j);
         tc::tmem_wait_st();
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
@@ -1315,16 +1334,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                         tc::tmem_wait_ld();
                         if (b + 1 < 2) tc::tmem_ld32_nowait(D_AK + lanes + ds_col + 32 * (b + 1), nxt);
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const int cc = 32 * b + j;
+                        for (int j = 0; j < 32; j += 4) {  // S = gamma S + D_S, two rows per packed FMA
+                            const int cc = 32 * b + j, p = cc / 2;
                             const float4 g = *reinterpret_cast<const float4 *>(&s.gam[ph][cc]);
-                            Sh[cc] = g.x * Sh[cc] + __uint_as_float(cur[j]);
-                            Sh[cc + 1] = g.y * Sh[cc + 1] + __uint_as_float(cur[j + 1]);
-                            Sh[cc + 2] = g.z * Sh[cc + 2] + __uint_as_float(cur[j + 2]);
-                            Sh[cc + 3] = g.w * Sh[cc + 3] + __uint_as_float(cur[j + 3]);
+                            Sh[p] = fma2(pk2(g.x, g.y), Sh[p], pk2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])));
+                            Sh[p + 1] = fma2(pk2(g.z, g.w), Sh[p + 1],
+                                             pk2(__uint_as_float(cur[j + 2]), __uint_as_float(cur[j + 3])));
                         }
                     }
-                    split32_tmem(&Sh[32 * b], tmem + lanes + kColSHi + 16 * b, tmem + lanes + kColSLo + 16 * b);
+                    split32_tmem_pk(&Sh[16 * b], tmem + lanes + kColSHi + 16 * b, tmem + lanes + kColSLo + 16 * b);
                 }
             }
             tc::tmem_wait_st();
@@ -1358,7 +1376,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const bool failed = fail;
         float *dst = Sout + (warp >= 4 ? 0 : (int64_t)64 * kD) + dv;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) dst[(int64_t)j * kD] = failed ? __int_as_float(0x7fc00000) : Sh[j];
+        for (int j = 0; j < 32; ++j) {
+            const float2 v = upk2(Sh[j]);
+            dst[(int64_t)(2 * j) * kD] = failed ? __int_as_float(0x7fc00000) : v.x;
+            dst[(int64_t)(2 * j + 1) * kD] = failed ? __int_as_float(0x7fc00000) : v.y;
+        }
     }
     if (warp == 0) tc::tmem_dealloc(tmem, kWalkTmemCols);
 }
