@@ -968,16 +968,9 @@ constexpr uint32_t kColSHi = 320, kColSLo = 384, kColUHi = 448, kColULo = 480;
 constexpr int kBarOR = 2, kBarU = 3;
 
 
-// 32 fp32 values of this thread's lane -> 16 columns of the hi plane and 16 of the lo plane
-__device__ __forceinline__ void split32_tmem(const float *x, uint32_t t_hi, uint32_t t_lo) {
-    uint32_t h[16], l[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) split_bf16x2(x[2 * j], x[2 * j + 1], h[j], l[j]);
-    tc::tmem_st16(t_hi, h);
-    tc::tmem_st16(t_lo, l);
-}
-// the same for 16 pairs (x0, x1) held as packed registers: hi = bf16 pair, lo = bf16 of
-// the pair minus hi (one packed subtraction; the same values as split_bf16x2)
+// 16 pairs of fp32 values of this thread's lane, held as packed registers -> 16 columns
+// of the hi plane and 16 of the lo plane: hi = the bf16 pair, lo = bf16 of the pair minus
+// hi (one packed subtraction; the same values as split_bf16x2)
 __device__ __forceinline__ void split32_tmem_pk(const uint64_t *x, uint32_t t_hi, uint32_t t_lo) {
     uint32_t h[16], l[16];
 #pragma unroll
@@ -1066,11 +1059,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     uint64_t Sh[32];  // key rows 2j, 2j + 1 of this half as one packed pair
     if (warp < 4) {
         // ------------- U and O warps; they also hold key rows 64 .. 127 of S -------------
-        float Upr[64];
+        uint64_t Upr[32];  // U' of tokens 2j, 2j + 1 of this value channel as one packed pair
         auto load_up = [&](int c) {
             const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) Upr[j] = add_up ? up[j * kD + dv] : 0.f;
+            for (int j = 0; j < 32; ++j)
+                Upr[j] = add_up ? pk2(up[(2 * j) * kD + dv], up[(2 * j + 1) * kD + dv]) : pk2(0.f, 0.f);
         };
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -1098,12 +1092,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 tc::tmem_ld32_nowait(D_UO + lanes + 32, d1);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    Upr[j] += __uint_as_float(d0[j]);
-                    Upr[32 + j] += __uint_as_float(d1[j]);
+                for (int j = 0; j < 32; j += 2) {  // two tokens per packed add
+                    Upr[j / 2] = add2(Upr[j / 2], pk2(__uint_as_float(d0[j]), __uint_as_float(d0[j + 1])));
+                    Upr[16 + j / 2] = add2(Upr[16 + j / 2], pk2(__uint_as_float(d1[j]), __uint_as_float(d1[j + 1])));
                 }
-                split32_tmem(&Upr[0], tmem + lanes + kColUHi, tmem + lanes + kColULo);
-                split32_tmem(&Upr[32], tmem + lanes + kColUHi + 16, tmem + lanes + kColULo + 16);
+                split32_tmem_pk(&Upr[0], tmem + lanes + kColUHi, tmem + lanes + kColULo);
+                split32_tmem_pk(&Upr[16], tmem + lanes + kColUHi + 16, tmem + lanes + kColULo + 16);
                 tc::tmem_wait_st();
             }
             tc::fence_before_sync();
