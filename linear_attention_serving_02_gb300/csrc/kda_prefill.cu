@@ -933,14 +933,18 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // Eight warps with fixed roles:
 //   warps 0-3  U and O: thread = value channel dv (TMEM lane dv). After group 1 they
 //              build U^T (and start loading the next chunk's U'); after group 2 they
-//              update key rows 64-127 of S (in fp32 registers) and write their S^T
-//              planes, stage o in shared memory from the output accumulators, and
-//              store it in 16-byte row chunks while the next chunk's group 1 runs.
-//   warps 4-7  state: thread = value channel dv, key rows 0-63 of S in fp32 registers.
-//              After group 2 they update those rows and write their S^T planes.
-//              Thread 128 also issues the MMAs and the bulk copies: [ -W ; Qhat ] one
-//              chunk ahead, [ A_qk ; Kend^T ] two chunks ahead into two slots. (An L2
-//              prefetch of later records measured slower: it holds the copy engine.)
+//              update key rows 64-127 of S and write their S^T planes, stage o in
+//              shared memory from the output accumulators, and store it in 16-byte row
+//              chunks while the next chunk's group 1 runs.
+//   warps 4-7  state: thread = value channel dv, key rows 0-63 of S. After group 2
+//              they update those rows and write their S^T planes. Thread 128 also
+//              issues the MMAs and the bulk copies: [ -W ; Qhat ] one chunk ahead,
+//              [ A_qk ; Kend^T ] two chunks ahead into two slots, and waits for them
+//              off the chain. (An L2 prefetch of later records measured slower: it
+//              holds the copy engine.)
+// The state rows and U' live in fp32 registers as packed pairs (rows 2j, 2j + 1; tokens
+// 2j, 2j + 1), so the update, U = U' + D_U and the split into bf16 planes run on the
+// two-lane FP32 instructions.
 // Named barriers hand the steps over: BAR_U (U^T planes ready), BAR_OR (output
 // accumulators read), and a state-warp barrier (S^T planes ready). Every role runs the
 // same barrier sequence whatever happens: a wait that gives up marks the CTA failed, the
