@@ -184,16 +184,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(smem_u32(p)));
 }
-__device__ __forceinline__ void ldsm_x2_t(uint32_t &r0, uint32_t &r1, const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
-                 : "=r"(r0), "=r"(r1)
-                 : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t &r0, uint32_t &r1, const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
-                 : "=r"(r0), "=r"(r1)
-                 : "r"(smem_u32(p)));
-}
 
 // A fragment (16x16) of a row-major bf16 tile at (row0, col0), row stride ld elements.
 __device__ __forceinline__ void load_a(uint32_t (&r)[4], const __nv_bfloat16 *base, int ld, int row0, int col0,
@@ -205,11 +195,6 @@ __device__ __forceinline__ void load_a(uint32_t (&r)[4], const __nv_bfloat16 *ba
 __device__ __forceinline__ void load_b_kn(uint32_t (&r)[4], const __nv_bfloat16 *base, int ld, int k0, int n0,
                                           int lane) {
     ldsm_x4_t(r, base + (size_t)(k0 + (lane & 7) + (((lane >> 3) & 1) << 3)) * ld + n0 + ((lane >> 4) << 3));
-}
-// B fragment of one n8 tile (rows n0..n0+7 of a tile stored [n][k] row-major), k0..k0+15.
-__device__ __forceinline__ void load_b_nk(uint32_t &r0, uint32_t &r1, const __nv_bfloat16 *base, int ld, int n0,
-                                          int k0, int lane) {
-    ldsm_x2(r0, r1, base + (size_t)(n0 + (lane & 7)) * ld + k0 + (((lane >> 3) & 1) << 3));
 }
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
@@ -224,11 +209,5 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// Cooperative copy of nbytes (a multiple of 16) by nthreads threads.
-__device__ __forceinline__ void cp_async_block(void *dst, const void *src, size_t nbytes, int tid, int nthreads) {
-    char *d = static_cast<char *>(dst);
-    const char *s = static_cast<const char *>(src);
-    for (size_t off = (size_t)tid * 16; off < nbytes; off += (size_t)nthreads * 16) cp_async16(d + off, s + off);
-}
 
 }  // namespace kda

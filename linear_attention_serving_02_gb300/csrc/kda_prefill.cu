@@ -405,12 +405,6 @@ __device__ __forceinline__ void load_b_nk16_sw(uint32_t (&r)[4], const __nv_bflo
     ldsm_x4(r, reinterpret_cast<const unsigned char *>(base) +
                    gram_off(n0 + (lane & 7) + ((lane >> 4) << 3), k0 + (((lane >> 3) & 1) << 3)));
 }
-// B fragment of one n8 tile (rows n0..n0+7, stored [n][k]) of a swizzled Gram tile, k0..k0+15
-__device__ __forceinline__ void load_b_nk_sw(uint32_t &r0, uint32_t &r1, const __nv_bfloat16 *base, int n0,
-                                             int k0, int lane) {
-    ldsm_x2(r0, r1, reinterpret_cast<const unsigned char *>(base) +
-                        gram_off(n0 + (lane & 7), k0 + (((lane >> 3) & 1) << 3)));
-}
 
 __device__ __forceinline__ int find_seq(const int32_t *chunk_off, int32_t N, int32_t slot) {
     // largest n with chunk_off[n] <= slot (empty sequences share an offset and are skipped)
