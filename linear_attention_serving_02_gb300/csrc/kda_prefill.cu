@@ -406,6 +406,17 @@ __device__ __forceinline__ void load_b_nk16_sw(uint32_t (&r)[4], const __nv_bflo
                    gram_off(n0 + (lane & 7) + ((lane >> 4) << 3), k0 + (((lane >> 3) & 1) << 3)));
 }
 
+// (x0 f0, x1 f1) for a bf16 pair x and fp32 factors f, split into bf16 hi and lo pairs:
+// one packed multiply and one packed subtraction (the values of the one-lane forms)
+__device__ __forceinline__ void scale_split_pk(uint32_t xbf2, float f0, float f1, uint32_t &hi, uint32_t &lo) {
+    const float2 x = bf16x2_to_float2(xbf2);
+    const uint64_t y = mul2(pk2(x.x, x.y), pk2(f0, f1));
+    const float2 v = upk2(y);
+    hi = pack_bf16x2(__floats2bfloat162_rn(v.x, v.y));
+    const float2 d = upk2(sub2(y, pk2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))));
+    lo = pack_bf16x2(__floats2bfloat162_rn(d.x, d.y));
+}
+
 __device__ __forceinline__ int find_seq(const int32_t *chunk_off, int32_t N, int32_t slot) {
     // largest n with chunk_off[n] <= slot (empty sequences share an offset and are skipped)
     int lo = 0, hi = N - 1;
@@ -579,19 +590,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
         uint32_t kh[4], kl[4];
 #pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) {
-            const float2 kk = bf16x2_to_float2(kw[p2]);
-            split_bf16x2(kk.x * f[2 * p2], kk.y * f[2 * p2 + 1], kh[p2], kl[p2]);
-        }
+        for (int p2 = 0; p2 < 4; ++p2) scale_split_pk(kw[p2], f[2 * p2], f[2 * p2 + 1], kh[p2], kl[p2]);
         if (aside) {
             const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[row][c]);
             const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
             uint32_t qh[4], ql[4];
 #pragma unroll
-            for (int p2 = 0; p2 < 4; ++p2) {
-                const float2 qq = bf16x2_to_float2(qw[p2]);
-                split_bf16x2(qq.x * f[2 * p2], qq.y * f[2 * p2 + 1], qh[p2], ql[p2]);
-            }
+            for (int p2 = 0; p2 < 4; ++p2) scale_split_pk(qw[p2], f[2 * p2], f[2 * p2 + 1], qh[p2], ql[p2]);
             const uint32_t off = gram_off(ar, c);
             *reinterpret_cast<uint4 *>(aqb[0] + off) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
             *reinterpret_cast<uint4 *>(aqb[1] + off) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
@@ -796,9 +801,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             uint32_t qh[4], ql[4], kh[4], kl[4];
 #pragma unroll
             for (int p2 = 0; p2 < 4; ++p2) {
-                const float2 qq = bf16x2_to_float2(qw[p2]), kk = bf16x2_to_float2(kw[p2]);
-                split_bf16x2(qq.x * f[2 * p2], qq.y * f[2 * p2 + 1], qh[p2], ql[p2]);
-                split_bf16x2(kk.x * f[2 * p2], kk.y * f[2 * p2 + 1], kh[p2], kl[p2]);
+                scale_split_pk(qw[p2], f[2 * p2], f[2 * p2 + 1], qh[p2], ql[p2]);
+                scale_split_pk(kw[p2], f[2 * p2], f[2 * p2 + 1], kh[p2], kl[p2]);
             }
             *reinterpret_cast<uint4 *>(Qh + il_off(i, c, kD)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
             *reinterpret_cast<uint4 *>(Qh + kStackWQ + il_off(i, c, kD)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
