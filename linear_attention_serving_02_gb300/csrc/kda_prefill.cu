@@ -408,13 +408,16 @@ __device__ __forceinline__ void load_b_nk16_sw(uint32_t (&r)[4], const __nv_bflo
 
 // (x0 f0, x1 f1) for a bf16 pair x and fp32 factors f, split into bf16 hi and lo pairs:
 // one packed multiply and one packed subtraction (the values of the one-lane forms)
-__device__ __forceinline__ void scale_split_pk(uint32_t xbf2, float f0, float f1, uint32_t &hi, uint32_t &lo) {
-    const float2 x = bf16x2_to_float2(xbf2);
-    const uint64_t y = mul2(pk2(x.x, x.y), pk2(f0, f1));
+// a packed pair y split into bf16 hi and lo pairs (one packed subtraction)
+__device__ __forceinline__ void split_pk(uint64_t y, uint32_t &hi, uint32_t &lo) {
     const float2 v = upk2(y);
     hi = pack_bf16x2(__floats2bfloat162_rn(v.x, v.y));
     const float2 d = upk2(sub2(y, pk2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))));
     lo = pack_bf16x2(__floats2bfloat162_rn(d.x, d.y));
+}
+__device__ __forceinline__ void scale_split_pk(uint32_t xbf2, float f0, float f1, uint32_t &hi, uint32_t &lo) {
+    const float2 x = bf16x2_to_float2(xbf2);
+    split_pk(mul2(pk2(x.x, x.y), pk2(f0, f1)), hi, lo);
 }
 
 __device__ __forceinline__ int find_seq(const int32_t *chunk_off, int32_t N, int32_t slot) {
@@ -817,10 +820,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 #pragma unroll
             for (int m = 0; m < 8; ++m) x[m] = __bfloat162float(s.ks[j + m][c]) * __expf(gl - G[j + m][c]);
             uint4 hi, lo;
-            split_bf16x2(x[0], x[1], hi.x, lo.x);
-            split_bf16x2(x[2], x[3], hi.y, lo.y);
-            split_bf16x2(x[4], x[5], hi.z, lo.z);
-            split_bf16x2(x[6], x[7], hi.w, lo.w);
+            split_pk(pk2(x[0], x[1]), hi.x, lo.x);
+            split_pk(pk2(x[2], x[3]), hi.y, lo.y);
+            split_pk(pk2(x[4], x[5]), hi.z, lo.z);
+            split_pk(pk2(x[6], x[7]), hi.w, lo.w);
             *reinterpret_cast<uint4 *>(KeT + il_off(c, j, kC)) = hi;
             *reinterpret_cast<uint4 *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
         }
@@ -838,7 +841,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     for (int e = tid; e < kC * (kC / 2); e += kIntraThreads) {
         const int i = e / (kC / 2), j = (e % (kC / 2)) * 2;
         uint32_t hi, lo;
-        split_bf16x2(s.T[i][j] * s.beta[j], s.T[i][j + 1] * s.beta[j + 1], hi, lo);
+        const float2 t = *reinterpret_cast<const float2 *>(&s.T[i][j]);
+        const float2 be = *reinterpret_cast<const float2 *>(&s.beta[j]);
+        split_pk(mul2(pk2(t.x, t.y), pk2(be.x, be.y)), hi, lo);
         *reinterpret_cast<uint32_t *>(&s.u.w.t[0][i][j]) = hi;
         *reinterpret_cast<uint32_t *>(&s.u.w.t[1][i][j]) = lo;
     }
