@@ -430,7 +430,12 @@ def run_prefill_workload(which, steps, warmup, world, seed):
               final state."""
     from linear_attention_serving_02_gb300 import kda
 
-    if which == "varlen":
+    if which == "prefill":
+        H, T = PREFILL_H, PREFILL_T
+        inp = inputs.prefill_inputs(T, H, 1, seed=seed, init_state=True, device="cuda")
+        cu = cu_host = None
+        n_seqs = 1
+    elif which == "varlen":
         H = 32
         lens = inputs.varlen_lengths(8, 1024, 32768, seed=0)
         cu_host = inputs.cu_seqlens_from_lengths(lens)
@@ -449,8 +454,8 @@ def run_prefill_workload(which, steps, warmup, world, seed):
     main = torch.cuda.current_stream()
 
     def prefill():
-        kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], cu_seqlens=cu,
-                              cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws)
+        kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], initial_state=inp["S0"],
+                              cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws)
 
     for _ in range(warmup):
         prefill()
@@ -645,11 +650,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--part", choices=["all", "speculative", "fused", "varlen", "long"], default="all",
+    ap.add_argument("--part", choices=["all", "speculative", "fused", "prefill", "varlen", "long"], default="all",
                     help="'speculative' times only the verify + fold pair, 'fused' only the fused decode "
-                         "(each about 3 GB on the device; for profiling); 'varlen' and 'long' time the "
-                         "prefill of the packed 8 x U[1024, 32768] x 32-head batch and of the 1M-token "
-                         "sequence; each prints its object")
+                         "(each about 3 GB on the device; for profiling); 'prefill', 'varlen' and 'long' "
+                         "time only the prefill of the 8192-token 12-head sequence (under 0.5 GB on the "
+                         "device: the small case for kernel counters), of the packed 8 x U[1024, 32768] x "
+                         "32-head batch and of the 1M-token sequence; each prints its object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -660,7 +666,7 @@ def main():
     rank, world, local = dist_setup(args.gpus)
     try:
         if args.part != "all":
-            if args.part in ("varlen", "long"):
+            if args.part in ("prefill", "varlen", "long"):
                 res = run_prefill_workload(args.part, args.steps, args.warmup, world, seed=1000 * rank)
             else:
                 run = run_speculative if args.part == "speculative" else run_fused_decode

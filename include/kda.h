@@ -134,7 +134,13 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 
 /*
  * Status recorded on the device by the last kda_chunk_prefill() that used this
- * workspace (KDA_OK or KDA_ERR_SEQLENS). Synchronises 'stream'.
+ * workspace. Synchronises 'stream'. Returns
+ *   KDA_OK           the kernels ran to the end;
+ *   KDA_ERR_SEQLENS  the device-side cu_seqlens check failed (final_state is NaN);
+ *   KDA_ERR_CUDA     a bounded wait inside the state walk gave up (a copy or a tensor-core
+ *                    group did not complete in time); the final states of the affected
+ *                    (sequence, head) pairs are NaN and their outputs are not valid;
+ *   or KDA_ERR_CUDA if the copy of the status word itself fails.
  */
 int kda_workspace_status(const void *workspace, void *stream);
 
@@ -158,7 +164,9 @@ int kda_workspace_status(const void *workspace, void *stream);
  *     1536 tokens x 12 heads.
  *   - The first call on a device looks up the scratch's device address on that device
  *     (cudaGetSymbolAddress, with the device current); make that first call before any
- *     stream capture.
+ *     stream capture. The address is kept for the life of the process, so do not use
+ *     this entry point after cudaDeviceReset() on that device: the reset unloads the
+ *     library's device code and the kept address no longer names the scratch.
  *   - All calls share the one scratch area and it keeps the last call's contents. The
  *     kernels need nothing in it to start at zero, but calls whose GPU work overlaps in
  *     time (different streams, or threads without ordering) race on it: order them.

@@ -17,7 +17,7 @@ cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t t
 cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
                            const float *Mseg, const float *Rseg, cudaStream_t st);
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
-                         const float *A, const float *b, const int32_t *status, const int32_t *seq_cu,
+                         const float *A, const float *b, int32_t *status, const int32_t *seq_cu,
                          const int32_t *chunk_off, int32_t N, int32_t H, int64_t nslots, uint8_t *records,
                          int num_sms, cudaStream_t st);
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
@@ -112,6 +112,45 @@ int device_info(DeviceInfo &info) {
 
 }  // namespace
 
+namespace kda {
+// Argument checks of the prefill entry points, in the order their error codes are
+// documented: head size and output type, sizes (seq_len bounded before the token count
+// is formed), pointers, alignment, the launch limits, then the host copy of cu_seqlens.
+// Everything but the workspace. KDA_OK with num_seqs == 0 means there is nothing to do.
+int prefill_check(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
+                  const float *b, const float *initial_state, const int32_t *cu_seqlens,
+                  const int32_t *cu_seqlens_host, int32_t batch, int64_t seq_len, int32_t num_seqs,
+                  int32_t num_heads, int32_t d_k, int32_t d_v, const void *o, int32_t o_dtype,
+                  const float *final_state, int64_t *total_out) {
+    if (d_k != kD || d_v != kD) return KDA_ERR_UNSUPPORTED;
+    if (o_dtype != KDA_OUT_BF16 && o_dtype != KDA_OUT_F32) return KDA_ERR_UNSUPPORTED;
+    if (batch < 0 || seq_len < 0 || num_seqs < 0 || num_heads <= 0 || num_heads > 65535) return KDA_ERR_SHAPE;
+    if (seq_len >= (int64_t)1 << 31) return KDA_ERR_SHAPE;  // no batch of it fits the int32 offsets either
+    const int64_t total = (int64_t)batch * seq_len;  // < 2^62: no overflow
+    if (total >= (int64_t)1 << 31) return KDA_ERR_SHAPE;  // token offsets are int32
+    if (cu_seqlens) {
+        if (batch != 1) return KDA_ERR_SHAPE;
+    } else if (num_seqs != batch) {
+        return KDA_ERR_SHAPE;
+    }
+    *total_out = total;
+    if (num_seqs == 0) return total == 0 ? KDA_OK : KDA_ERR_SHAPE;
+    if (!final_state || !A) return KDA_ERR_NULL;
+    if (total > 0 && (!q || !k || !v || !z || !b || !o)) return KDA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) || !aligned(o, 16) ||
+        !aligned(final_state, 16) || !aligned(initial_state, 16) || !aligned(A, 4) || !aligned(b, 4))
+        return KDA_ERR_ALIGN;
+    // (chunk slot, head) items are counted in int32 by the intra-chunk kernel
+    if (chunk_bound(total, num_seqs) * num_heads > INT32_MAX) return KDA_ERR_SHAPE;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || (int64_t)cu_seqlens_host[num_seqs] != total) return KDA_ERR_SEQLENS;
+        for (int32_t n = 0; n < num_seqs; ++n)
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_SEQLENS;
+    }
+    return KDA_OK;
+}
+}  // namespace kda
+
 extern "C" {
 
 const char *kda_status_string(int status) {
@@ -147,33 +186,15 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                       const int32_t *cu_seqlens_host, int32_t batch, int64_t seq_len, int32_t num_seqs,
                       int32_t num_heads, int32_t d_k, int32_t d_v, void *o, int32_t o_dtype, float *final_state,
                       void *workspace, size_t workspace_bytes, void *stream) {
-    if (d_k != kda::kD || d_v != kda::kD) return KDA_ERR_UNSUPPORTED;
-    if (o_dtype != KDA_OUT_BF16 && o_dtype != KDA_OUT_F32) return KDA_ERR_UNSUPPORTED;
-    if (batch < 0 || seq_len < 0 || num_seqs < 0 || num_heads <= 0 || num_heads > 65535) return KDA_ERR_SHAPE;
-    const int64_t total = (int64_t)batch * seq_len;
-    if (total >= (int64_t)1 << 31) return KDA_ERR_SHAPE;  // token offsets are int32
-    if (cu_seqlens) {
-        if (batch != 1) return KDA_ERR_SHAPE;
-    } else if (num_seqs != batch) {
-        return KDA_ERR_SHAPE;
-    }
-    if (num_seqs == 0) return total == 0 ? KDA_OK : KDA_ERR_SHAPE;
-    if (!final_state || !workspace || !A) return KDA_ERR_NULL;
-    if (total > 0 && (!q || !k || !v || !z || !b || !o)) return KDA_ERR_NULL;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) || !aligned(o, 16) ||
-        !aligned(final_state, 16) || !aligned(initial_state, 16) || !aligned(A, 4) || !aligned(b, 4))
-        return KDA_ERR_ALIGN;
+    int64_t total = 0;
+    int rc = kda::prefill_check(q, k, v, z, A, b, initial_state, cu_seqlens, cu_seqlens_host, batch, seq_len,
+                                num_seqs, num_heads, d_k, d_v, o, o_dtype, final_state, &total);
+    if (rc != KDA_OK || num_seqs == 0) return rc;
+    if (!workspace) return KDA_ERR_NULL;
     if (!aligned(workspace, 256)) return KDA_ERR_ALIGN;
-    // (chunk slot, head) items are counted in int32 by the intra-chunk kernel
-    if (ws_layout(total, num_seqs, num_heads).nslots * num_heads > INT32_MAX) return KDA_ERR_SHAPE;
     if (workspace_bytes < kda_chunk_prefill_workspace_size(total, num_seqs, num_heads)) return KDA_ERR_WORKSPACE;
-    if (cu_seqlens_host) {
-        if (cu_seqlens_host[0] != 0 || (int64_t)cu_seqlens_host[num_seqs] != total) return KDA_ERR_SEQLENS;
-        for (int32_t n = 0; n < num_seqs; ++n)
-            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_SEQLENS;
-    }
     DeviceInfo dev;
-    int rc = device_info(dev);
+    rc = device_info(dev);
     if (rc != KDA_OK) return rc;
     if (dev.major * 10 + dev.minor < 100 || dev.smem_optin < kda::intra_smem_bytes()) return KDA_ERR_DEVICE;
 

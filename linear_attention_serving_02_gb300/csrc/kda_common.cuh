@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kda_f32x2.cuh"
+
 namespace kda {
 
 constexpr int kD = 128;        // d_k = d_v
@@ -22,36 +24,45 @@ constexpr int kLd64 = kC + 8;   // 64-wide tiles: 144 B per row
 
 // ---------------------------------------------------------------------------------
 // Chunk record: everything the serial state walk needs about one (chunk, head). The
-// operand tiles are stored as the exact shared-memory images the tensor core reads
-// (interleaved K-major core-matrix layout, see kda_tc.cuh). Split-bf16 operands have a
-// hi and a lo plane. Tiles that one MMA reads together are stacked along the row
-// (N) dimension, so that each MMA group of the walk is one wide instruction chain:
-//   WQ   [hi | lo] of the 128 x 128 stack  [ -W ; Qhat ]
-//          rows 0..63   -W = -T' Khat      (row: token i, K: key channel c)
-//          rows 64..127 q_i * exp(G_i)      (row: token i, K: key channel c)
-//   AK   [hi | lo] of the 192 x 64 stack   [ A_qk ; Kend^T ]
-//          rows 0..63   decayed causal Q K^T, diagonal included (row: i, K: token j)
-//          rows 64..191 k_j * exp(G_last - G_j), transposed      (row: c, K: token j)
+// operand tiles are stored as the exact shared-memory images the tensor core reads,
+// in the no-swizzle canonical layouts of kda_tc.cuh: core matrices of 8 rows x 16 bytes.
+//   [ -W ; Qhat ]  K-major, 128 rows (row = token, K = key channel), three 16 KB planes
+//          W    -W = -T' Khat in bf16 (rows 0..63). One bf16 plane is enough here: the
+//               rounding of W moves the outputs by less than a tenth of their error bar.
+//          Qh   q_i * exp(G_i), hi plane (rows 64..127)
+//          Ql   the lo plane of the same (hi + lo = the fp32 value to ~16 bits)
+//   AK  [ A_qk ; Kend^T ]  MN-major (N = 192, K = 64 tokens j), a hi and a lo plane
+//          n 0..63    decayed causal Q K^T, diagonal included (n = query token i)
+//          n 64..191  k_j * exp(G_last - G_j), transposed     (n = key channel c)
 //   gam  [128]   fp32   exp(G_last), the chunk's total decay
-//   Up   [64][128] fp32 U' = T' V, token-major (row i, column = value channel)
+//   Up   [64][128] fp32 U' = T' V, token-major (row i, column = value channel); the
+//        16-byte units (4 channels) of row i are XOR-swizzled by i % 32: channel c of row i
+//        is at i * 128 + 4 ((c / 4) ^ (i % 32)) + c % 4
 // ---------------------------------------------------------------------------------
 constexpr size_t kPlaneQK = (size_t)kC * kD * 2;   // 64 x 128 bf16 tile
 constexpr size_t kPlaneKT = (size_t)kD * kC * 2;   // 128 x 64 bf16 tile
 constexpr size_t kPlaneCC = (size_t)kC * kC * 2;   // 64 x 64 bf16 tile
-constexpr size_t kStackWQ = 2 * kPlaneQK;          // one plane of [ -W ; Qhat ]: 128 x 128
 constexpr size_t kStackAK = kPlaneCC + kPlaneKT;   // one plane of [ A_qk ; Kend^T ]: 192 x 64
-constexpr size_t kRecWQ = 0;
-constexpr size_t kRecAK = kRecWQ + 2 * kStackWQ;
+constexpr size_t kRecW = 0;                        // -W, then Qhat hi and lo: one 48 KB run
+constexpr size_t kRecQh = kRecW + kPlaneQK;
+constexpr size_t kRecQl = kRecQh + kPlaneQK;
+constexpr size_t kRecWQBytes = 3 * kPlaneQK;
+constexpr size_t kRecAK = kRecW + kRecWQBytes;
 constexpr size_t kRecGam = kRecAK + 2 * kStackAK;
 constexpr size_t kRecUp = kRecGam + kD * 4;
 constexpr size_t kRecBytes = kRecUp + (size_t)kC * kD * 4;
-// where each tile's hi plane starts; its lo plane is one stack further
-constexpr size_t kRecWn = kRecWQ;
-constexpr size_t kRecQh = kRecWQ + kPlaneQK;
+// where each part of AK starts (its lo plane is one stack further)
 constexpr size_t kRecAqk = kRecAK;
 constexpr size_t kRecKeT = kRecAK + kPlaneCC;
 static_assert(kRecBytes % 128 == 0, "chunk records must stay 128-byte aligned");
 static_assert(kRecAK % 16 == 0 && kRecGam % 16 == 0 && kRecUp % 16 == 0, "record fields must be 16-byte aligned");
+
+// byte offset of element (n, j) of the MN-major [ A_qk ; Kend^T ] plane: core matrices of
+// 8 tokens j (K) x 8 consecutive n (16 bytes); the 8 K-groups of one n-group are adjacent
+// (K-direction stride 128 B), n-groups are 1024 B apart
+__host__ __device__ constexpr uint32_t ak_off(int n, int j) {
+    return (uint32_t)((n >> 3) * 1024 + (j >> 3) * 128 + (j & 7) * 16 + (n & 7) * 2);
+}
 
 // byte offset of element (r, k) in an interleaved K-major tile with K elements per row
 __host__ __device__ constexpr uint32_t il_off(int r, int k, int K) {
@@ -204,10 +215,75 @@ __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src) 
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+// one arrival on the mbarrier once all of this thread's earlier cp.async copies have landed
+// (the arrival counts against the barrier's initial count)
+__device__ __forceinline__ void cp_async_arrive(uint64_t *mbar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// named barriers (bar.sync / bar.arrive) over a subset of a CTA's warps
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n));
+}
+
+// Programmatic dependent launch: the kernels after the plan kernel are launched while
+// their predecessor runs. Each waits for the predecessor to finish (and its memory to be
+// visible) before anything else; each lets its successor launch once all its own CTAs
+// are resident, so a waiting successor never holds an SM a predecessor CTA still needs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// a launch that may start while the previous kernel on the stream runs (the kernel
+// waits for it with griddepcontrol.wait before touching its results)
+template <typename... Params, typename... Args>
+inline cudaError_t launch_after(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+// a packed pair y split into bf16 hi and lo pairs (one packed subtraction; the values of
+// split_bf16x2)
+__device__ __forceinline__ void split_pk(uint64_t y, uint32_t &hi, uint32_t &lo) {
+    const float2 v = upk2(y);
+    hi = pack_bf16x2(__floats2bfloat162_rn(v.x, v.y));
+    const float2 d = upk2(sub2(y, pk2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))));
+    lo = pack_bf16x2(__floats2bfloat162_rn(d.x, d.y));
+}
+// (x0 f0, x1 f1) for a bf16 pair x and fp32 factors f, split into bf16 hi and lo pairs:
+// one packed multiply and one packed subtraction
+__device__ __forceinline__ void scale_split_pk(uint32_t xbf2, float f0, float f1, uint32_t &hi, uint32_t &lo) {
+    const float2 x = bf16x2_to_float2(xbf2);
+    split_pk(mul2(pk2(x.x, x.y), pk2(f0, f1)), hi, lo);
+}
+
+// largest n with chunk_off[n] <= slot (empty sequences share an offset and are skipped)
+__device__ __forceinline__ int find_seq(const int32_t *chunk_off, int32_t N, int32_t slot) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (chunk_off[mid] <= slot)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
 
 }  // namespace kda

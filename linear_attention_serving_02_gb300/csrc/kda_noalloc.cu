@@ -21,6 +21,14 @@
 
 #include "kda.h"
 
+namespace kda {
+int prefill_check(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
+                  const float *b, const float *initial_state, const int32_t *cu_seqlens,
+                  const int32_t *cu_seqlens_host, int32_t batch, int64_t seq_len, int32_t num_seqs,
+                  int32_t num_heads, int32_t d_k, int32_t d_v, const void *o, int32_t o_dtype,
+                  const float *final_state, int64_t *total_out);
+}
+
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
@@ -51,11 +59,14 @@ extern "C" int kda_chunk_prefill_noalloc(const uint16_t *q, const uint16_t *k, c
                                          const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int32_t batch,
                                          int64_t seq_len, int32_t num_seqs, int32_t num_heads, int32_t d_k,
                                          int32_t d_v, void *o, int32_t o_dtype, float *final_state, void *stream) {
-    // a batch whose tables and chunk records do not fit the fixed scratch is refused
-    // before anything is looked up or launched
-    if (batch >= 0 && seq_len >= 0 && num_seqs >= 0 && num_heads > 0 &&
-        kda_chunk_prefill_workspace_size((int64_t)batch * seq_len, num_seqs, num_heads) >
-            (size_t)KDA_NOALLOC_SCRATCH_BYTES)
+    // the arguments are checked exactly as kda_chunk_prefill() checks them, so the same
+    // error codes come back; only then is a batch whose tables and chunk records do not
+    // fit the fixed scratch refused, before anything is looked up or launched
+    int64_t total = 0;
+    const int bad = kda::prefill_check(q, k, v, z, A, b, initial_state, cu_seqlens, cu_seqlens_host, batch, seq_len,
+                                       num_seqs, num_heads, d_k, d_v, o, o_dtype, final_state, &total);
+    if (bad != KDA_OK || num_seqs == 0) return bad;
+    if (kda_chunk_prefill_workspace_size(total, num_seqs, num_heads) > (size_t)KDA_NOALLOC_SCRATCH_BYTES)
         return KDA_ERR_WORKSPACE;
     void *scratch = nullptr;
     const int rc = scratch_on_current_device(&scratch);

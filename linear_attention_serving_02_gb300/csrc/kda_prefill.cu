@@ -44,13 +44,6 @@
 
 namespace kda {
 
-// Programmatic dependent launch: the kernels after the plan kernel are launched while
-// their predecessor runs. Each waits for the predecessor to finish (and its memory to be
-// visible) before anything else; each lets its successor launch once all its own CTAs
-// are resident, so a waiting successor never holds an SM a predecessor CTA still needs.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
-
 // ---------------------------------------------------------------------------------
 // plan: seq_cu[N+1] and chunk_off[N+1] (prefix sums of ceil(len / C)) in the workspace
 // ---------------------------------------------------------------------------------
@@ -350,576 +343,6 @@ __global__ void __launch_bounds__(kCombineThreads)
 }
 
 // ---------------------------------------------------------------------------------
-// intra-chunk kernel
-// ---------------------------------------------------------------------------------
-// named barriers (bar.sync / bar.arrive) over a subset of a CTA's warps
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
-__device__ __forceinline__ void named_arrive(int id, int n) {
-    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n));
-}
-
-struct IntraSmem {
-    float G[2][kC][kD + 4];  // z of the chunk, then (in place) the cumulative log decay; the
-                             // other buffer receives the next chunk's z meanwhile
-    float beta[kC];
-    float colsum[4][kD];           // per-quarter column totals of the cumulative sum
-    float Akk[kC][kC + 4];         // rows 16-byte aligned for float4 reads; the 4-float pad
-    float T[kC][kC + 4];           // puts 8 consecutive rows on distinct banks
-    float X[3][kTile][kTile];      // off-diagonal block products of the solve
-    __nv_bfloat16 qs[kC][kLd128];  // the chunk's q, k, v (rows past the sequence end are zero)
-    __nv_bfloat16 ks[kC][kLd128];
-    __nv_bfloat16 vs[kC][kLd128];
-    union {
-        struct {  // operands of the decayed Gram products of one 32-token tile row,
-                  // 256-byte rows with the 16-byte chunks XOR-swizzled by row (gram_off)
-            __nv_bfloat16 aq[2][2 * kTile][kD];
-            __nv_bfloat16 ak[2][2 * kTile][kD];
-            __nv_bfloat16 bk[2][kC][kD];
-        } g;
-        struct {  // operands of W = T' Khat and U' = T' V
-            __nv_bfloat16 kh[2][kC][kLd128];
-            __nv_bfloat16 t[2][kC][kLd64];
-        } w;
-    } u;
-};
-
-constexpr int kIntraThreads = 512;
-constexpr int kSolveWarps = 8;  // the UT solve's warps; the other eight write the record's elementwise parts
-
-// Byte offset of element (row, col) in a 256-byte-row bf16 Gram operand tile: the 16-byte
-// chunk index is XORed with row % 8, so that the eight rows one ldmatrix phase reads and
-// the rows a warp's 16-byte stores write fall on distinct banks without padding.
-__device__ __forceinline__ uint32_t gram_off(int row, int col) {
-    return (uint32_t)(row * (kD * 2) + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2);
-}
-// A fragment (16 x 16) at (row0, col0) of a swizzled Gram tile
-__device__ __forceinline__ void load_a_sw(uint32_t (&r)[4], const __nv_bfloat16 *base, int row0, int col0,
-                                          int lane) {
-    ldsm_x4(r, reinterpret_cast<const unsigned char *>(base) +
-                   gram_off(row0 + (lane & 15), col0 + ((lane >> 4) << 3)));
-}
-// B fragments of two n8 tiles (rows n0..n0+15, stored [n][k]) of a swizzled Gram tile,
-// k0..k0+15: r[0], r[1] = tile n0; r[2], r[3] = tile n0 + 8
-__device__ __forceinline__ void load_b_nk16_sw(uint32_t (&r)[4], const __nv_bfloat16 *base, int n0, int k0,
-                                               int lane) {
-    ldsm_x4(r, reinterpret_cast<const unsigned char *>(base) +
-                   gram_off(n0 + (lane & 7) + ((lane >> 4) << 3), k0 + (((lane >> 3) & 1) << 3)));
-}
-
-// (x0 f0, x1 f1) for a bf16 pair x and fp32 factors f, split into bf16 hi and lo pairs:
-// one packed multiply and one packed subtraction (the values of the one-lane forms)
-// a packed pair y split into bf16 hi and lo pairs (one packed subtraction)
-__device__ __forceinline__ void split_pk(uint64_t y, uint32_t &hi, uint32_t &lo) {
-    const float2 v = upk2(y);
-    hi = pack_bf16x2(__floats2bfloat162_rn(v.x, v.y));
-    const float2 d = upk2(sub2(y, pk2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))));
-    lo = pack_bf16x2(__floats2bfloat162_rn(d.x, d.y));
-}
-__device__ __forceinline__ void scale_split_pk(uint32_t xbf2, float f0, float f1, uint32_t &hi, uint32_t &lo) {
-    const float2 x = bf16x2_to_float2(xbf2);
-    split_pk(mul2(pk2(x.x, x.y), pk2(f0, f1)), hi, lo);
-}
-
-__device__ __forceinline__ int find_seq(const int32_t *chunk_off, int32_t N, int32_t slot) {
-    // largest n with chunk_off[n] <= slot (empty sequences share an offset and are skipped)
-    int lo = 0, hi = N - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (chunk_off[mid] <= slot)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
-__global__ void __launch_bounds__(kIntraThreads, 1)
-    kda_intra_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
-                     const float *__restrict__ bgate, const int32_t *__restrict__ status,
-                     const int32_t *__restrict__ seq_cu, const int32_t *__restrict__ chunk_off, int32_t N, int32_t H,
-                     uint8_t *__restrict__ records) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    IntraSmem &s = *reinterpret_cast<IntraSmem *>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait();
-    pdl_trigger();
-    if (*status != 0 || N <= 0) return;
-    // persistent: CTA b takes items b, b + gridDim.x, ...; item = slot * H + h
-    const int n_items = chunk_off[N] * H;
-    int item = blockIdx.x;
-    if (item >= n_items) return;
-    const int64_t rowstride = (int64_t)H * kD;  // elements between consecutive tokens
-
-    struct Item {
-        int slot, h;
-        int64_t t0;
-        int L;
-    };
-    auto item_of = [&](int it) {
-        Item r;
-        r.slot = it / H;
-        r.h = it % H;
-        const int n = find_seq(chunk_off, N, r.slot);
-        r.t0 = (int64_t)seq_cu[n] + (int64_t)(r.slot - chunk_off[n]) * kC;
-        r.L = (int)min((int64_t)kC, (int64_t)seq_cu[n + 1] - r.t0);
-        return r;
-    };
-    // z of an item into a G buffer (rows past the sequence end are zero), as one copy group
-    auto stage_z = [&](const Item &it, float (*Gd)[kD + 4]) {
-        for (int e = tid; e < kC * (kD / 4); e += kIntraThreads) {  // 32 x 16 B per row
-            const int i = e / (kD / 4), c = (e % (kD / 4)) * 4;
-            float *dst = &Gd[i][c];
-            if (i < it.L)
-                cp_async16(dst, z + (it.t0 + i) * rowstride + (int64_t)it.h * kD + c);
-            else
-                *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        cp_async_commit();
-    };
-
-    // q and k (one copy group) and v (another) of an item; rows past the end are zero
-    auto stage_rows = [&](const Item &it, int first, int count) {
-        for (int e = tid; e < count * kC * (kD / 8); e += kIntraThreads) {  // 16 x 16 B per row
-            const int which = first + e / (kC * (kD / 8));
-            const int r = e % (kC * (kD / 8));
-            const int i = r / (kD / 8), c = (r % (kD / 8)) * 8;
-            const __nv_bfloat16 *src = which == 0 ? q : (which == 1 ? k : v);
-            __nv_bfloat16 *dst = which == 0 ? &s.qs[i][c] : (which == 1 ? &s.ks[i][c] : &s.vs[i][c]);
-            if (i < it.L)
-                cp_async16(dst, src + (it.t0 + i) * rowstride + (int64_t)it.h * kD + c);
-            else
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        cp_async_commit();
-    };
-
-    // Copy groups in flight at the top of every iteration, oldest first: this chunk's z,
-    // its q and k, its v. The next chunk's z is added after the gate, its q and k once
-    // this chunk no longer reads them (after the UT phase), its v at the end.
-    Item cur = item_of(item);
-    stage_z(cur, s.G[0]);
-    stage_rows(cur, 0, 2);
-    stage_rows(cur, 2, 1);
-    for (int iter = 0; item < n_items; ++iter, item += gridDim.x) {
-    float(*G)[kD + 4] = s.G[iter & 1];
-    const int h = cur.h;
-    const int64_t t0 = cur.t0;
-    const int L = cur.L;
-    uint8_t *rec = records + ((int64_t)cur.slot * H + h) * (int64_t)kRecBytes;
-    const bool has_next = item + (int)gridDim.x < n_items;
-    const Item nxt = has_next ? item_of(item + gridDim.x) : cur;
-    const float eA = expf(A[h]);  // loaded here, off the gate's critical path
-
-    if (tid >= kD && tid < kD + kC) {
-        const int i = tid - kD;
-        s.beta[i] = (i < L) ? sigmoid_f(bgate[(t0 + i) * H + h]) : 0.f;
-    }
-    for (int e = tid; e < kC * (kC + 4); e += kIntraThreads) (&s.Akk[0][0])[e] = 0.f;
-    // A_qk goes to the record straight from the MMA fragments; the blocks above the
-    // diagonal stay zero (ordered before those stores by the barriers in between)
-    for (int e = tid; e < (int)(2 * kPlaneCC / 16); e += kIntraThreads) {  // the hi and the lo plane
-        const int plane = e / (int)(kPlaneCC / 16), off = e % (int)(kPlaneCC / 16);
-        *reinterpret_cast<uint4 *>(rec + kRecAqk + plane * kStackAK + (size_t)off * 16) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    cp_async_wait<2>();  // this chunk's z (its q, k and v may still be in flight)
-    __syncthreads();
-
-    // ---- gate and cumulative log decay, in place over z (rows past the end add 0) ----
-    {
-        // thread (column c, quarter qt) takes 16 consecutive rows of its column: the gate
-        // log a = g_min sigmoid(e^A z), then its running sum in registers; the totals of
-        // the quarters below are added after one barrier. The exponential is __expf: its
-        // error grows with |e^A z|, but where that is large the sigmoid saturates, and
-        // where the sigmoid is sensitive (|e^A z| < ~5) the relative error is ~3e-7, so
-        // log a moves by < 1e-6. The division is __fdividef (2 ulp; an infinite
-        // denominator, z = -inf, gives 0, i.e. a = 1 exactly).
-        const int c = tid % kD, qt = tid / kD;
-        float g[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int i = qt * 16 + m;
-            g[m] = (i < L) ? __fdividef(kGMin, 1.0f + __expf(-eA * G[i][c])) : 0.f;
-        }
-#pragma unroll
-        for (int m = 1; m < 16; ++m) g[m] += g[m - 1];
-        s.colsum[qt][c] = g[15];
-        __syncthreads();
-        float below = 0.f;
-        for (int p = 0; p < qt; ++p) below += s.colsum[p][c];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) G[qt * 16 + m][c] = (qt > 0) ? g[m] + below : g[m];
-    }
-    // the next chunk's z goes to the other buffer (last read by the previous chunk); it is
-    // issued after the gate so that its landing does not compete with the gate's reads
-    if (has_next)
-        stage_z(nxt, s.G[(iter + 1) & 1]);
-    else
-        cp_async_commit();  // an empty group keeps the group arithmetic uniform
-    __syncthreads();
-
-    cp_async_wait<2>();
-    __syncthreads();  // q and k in place (v and the next chunk's z may still be in flight)
-
-    // ---- decayed Gram matrices, one 32-token tile row at a time -----------------
-    // Tile row a (tokens 32a .. 32a+31) takes the reference token m = 32a + 16, so that
-    // exp(G_i - G_j) = exp(G_i - G_m) * exp(G_m - G_j) with neither factor beyond e^80
-    // (at most 16 tokens of log decay >= -5 between i or j and m on the side where the
-    // factor exceeds 1), inside the range of fp32 and bf16; a factor that underflows
-    // belongs to a product below e^-20, negligible next to the O(1) entries.
-    unsigned char *const aqb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.aq[0][0][0]),
-                                   reinterpret_cast<unsigned char *>(&s.u.g.aq[1][0][0])};
-    unsigned char *const akb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.ak[0][0][0]),
-                                   reinterpret_cast<unsigned char *>(&s.u.g.ak[1][0][0])};
-    unsigned char *const bkb[2] = {reinterpret_cast<unsigned char *>(&s.u.g.bk[0][0][0]),
-                                   reinterpret_cast<unsigned char *>(&s.u.g.bk[1][0][0])};
-    // G of the reference token m on channels c .. c+7
-    auto ref8 = [&](int m, int c, float (&gm)[8]) {
-        const float4 m0 = *reinterpret_cast<const float4 *>(&G[m][c]);
-        const float4 m1 = *reinterpret_cast<const float4 *>(&G[m][c + 4]);
-        gm[0] = m0.x; gm[1] = m0.y; gm[2] = m0.z; gm[3] = m0.w;
-        gm[4] = m1.x; gm[5] = m1.y; gm[6] = m1.z; gm[7] = m1.w;
-    };
-    // one 8-channel item of an operand row: the A side (q and k of token i, factor
-    // exp(G_i - G_m)) or the B side (k of key j, factor exp(G_m - G_j)), split into planes
-    auto prep_item = [&](bool aside, int row, int ar, int c, const float (&gm)[8]) {
-        const float4 g0 = *reinterpret_cast<const float4 *>(&G[row][c]);
-        const float4 g1 = *reinterpret_cast<const float4 *>(&G[row][c + 4]);
-        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        float f[8];
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm) f[mm] = __expf(aside ? g[mm] - gm[mm] : gm[mm] - g[mm]);
-        const uint4 kraw = *reinterpret_cast<const uint4 *>(&s.ks[row][c]);
-        const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
-        uint32_t kh[4], kl[4];
-#pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) scale_split_pk(kw[p2], f[2 * p2], f[2 * p2 + 1], kh[p2], kl[p2]);
-        if (aside) {
-            const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[row][c]);
-            const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
-            uint32_t qh[4], ql[4];
-#pragma unroll
-            for (int p2 = 0; p2 < 4; ++p2) scale_split_pk(qw[p2], f[2 * p2], f[2 * p2 + 1], qh[p2], ql[p2]);
-            const uint32_t off = gram_off(ar, c);
-            *reinterpret_cast<uint4 *>(aqb[0] + off) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-            *reinterpret_cast<uint4 *>(aqb[1] + off) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
-            *reinterpret_cast<uint4 *>(akb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-            *reinterpret_cast<uint4 *>(akb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
-        } else {
-            const uint32_t off = gram_off(row, c);
-            *reinterpret_cast<uint4 *>(bkb[0] + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-            *reinterpret_cast<uint4 *>(bkb[1] + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
-        }
-    };
-    for (int a = 0; a < kC / (2 * kTile); ++a) {
-        const int r0 = a * 2 * kTile;  // first token of the tile row
-        const int m = r0 + kTile;      // reference token
-        const int nb = r0 + 2 * kTile; // key rows j = 0 .. r0+31
-        // Operands, 8 channels per item (16-byte loads and stores): the A operands (q and
-        // k of the tile row, sharing the factor exp(G_i - G_m)) are items 0 .. 511, the B
-        // operand (keys j with the factor exp(G_m - G_j)) the rest. A thread's channel
-        // slice, tid % 16, is the same for all its items, so G_m is read once. Keys 32 ..
-        // 63 of the second tile row, which the first does not use, were built by the warps
-        // that had no MMA task in the first round; so each round builds keys 0 .. 31 here.
-        {
-            const int c = (tid & 15) * 8;
-            float gm[8];
-            ref8(m, c, gm);
-            for (int e = tid; e < 4 * kTile * 16; e += kIntraThreads) {
-                const bool aside = e < 2 * kTile * 16;
-                const int ar = e >> 4;                            // A-side row in the tile row
-                const int row = aside ? r0 + ar : ar - 2 * kTile;  // token i (A side) or j (B side)
-                prep_item(aside, row, ar, c, gm);
-            }
-        }
-        __syncthreads();
-        // MMA tasks: (matrix, 16-row m tile, 16-key n tile: two n8 tiles sharing the A
-        // fragments), skipping n tiles wholly above the diagonal: m tile 0 (rows r0..r0+15)
-        // takes keys below r0+16, m tile 1 all keys below r0+32
-        const int n16_0 = (r0 + kTile) / 16, n16_1 = nb / 16;
-        const int per_mat = n16_0 + n16_1;
-        if (a == 0 && warp >= 2 * per_mat) {
-            // no MMA task in this round: keys 32 .. 63 of the next tile row (reference 48),
-            // rows of the B buffer that this round's products do not read
-            const int t2 = tid - 2 * per_mat * 32, nthr = kIntraThreads - 2 * per_mat * 32;
-            const int c = (t2 & 15) * 8;  // nthr is a multiple of 16: the slice stays fixed
-            float gm[8];
-            ref8(3 * kTile, c, gm);
-            for (int e = t2; e < 2 * kTile * 16; e += nthr) prep_item(false, 2 * kTile + (e >> 4), 0, c, gm);
-        }
-        for (int p = warp; p < 2 * per_mat; p += kIntraThreads / 32) {
-            const int mat = p / per_mat;  // 0: A_qk, 1: A_kk
-            const int q = p % per_mat;
-            const int mt = q < n16_0 ? 0 : 1;
-            const int n0 = (mt == 0 ? q : q - n16_0) * 16;
-            const __nv_bfloat16 *ah_base = mat ? &s.u.g.ak[0][0][0] : &s.u.g.aq[0][0][0];
-            const __nv_bfloat16 *al_base = mat ? &s.u.g.ak[1][0][0] : &s.u.g.aq[1][0][0];
-            float a0[2][4], a1[2][4], a2[2][4];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) a0[h2][e] = a1[h2][e] = a2[h2][e] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                uint32_t ah[4], al[4], bh[4], bl[4];
-                load_a_sw(ah, ah_base, mt * kTile, ks * 16, lane);
-                load_a_sw(al, al_base, mt * kTile, ks * 16, lane);
-                load_b_nk16_sw(bh, &s.u.g.bk[0][0][0], n0, ks * 16, lane);
-                load_b_nk16_sw(bl, &s.u.g.bk[1][0][0], n0, ks * 16, lane);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {  // the three split products in separate chains
-                    mma_bf16(a0[h2], ah, bh[2 * h2], bh[2 * h2 + 1]);
-                    mma_bf16(a1[h2], ah, bl[2 * h2], bl[2 * h2 + 1]);
-                    mma_bf16(a2[h2], al, bh[2 * h2], bh[2 * h2 + 1]);
-                }
-            }
-            const int g = lane >> 2, t4 = lane & 3;
-            const int ib = r0 + mt * kTile + g;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                float acc[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = a0[h2][e] + (a1[h2][e] + a2[h2][e]);
-                const int jb = n0 + h2 * 8 + 2 * t4;
-                if (mat == 0) {  // A_qk (diagonal included), split, into the record
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int i = ib + hr * 8, j = jb;
-                        uint32_t hi, lo;
-                        split_bf16x2(j <= i ? acc[2 * hr] : 0.f, j + 1 <= i ? acc[2 * hr + 1] : 0.f, hi, lo);
-                        *reinterpret_cast<uint32_t *>(rec + kRecAqk + il_off(i, j, kC)) = hi;
-                        *reinterpret_cast<uint32_t *>(rec + kRecAqk + kStackAK + il_off(i, j, kC)) = lo;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = ib + ((e >> 1) << 3);
-                        const int j = jb + (e & 1);
-                        s.Akk[i][j] = (j < i) ? s.beta[i] * acc[e] : 0.f;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    // ---- UT transform on warps 0-7: T = (I + A_kk)^-1, unit lower triangular. -----
-    // ---- Meanwhile warps 8-15 write Qhat, Kend^T and gamma to the record and build -
-    // ---- the Khat operand planes: they need only q, k and G. -----------------------
-    if (warp < kSolveWarps) {
-        // diagonal 16x16 blocks, warp a solving block a: lane i holds row i of A_aa and
-        // of T_aa in registers (lanes 16-31 mirror lanes 0-15 and store nothing); T
-        // starts as I and, for m = 0 .. 14 in order, every row i > m subtracts
-        // A[i][m] * (row m, now final), broadcast by shuffles. No shared-memory reads in
-        // the loop, and the terms of each entry add in the order of forward substitution.
-        if (warp < 4) {
-            const int base = warp * kTile, i = lane & 15;
-            float a[kTile], t[kTile];
-#pragma unroll
-            for (int q4 = 0; q4 < kTile; q4 += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(&s.Akk[base + i][base + q4]);
-                a[q4] = v.x; a[q4 + 1] = v.y; a[q4 + 2] = v.z; a[q4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int j = 0; j < kTile; ++j) t[j] = (j == i) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < kTile - 1; ++m) {
-#pragma unroll
-                for (int j = 0; j <= m; ++j) {  // row m is zero beyond its diagonal
-                    const float tm = __shfl_sync(0xffffffffu, t[j], m, 16);
-                    if (i > m) t[j] = __fmaf_rn(-a[m], tm, t[j]);
-                }
-            }
-            if (lane < kTile) {
-#pragma unroll
-                for (int q4 = 0; q4 < kTile; q4 += 4)
-                    *reinterpret_cast<float4 *>(&s.T[base + i][base + q4]) =
-                        make_float4(t[q4], t[q4 + 1], t[q4 + 2], t[q4 + 3]);
-            }
-        } else {
-            for (int e = tid - 128; e < kC * kC; e += kSolveWarps * 32 - 128) {
-                const int i = e / kC, j = e % kC;
-                if ((j >> 4) > (i >> 4)) s.T[i][j] = 0.f;
-            }
-        }
-        named_sync(1, kSolveWarps * 32);
-        // off-diagonal blocks by distance l: T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb.
-        // Thread (block, row rr, column quad cq) makes four outputs, reading a float4 of
-        // A along k and a float4 of T per k: about one shared load per three FMAs.
-        for (int l = 1; l < kC / kTile; ++l) {
-            const int nblk = kC / kTile - l;
-            const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = (tid & 3) * 4;
-            const int b = blk, a = b + l;
-            if (tid < nblk * 64) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int m = b; m < a; ++m) {
-#pragma unroll
-                    for (int x4 = 0; x4 < kTile; x4 += 4) {
-                        const float4 av = *reinterpret_cast<const float4 *>(&s.Akk[a * kTile + rr][m * kTile + x4]);
-                        const float am[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float4 tv = *reinterpret_cast<const float4 *>(&s.T[m * kTile + x4 + u][b * kTile + cq]);
-                            acc.x += am[u] * tv.x; acc.y += am[u] * tv.y; acc.z += am[u] * tv.z; acc.w += am[u] * tv.w;
-                        }
-                    }
-                }
-                *reinterpret_cast<float4 *>(&s.X[blk][rr][cq]) = acc;
-            }
-            named_sync(1, kSolveWarps * 32);
-            if (tid < nblk * 64) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int x4 = 0; x4 < kTile; x4 += 4) {
-                    const float4 tv = *reinterpret_cast<const float4 *>(&s.T[a * kTile + rr][a * kTile + x4]);
-                    const float tm[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float4 xv = *reinterpret_cast<const float4 *>(&s.X[blk][x4 + u][cq]);
-                        acc.x += tm[u] * xv.x; acc.y += tm[u] * xv.y; acc.z += tm[u] * xv.z; acc.w += tm[u] * xv.w;
-                    }
-                }
-                *reinterpret_cast<float4 *>(&s.T[a * kTile + rr][b * kTile + cq]) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-            }
-            named_sync(1, kSolveWarps * 32);
-        }
-    } else {
-        const int t2 = tid - kSolveWarps * 32;
-        constexpr int kElemThreads = kIntraThreads - kSolveWarps * 32;
-        // Khat = k * exp(G) (the B operand of W, into the dead Gram operand space) and
-        // Qhat = q * exp(G) (into the record) share their factors: one thread makes 8
-        // channels of one row of both, as 16-byte chunks; consecutive threads fill
-        // consecutive 16-byte chunks of the record tile
-        uint8_t *Qh = rec + kRecQh;
-        for (int e = t2; e < kC * (kD / 8); e += kElemThreads) {
-            const int c8 = (e >> 3) & 15, i = (e >> 7) * 8 + (e & 7), c = c8 * 8;
-            const float4 g0 = *reinterpret_cast<const float4 *>(&G[i][c]);
-            const float4 g1 = *reinterpret_cast<const float4 *>(&G[i][c + 4]);
-            const float f[8] = {__expf(g0.x), __expf(g0.y), __expf(g0.z), __expf(g0.w),
-                                __expf(g1.x), __expf(g1.y), __expf(g1.z), __expf(g1.w)};
-            const uint4 qraw = *reinterpret_cast<const uint4 *>(&s.qs[i][c]);
-            const uint4 kraw = *reinterpret_cast<const uint4 *>(&s.ks[i][c]);
-            const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w}, kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
-            uint32_t qh[4], ql[4], kh[4], kl[4];
-#pragma unroll
-            for (int p2 = 0; p2 < 4; ++p2) {
-                scale_split_pk(qw[p2], f[2 * p2], f[2 * p2 + 1], qh[p2], ql[p2]);
-                scale_split_pk(kw[p2], f[2 * p2], f[2 * p2 + 1], kh[p2], kl[p2]);
-            }
-            *reinterpret_cast<uint4 *>(Qh + il_off(i, c, kD)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-            *reinterpret_cast<uint4 *>(Qh + kStackWQ + il_off(i, c, kD)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
-            *reinterpret_cast<uint4 *>(&s.u.w.kh[0][i][c]) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-            *reinterpret_cast<uint4 *>(&s.u.w.kh[1][i][c]) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
-        }
-        uint8_t *KeT = rec + kRecKeT;
-        for (int e = t2; e < kD * (kC / 8); e += kElemThreads) {
-            const int j8 = (e >> 3) & 7, c = (e >> 6) * 8 + (e & 7), j = j8 * 8;
-            const float gl = G[kC - 1][c];
-            float x[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) x[m] = __bfloat162float(s.ks[j + m][c]) * __expf(gl - G[j + m][c]);
-            uint4 hi, lo;
-            split_pk(pk2(x[0], x[1]), hi.x, lo.x);
-            split_pk(pk2(x[2], x[3]), hi.y, lo.y);
-            split_pk(pk2(x[4], x[5]), hi.z, lo.z);
-            split_pk(pk2(x[6], x[7]), hi.w, lo.w);
-            *reinterpret_cast<uint4 *>(KeT + il_off(c, j, kC)) = hi;
-            *reinterpret_cast<uint4 *>(KeT + kStackAK + il_off(c, j, kC)) = lo;
-        }
-        float *gam = reinterpret_cast<float *>(rec + kRecGam);
-        if (t2 < kD) gam[t2] = expf(G[kC - 1][t2]);
-    }
-    __syncthreads();
-    // q and k are read no more: the next chunk's come in behind the remaining phases
-    if (has_next)
-        stage_rows(nxt, 0, 2);
-    else
-        cp_async_commit();
-
-    // ---- the other W / U' operand: T' = T Diag(beta), split -----------------------
-    for (int e = tid; e < kC * (kC / 2); e += kIntraThreads) {
-        const int i = e / (kC / 2), j = (e % (kC / 2)) * 2;
-        uint32_t hi, lo;
-        const float2 t = *reinterpret_cast<const float2 *>(&s.T[i][j]);
-        const float2 be = *reinterpret_cast<const float2 *>(&s.beta[j]);
-        split_pk(mul2(pk2(t.x, t.y), pk2(be.x, be.y)), hi, lo);
-        *reinterpret_cast<uint32_t *>(&s.u.w.t[0][i][j]) = hi;
-        *reinterpret_cast<uint32_t *>(&s.u.w.t[1][i][j]) = lo;
-    }
-    // groups in flight: this chunk's v, the next chunk's z, its q and k
-    cp_async_wait<2>();
-    __syncthreads();  // v in place too
-
-    // ---- W = T' Khat (split x split), U' = T' V (split x exact bf16) ------------
-    // warp w owns output columns 16 (w % 8) .. +15; the two halves of the warps split the
-    // 16-row tiles of the triangle evenly: rows {0, 3} and {1, 2} (k-steps 0..a each)
-    {
-        float accW[2][2][4], accU[2][2][4];
-#pragma unroll
-        for (int ai = 0; ai < 2; ++ai)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    accW[ai][nt][e] = 0.f;
-                    accU[ai][nt][e] = 0.f;
-                }
-        const int n0 = (warp & 7) * 16;
-        const int half = warp >> 3;
-#pragma unroll
-        for (int ai = 0; ai < 2; ++ai) {
-            const int a = half == 0 ? (ai == 0 ? 0 : 3) : (ai == 0 ? 1 : 2);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                if (ks > a) break;  // T' is lower triangular
-                uint32_t th[4], tl[4], kh[4], kl[4], vb[4];
-                load_a(th, &s.u.w.t[0][0][0], kLd64, a * 16, ks * 16, lane);
-                load_a(tl, &s.u.w.t[1][0][0], kLd64, a * 16, ks * 16, lane);
-                load_b_kn(kh, &s.u.w.kh[0][0][0], kLd128, ks * 16, n0, lane);
-                load_b_kn(kl, &s.u.w.kh[1][0][0], kLd128, ks * 16, n0, lane);
-                load_b_kn(vb, &s.vs[0][0], kLd128, ks * 16, n0, lane);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    mma_split3(accW[ai][nt], th, tl, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
-                    mma_bf16(accU[ai][nt], tl, vb[2 * nt], vb[2 * nt + 1]);
-                    mma_bf16(accU[ai][nt], th, vb[2 * nt], vb[2 * nt + 1]);
-                }
-            }
-        }
-        // write -W (split, interleaved tiles) and U' (fp32, token-major) to the record
-        uint8_t *Wn = rec + kRecWn;
-        float *Up = reinterpret_cast<float *>(rec + kRecUp);
-        const int g = lane >> 2, t4 = lane & 3;
-#pragma unroll
-        for (int ai = 0; ai < 2; ++ai) {
-            const int a = half == 0 ? (ai == 0 ? 0 : 3) : (ai == 0 ? 1 : 2);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int i = a * 16 + g + hr * 8;
-                    const int c = n0 + nt * 8 + 2 * t4;
-                    uint32_t hi, lo;
-                    split_bf16x2(-accW[ai][nt][2 * hr], -accW[ai][nt][2 * hr + 1], hi, lo);
-                    *reinterpret_cast<uint32_t *>(Wn + il_off(i, c, kD)) = hi;
-                    *reinterpret_cast<uint32_t *>(Wn + kStackWQ + il_off(i, c, kD)) = lo;
-                    *reinterpret_cast<float2 *>(Up + (size_t)i * kD + c) =
-                        make_float2(accU[ai][nt][2 * hr], accU[ai][nt][2 * hr + 1]);
-                }
-        }
-    }
-    __syncthreads();  // this chunk's shared memory is free for the next one
-    if (has_next)
-        stage_rows(nxt, 2, 1);  // v
-    else
-        cp_async_commit();
-    cur = nxt;
-    }
-    cp_async_wait<0>();  // nothing left in flight (the last group is empty)
-}
-
-// ---------------------------------------------------------------------------------
 // state walk: one CTA per (sequence, head) carries the full 128 x 128 state through
 // the chunks of its sequence on the tcgen05 tensor cores, accumulators in TMEM.
 //
@@ -955,7 +378,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
 // every MMA group so that the U and O warps' waits keep their arrivals in order.
 // ---------------------------------------------------------------------------------
 struct WalkSmem {
-    unsigned char wq[2 * kStackWQ];      // [ -W ; Qhat ] hi | lo
+    unsigned char wq[kRecWQBytes];       // -W, Qhat hi, Qhat lo (rows 0..63, 64..127, 64..127)
     unsigned char ak[2][2 * kStackAK];   // [ A_qk ; Kend^T ] hi | lo, of chunks c (slot c & 1)
     alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1), the state warps' copy
     alignas(16) float gam_uo[2][kD];     // the same, the U and O warps' copy
@@ -1067,11 +490,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     if (warp < 4) {
         // ------------- U and O warps; they also hold key rows 64 .. 127 of S -------------
         uint64_t Upr[32];  // U' of tokens 2j, 2j + 1 of this value channel as one packed pair
+        // U' row i holds its 16-byte units (4 channels) XOR-swizzled by i % 32
+        auto up_at = [&](int i) { return i * kD + ((((dv >> 2) ^ (i & 31))) << 2) + (dv & 3); };
         auto load_up = [&](int c) {
             const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                Upr[j] = add_up ? pk2(up[(2 * j) * kD + dv], up[(2 * j + 1) * kD + dv]) : pk2(0.f, 0.f);
+                Upr[j] = add_up ? pk2(up[up_at(2 * j)], up[up_at(2 * j + 1)]) : pk2(0.f, 0.f);
         };
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -1191,19 +616,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // ----------------- state warps (thread 128 issues the MMAs) -----------------
         const bool issuer = (tid == 128);
         const uint32_t kIdG1 = tc::idesc_bf16_m128(maps ? 64 : 128);
-        const uint32_t kIdG2 = tc::idesc_bf16_m128(maps ? 128 : 192);
+        const uint32_t kIdQl = tc::idesc_bf16_m128(64);
+        // [ A_qk ; Kend^T ] is stored MN-major (its rows n contiguous per token): B transposed
+        const uint32_t kIdG2 = tc::idesc_bf16(128, maps ? 128 : 192, 1);
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
         // phase bookkeeping (issuer); the [ A_qk ; Kend^T ] slot of chunk c is (c - c_begin) & 1
         int n_wq = 0, w_wq = 0, n_m1 = 0, n_m2 = 0, n_ak0 = 0, n_ak1 = 0, w_ak0 = 0, w_ak1 = 0;
         auto issue_wq = [&](int c) {
-            if (maps) {  // the -W rows of the hi and the lo plane
-                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kPlaneQK));
-                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)kPlaneQK, &s.bar_wq);
-                tc::bulk_g2s(s.wq + kStackWQ, rec_of(c) + kRecWQ + kStackWQ, (uint32_t)kPlaneQK, &s.bar_wq);
-            } else {
-                tc::mbar_arrive_expect_tx(&s.bar_wq, (uint32_t)(2 * kStackWQ));
-                tc::bulk_g2s(s.wq, rec_of(c) + kRecWQ, (uint32_t)(2 * kStackWQ), &s.bar_wq);
-            }
+            const uint32_t bytes = (uint32_t)(maps ? kPlaneQK : kRecWQBytes);  // -W only, or all three
+            tc::mbar_arrive_expect_tx(&s.bar_wq, bytes);
+            tc::bulk_g2s(s.wq, rec_of(c) + kRecW, bytes, &s.bar_wq);
             ++n_wq;
         };
         auto issue_ak = [&](int c) {
@@ -1240,14 +662,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         auto issue_g1 = [&](int c, bool ready) {
             tc::fence_after_sync();
             if (ready) {
-                const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)kStackWQ;
+                // S^T hi and lo times the hi plane of [ -W ; Qhat ], and S^T hi times Qhat lo
+                // into the D_O1 half (W has one plane; a map walk has no Qhat)
+                const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)(2 * kPlaneQK);
 #pragma unroll 1
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t a0 = tmem + kColSHi + 8 * ks, a1 = tmem + kColSLo + 8 * ks;
-                    const uint64_t b0 = tc::desc_k(b0s, kD, ks), b1 = tc::desc_k(b1s, kD, ks);
+                    const uint64_t b0 = tc::desc_k(b0s, kD, ks);
                     tc::mma_ts(D_UO, a0, b0, kIdG1, ks > 0);
-                    tc::mma_ts(D_UO, a0, b1, kIdG1, 1);
                     tc::mma_ts(D_UO, a1, b0, kIdG1, 1);
+                    if (!maps) tc::mma_ts(D_UO + 64, a0, tc::desc_k(b1s, kD, ks), kIdQl, 1);
                 }
             }
             tc::commit(&s.bar_m1);  // also after a failure: the U and O warps wait for it in order
@@ -1389,25 +813,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 // ---------------------------------------------------------------------------------
 // host-side launchers (called from kda_api.cu)
 // ---------------------------------------------------------------------------------
-size_t intra_smem_bytes() { return sizeof(IntraSmem); }
-
-// a launch that may start while the previous kernel on the stream runs (the kernel
-// waits for it with griddepcontrol.wait before touching its results)
-template <typename... Params, typename... Args>
-static cudaError_t launch_after(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
-}
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
                         int32_t *n_units, const SegPlan &sp, cudaStream_t st) {
@@ -1428,25 +833,6 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
     dim3 grid((unsigned)N, (unsigned)H, kD / 16);
     return launch_after(kda_combine_kernel, grid, dim3(kCombineThreads), sizeof(CombineSmem), st, status, chains, H,
                         Sin, Mseg, Rseg);
-}
-
-cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
-                         const float *A, const float *b, const int32_t *status, const int32_t *seq_cu,
-                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t nslots, uint8_t *records,
-                         int num_sms, cudaStream_t st) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kda_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sizeof(IntraSmem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    if (nslots <= 0) return cudaSuccess;
-    // persistent: one CTA per SM (the shared memory allows no more) walks the items
-    const int64_t items = nslots * H;
-    const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)num_sms);
-    return launch_after(kda_intra_kernel, dim3(grid), dim3(kIntraThreads), sizeof(IntraSmem), st, q, k, v, z, A, b,
-                        status, seq_cu, chunk_off, N, H, records);
 }
 
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,

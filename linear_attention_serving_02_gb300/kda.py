@@ -94,8 +94,59 @@ def kda_chunk_prefill_workspace_size(total_tokens, num_seqs, num_heads):
 
 
 def kda_chunk_prefill_launch_count(total_tokens, num_seqs, num_heads):
-    """Kernels one kda_chunk_prefill call with these sizes launches (3, or 6 for a segmented walk)."""
+    """Kernels one kda_chunk_prefill call with these sizes launches (3, or 5 for a segmented walk)."""
     return int(library().kda_chunk_prefill_launch_count(int(total_tokens), int(num_seqs), int(num_heads)))
+
+
+def _prefill_args(q, k, v, z, A, b, initial_state, cu_seqlens, cu_seqlens_host, o, final_state, o_dtype):
+    """Checks and sizes shared by both prefill entry points. Returns (batch, seq_len,
+    num_seqs, H, host cu_seqlens or None, o, final_state), allocating o and final_state
+    with torch when they are not given."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    _need(z, "z", torch.float32)
+    _need(A, "A", torch.float32)
+    _need(b, "b", torch.float32)
+    if q.dim() < 3 or q.shape[-1] != D or k.shape != q.shape or v.shape != q.shape or z.shape != q.shape:
+        raise ValueError("q, k, v and z must share one shape [..., H, 128]")
+    H = q.shape[-2]
+    if A.numel() != H or b.shape != q.shape[:-1]:
+        raise ValueError("A must hold H values and b be shaped like q without its last dimension")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be a 1-D tensor of num_seqs + 1 offsets")
+        if q.dim() == 4 and q.shape[0] != 1:
+            raise ValueError("a packed varlen batch wants q as [T_total, H, 128] or [1, T_total, H, 128]")
+        batch, seq_len = 1, q.numel() // (H * D)
+        num_seqs = cu_seqlens.numel() - 1
+    else:
+        if q.dim() != 4:
+            raise ValueError("dense batch wants q as [B, T, H, 128]")
+        batch, seq_len = q.shape[0], q.shape[1]
+        num_seqs = batch
+    hc = None
+    if cu_seqlens_host is not None:
+        if cu_seqlens_host.is_cuda or cu_seqlens_host.dim() != 1 or cu_seqlens_host.numel() != num_seqs + 1:
+            raise ValueError("cu_seqlens_host must be a 1-D CPU tensor of num_seqs + 1 entries")
+        hc = cu_seqlens_host.to(torch.int32).contiguous()
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32)
+        if tuple(initial_state.shape) != (num_seqs, H, D, D):
+            raise ValueError("initial_state must be [num_seqs, H, 128, 128]")
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bf16 or fp32")
+    _need(o, "o", o.dtype)
+    if o.shape != q.shape:
+        raise ValueError("o must be shaped like q")
+    if final_state is None:
+        final_state = torch.empty((num_seqs, H, D, D), dtype=torch.float32, device=q.device)
+    _need(final_state, "final_state", torch.float32)
+    if tuple(final_state.shape) != (num_seqs, H, D, D):
+        raise ValueError("final_state must be [num_seqs, H, 128, 128]")
+    return batch, seq_len, num_seqs, H, hc, o, final_state
 
 
 def kda_chunk_prefill(q, k, v, z, A, b, initial_state=None, cu_seqlens=None, cu_seqlens_host=None,
@@ -108,38 +159,9 @@ def kda_chunk_prefill(q, k, v, z, A, b, initial_state=None, cu_seqlens=None, cu_
     copy of it (validated on the host). o / final_state / workspace are allocated with
     torch when not given.
     """
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, name, torch.bfloat16)
-    _need(z, "z", torch.float32)
-    _need(A, "A", torch.float32)
-    _need(b, "b", torch.float32)
-    H = q.shape[-2]
-    if q.shape[-1] != D or v.shape[-1] != D:
-        raise ValueError("head size must be 128")
-    if cu_seqlens is not None:
-        _need(cu_seqlens, "cu_seqlens", torch.int32)
-        batch, seq_len = 1, q.numel() // (H * D)
-        num_seqs = cu_seqlens.numel() - 1
-    else:
-        if q.dim() != 4:
-            raise ValueError("dense batch wants q as [B, T, H, 128]")
-        batch, seq_len = q.shape[0], q.shape[1]
-        num_seqs = batch
+    batch, seq_len, num_seqs, H, hc, o, final_state = _prefill_args(
+        q, k, v, z, A, b, initial_state, cu_seqlens, cu_seqlens_host, o, final_state, o_dtype)
     total = batch * seq_len
-    hc = None
-    if cu_seqlens_host is not None:
-        hc = cu_seqlens_host.to(torch.int32).contiguous()
-        if hc.is_cuda or hc.numel() != num_seqs + 1:
-            raise ValueError("cu_seqlens_host must be a CPU tensor of num_seqs + 1 entries")
-    if initial_state is not None:
-        _need(initial_state, "initial_state", torch.float32)
-    if o is None:
-        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
-    if o.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("o must be bf16 or fp32")
-    if final_state is None:
-        final_state = torch.empty((num_seqs, H, D, D), dtype=torch.float32, device=q.device)
-    _need(final_state, "final_state", torch.float32)
     need = kda_chunk_prefill_workspace_size(total, num_seqs, H)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -271,24 +293,8 @@ def kda_chunk_prefill_noalloc(q, k, v, z, A, b, initial_state=None, cu_seqlens=N
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp, i32, vp, vp]
         fn.restype = ctypes.c_int
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, name, torch.bfloat16)
-    _need(z, "z", torch.float32)
-    _need(A, "A", torch.float32)
-    _need(b, "b", torch.float32)
-    H = q.shape[-2]
-    if cu_seqlens is not None:
-        _need(cu_seqlens, "cu_seqlens", torch.int32)
-        batch, seq_len = 1, q.numel() // (H * D)
-        num_seqs = cu_seqlens.numel() - 1
-    else:
-        batch, seq_len = q.shape[0], q.shape[1]
-        num_seqs = batch
-    hc = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
-    if o is None:
-        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
-    if final_state is None:
-        final_state = torch.empty((num_seqs, H, D, D), dtype=torch.float32, device=q.device)
+    batch, seq_len, num_seqs, H, hc, o, final_state = _prefill_args(
+        q, k, v, z, A, b, initial_state, cu_seqlens, cu_seqlens_host, o, final_state, o_dtype)
     rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(b), _ptr(initial_state), _ptr(cu_seqlens), _ptr(hc),
             batch, seq_len, num_seqs, H, D, D, _ptr(o), KDA_OUT_F32 if o.dtype == torch.float32 else KDA_OUT_BF16,
             _ptr(final_state), _stream(stream))

@@ -118,6 +118,44 @@ def test_prefill_argument_checks(over, code):
     assert _prefill(**over) == code
 
 
+def _prefill_noalloc(**over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, A=FAKE, b=FAKE, initial_state=None, cu=None, cu_host=None,
+                batch=1, seq_len=256, num_seqs=1, num_heads=2, d_k=128, d_v=128, o=FAKE, o_dtype=0,
+                final_state=FAKE, stream=None)
+    args.update(over)
+    fn = kda.library().kda_chunk_prefill_noalloc
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp, i32, vp, vp]
+    fn.restype = ctypes.c_int
+    return fn(args["q"], args["k"], args["v"], args["z"], args["A"], args["b"], args["initial_state"], args["cu"],
+              args["cu_host"], args["batch"], args["seq_len"], args["num_seqs"], args["num_heads"], args["d_k"],
+              args["d_v"], args["o"], args["o_dtype"], args["final_state"], args["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(d_k=64), dict(o_dtype=7), dict(num_heads=0), dict(seq_len=-1), dict(batch=2, num_seqs=1),
+    dict(batch=2, num_seqs=2, cu=FAKE), dict(seq_len=1 << 31), dict(batch=2, seq_len=1 << 40),
+    dict(num_heads=65536), dict(seq_len=1 << 30, num_heads=4096), dict(q=None), dict(final_state=None),
+    dict(A=None), dict(q=FAKE + 8), dict(initial_state=FAKE + 8),
+    # the same bad sizes on a batch too large for the fixed scratch: the argument error wins
+    dict(d_k=64, seq_len=1 << 20, num_heads=12), dict(num_heads=70000, seq_len=1 << 20),
+    dict(batch=3, num_seqs=3, cu=FAKE, seq_len=1 << 20, num_heads=12),
+])
+def test_noalloc_argument_checks_match_the_workspace_entry_point(over):
+    """The entry point without a workspace checks its arguments exactly as
+    kda_chunk_prefill does and returns the same codes; none of these calls reaches the
+    scratch lookup or a launch."""
+    expect = _prefill(**over)
+    assert expect not in (KDA_OK, KDA_ERR_WORKSPACE)
+    assert _prefill_noalloc(**over) == expect
+
+
+def test_noalloc_refuses_a_batch_larger_than_its_scratch_on_the_host():
+    assert _prefill_noalloc(seq_len=1 << 20, num_heads=12) == KDA_ERR_WORKSPACE
+    ptr, keep = _host_cu([0, 100, 90, 256])
+    assert _prefill_noalloc(cu=FAKE, cu_host=ptr, num_seqs=3) == KDA_ERR_SEQLENS
+
+
 def test_prefill_host_cu_seqlens_checks():
     for vals, code in (([0, 100, 90, 256], KDA_ERR_SEQLENS),   # falls
                        ([1, 100, 200, 256], KDA_ERR_SEQLENS),  # does not start at 0

@@ -118,6 +118,65 @@ def test_strongest_decay_everywhere():
     assert_prefill_close(o, S, o_ref, S_ref, "decay bound")
 
 
+def _decay_pattern(inp, start, moderate=0.5):
+    """z on every chunk position p = t mod 64: the bound decay (z = +inf, log a = -5
+    exactly) on p in [start, start + 16), a moderate decay on the 16 positions before
+    (log a between -0.4 and -0.6 across the channels, so that 16 tokens sum to about
+    -6.4 .. -9.6), and no decay (z = -inf, a = 1) elsewhere."""
+    z = inp["z"]
+    T, H = z.shape[1], z.shape[2]
+    p = torch.arange(T) % 64
+    eA = torch.exp(inp["A"].double())                          # [H]
+    f = 0.8 + 0.4 * torch.arange(128, dtype=torch.float64) / 127  # per channel
+    frac = moderate / 5.0 * f                                   # sigmoid value giving log a = -moderate f
+    zmod = (torch.log(frac / (1 - frac))[None, :] / eA[:, None]).float()  # [H, 128]
+    out = torch.full_like(z, -float("inf"))
+    bound = ((p >= start) & (p < start + 16))
+    mod = ((p >= start - 16) & (p < start)) | ((p - 64 >= start - 16) & (p - 64 < start))
+    out[0, bound] = float("inf")
+    out[0, mod] = zmod
+    inp["z"] = out
+    return inp
+
+
+@pytest.mark.parametrize("start", [1, 17, 33, 48])
+def test_bound_decay_next_to_a_moderate_run(start):
+    """Sixteen tokens at the decay bound right after sixteen of moderate decay, no decay
+    elsewhere: the factors of the decayed Gram products around a reference token reach
+    e^80 on one side while the other side's factor approaches the fp32/bf16 underflow
+    (about e^-87), which is where a factoring that lets one factor exceed 1 while the
+    other underflows would lose products of size e^-7 ('From Linear Attention to KDA',
+    §5.4 bounded decay, §8 tiles). Element by element against the oracle, at several
+    positions of the pattern within the 64-token chunk."""
+    T, H = 200, 2
+    inp = _decay_pattern(inputs.prefill_inputs(T, H, 1, seed=14 + start, init_state=True), start)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"])
+    o, S = gpu_prefill(inp)
+    assert torch.isfinite(o).all() and torch.isfinite(S).all()
+    assert_prefill_close(o, S, o_ref, S_ref, "decay pattern at %d" % start)
+
+
+def test_full_write_strength_retrieves_the_last_value():
+    """b = +inf gives beta = 1 exactly on every token. The delta rule then makes the last
+    key retrieve its value: S_T^T k_T = v_T up to the deviation of ||k_T|| from 1 (k is
+    normalised in fp32, then rounded to bf16). S_T^T k_T is compared with the oracle's,
+    and o and S element by element ('From Linear Attention to KDA', §5.1)."""
+    T, H = 150, 2
+    inp = inputs.prefill_inputs(T, H, 1, seed=15, init_state=True)
+    inp["b"] = torch.full_like(inp["b"], float("inf"))
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"])
+    o, S = gpu_prefill(inp)
+    assert_prefill_close(o, S, o_ref, S_ref, "beta = 1")
+    k_last = np64(inp["k"][0, T - 1])                       # [H, 128]
+    v_last = np64(inp["v"][0, T - 1])
+    r_gpu = np.einsum("hcj,hc->hj", np64(S[0]), k_last)
+    r_ref = np.einsum("hcj,hc->hj", S_ref[0], k_last)
+    rms = float(np.sqrt(np.mean(r_ref ** 2)))
+    assert np.max(np.abs(r_gpu - r_ref)) <= 5e-3 * rms
+    # the oracle itself retrieves v_T to the bf16 norm error of k_T
+    assert np.max(np.abs(r_ref - v_last)) <= 2e-2 * float(np.sqrt(np.mean(v_last ** 2)))
+
+
 def test_invalid_device_cu_seqlens_is_reported():
     """Without a host copy, a falling cu_seqlens is caught on the device: the workspace
     status says so, final_state is NaN and o is left untouched."""
