@@ -421,13 +421,15 @@ def run_fused_decode(steps, warmup, world, seed):
 
 
 def run_prefill_workload(which, steps, warmup, world, seed):
-    """Prefill alone on the pages' other prefill workloads, device-timed with CUDA events
+    """Prefill alone on one of the pages' prefill workloads, device-timed with CUDA events
     (bf16 o; inputs drawn on the device, so nothing here is oracle-checked: the parity
     tests cover these shapes):
+      prefill one 8192-token sequence, 12 heads, initial state ~ N(0, 0.02^2);
       varlen  8 packed sequences of U[1024, 32768] tokens (from seed 0), 32 heads, zero
               initial states;
       long    one 1,048,576-token sequence, 12 heads, then 128 recurrent decode steps on its
-              final state."""
+              final state.
+    Each timed call's inputs are larger than L2, so no flush runs between calls."""
     from linear_attention_serving_02_gb300 import kda
 
     if which == "prefill":
@@ -482,7 +484,25 @@ def run_prefill_workload(which, steps, warmup, world, seed):
         e1.synchronize()
         res["decode_128_steps_ms"] = e0.elapsed_time(e1)
     res["finite"] = bool(torch.isfinite(S).all())
+    del inp, ws, o, S
+    torch.cuda.empty_cache()
     return res
+
+
+def prefill_roofline(res, hbm, tf_burst, peak_kind):
+    """Roofline of a whole prefill call (all its kernels): the algorithmic bytes are its
+    mandatory I/O (1540 B per token-head); the DRAM traffic is the per-token-head figure of
+    the committed small-case capture (profiles/traffic.json, 8192 x 12) scaled to this
+    call's token-heads, or null once the prefill kernels have changed since the capture."""
+    th = res["tokens"] * res["heads"]
+    t = res["prefill_ms"] * 1e-3
+    gbs = PREFILL_BYTES_PER_TH * th / t / 1e9
+    tfl = PREFILL_FLOPS_PER_TH * th / t / 1e12
+    per_th = traffic_record(None, "kda_chunk_prefill")
+    return {"kernel": "kda_chunk_prefill (all its kernels)", "bound": "hbm", "achieved": gbs, "peak": hbm,
+            "unit": "GB/s", "frac": gbs / hbm, "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TH * th, "mma_tflops": tfl,
+            "mma_frac_of_bf16": tfl / tf_burst, "traffic": None if per_th is None else per_th * th}
 
 
 # ------------------------------------------------------------------------------------
@@ -512,8 +532,9 @@ def oracle_sample(pre_cpu, prefill_heads, decode_pairs, seed=0):
 
 
 def traffic_record(kernel_file, kernel_name):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
-    source of that kernel (else None)."""
+    """DRAM bytes from a committed ncu summary (profiles/traffic.json), if it was taken on
+    the current sources of that kernel (else None): bytes per launch for a kernel, bytes
+    per token-head for the whole prefill."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -526,7 +547,8 @@ def traffic_record(kernel_file, kernel_name):
                 src += f.read()
         if hashlib.sha1(src).hexdigest() != rec["sources_sha1"]:
             return None
-        return float(rec["dram_bytes_per_launch"])
+        key = "dram_bytes_per_launch" if "dram_bytes_per_launch" in rec else "dram_bytes_per_token_head"
+        return float(rec[key])
     except Exception:
         return None
 
@@ -579,6 +601,12 @@ def main_ours(args, rank, world, local):
         spec[part]["frac_of_hbm"] = spec[part]["achieved_gbs"] / hbm
     fused = run_fused_decode(max(1, min(args.steps, 50)), args.warmup, world, seed=1000 * rank)
     fused["frac_of_hbm"] = fused["achieved_gbs"] / hbm
+    # the pages' two larger prefill workloads, each on its own (a few calls: each is
+    # milliseconds long and its inputs are many times larger than L2)
+    pre_varlen = run_prefill_workload("varlen", max(1, min(args.steps, 5)), args.warmup, world, seed=1000 * rank)
+    pre_varlen["roofline"] = prefill_roofline(pre_varlen, hbm, tf_burst, peak_kind)
+    pre_long = run_prefill_workload("long", max(1, min(args.steps, 3)), args.warmup, world, seed=1000 * rank)
+    pre_long["roofline"] = prefill_roofline(pre_long, hbm, tf_burst, peak_kind)
 
     pre_t = max_over_ranks(sum(pre_ms) / 1e3, world)
     dec_t = max_over_ranks(sum(dec_ms) / 1e3, world)
@@ -600,10 +628,12 @@ def main_ours(args, rank, world, local):
     roof_dec = {"kernel": "kda_decode_kernel<128>", "bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": dec_gbs / hbm, "peak_kind": peak_kind + " (burst copy)",
                 "traffic": dec_traffic, "algorithmic_bytes_per_launch": DECODE_BYTES_PER_TH * th_dec}
+    pre_traffic = traffic_record(None, "kda_chunk_prefill")
     roof_pre = {"kernel": "kda_chunk_prefill (all its kernels)", "bound": "hbm", "achieved": pre_gbs,
                 "peak": hbm, "unit": "GB/s", "frac": pre_gbs / hbm, "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TH * th_pre,
-                "mma_tflops": pre_tflops, "mma_frac_of_bf16": pre_tflops / tf_burst, "traffic": None}
+                "mma_tflops": pre_tflops, "mma_frac_of_bf16": pre_tflops / tf_burst,
+                "traffic": None if pre_traffic is None else pre_traffic * th_pre}
     dominant = roof_dec if dec_t >= pre_t else roof_pre
 
     if rank != 0:
@@ -630,6 +660,8 @@ def main_ours(args, rank, world, local):
                     "tokens_per_s": world * K * PREFILL_T / pre_t, "ms": 1e3 * pre_launch, "roofline": roof_pre},
         "decode": {"value": world * K * DECODE_N / dec_t, "unit": "token/s (one per sequence)",
                    "token_heads_per_s": world * K * th_dec / dec_t, "ms": 1e3 * dec_launch, "roofline": roof_dec},
+        "prefill_varlen": pre_varlen,
+        "prefill_long": pre_long,
         "speculative": spec,
         "fused_decode": fused,
         "roofline": dominant,

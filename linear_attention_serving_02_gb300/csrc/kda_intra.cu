@@ -48,10 +48,10 @@
 //   all        Khat (the [W | U'] operand), Qhat, Kend^T, gamma (record), while the chain runs
 //   12 warps   A_qk -> record, A_kk -> shared memory
 //   all        the next item's q, k and the z of the one after it are requested
-//   warps 0-7  UT solve (a latency chain; running other work beside it on the same
-//              schedulers doubled its time, so the other warps wait)
-//   all        the next item's gate (its z landed long before)
-//   all        T' split; [W | U'] chain; -W and U' staged in shared memory, two bulk stores
+//   warps 0-3  the UT solve's diagonal blocks (a latency chain: running other work beside
+//              it on the same schedulers doubled its time), then all warps its other blocks
+//   all        T' split; [W | U'] chain issued; the next item's gate while it runs
+//   all        -W and U' staged in shared memory, two bulk stores
 // Inputs arrive by cp.async; every thread arrives once per load on that load's mbarrier
 // (count 512), so any warp can wait for a whole tile.
 
@@ -66,7 +66,6 @@ namespace kda {
 namespace {
 
 constexpr int kIntraThreads = 512;
-constexpr int kSolveWarps = 8;  // the UT solve's warps
 constexpr int kLdG = kD + 4;    // G row stride (floats): 528 bytes, so rows start 4 banks apart
 constexpr int kLdQK = kD + 8;   // q, k row stride (bf16): 272 bytes, likewise
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x log2(e))
@@ -85,7 +84,8 @@ struct IntraSmem {
         struct {  // after the Gram chain has completed
             float Akk[kC][kC + 4];  // rows 16-byte aligned; the pad spreads rows over banks
             float T[kC][kC + 4];
-            float X[3][kTile][kTile];  // off-diagonal block products of the solve
+            float X[2][kTile][kTile + 4];     // products of the solve's doubling steps (rows
+            float Y[2 * kTile][2 * kTile + 4];  // 16-byte aligned for float4 access)
             alignas(1024) unsigned char tp[2][kC * kC * 2];  // A of [W | U']: T' hi and lo, K-major
         } s;
         struct {  // after the [W | U'] chain has completed: the record's -W and U'
@@ -225,9 +225,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // log a = g_min sigmoid(e^A z) (z = +inf gives -5), a running sum along its rows, and
     // the quads' totals scanned over the 16 lanes of the channel quad by shuffles. Stored
     // as G log2(e). The division is __fdividef: an infinite denominator (z = -inf) gives
-    // 0, i.e. a = 1 exactly. bv is the thread's b value (threads below it.L), loaded earlier.
-    auto gate = [&](const Item &it, int b, int par, float bv) {
-        const float eA = expf(A[it.h]);
+    // 0, i.e. a = 1 exactly. pre holds the thread's b value (threads below it.L) and A_h,
+    // loaded ahead of time by gate_inputs.
+    auto gate = [&](const Item &it, int b, int par, float2 pre) {
+        const float bv = pre.x, eA = expf(pre.y);
         intra_wait(&s.bar_z[b], (uint32_t)par, fail, status);
         float *Gb = s.G[b];
         const int ro = lane & 15, cq = 2 * warp + (lane >> 4), r0 = 4 * ro, c0 = 4 * cq;
@@ -269,7 +270,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
         if (tid < kC) s.beta[b][tid] = (tid < it.L) ? sigmoid_f(bv) : 0.f;
     };
-    auto load_b = [&](const Item &it) { return tid < it.L ? bgate[(it.t0 + tid) * H + it.h] : 0.f; };
+    auto gate_inputs = [&](const Item &it) {
+        return make_float2(tid < it.L ? bgate[(it.t0 + tid) * H + it.h] : 0.f, A[it.h]);
+    };
 
     // ---- prologue: the first item's inputs and gate, the second item's z ---------------
     int item = blockIdx.x, iters = 0;
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     if (item + (int)gridDim.x < n_items) stage_z(nxt, 1);
     stage_qk(cur);
     stage_v(cur);
-    gate(cur, 0, 0, load_b(cur));
+    gate(cur, 0, 0, gate_inputs(cur));
     __syncthreads();
 
     for (; item < n_items; ++iters, item += gridDim.x) {
@@ -289,7 +292,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         uint8_t *rec = records + ((int64_t)cur.slot * H + h) * (int64_t)kRecBytes;
         const bool has_next = item + (int)gridDim.x < n_items;
         const bool has_next2 = item + 2 * (int)gridDim.x < n_items;
-        const Item nxt2 = has_next2 ? item_of(item + 2 * gridDim.x) : nxt;  // used after the solve
         const uint32_t ph = (uint32_t)(iters & 1);
 
         intra_wait(&s.bar_qk, ph, fail, status);  // this item's q and k have landed
@@ -370,6 +372,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             tc::commit(&s.bar_gram);
         }
 
+        // the item after next (its lookup reads the tables in global memory; wanted after the
+        // Gram results)
+        const Item nxt2 = has_next2 ? item_of(item + 2 * gridDim.x) : nxt;
+
         // ---- while the Gram chain runs: Khat (the [W | U'] operand), Qhat and Kend^T (the
         // ---- record); Khat and Qhat share 2^(G_j log2 e). Job (c8, j): token j, 8 channels.
         for (int job = tid; job < kC * (kD / 8); job += kIntraThreads) {
@@ -446,92 +452,98 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // next item for its gate
         if (has_next) stage_qk(nxt);
         if (has_next2) stage_z(nxt2, b);
-        const float bv = has_next ? load_b(nxt) : 0.f;
+        const float2 pre = has_next ? gate_inputs(nxt) : make_float2(0.f, 0.f);
 
-        if (warp < kSolveWarps) {
-            // ---- UT transform on warps 0-7: T = (I + A_kk)^-1, unit lower triangular ------
-            // diagonal 16 x 16 blocks, warp a solving block a: lane i holds row i of A_aa and
-            // of T_aa in registers (lanes 16-31 mirror lanes 0-15 and store nothing); T
-            // starts as I and, for m = 0 .. 14 in order, every row i > m subtracts
-            // A[i][m] * (row m, now final), broadcast by shuffles
-            if (warp < 4) {
-                const int base = warp * kTile, i = lane & 15;
-                float a[kTile], t[kTile];
+        // ---- UT transform: T = (I + A_kk)^-1, unit lower triangular ---------------------
+        // The diagonal 16 x 16 blocks on warps 0-3, warp a solving block a: lane i holds row
+        // i of A_aa and of T_aa in registers (lanes 16-31 mirror lanes 0-15 and store
+        // nothing); T starts as I and, for m = 0 .. 14 in order, every row i > m subtracts
+        // A[i][m] * (row m, now final), broadcast by shuffles. The other warps zero the
+        // blocks above the diagonal.
+        if (warp < 4) {
+            const int base = warp * kTile, i = lane & 15;
+            float a[kTile], t[kTile];
 #pragma unroll
-                for (int q4 = 0; q4 < kTile; q4 += 4) {
-                    const float4 av = *reinterpret_cast<const float4 *>(&s.u.s.Akk[base + i][base + q4]);
-                    a[q4] = av.x; a[q4 + 1] = av.y; a[q4 + 2] = av.z; a[q4 + 3] = av.w;
-                }
+            for (int q4 = 0; q4 < kTile; q4 += 4) {
+                const float4 av = *reinterpret_cast<const float4 *>(&s.u.s.Akk[base + i][base + q4]);
+                a[q4] = av.x; a[q4 + 1] = av.y; a[q4 + 2] = av.z; a[q4 + 3] = av.w;
+            }
 #pragma unroll
-                for (int j = 0; j < kTile; ++j) t[j] = (j == i) ? 1.f : 0.f;
+            for (int j = 0; j < kTile; ++j) t[j] = (j == i) ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < kTile - 1; ++m) {
+            for (int m = 0; m < kTile - 1; ++m) {
 #pragma unroll
-                    for (int j = 0; j <= m; ++j) {  // row m is zero beyond its diagonal
-                        const float tm = __shfl_sync(0xffffffffu, t[j], m, 16);
-                        if (i > m) t[j] = __fmaf_rn(-a[m], tm, t[j]);
-                    }
-                }
-                if (lane < kTile) {
-#pragma unroll
-                    for (int q4 = 0; q4 < kTile; q4 += 4)
-                        *reinterpret_cast<float4 *>(&s.u.s.T[base + i][base + q4]) =
-                            make_float4(t[q4], t[q4 + 1], t[q4 + 2], t[q4 + 3]);
-                }
-            } else {
-                for (int e = tid - 128; e < kC * kC; e += kSolveWarps * 32 - 128) {
-                    const int i = e / kC, j = e % kC;
-                    if ((j >> 4) > (i >> 4)) s.u.s.T[i][j] = 0.f;
+                for (int j = 0; j <= m; ++j) {  // row m is zero beyond its diagonal
+                    const float tm = __shfl_sync(0xffffffffu, t[j], m, 16);
+                    if (i > m) t[j] = __fmaf_rn(-a[m], tm, t[j]);
                 }
             }
-            named_sync(1, kSolveWarps * 32);
-            // off-diagonal blocks by distance l: T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb.
-            // Thread (block, row rr, column quad cq) makes four outputs.
-            for (int l = 1; l < kC / kTile; ++l) {
-                const int nblk = kC / kTile - l;
-                const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = (tid & 3) * 4;
-                const int bb = blk, a = bb + l;
-                if (tid < nblk * 64) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int m = bb; m < a; ++m) {
+            if (lane < kTile) {
 #pragma unroll
-                        for (int x4 = 0; x4 < kTile; x4 += 4) {
-                            const float4 av =
-                                *reinterpret_cast<const float4 *>(&s.u.s.Akk[a * kTile + rr][m * kTile + x4]);
-                            const float am[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const float4 tv =
-                                    *reinterpret_cast<const float4 *>(&s.u.s.T[m * kTile + x4 + u][bb * kTile + cq]);
-                                acc.x += am[u] * tv.x; acc.y += am[u] * tv.y;
-                                acc.z += am[u] * tv.z; acc.w += am[u] * tv.w;
-                            }
-                        }
-                    }
-                    *reinterpret_cast<float4 *>(&s.u.s.X[blk][rr][cq]) = acc;
-                }
-                named_sync(1, kSolveWarps * 32);
-                if (tid < nblk * 64) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int x4 = 0; x4 < kTile; x4 += 4) {
-                        const float4 tv = *reinterpret_cast<const float4 *>(&s.u.s.T[a * kTile + rr][a * kTile + x4]);
-                        const float tm[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float4 xv = *reinterpret_cast<const float4 *>(&s.u.s.X[blk][x4 + u][cq]);
-                            acc.x += tm[u] * xv.x; acc.y += tm[u] * xv.y;
-                            acc.z += tm[u] * xv.z; acc.w += tm[u] * xv.w;
-                        }
-                    }
-                    *reinterpret_cast<float4 *>(&s.u.s.T[a * kTile + rr][bb * kTile + cq]) =
-                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-                }
-                named_sync(1, kSolveWarps * 32);
+                for (int q4 = 0; q4 < kTile; q4 += 4)
+                    *reinterpret_cast<float4 *>(&s.u.s.T[base + i][base + q4]) =
+                        make_float4(t[q4], t[q4 + 1], t[q4 + 2], t[q4 + 3]);
+            }
+        } else {
+            for (int e = tid - 128; e < kC * kC; e += kIntraThreads - 128) {
+                const int i = e / kC, j = e % kC;
+                if ((j >> 4) > (i >> 4)) s.u.s.T[i][j] = 0.f;
             }
         }
         __syncthreads();
-        if (has_next) gate(nxt, b ^ 1, ((iters + 1) >> 1) & 1, bv);  // the next item's gate
+        // The blocks below the diagonal by doubling, the sums in k order:
+        //   16 -> 32:  T_10 = -T_11 (A_10 T_00),  T_32 = -T_33 (A_32 T_22)
+        //   32 -> 64:  T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32])
+        // (the inverse of a block lower triangular matrix, one halving of the block size at a
+        // time: four dependent products instead of the six of a block-by-block solve). Each
+        // thread makes 4 consecutive columns of one row with float4 loads; a warp spans a
+        // few rows and all column quads, so its loads are broadcasts or one 128-byte row.
+        auto dot4 = [&](const float *arow, const float *bmat, int ldb, int k0, int k1, float4 &acc) {
+            for (int k = k0; k < k1; k += 4) {
+                const float4 av = *reinterpret_cast<const float4 *>(arow + k);
+                const float am[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 bv = *reinterpret_cast<const float4 *>(bmat + (k + u) * ldb);
+                    acc.x = __fmaf_rn(am[u], bv.x, acc.x);
+                    acc.y = __fmaf_rn(am[u], bv.y, acc.y);
+                    acc.z = __fmaf_rn(am[u], bv.z, acc.z);
+                    acc.w = __fmaf_rn(am[u], bv.w, acc.w);
+                }
+            }
+        };
+        if (tid < 128) {  // X[p] = A_(2p+1, 2p) T_(2p, 2p): thread (p, row r, column quad cq)
+            const int p = tid >> 6, r = (tid >> 2) & 15, cq = tid & 3;
+            const int r0 = 16 * (2 * p + 1), c0 = 32 * p;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            dot4(&s.u.s.Akk[r0 + r][c0], &s.u.s.T[c0][c0 + 4 * cq], kC + 4, 0, kTile, acc);
+            *reinterpret_cast<float4 *>(&s.u.s.X[p][r][4 * cq]) = acc;
+        }
+        __syncthreads();
+        if (tid < 128) {  // T_(2p+1, 2p) = -T_(2p+1, 2p+1) X[p]
+            const int p = tid >> 6, r = (tid >> 2) & 15, cq = tid & 3;
+            const int r0 = 16 * (2 * p + 1), c0 = 32 * p;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            dot4(&s.u.s.T[r0 + r][r0], &s.u.s.X[p][0][4 * cq], kTile + 4, 0, kTile, acc);
+            *reinterpret_cast<float4 *>(&s.u.s.T[r0 + r][c0 + 4 * cq]) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        __syncthreads();
+        if (tid < 256) {  // Y = A[32:64, 0:32] T[0:32, 0:32]: thread (row r, column quad cq);
+                          // T[k][16 ..] = 0 for k < 16
+            const int r = tid >> 3, cq = tid & 7;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            dot4(&s.u.s.Akk[2 * kTile + r][0], &s.u.s.T[0][4 * cq], kC + 4, cq < 4 ? 0 : kTile, 2 * kTile, acc);
+            *reinterpret_cast<float4 *>(&s.u.s.Y[r][4 * cq]) = acc;
+        }
+        __syncthreads();
+        if (tid < 256) {  // T[32 + r, 0:32] = -T[32 + r, 32:64] Y; T[32 + r][48 ..] = 0 for r < 16
+            const int r = tid >> 3, cq = tid & 7;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            dot4(&s.u.s.T[2 * kTile + r][2 * kTile], &s.u.s.Y[0][4 * cq], 2 * kTile + 4, 0,
+                 r < kTile ? kTile : 2 * kTile, acc);
+            *reinterpret_cast<float4 *>(&s.u.s.T[2 * kTile + r][4 * cq]) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        __syncthreads();
 
         // ---- T' = T Diag(beta), split: the A operand of [W | U'] (K-major, M = 64 rows i,
         // ---- K = 64 tokens j; 8-token groups outermost) ------------------------------------
@@ -569,6 +581,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             }
             tc::commit(&s.bar_wu);
         }
+        // while the [W | U'] chain runs: the next item's gate (its z landed long before)
+        if (has_next) gate(nxt, b ^ 1, ((iters + 1) >> 1) & 1, pre);
         intra_wait(&s.bar_wu, ph, fail, status);
         tc::fence_after_sync();
         // the V half of the operand is free: the next item's v comes in behind the epilogue
