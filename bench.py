@@ -489,6 +489,35 @@ def run_prefill_workload(which, steps, warmup, world, seed):
     return res
 
 
+def run_decode_only(steps, warmup, world, seed):
+    """The decode step alone (256 sequences x 96 heads, 1.6 GB state updated in place), for
+    kernel counters on a small process; L2 flushed between steps."""
+    from linear_attention_serving_02_gb300 import kda
+
+    state = inputs.decode_state(DECODE_N, DECODE_H, seed=seed + 1, device="cuda")
+    dec = [inputs.decode_step_inputs(DECODE_N, DECODE_H, seed=seed + 1, step=i, device="cuda") for i in range(4)]
+    o = torch.empty((DECODE_N, DECODE_H, D), dtype=torch.float32, device="cuda")
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        flush()
+        d = dec[i % len(dec)]
+        kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["z"], d["A"], d["b"], state, o=o)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush()
+        d = dec[(warmup + j) % len(dec)]
+        evs[j][0].record(stream)
+        kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["z"], d["A"], d["b"], state, o=o)
+        evs[j][1].record(stream)
+    torch.cuda.synchronize()
+    t = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e-3, world)
+    nbytes = DECODE_BYTES_PER_TH * DECODE_N * DECODE_H
+    return {"sequences": DECODE_N, "heads": DECODE_H, "ms": 1e3 * t, "achieved_gbs": nbytes / t / 1e9,
+            "finite": bool(torch.isfinite(state).all())}
+
+
 def prefill_roofline(res, hbm, tf_burst, peak_kind):
     """Roofline of a whole prefill call (all its kernels): the algorithmic bytes are its
     mandatory I/O (1540 B per token-head); the DRAM traffic is the per-token-head figure of
@@ -682,9 +711,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--part", choices=["all", "speculative", "fused", "prefill", "varlen", "long"], default="all",
-                    help="'speculative' times only the verify + fold pair, 'fused' only the fused decode "
-                         "(each about 3 GB on the device; for profiling); 'prefill', 'varlen' and 'long' "
+    ap.add_argument("--part", choices=["all", "speculative", "fused", "decode", "prefill", "varlen", "long"],
+                    default="all",
+                    help="'speculative' times only the verify + fold pair, 'fused' only the fused decode, "
+                         "'decode' only the decode step (each 2-3 GB on the device; for profiling); "
+                         "'prefill', 'varlen' and 'long' "
                          "time only the prefill of the 8192-token 12-head sequence (under 0.5 GB on the "
                          "device: the small case for kernel counters), of the packed 8 x U[1024, 32768] x "
                          "32-head batch and of the 1M-token sequence; each prints its object")
@@ -701,7 +732,7 @@ def main():
             if args.part in ("prefill", "varlen", "long"):
                 res = run_prefill_workload(args.part, args.steps, args.warmup, world, seed=1000 * rank)
             else:
-                run = run_speculative if args.part == "speculative" else run_fused_decode
+                run = {"speculative": run_speculative, "fused": run_fused_decode, "decode": run_decode_only}[args.part]
                 res = run(args.steps, args.warmup, world, seed=1000 * rank)
             if rank == 0:
                 print(json.dumps({args.part: res}), flush=True)

@@ -160,8 +160,8 @@ int kda_workspace_status(const void *workspace, void *stream);
  *
  *   - A batch whose workspace (kda_chunk_prefill_workspace_size(total_tokens, num_seqs,
  *     num_heads)) exceeds KDA_NOALLOC_SCRATCH_BYTES is refused with KDA_ERR_WORKSPACE
- *     before anything is launched. 64 MiB holds, for example, 2048 tokens x 8 heads or
- *     1536 tokens x 12 heads.
+ *     before anything is launched. 64 MiB holds, for example, 3072 tokens x 8 heads or
+ *     2048 tokens x 12 heads.
  *   - The first call on a device looks up the scratch's device address on that device
  *     (cudaGetSymbolAddress, with the device current); make that first call before any
  *     stream capture. The address is kept for the life of the process, so do not use
