@@ -189,15 +189,15 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // z of an item into G buffer b, q and k, v: every thread copies its 16-byte units with
     // cp.async and arrives on the load's mbarrier when they have landed. Rows of z past the
     // sequence end are not copied (the gate ignores them); those of q, k, v are zeroed.
-    auto stage_z = [&](const Item &it, int b) {
-        for (int e = tid; e < it.L * (kD / 4); e += kIntraThreads) {
+    auto stage_z = [&](const Item &it, int b, int t0 = 0, int nt = kIntraThreads) {
+        for (int e = tid - t0; e >= 0 && e < it.L * (kD / 4); e += nt) {
             const int i = e / (kD / 4), c = (e % (kD / 4)) * 4;
             cp_async16(s.G[b] + i * kLdG + c, z + (it.t0 + i) * rowstride + (int64_t)it.h * kD + c);
         }
         cp_async_arrive(&s.bar_z[b]);
     };
-    auto stage_qk = [&](const Item &it) {
-        for (int e = tid; e < 2 * kC * (kD / 8); e += kIntraThreads) {
+    auto stage_qk = [&](const Item &it, int t0 = 0, int nt = kIntraThreads) {
+        for (int e = tid - t0; e >= 0 && e < 2 * kC * (kD / 8); e += nt) {
             const int which = e & 1, i = (e >> 1) / (kD / 8), c = ((e >> 1) % (kD / 8)) * 8;
             __nv_bfloat16 *dst = (which ? s.k : s.q) + i * kLdQK + c;
             if (i < it.L)
@@ -447,11 +447,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
         tc::fence_before_sync();
         __syncthreads();
-        // q, k and this item's G are read no more: the next item's q and k, and the z of
-        // the item after it (into this G buffer), come in behind the rest; so does b of the
-        // next item for its gate
-        if (has_next) stage_qk(nxt);
-        if (has_next2) stage_z(nxt2, b);
         const float2 pre = has_next ? gate_inputs(nxt) : make_float2(0.f, 0.f);
 
         // ---- UT transform: T = (I + A_kk)^-1, unit lower triangular ---------------------
@@ -489,6 +484,15 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 const int i = e / kC, j = e % kC;
                 if ((j >> 4) > (i >> 4)) s.u.s.T[i][j] = 0.f;
             }
+            // q, k and this item's G are read no more: the next item's q and k, and the z of
+            // the item after it (into this G buffer), are requested by these warps while
+            // warps 0-3 solve (every thread still arrives on the loads' mbarriers)
+            if (has_next) stage_qk(nxt, 128, kIntraThreads - 128);
+            if (has_next2) stage_z(nxt2, b, 128, kIntraThreads - 128);
+        }
+        if (warp < 4) {
+            if (has_next) cp_async_arrive(&s.bar_qk);
+            if (has_next2) cp_async_arrive(&s.bar_z[b]);
         }
         __syncthreads();
         // The blocks below the diagonal by doubling, the sums in k order:
