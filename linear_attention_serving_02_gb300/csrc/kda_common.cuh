@@ -116,19 +116,34 @@ struct SegPlan {
 // Segment length (in chunks) of the segmented walk, or 0 for a plain walk. A pure
 // function of the batch size, so that the workspace size can be computed without a
 // device: segments pay when there are fewer (sequence, head) chains than about a wave
-// of the GPU's 152 SMs and the chains are long.
+// of the GPU's 152 SMs and the chains are long. The length minimises a cost model of
+// the three phases, in units of one output-walk chunk step, fitted to measured walks:
+// with S segments of P chunks, phase A runs 2 S - 3 map walks per chain in
+// ceil((2 S - 3) chains / 152) waves of P + 2 steps (a map step costs about 0.83 of an
+// output step; the 2 covers a walk's start and end), the combine S - 2 chained products
+// (about 1.2 steps each), and phase C S walks per chain in ceil(S chains / 152) waves of
+// P + 2 steps. For 8192 tokens x 12 heads this keeps 7 segments of 19 chunks; for
+// 1,048,576 tokens x 12 heads it takes 38 segments of 432 chunks (phase A in six waves).
 __host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
     const int64_t chains = num_seqs * num_heads;
     if (chains <= 0) return 0;
     const int64_t slots = chunk_bound(total_tokens, num_seqs);
     const int64_t avg = slots / num_seqs;
     if (chains * 2 >= 152 || avg < 24) return 0;
-    // phase A runs 2 S - 3 walks per chain: at most one wave
-    int64_t S = (152 / chains + 3) / 2;
-    if (S < 2) S = 2;
-    int64_t P = (avg + S - 1) / S;
-    if (P < 4) P = 4;
-    return (int)P;
+    int64_t best_p = 4;
+    double best = 1e300;
+    for (int64_t S = 2; S <= 64; ++S) {
+        int64_t P = (avg + S - 1) / S;
+        if (P < 4) P = 4;
+        const int64_t segs = (avg + P - 1) / P;  // the segments a chain of avg chunks gets
+        const int64_t waves_a = ((2 * segs - 3) * chains + 151) / 152, waves_c = (segs * chains + 151) / 152;
+        const double cost = 0.83 * (double)(waves_a * (P + 2)) + 1.2 * (double)(segs - 2) + (double)(waves_c * (P + 2));
+        if (cost < best) {
+            best = cost;
+            best_p = P;
+        }
+    }
+    return (int)best_p;
 }
 __host__ __device__ inline int64_t segment_bound(int64_t total_tokens, int64_t num_seqs, int P) {
     return (chunk_bound(total_tokens, num_seqs) + (int64_t)(P - 1) * num_seqs) / P;
