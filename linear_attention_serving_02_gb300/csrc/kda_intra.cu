@@ -355,12 +355,13 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         __syncthreads();
         if (tid == 0) {
             // 8 k-steps of 16 channels: A hi x B hi and A lo x B hi (N = 192), A hi x B lo on
-            // the q rows (N = 96, the first 96 columns)
+            // the q rows (N = 96, the first 96 columns); unrolled, as issuing MMAs from one
+            // thread in a loop cost ~90 cycles each
             tc::fence_after_sync();
             if (!fail) {
                 const uint32_t idG = tc::idesc_bf16(128, 192, 0), idQ = tc::idesc_bf16(128, 96, 0);
                 const uint32_t bh = tc::smem_addr(s.u.g.hi), bl = tc::smem_addr(s.u.g.lo);
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint64_t dh = tc::desc(bh + (uint32_t)ks * 6144u, 3072u, 128u);
                     const uint64_t dl = tc::desc(bl + (uint32_t)ks * 3072u, 1536u, 128u);
@@ -576,7 +577,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 const uint32_t idW = tc::idesc_bf16(64, 256, 1);
                 const uint32_t th = tc::smem_addr(s.u.s.tp[0]), tl = tc::smem_addr(s.u.s.tp[1]);
                 const uint32_t kvb = tc::smem_addr(s.kv);
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint64_t bd = tc::desc(kvb + (uint32_t)ks * 256u, 128u, 1024u);
                     tc::mma_ss(D_W, tc::desc(th + (uint32_t)ks * 2048u, 1024u, 128u), bd, idW, ks > 0);

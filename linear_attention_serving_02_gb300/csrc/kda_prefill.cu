@@ -358,16 +358,19 @@ __global__ void __launch_bounds__(kCombineThreads)
 //
 // Eight warps with fixed roles:
 //   warps 0-3  U and O: thread = value channel dv (TMEM lane dv). After group 1 they
-//              build U^T (and start loading the next chunk's U'); after group 2 they
-//              update key rows 64-127 of S and write their S^T planes, stage o in
-//              shared memory from the output accumulators, and store it in 16-byte row
-//              chunks while the next chunk's group 1 runs.
+//              build U^T, then copy the next chunk's U' and [ -W ; Qhat ] into shared
+//              memory while group 2 runs; after group 2 they update key rows 64-127 of
+//              S and write their S^T planes, stage o in shared memory from the output
+//              accumulators, and store it in 16-byte row chunks while the next chunk's
+//              group 1 runs.
 //   warps 4-7  state: thread = value channel dv, key rows 0-63 of S. After group 2
-//              they update those rows and write their S^T planes. Thread 128 also
-//              issues the MMAs and the bulk copies: [ -W ; Qhat ] one chunk ahead,
-//              [ A_qk ; Kend^T ] two chunks ahead into two slots, and waits for them
-//              off the chain. (An L2 prefetch of later records measured slower: it
-//              holds the copy engine.)
+//              they update those rows and write their S^T planes, then copy the
+//              [ A_qk ; Kend^T ] of the chunk after next into the slot group 2 has freed.
+//              Thread 128 also issues the MMAs.
+// The record tiles move by 16-byte cp.async, issued by the warps that wait anyway at
+// that point: a bulk copy held its issuing thread for up to a thousand cycles, and on
+// the MMA thread that sat on the chain. Each copying thread waits for its own copies and
+// fences them for the tensor cores' proxy before the barrier that hands the tile over.
 // The state rows and U' live in fp32 registers as packed pairs (rows 2j, 2j + 1; tokens
 // 2j, 2j + 1), so the update, U = U' + D_U and the split into bf16 planes run on the
 // two-lane FP32 instructions.
@@ -380,10 +383,11 @@ __global__ void __launch_bounds__(kCombineThreads)
 struct WalkSmem {
     unsigned char wq[kRecWQBytes];       // -W, Qhat hi, Qhat lo (rows 0..63, 64..127, 64..127)
     unsigned char ak[2][2 * kStackAK];   // [ A_qk ; Kend^T ] hi | lo, of chunks c (slot c & 1)
+    alignas(16) float up[kC * kD];       // U' of the current chunk, rows as in the record
     alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1), the state warps' copy
     alignas(16) float gam_uo[2][kD];     // the same, the U and O warps' copy
     unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
-    uint64_t bar_wq, bar_ak[2], bar_m1, bar_m2;
+    uint64_t bar_m1, bar_m2;
     uint32_t tmem_base;
     int fail;
 };
@@ -461,9 +465,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            tc::mbar_init(&s.bar_wq, 1);
-            tc::mbar_init(&s.bar_ak[0], 1);
-            tc::mbar_init(&s.bar_ak[1], 1);
             tc::mbar_init(&s.bar_m1, 1);
             tc::mbar_init(&s.bar_m2, 1);
             tc::mbar_init_fence();
@@ -487,16 +488,38 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     // this thread's half of its value column of S: key rows 0 .. 63 in the state warps,
     // 64 .. 127 in the U and O warps, so that both halves are updated at the same time
     uint64_t Sh[32];  // key rows 2j, 2j + 1 of this half as one packed pair
+    // tokens 32 half .. 32 half + 31 of o = D_O1 + D_O2 for this thread's value channel,
+    // into the [token][channel] staging tile (fp32, or bf16 in its first half)
+    auto stage_o = [&](int half) {
+        uint32_t d1[32], d2[32];
+        tc::fence_after_sync();
+        tc::tmem_ld32_nowait(D_UO + lanes + 64 + 32 * half, d1);
+        tc::tmem_ld32_nowait(D_AK + lanes + 32 * half, d2);
+        tc::tmem_wait_ld();
+        float *stage = reinterpret_cast<float *>(s.ut);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int i = 32 * half + j;
+            const float ov = __uint_as_float(d1[j]) + __uint_as_float(d2[j]);
+            if (o_f32)
+                stage[i * kD + dv] = ov;
+            else
+                reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov);
+        }
+    };
     if (warp < 4) {
         // ------------- U and O warps; they also hold key rows 64 .. 127 of S -------------
-        uint64_t Upr[32];  // U' of tokens 2j, 2j + 1 of this value channel as one packed pair
-        // U' row i holds its 16-byte units (4 channels) XOR-swizzled by i % 32
+        // U' row i holds its 16-byte units (4 channels) XOR-swizzled by i % 32: a warp's
+        // reads of one row hit 32 distinct banks
         auto up_at = [&](int i) { return i * kD + ((((dv >> 2) ^ (i & 31))) << 2) + (dv & 3); };
-        auto load_up = [&](int c) {
-            const float *up = reinterpret_cast<const float *>(rec_of(c) + kRecUp);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                Upr[j] = add_up ? pk2(up[up_at(2 * j)], up[up_at(2 * j + 1)]) : pk2(0.f, 0.f);
+        // chunk c's U' and [ -W ; Qhat ] (a map walk: -W alone) by this thread's share of
+        // 16-byte units, as one cp.async group
+        auto copy_up_wq = [&](int c) {
+            const unsigned char *rec = rec_of(c);
+            const int wq_units = (maps ? kPlaneQK : kRecWQBytes) / 16;
+            for (int u = tid; u < wq_units; u += 128) cp_async16(s.wq + 16 * u, rec + kRecW + 16 * u);
+            if (add_up)
+                for (int u = tid; u < kC * kD / 4; u += 128) cp_async16(s.up + 4 * u, rec + kRecUp + 16 * u);
         };
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -508,7 +531,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         for (int j = 0; j < 32; j += 16)
             split32_tmem_pk(&Sh[j], tmem + lanes + kColSHi + 32 + j, tmem + lanes + kColSLo + 32 + j);
         tc::tmem_wait_st();
-        if (c_begin < c_end) load_up(c_begin);
+        if (c_begin < c_end) copy_up_wq(c_begin);
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async();  // the first [ -W ; Qhat ], for group 1
+        named_sync(5, 128);   // the first U', for every U and O thread
         tc::fence_before_sync();
         named_arrive(kBarOR, 256);  // initial planes of rows 64 .. 127 written; nothing to read yet
         for (int c = c_begin; c < c_end; ++c) {
@@ -516,6 +543,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const int64_t t0 = t_begin + (int64_t)(c - c_begin) * kC;
             const int L = (int)min((int64_t)kC, t_end - t0);
             const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
+            // U' of this chunk into registers while group 1 runs
+            uint64_t Upr[32];  // U' of tokens 2j, 2j + 1 of this value channel as one packed pair
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                Upr[j] = add_up ? pk2(s.up[up_at(2 * j)], s.up[up_at(2 * j + 1)]) : pk2(0.f, 0.f);
             // U^T = U'^T + D_U, written as split planes for group 2
             if (wait_in_order(&s.bar_m1, ph, fail)) {
                 tc::fence_after_sync();
@@ -535,10 +567,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             tc::fence_before_sync();
             named_arrive(kBarU, 256);  // U^T planes complete; group 1 is done with [ -W ; Qhat ]
             s.gam_uo[ph][dv] = gnext;
-            // U' of the next chunk: issued now, ahead of this chunk's output stores, so that
-            // it does not queue behind them (the registers are free once the planes are out)
-            if (c + 1 < c_end) load_up(c + 1);
-            named_sync(5, 128);  // gamma of this chunk in place (this group's copy)
+            named_sync(5, 128);  // gamma of this chunk in place (this group's copy); U' read
+            // the next chunk's U' and [ -W ; Qhat ] land while group 2 runs (this thread saw
+            // group 1 complete, so the buffer is free)
+            if (c + 1 < c_end && !fail) copy_up_wq(c + 1);
+            cp_async_commit();
             const bool m2ok = wait_in_order(&s.bar_m2, ph, fail);
             // S <- Diag(gamma) S + D_S on key rows 64 .. 127, and their split planes
             {
@@ -566,34 +599,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 split32_tmem_pk(&Sh[16], tmem + lanes + kColSHi + 48, tmem + lanes + kColSLo + 48);
                 tc::tmem_wait_st();
             }
-            // o = (D_O1 + D_O2)^T for this thread's value channel, staged as [token][channel]
-            // in shared memory (the previous chunk's tile has been written out)
+            // tokens 0 .. 31 of o = (D_O1 + D_O2)^T for this thread's value channel, staged
+            // as [token][channel] in shared memory (the state warps stage tokens 32 .. 63)
             const bool ok = m2ok && write_o;
-            if (ok) {
-                float *stage = reinterpret_cast<float *>(s.ut);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t d1[32], d2[32];
-                    tc::tmem_ld32_nowait(D_UO + lanes + 64 + 32 * half, d1);
-                    tc::tmem_ld32_nowait(D_AK + lanes + 32 * half, d2);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int i = 32 * half + j;
-                        const float ov = __uint_as_float(d1[j]) + __uint_as_float(d2[j]);
-                        if (o_f32)
-                            stage[i * kD + dv] = ov;
-                        else
-                            reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov);
-                    }
-                }
-            }
+            if (ok) stage_o(0);
+            cp_async_wait<0>();
+            fence_proxy_async();  // the next [ -W ; Qhat ] in place, for group 1
             tc::fence_before_sync();
-            named_arrive(kBarOR, 256);  // rows 64 .. 127 of the next S^T planes written, D_S and
-                                        // the output accumulators read: the next group 1 may start
+            named_sync(kBarOR, 256);  // rows 64 .. 127 of the next S^T planes written, D_S and
+                                      // the output accumulators read: the next group 1 may start.
+                                      // Also: the whole o tile staged, the next U' visible.
             // write the staged tile out in 16-byte row chunks while the next group 1 runs
-            if (write_o) {  // uniform over the CTA: the named barriers below stay matched
-                named_sync(5, 128);
+            if (write_o) {  // uniform over the CTA: the named barrier below stays matched
                 if (ok) {
                     const float *stage = reinterpret_cast<const float *>(s.ut);
                     const int chunks_per_row = o_f32 ? kD / 4 : kD / 8;  // 16-byte chunks
@@ -620,70 +637,57 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // [ A_qk ; Kend^T ] is stored MN-major (its rows n contiguous per token): B transposed
         const uint32_t kIdG2 = tc::idesc_bf16(128, maps ? 128 : 192, 1);
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
-        // phase bookkeeping (issuer); the [ A_qk ; Kend^T ] slot of chunk c is (c - c_begin) & 1
-        int n_wq = 0, w_wq = 0, n_m1 = 0, n_m2 = 0, n_ak0 = 0, n_ak1 = 0, w_ak0 = 0, w_ak1 = 0;
-        auto issue_wq = [&](int c) {
-            const uint32_t bytes = (uint32_t)(maps ? kPlaneQK : kRecWQBytes);  // -W only, or all three
-            tc::mbar_arrive_expect_tx(&s.bar_wq, bytes);
-            tc::bulk_g2s(s.wq, rec_of(c) + kRecW, bytes, &s.bar_wq);
-            ++n_wq;
-        };
-        auto issue_ak = [&](int c) {
-            const int slot = (c - c_begin) & 1;
-            unsigned char *dst = s.ak[slot];
-            uint64_t *bar = &s.bar_ak[slot];
-            if (maps) {  // the Kend^T rows of the hi and the lo plane
-                tc::mbar_arrive_expect_tx(bar, (uint32_t)(2 * kPlaneKT));
-                tc::bulk_g2s(dst + kPlaneCC, rec_of(c) + kRecAK + kPlaneCC, (uint32_t)kPlaneKT, bar);
-                tc::bulk_g2s(dst + kStackAK + kPlaneCC, rec_of(c) + kRecAK + kStackAK + kPlaneCC, (uint32_t)kPlaneKT,
-                             bar);
+        int n_m1 = 0, n_m2 = 0;  // MMA groups committed (issuer)
+        // chunk c's [ A_qk ; Kend^T ] into slot (c - c_begin) & 1 by this thread's share of
+        // 16-byte units (a map walk: the Kend^T rows of the hi and the lo plane)
+        auto copy_ak = [&](int c) {
+            unsigned char *dst = s.ak[(c - c_begin) & 1];
+            const unsigned char *src = rec_of(c) + kRecAK;
+            if (maps) {
+                for (int u = tid - 128; u < kPlaneKT / 16; u += 128) {
+                    cp_async16(dst + kPlaneCC + 16 * u, src + kPlaneCC + 16 * u);
+                    cp_async16(dst + kStackAK + kPlaneCC + 16 * u, src + kStackAK + kPlaneCC + 16 * u);
+                }
             } else {
-                tc::mbar_arrive_expect_tx(bar, (uint32_t)(2 * kStackAK));
-                tc::bulk_g2s(dst, rec_of(c) + kRecAK, (uint32_t)(2 * kStackAK), bar);
+                for (int u = tid - 128; u < 2 * kStackAK / 16; u += 128) cp_async16(dst + 16 * u, src + 16 * u);
             }
-            ++(slot ? n_ak1 : n_ak0);
         };
-        // group 1 of chunk c: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
-        // The copy waits run off the chain (an mbarrier wait costs a few hundred cycles
-        // even when the data has long landed; right after a barrier it held the group's
-        // issue that long): chunk c + 1's [ A_qk ; Kend^T ] while chunk c's group 2 runs,
-        // its [ -W ; Qhat ] at the end of chunk c's state update.
-        auto wait_wq = [&](int c) {
-            if (!wait_or_fail(&s.bar_wq, (uint32_t)((c - c_begin) & 1), fail)) return false;
-            ++w_wq;
-            return true;
-        };
-        auto wait_ak = [&](int c) {
-            const int slot = (c - c_begin) & 1;
-            if (!wait_or_fail(&s.bar_ak[slot], (uint32_t)(((c - c_begin) >> 1) & 1), fail)) return false;
-            ++(slot ? w_ak1 : w_ak0);
-            return true;
-        };
-        auto issue_g1 = [&](int c, bool ready) {
+        // group 1 of the next chunk: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
+        auto issue_g1 = [&]() {
             tc::fence_after_sync();
-            if (ready) {
+            if (!fail) {
                 // S^T hi and lo times the hi plane of [ -W ; Qhat ], and S^T hi times Qhat lo
                 // into the D_O1 half (W has one plane; a map walk has no Qhat)
+                // (unrolled: a loop issuing from one thread cost ~90 cycles per MMA, about
+                // what an N = 128 MMA takes to run)
                 const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)(2 * kPlaneQK);
-#pragma unroll 1
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t a0 = tmem + kColSHi + 8 * ks, a1 = tmem + kColSLo + 8 * ks;
-                    const uint64_t b0 = tc::desc_k(b0s, kD, ks);
-                    tc::mma_ts(D_UO, a0, b0, kIdG1, ks > 0);
-                    tc::mma_ts(D_UO, a1, b0, kIdG1, 1);
-                    if (!maps) tc::mma_ts(D_UO + 64, a0, tc::desc_k(b1s, kD, ks), kIdQl, 1);
+                if (maps) {
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint64_t b0 = tc::desc_k(b0s, kD, ks);
+                        tc::mma_ts(D_UO, tmem + kColSHi + 8 * ks, b0, kIdG1, ks > 0);
+                        tc::mma_ts(D_UO, tmem + kColSLo + 8 * ks, b0, kIdG1, 1);
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint64_t b0 = tc::desc_k(b0s, kD, ks);
+                        tc::mma_ts(D_UO, tmem + kColSHi + 8 * ks, b0, kIdG1, ks > 0);
+                        tc::mma_ts(D_UO, tmem + kColSLo + 8 * ks, b0, kIdG1, 1);
+                        tc::mma_ts(D_UO + 64, tmem + kColSHi + 8 * ks, tc::desc_k(b1s, kD, ks), kIdQl, 1);
+                    }
                 }
             }
             tc::commit(&s.bar_m1);  // also after a failure: the U and O warps wait for it in order
             ++n_m1;
         };
         // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T
-        auto issue_g2 = [&](int c, bool ready) {
+        auto issue_g2 = [&](int c) {
             tc::fence_after_sync();
             const int slot = (c - c_begin) & 1;
-            if (ready) {
+            if (!fail) {
                 const uint32_t b0s = tc::smem_addr(s.ak[slot]) + ak_off, b1s = b0s + (uint32_t)kStackAK;
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint32_t a0 = tmem + kColUHi + 8 * ks, a1 = tmem + kColULo + 8 * ks;
                     const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
@@ -696,13 +700,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             ++n_m2;
         };
 
-        // the first chunk's record (and the second's [ A_qk ; Kend^T ]) are copied while
-        // the initial state is read
-        if (issuer && c_begin < c_end) {
-            issue_wq(c_begin);
-            issue_ak(c_begin);
-            if (c_begin + 1 < c_end) issue_ak(c_begin + 1);
-        }
+        // the first two chunks' [ A_qk ; Kend^T ] are copied while the initial state is read:
+        // one cp.async group per chunk, here and in every step, so that the group of chunk
+        // c is always the second newest when its group 2 is issued
+        if (c_begin < c_end) copy_ak(c_begin);
+        cp_async_commit();
+        if (c_begin + 1 < c_end) copy_ak(c_begin + 1);
+        cp_async_commit();
         // key rows 0 .. 63 of this thread's value column (the U and O warps hold the rest)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -716,30 +720,19 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         tc::tmem_wait_st();
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
-        bool wq_ok = false, ak_ok = false;
-        if (issuer && c_begin < c_end) {
-            wq_ok = wait_wq(c_begin);
-            ak_ok = wait_ak(c_begin);
-        }
-        __syncwarp();
         named_sync(kBarOR, 256);
-        if (issuer && c_begin < c_end) issue_g1(c_begin, wq_ok);
+        if (issuer && c_begin < c_end) issue_g1();
         __syncwarp();
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
             const float gnext = reinterpret_cast<const float *>(rec_of(c) + kRecGam)[dv];
-            // the next [ -W ; Qhat ] copy starts as soon as group 1 of this chunk is done
-            // with the buffer, before the U epilogue
-            if (issuer && c + 1 < c_end && wait_or_fail(&s.bar_m1, ph, fail)) issue_wq(c + 1);
+            cp_async_wait<1>();   // this thread's share of chunk c's [ A_qk ; Kend^T ]
+            fence_proxy_async();  // ... for group 2
             __syncwarp();
             named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
-            if (issuer) issue_g2(c, ak_ok);
-            // while group 2 runs: the next chunk's [ A_qk ; Kend^T ] (issued a chunk ago)
-            if (issuer) ak_ok = c + 1 < c_end && wait_ak(c + 1);
+            if (issuer) issue_g2(c);
             __syncwarp();
             const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
-            // group 2 is done with this slot of [ A_qk ; Kend^T ]: the chunk after next lands there
-            if (issuer && ok && c + 2 < c_end) issue_ak(c + 2);
             s.gam[ph][dv] = gnext;
             named_sync(4, 128);  // gamma of this chunk in place
             // S <- Diag(gamma) S + D_S on key rows 0 .. 63 and their split planes, in blocks
@@ -771,27 +764,28 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 }
             }
             tc::tmem_wait_st();
+            if (ok && write_o) stage_o(1);  // tokens 32 .. 63 of o (the U and O warps store the tile)
             tc::fence_before_sync();
-            wq_ok = false;  // the next chunk's [ -W ; Qhat ], issued after this chunk's group 1
-            if (issuer && c + 1 < c_end) wq_ok = wait_wq(c + 1);
-            __syncwarp();
             named_sync(4, 128);       // rows 0 .. 63 of the next S^T planes complete
-            named_sync(kBarOR, 256);  // the U and O warps have written rows 64 .. 127 and read
-                                      // this chunk's D_S and output accumulators
-            if (issuer && c + 1 < c_end) issue_g1(c + 1, wq_ok);
+            named_sync(kBarOR, 256);  // the U and O warps have written rows 64 .. 127, read this
+                                      // chunk's D_S and output accumulators, and copied the next
+                                      // [ -W ; Qhat ]
+            if (issuer && c + 1 < c_end) issue_g1();
             __syncwarp();
+            // group 2 is done with this slot (every state thread saw it complete): the chunk
+            // after next lands there while the next groups run
+            if (ok && c + 2 < c_end) copy_ak(c + 2);
+            cp_async_commit();
         }
         if (issuer && fail) {
-            // a wait gave up: let copies and MMAs still in flight land (bounded) before
-            // shared memory and TMEM are released, and report through the status word
-            if (n_wq > w_wq) tc::mbar_wait(&s.bar_wq, (uint32_t)(w_wq & 1));
-            if (n_ak0 > w_ak0) tc::mbar_wait(&s.bar_ak[0], (uint32_t)(w_ak0 & 1));
-            if (n_ak1 > w_ak1) tc::mbar_wait(&s.bar_ak[1], (uint32_t)(w_ak1 & 1));
+            // a wait gave up: let MMAs still in flight land (bounded) before shared memory
+            // and TMEM are released, and report through the status word
             if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
             if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
             atomicExch(status, -7);
         }
     }
+    cp_async_wait<0>();  // no copy of this thread still in flight when the CTA ends
 
     tc::fence_before_sync();
     __syncthreads();
