@@ -70,6 +70,12 @@ constexpr int kLdG = kD + 4;    // G row stride (floats): 528 bytes, so rows sta
 constexpr int kLdQK = kD + 8;   // q, k row stride (bf16): 272 bytes, likewise
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x log2(e))
 
+struct Item {
+    int slot, h;
+    int64_t t0;
+    int L;
+};
+
 struct IntraSmem {
     float G[2][kC * kLdG];  // z, then (in place) G log2(e); the other buffer is the next item's
     __nv_bfloat16 q[kC * kLdQK];  // q and k of the item (rows past the sequence end are zero)
@@ -94,6 +100,7 @@ struct IntraSmem {
         } e;
     } u;
     float beta[2][kC];
+    Item nxt2;  // the item after next, looked up by an idle thread during the Gram operands
     uint64_t bar_z[2], bar_qk, bar_v, bar_gram, bar_wu;
     uint32_t tmem_base;
     int fail;
@@ -127,12 +134,6 @@ __device__ __forceinline__ bool intra_wait(uint64_t *bar, uint32_t parity, volat
     atomicExch(status, -7);  // KDA_ERR_CUDA
     return false;
 }
-
-struct Item {
-    int slot, h;
-    int64_t t0;
-    int L;
-};
 
 }  // namespace
 
@@ -322,6 +323,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             tc::tmem_st16(tmem + lanes + (uint32_t)(c0 >> 1), hi);
             tc::tmem_st16(tmem + lanes + 64u + (uint32_t)(c0 >> 1), lo);
             tc::tmem_wait_st();
+        } else if (warp == kIntraThreads / 32 - 1 && lane == 0 && has_next2) {
+            s.nxt2 = item_of(item + 2 * gridDim.x);  // its dependent loads, off every other warp
         }
         // B (row versions) into shared memory by every thread: job (c8, nq) makes 8
         // channels of the q row version nq (split) and of the matching k row (hi only),
@@ -373,13 +376,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             tc::commit(&s.bar_gram);
         }
 
-        // the item after next (its lookup reads the tables in global memory; wanted after the
-        // Gram results)
-        const Item nxt2 = has_next2 ? item_of(item + 2 * gridDim.x) : nxt;
+        const Item nxt2 = has_next2 ? s.nxt2 : nxt;  // the item after next
 
         // ---- while the Gram chain runs: Khat (the [W | U'] operand), Qhat and Kend^T (the
         // ---- record); Khat and Qhat share 2^(G_j log2 e). Job (c8, j): token j, 8 channels.
-        for (int job = tid; job < kC * (kD / 8); job += kIntraThreads) {
+        // ---- Warp 0 issued the chain: its jobs go to warps 3 and 7, which read no Gram results.
+        auto khat_job = [&](int job) {
             const int j = job & (kC - 1), c = 8 * (job >> 6);
             float gj[8], gl[8];
             g_load8(G, j, c, gj);
@@ -405,8 +407,16 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             *reinterpret_cast<uint4 *>(rec + kRecAK + ak_off(kC + c, j)) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
             *reinterpret_cast<uint4 *>(rec + kRecAK + kStackAK + ak_off(kC + c, j)) =
                 make_uint4(el[0], el[1], el[2], el[3]);
+        };
+        static_assert(kC * (kD / 8) == 2 * kIntraThreads, "two Khat jobs per thread");
+        if (warp != 0) {
+            khat_job(tid);
+            khat_job(tid + kIntraThreads);
         }
-        if (tid < kD) reinterpret_cast<float *>(rec + kRecGam)[tid] = tc::ex2(grow(G, kC - 1)[tid]);
+        if (warp == 3) khat_job(tid - 96);                  // jobs 0 .. 31
+        if (warp == 7) khat_job(kIntraThreads + tid - 224);  // jobs 512 .. 543
+        if (tid >= 128 && tid < 128 + kD)
+            reinterpret_cast<float *>(rec + kRecGam)[tid - 128] = tc::ex2(grow(G, kC - 1)[tid - 128]);
 
         // ---- the Gram results: A_qk to the record, A_kk (times beta) to shared memory ----
         // Warp w of lane quarter qd = w % 4 < 3 reads 8 query columns 8 (w / 4) .. of its
