@@ -280,6 +280,50 @@ def test_segmented_walk_random(seed):
     assert_prefill_close(o, S, o_ref, S_ref, "segmented random %s x %d" % (lens, H))
 
 
+def _slow_memory(inp, log_a=0.001, b_mean=-3.0, seed=0):
+    """Weak decay and weak writes, so that the state keeps its memory over many chunks:
+    z set per channel for log a = -log_a f (f from 0.5 to 1.5 over the channels), b around
+    b_mean (beta about 0.05). The synthetic default decays by about e^-160 per chunk, which
+    leaves every segment map M of the segmented walk at zero; here M is far from it."""
+    T, H = inp["z"].shape[1], inp["z"].shape[2]
+    eA = torch.exp(inp["A"].double())
+    f = 0.5 + torch.arange(128, dtype=torch.float64) / 127
+    frac = log_a / 5.0 * f
+    z = (torch.log(frac / (1 - frac))[None, :] / eA[:, None]).float()
+    inp["z"] = z[None, None].expand(1, T, H, 128).contiguous()
+    g = torch.Generator().manual_seed(seed)
+    inp["b"] = (b_mean + 0.5 * torch.randn(inp["b"].shape, generator=g)).float()
+    return inp
+
+
+@pytest.mark.parametrize("lens,H", [([3000, 1800], 2), ([5000], 1)])
+def test_segmented_walk_slow_memory(lens, H):
+    """The segmented walk where the segment maps matter: with weak decay and weak writes
+    the map M of a segment (its state from the identity) stays of order one, so the phase-B
+    products M S_in carry the state from segment to segment ('From Linear Attention to
+    KDA', §7.5). Against the oracle, element by element."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    n = len(lens)
+    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == 5, (lens, H)
+    inp = _slow_memory(inputs.prefill_inputs(cu[-1], H, n, seed=31, init_state=True), seed=32)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu)
+    assert_prefill_close(o, S, o_ref, S_ref, "segmented, slow memory %s" % lens)
+
+
+def test_plain_walk_slow_memory():
+    """The same weak decay and writes on the plain walk (many chains), 1,500 tokens."""
+    lens = [1500] * 40
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    assert kda.kda_chunk_prefill_launch_count(cu[-1], len(lens), 2) == 3
+    inp = _slow_memory(inputs.prefill_inputs(cu[-1], 2, len(lens), seed=33, init_state=True), seed=34)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu)
+    assert_prefill_close(o, S, o_ref, S_ref, "plain, slow memory")
+
+
 @pytest.mark.parametrize("seed", range(4))
 def test_plain_walk_random(seed):
     """Random batches of many short sequences (one plain walk unit per chain, checked
