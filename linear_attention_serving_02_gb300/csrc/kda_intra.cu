@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // which share their factors. Consecutive threads take consecutive rows.
         if (tid == 0) tc::bulk_wait_read0();  // the last item's staged -W and U' have been read
         __syncthreads();
+#pragma unroll
         for (int job = tid; job < 96 * (kD / 8); job += kIntraThreads) {
             const int c8 = job / 96, nq = job % 96;
             const int i = (nq < 64) ? nq : nq - 32;
@@ -514,6 +515,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         // thread makes 4 consecutive columns of one row with float4 loads; a warp spans a
         // few rows and all column quads, so its loads are broadcasts or one 128-byte row.
         auto dot4 = [&](const float *arow, const float *bmat, int ldb, int k0, int k1, float4 &acc) {
+#pragma unroll 4
             for (int k = k0; k < k1; k += 4) {
                 const float4 av = *reinterpret_cast<const float4 *>(arow + k);
                 const float am[4] = {av.x, av.y, av.z, av.w};
