@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // cp.async and arrives on the load's mbarrier when they have landed. Rows of z past the
     // sequence end are not copied (the gate ignores them); those of q, k, v are zeroed.
     auto stage_z = [&](const Item &it, int b, int t0 = 0, int nt = kIntraThreads) {
+#pragma unroll 4
         for (int e = tid - t0; e >= 0 && e < it.L * (kD / 4); e += nt) {
             const int i = e / (kD / 4), c = (e % (kD / 4)) * 4;
             cp_async16(s.G[b] + i * kLdG + c, z + (it.t0 + i) * rowstride + (int64_t)it.h * kD + c);
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         cp_async_arrive(&s.bar_z[b]);
     };
     auto stage_qk = [&](const Item &it, int t0 = 0, int nt = kIntraThreads) {
+#pragma unroll 4
         for (int e = tid - t0; e >= 0 && e < 2 * kC * (kD / 8); e += nt) {
             const int which = e & 1, i = (e >> 1) / (kD / 8), c = ((e >> 1) % (kD / 8)) * 8;
             __nv_bfloat16 *dst = (which ? s.k : s.q) + i * kLdQK + c;
@@ -211,6 +213,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     // v goes straight into the V half of the [Khat | V] operand (MN-major: the 16 bytes of
     // token j, channels 8 c8 .. 8 c8 + 7 are one core-matrix row)
     auto stage_v = [&](const Item &it) {
+#pragma unroll 4
         for (int e = tid; e < kC * (kD / 8); e += kIntraThreads) {
             const int j = e & (kC - 1), c8 = e >> 6;  // consecutive threads: consecutive tokens
             unsigned char *dst = s.kv + ak_off(kD + 8 * c8, j);
