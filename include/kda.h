@@ -66,6 +66,21 @@ const char *kda_status_string(int status);
 int kda_version(void);
 
 /*
+ * Test hook for the state walk's failure path (no counterpart on the pages). On the
+ * current device, every later kda_chunk_prefill call leaves out the MMA-completion signal
+ * of chunk slot skip_commit_chunk in its state walks (-1: none), and every wait of the
+ * walk gives up after wait_limit_ns nanoseconds of the GPU clock (default 2e9). A walk
+ * whose wait gives up skips the rest of its work, writes NaN into its final state and
+ * sets the workspace status word to KDA_ERR_CUDA (see kda_workspace_status); no GPU fault
+ * is involved and the context stays usable. Restore with (-1, 2000000000) before normal
+ * use. The setting is global to the device and the process and not synchronised with
+ * work in flight: call it with the device idle.
+ *
+ * Returns KDA_OK, KDA_ERR_SHAPE for wait_limit_ns == 0, or KDA_ERR_CUDA.
+ */
+int kda_debug_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns);
+
+/*
  * Bytes of device workspace kda_chunk_prefill() needs for a batch of total_tokens
  * tokens in num_seqs sequences and num_heads heads. The size is an upper bound that
  * depends only on these three numbers, so one buffer serves every batch up to them.

@@ -37,6 +37,7 @@ cudaError_t launch_fused_decode(const __nv_bfloat16 *xq, const __nv_bfloat16 *xk
                                 const float *b, const float *g, const float *norm_w, float eps_l2, float eps_rms,
                                 float *state, float *y, int32_t N, int32_t H, int num_sms, cudaStream_t st);
 size_t intra_smem_bytes();
+cudaError_t set_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns);
 }  // namespace kda
 
 namespace {
@@ -169,6 +170,11 @@ const char *kda_status_string(int status) {
 }
 
 int kda_version(void) { return 100; }
+
+int kda_debug_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns) {
+    if (wait_limit_ns == 0) return KDA_ERR_SHAPE;
+    return kda::set_walk_fault(skip_commit_chunk, wait_limit_ns) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
 
 size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
     if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return 0;

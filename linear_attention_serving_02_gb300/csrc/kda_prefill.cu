@@ -418,10 +418,16 @@ __device__ __forceinline__ void split32_tmem_pk(const uint64_t *x, uint32_t t_hi
     tc::tmem_st16(t_lo, l);
 }
 
+// Test hook (kda_debug_walk_fault): the walk's MMA issuer leaves out the group-1 commit of
+// chunk g_walk_skip_commit, and every wait of the walk gives up after g_walk_wait_ns, so
+// a wait runs out with no fault; -1 and the default limit otherwise.
+__device__ int g_walk_skip_commit = -1;
+__device__ unsigned long long g_walk_wait_ns = tc::kWaitLimitNs;
+
 // bounded wait that gives up at once when the CTA has already failed
-__device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int &fail) {
+__device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int &fail, uint64_t limit) {
     if (fail) return false;
-    if (tc::mbar_wait(bar, parity)) return true;
+    if (tc::mbar_wait(bar, parity, limit)) return true;
     fail = 1;
     return false;
 }
@@ -430,8 +436,8 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
 // BAR_U / BAR_OR arrivals behind the state warps' matching syncs (a named barrier counts
 // arrivals, so one side may never arrive twice before the other has synced). True when
 // the data behind the barrier is valid.
-__device__ __forceinline__ bool wait_in_order(uint64_t *bar, uint32_t parity, volatile int &fail) {
-    if (!tc::mbar_wait(bar, parity)) fail = 1;
+__device__ __forceinline__ bool wait_in_order(uint64_t *bar, uint32_t parity, volatile int &fail, uint64_t limit) {
+    if (!tc::mbar_wait(bar, parity, limit)) fail = 1;
     return !fail;
 }
 
@@ -447,6 +453,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     pdl_trigger();
     if ((int)blockIdx.x >= *n_units) return;
     const WalkUnit unit = units[blockIdx.x];
+    const uint64_t wlim = g_walk_wait_ns;
+    const int skip_commit = g_walk_skip_commit;
     const float *S0 = unit.in ? unit.in + (size_t)h * kStateFloats : nullptr;
     float *Sout = unit.out ? unit.out + (size_t)h * kStateFloats : nullptr;
     const bool write_o = (unit.flags & kUnitWriteO) != 0;
@@ -549,7 +557,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             for (int j = 0; j < 32; ++j)
                 Upr[j] = add_up ? pk2(s.up[up_at(2 * j)], s.up[up_at(2 * j + 1)]) : pk2(0.f, 0.f);
             // U^T = U'^T + D_U, written as split planes for group 2
-            if (wait_in_order(&s.bar_m1, ph, fail)) {
+            if (wait_in_order(&s.bar_m1, ph, fail, wlim)) {
                 tc::fence_after_sync();
                 uint32_t d0[32], d1[32];
                 tc::tmem_ld32_nowait(D_UO + lanes, d0);
@@ -572,7 +580,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             // group 1 complete, so the buffer is free)
             if (c + 1 < c_end && !fail) copy_up_wq(c + 1);
             cp_async_commit();
-            const bool m2ok = wait_in_order(&s.bar_m2, ph, fail);
+            const bool m2ok = wait_in_order(&s.bar_m2, ph, fail, wlim);
             // S <- Diag(gamma) S + D_S on key rows 64 .. 127, and their split planes
             {
                 uint32_t dA[32], dB[32];
@@ -653,7 +661,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             }
         };
         // group 1 of the next chunk: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
-        auto issue_g1 = [&]() {
+        auto issue_g1 = [&](int c) {
             tc::fence_after_sync();
             if (!fail) {
                 // S^T hi and lo times the hi plane of [ -W ; Qhat ], and S^T hi times Qhat lo
@@ -678,8 +686,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     }
                 }
             }
-            tc::commit(&s.bar_m1);  // also after a failure: the U and O warps wait for it in order
-            ++n_m1;
+            if (c != skip_commit) {  // (test hook: left out for one chunk)
+                tc::commit(&s.bar_m1);  // also after a failure: the U and O warps wait for it in order
+                ++n_m1;
+            }
         };
         // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T
         auto issue_g2 = [&](int c) {
@@ -721,7 +731,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
         named_sync(kBarOR, 256);
-        if (issuer && c_begin < c_end) issue_g1();
+        if (issuer && c_begin < c_end) issue_g1(c_begin);
         __syncwarp();
         for (int c = c_begin; c < c_end; ++c) {
             const uint32_t ph = (uint32_t)((c - c_begin) & 1);
@@ -732,7 +742,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             named_sync(kBarU, 256);  // U^T planes of this chunk written (group 1 has finished)
             if (issuer) issue_g2(c);
             __syncwarp();
-            const bool ok = wait_or_fail(&s.bar_m2, ph, fail);
+            const bool ok = wait_or_fail(&s.bar_m2, ph, fail, wlim);
             s.gam[ph][dv] = gnext;
             named_sync(4, 128);  // gamma of this chunk in place
             // S <- Diag(gamma) S + D_S on key rows 0 .. 63 and their split planes, in blocks
@@ -770,7 +780,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             named_sync(kBarOR, 256);  // the U and O warps have written rows 64 .. 127, read this
                                       // chunk's D_S and output accumulators, and copied the next
                                       // [ -W ; Qhat ]
-            if (issuer && c + 1 < c_end) issue_g1();
+            if (issuer && c + 1 < c_end) issue_g1(c + 1);
             __syncwarp();
             // group 2 is done with this slot (every state thread saw it complete): the chunk
             // after next lands there while the next groups run
@@ -780,8 +790,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         if (issuer && fail) {
             // a wait gave up: let MMAs still in flight land (bounded) before shared memory
             // and TMEM are released, and report through the status word
-            if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1));
-            if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1));
+            if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1), wlim);
+            if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1), wlim);
             atomicExch(status, -7);
         }
     }
@@ -807,6 +817,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 // ---------------------------------------------------------------------------------
 // host-side launchers (called from kda_api.cu)
 // ---------------------------------------------------------------------------------
+cudaError_t set_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns) {
+    const unsigned long long lim = wait_limit_ns;
+    cudaError_t e = cudaMemcpyToSymbol(g_walk_skip_commit, &skip_commit_chunk, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_walk_wait_ns, &lim, sizeof(lim));
+    return e;
+}
+
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
                         int32_t *n_units, const SegPlan &sp, cudaStream_t st) {

@@ -127,19 +127,35 @@ __device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(mbar)), "r"(bytes));
 }
-// Wait for the phase of the given parity to complete. Gives up after a bounded number of
-// polls (each poll may suspend the thread briefly) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
+// the GPU's nanosecond clock
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// a wait gives up (returns false) after this long: every wait in these kernels ends within
+// microseconds, so running out means that an arrival will not come
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Wait for the phase of the given parity to complete. Gives up after limit_ns of the clock
+// (each poll may suspend the thread briefly) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_addr(mbar);
-    for (int it = 0; it < (1 << 24); ++it) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         uint32_t done;
         asm volatile(
             "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
             : "r"(a), "r"(parity));
         if (done) return true;
+        if ((it & 63) == 0) {  // the clock every 64 polls
+            const uint64_t now = globaltimer();
+            if (it == 0)
+                t0 = now;
+            else if (now - t0 > limit_ns)
+                return false;
+        }
     }
-    return false;
 }
 
 // bulk copy global -> this CTA's shared memory, completion counted on mbar (bytes % 16 == 0)

@@ -46,6 +46,8 @@ def library():
         lib.kda_chunk_prefill.restype = ctypes.c_int
         lib.kda_workspace_status.argtypes = [vp, vp]
         lib.kda_workspace_status.restype = ctypes.c_int
+        lib.kda_debug_walk_fault.argtypes = [i32, ctypes.c_uint64]
+        lib.kda_debug_walk_fault.restype = ctypes.c_int
         lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
         lib.kda_recurrent_decode.restype = ctypes.c_int
         lib.kda_recurrent_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
@@ -301,3 +303,12 @@ def kda_chunk_prefill_noalloc(q, k, v, z, A, b, initial_state=None, cu_seqlens=N
     if rc != 0:
         raise KdaError("kda_chunk_prefill_noalloc", rc)
     return o, final_state
+
+
+def kda_debug_walk_fault(skip_commit_chunk, wait_limit_ns):
+    """Test hook of the state walk's failure path (include/kda.h): the walks leave out the
+    MMA-completion signal of chunk slot skip_commit_chunk (-1: none) and give up a wait after
+    wait_limit_ns nanoseconds. Restore with (-1, 2_000_000_000)."""
+    rc = library().kda_debug_walk_fault(ctypes.c_int32(skip_commit_chunk), ctypes.c_uint64(wait_limit_ns))
+    if rc != 0:
+        raise KdaError("kda_debug_walk_fault", rc)
