@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const float bv = pre.x, eA = expf(pre.y);
         intra_wait(&s.bar_z[b], (uint32_t)par, fail, status);
         float *Gb = s.G[b];
-        const int ro = lane & 15, cq = 2 * warp + (lane >> 4), r0 = 4 * ro, c0 = 4 * cq;
+        // lane = 2 ro + (cq % 2): the 8 lanes of a shared-memory phase take 4 row quads of 2
+        // channel quads, 4 distinct bank groups (row quads 4 rows apart share two)
+        const int ro = lane >> 1, cq = 2 * warp + (lane & 1), r0 = 4 * ro, c0 = 4 * cq;
         const uint64_t mA = pk2(-eA * kLog2e, -eA * kLog2e), one = pk2(1.f, 1.f);
         uint64_t g[4][2];  // rows r0 + m, channel pairs (c0, c0 + 1), (c0 + 2, c0 + 3)
 #pragma unroll
@@ -250,7 +252,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 g[m][p] = m ? add2(g[m - 1][p], la) : la;
             }
         }
-        // exclusive prefix of the quad totals over ro (the 16 lanes with the same cq)
+        // exclusive prefix of the quad totals over ro (the 16 lanes with the same cq, every
+        // second lane)
         float tot[4];
         {
             const float2 x0 = upk2(g[3][0]), x1 = upk2(g[3][1]);
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         for (int d = 1; d < 16; d <<= 1) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const float y = __shfl_up_sync(0xffffffffu, inc[c], d, 16);
+                const float y = __shfl_up_sync(0xffffffffu, inc[c], 2 * d);  // row quad ro - d
                 if (ro >= d) inc[c] += y;
             }
         }
