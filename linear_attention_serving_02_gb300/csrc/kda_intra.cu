@@ -201,7 +201,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     auto stage_qk = [&](const Item &it, int t0 = 0, int nt = kIntraThreads) {
 #pragma unroll 4
         for (int e = tid - t0; e >= 0 && e < 2 * kC * (kD / 8); e += nt) {
-            const int which = e & 1, i = (e >> 1) / (kD / 8), c = ((e >> 1) % (kD / 8)) * 8;
+            // 16 consecutive units of one row of q, then of k: q and k lie a multiple of 128
+            // bytes apart, so alternating them per unit put two lanes on each bank group
+            const int which = (e >> 4) & 1, i = e >> 5, c = (e & 15) * 8;
             __nv_bfloat16 *dst = (which ? s.k : s.q) + i * kLdQK + c;
             if (i < it.L)
                 cp_async16(dst, (which ? k : q) + (it.t0 + i) * rowstride + (int64_t)it.h * kD + c);
