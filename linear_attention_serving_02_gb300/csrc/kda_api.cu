@@ -18,8 +18,8 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
                            const float *Mseg, const float *Rseg, cudaStream_t st);
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                          const float *A, const float *b, int32_t *status, const int32_t *seq_cu,
-                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t nslots, uint8_t *records,
-                         int num_sms, cudaStream_t st);
+                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t nslots,
+                         uint8_t *records, int num_sms, cudaStream_t st);
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
                         int32_t H, const uint8_t *records, void *o, int o_f32, cudaStream_t st);
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
@@ -233,7 +233,7 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
         return KDA_ERR_CUDA;
     if (kda::launch_intra(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k),
                           reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, status, seq_cu, chunk_off, num_seqs,
-                          num_heads, w.nslots, records, dev.sms, st) != cudaSuccess)
+                          num_heads, cu_seqlens ? 0 : seq_len, w.nslots, records, dev.sms, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (w.P == 0) {
         if (kda::launch_walk(status, units, counts, num_seqs, num_heads, records, o, o_f32, st) != cudaSuccess)

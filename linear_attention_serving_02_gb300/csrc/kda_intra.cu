@@ -126,12 +126,11 @@ __device__ __forceinline__ uint32_t scale_bf16(uint32_t xbf2, float f0, float f1
 // i % 32, so that the 16 rows a warp stages at once fall on distinct banks
 __device__ __forceinline__ int up_unit(int i, int u) { return u ^ (i & 31); }
 
-// bounded mbarrier wait; a wait that gives up marks the CTA failed (and reports it)
-__device__ __forceinline__ bool intra_wait(uint64_t *bar, uint32_t parity, volatile int &fail, int32_t *status) {
+// bounded mbarrier wait; a wait that gives up marks the CTA failed (reported at the end)
+__device__ __forceinline__ bool intra_wait(uint64_t *bar, uint32_t parity, volatile int &fail, int32_t *) {
     if (fail) return false;  // after a failure nothing waits again: the kernel only runs out
     if (tc::mbar_wait(bar, parity)) return true;
     fail = 1;
-    atomicExch(status, -7);  // KDA_ERR_CUDA
     return false;
 }
 
@@ -142,16 +141,28 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
                      const float *__restrict__ bgate, int32_t *__restrict__ status,
                      const int32_t *__restrict__ seq_cu, const int32_t *__restrict__ chunk_off, int32_t N, int32_t H,
-                     uint8_t *__restrict__ records) {
+                     int64_t dense_len, uint8_t *__restrict__ records) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait();
+    // N sequences of dense_len tokens each (dense_len > 0, no cu_seqlens): the sequence
+    // tables are closed forms, so nothing here waits for the plan kernel before the end
+    // (it writes only the walk's tables and a status of 0); every CTA waits for it before it
+    // exits, which keeps its tables complete for the walk that waits for this kernel.
+    const bool dense = dense_len > 0;
+    const int cps = dense ? (int)((dense_len + kC - 1) / kC) : 0;  // chunks per sequence
+    if (!dense) pdl_wait();
     pdl_trigger();
-    if (*status != 0 || N <= 0) return;
+    if ((!dense && *status != 0) || N <= 0) {
+        if (dense) pdl_wait();
+        return;
+    }
     // persistent: CTA b takes items b, b + gridDim.x, ...; item = slot * H + h
-    const int n_items = chunk_off[N] * H;
-    if ((int)blockIdx.x >= n_items) return;
+    const int n_items = (dense ? N * cps : chunk_off[N]) * H;
+    if ((int)blockIdx.x >= n_items) {
+        if (dense) pdl_wait();
+        return;
+    }
     const int64_t rowstride = (int64_t)H * kD;  // elements between consecutive tokens
 
     if (warp == 0) {
@@ -182,6 +193,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         Item r;
         r.slot = it / H;
         r.h = it % H;
+        if (dense) {
+            const int n = r.slot / cps, ci = r.slot - n * cps;
+            r.t0 = (int64_t)n * dense_len + (int64_t)ci * kC;
+            r.L = (int)min((int64_t)kC, dense_len - (int64_t)ci * kC);
+            return r;
+        }
         const int n = find_seq(chunk_off, N, r.slot);
         r.t0 = (int64_t)seq_cu[n] + (int64_t)(r.slot - chunk_off[n]) * kC;
         r.L = (int)min((int64_t)kC, (int64_t)seq_cu[n + 1] - r.t0);
@@ -673,6 +690,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         tc::mbar_wait(&s.bar_gram, (uint32_t)((iters - 1) & 1));
         tc::mbar_wait(&s.bar_wu, (uint32_t)((iters - 1) & 1));
     }
+    if (dense) pdl_wait();  // the plan kernel has finished (its status write comes first)
+    if (tid == 0 && fail) atomicExch(status, -7);  // KDA_ERR_CUDA
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
@@ -681,8 +700,8 @@ size_t intra_smem_bytes() { return sizeof(IntraSmem); }
 
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                          const float *A, const float *b, int32_t *status, const int32_t *seq_cu,
-                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t nslots, uint8_t *records,
-                         int num_sms, cudaStream_t st) {
+                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t nslots,
+                         uint8_t *records, int num_sms, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kda_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -695,7 +714,7 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
     const int64_t items = nslots * H;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)num_sms);
     return launch_after(kda_intra_kernel, dim3(grid), dim3(kIntraThreads), sizeof(IntraSmem), st, q, k, v, z, A, b,
-                        status, seq_cu, chunk_off, N, H, records);
+                        status, seq_cu, chunk_off, N, H, dense_len, records);
 }
 
 }  // namespace kda
