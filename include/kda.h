@@ -91,9 +91,9 @@ size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, 
 /*
  * Number of kernels one kda_chunk_prefill() call with these sizes launches on its
  * stream: 0 when num_seqs is 0, 3 (plan, intra-chunk, state walk) when every
- * (sequence, head) chain walks its chunks in one pass, 5 when the chains are too few
- * to fill the GPU and the walk is split into segments (plan, intra-chunk, segment
- * walk, segment chaining, output walk). Depends only on the three sizes,
+ * (sequence, head) chain walks its chunks in one pass, 4 when the chains are too few
+ * to fill the GPU and the walk is split into segments (plan, intra-chunk, segment-map
+ * walk, output walk that first chains the maps). Depends only on the three sizes,
  * like the workspace. Returns -1 for negative arguments.
  */
 int32_t kda_chunk_prefill_launch_count(int64_t total_tokens, int32_t num_seqs, int32_t num_heads);

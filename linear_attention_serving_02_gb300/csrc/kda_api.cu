@@ -14,14 +14,14 @@ struct WalkUnit;
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
                         int32_t *n_units, const SegPlan &sp, cudaStream_t st);
-cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
-                           const float *Mseg, const float *Rseg, cudaStream_t st);
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                          const float *A, const float *b, int32_t *status, const int32_t *seq_cu,
                          const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t nslots,
                          uint8_t *records, int num_sms, cudaStream_t st);
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
-                        int32_t H, const uint8_t *records, void *o, int o_f32, cudaStream_t st);
+                        int32_t H, const uint8_t *records, void *o, int o_f32, int chained, cudaStream_t st);
+cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
+                           const float *Mseg, const float *Rseg, cudaStream_t st);
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                           const float *A, const float *b, float *state, float *o, int32_t N, int32_t H,
                           int num_sms, cudaStream_t st);
@@ -184,7 +184,8 @@ size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, 
 int32_t kda_chunk_prefill_launch_count(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
     if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return -1;
     if (num_seqs == 0) return 0;
-    return kda::walk_segment_chunks(total_tokens, num_seqs, num_heads) ? 5 : 3;
+    if (!kda::walk_segment_chunks(total_tokens, num_seqs, num_heads)) return 3;
+    return kda::walk_chain_mode(total_tokens, num_seqs, num_heads) ? 4 : 5;
 }
 
 int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
@@ -227,6 +228,7 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
         sp.nA = counts + 1;
         sp.nC = counts + 2;
         sp.chains = reinterpret_cast<int32_t *>(ws + w.chains);
+        sp.chain_mode = kda::walk_chain_mode(total, num_seqs, num_heads) ? 1 : 0;
     }
     if (kda::launch_plan(cu_seqlens, num_seqs, seq_len, total, status, seq_cu, chunk_off, num_heads, initial_state,
                          final_state, units, counts, sp, st) != cudaSuccess)
@@ -236,17 +238,20 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                           num_heads, cu_seqlens ? 0 : seq_len, w.nslots, records, dev.sms, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (w.P == 0) {
-        if (kda::launch_walk(status, units, counts, num_seqs, num_heads, records, o, o_f32, st) != cudaSuccess)
+        if (kda::launch_walk(status, units, counts, num_seqs, num_heads, records, o, o_f32, 0, st) != cudaSuccess)
             return KDA_ERR_CUDA;
         return KDA_OK;
     }
-    // segmented walk: phase A (segment maps), phase B (chain them), phase C (outputs)
-    if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, st) !=
-        cudaSuccess)
+    // segmented walk: phase A (segment maps), phase B (chain them: the combine kernel, or in
+    // the chained form each output walk itself), phase C (outputs)
+    if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, sp.chain_mode,
+                         st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_combine(status, sp.chains, num_seqs, num_heads, sp.Sin, sp.Mseg, sp.Rseg, st) != cudaSuccess)
+    if (!sp.chain_mode &&
+        kda::launch_combine(status, sp.chains, num_seqs, num_heads, sp.Sin, sp.Mseg, sp.Rseg, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_walk(status, sp.unitsC, sp.nC, w.seg_bound, num_heads, records, o, o_f32, st) != cudaSuccess)
+    if (kda::launch_walk(status, sp.unitsC, sp.nC, w.seg_bound, num_heads, records, o, o_f32, sp.chain_mode,
+                         st) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
 }

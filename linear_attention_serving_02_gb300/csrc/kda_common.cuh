@@ -92,15 +92,23 @@ __host__ __device__ inline int64_t chunk_bound(int64_t total_tokens, int64_t num
 struct WalkUnit {
     const float *in;  // state at the start for head 0 ([128][128], row = key channel), head h
                       // at in + h * 128 * 128; nullptr: zero (or the identity, see flags)
-    float *out;       // state at the end, same layout; nullptr: not kept
+    float *out;       // state at the end, same layout (or split planes, kUnitOutPlanes);
+                      // nullptr: not kept
+    // maps applied to the start state before the walk, in order: X <- M_j X + R_j for
+    // j = 1 .. chain. M_j of head h is at maps + ((j - 1) H + h) * 128 * 128 floats, stored
+    // as split bf16 planes (kUnitOutPlanes); R_j at offs, same indexing, fp32 rows
+    const float *maps, *offs;
     int32_t c_begin, c_end;  // chunk-record slots
     int32_t t_begin, t_end;  // tokens of those chunks (the last chunk may be partial)
     int32_t flags;
-    int32_t pad;
+    int32_t chain;
 };
-constexpr int kUnitWriteO = 1;    // write the outputs o of these chunks
-constexpr int kUnitAddUp = 2;     // U = U' - W S (else U = -W S: the homogeneous map)
-constexpr int kUnitIdentity = 4;  // start from the identity when in == nullptr
+constexpr int kUnitWriteO = 1;     // write the outputs o of these chunks
+constexpr int kUnitAddUp = 2;      // U = U' - W S (else U = -W S: the homogeneous map)
+constexpr int kUnitIdentity = 4;   // start from the identity when in == nullptr
+constexpr int kUnitOutPlanes = 8;  // keep the end state S as the two bf16 planes (hi, then
+                                   // lo = bf16(S - hi)) of the tensor-core operand B[n][k] =
+                                   // S[n][k], interleaved K-major (il_off(n, k, 128)), 32 KB each
 constexpr size_t kStateFloats = (size_t)kD * kD;
 
 // Tables of the segmented walk, built by the plan kernel when P > 0 (segment length in
@@ -110,7 +118,8 @@ struct SegPlan {
     float *Sin, *Mseg, *Rseg;  // per (segment, head): input state, map M, offset R
     WalkUnit *unitsA, *unitsC;
     int32_t *nA, *nC;
-    int32_t *chains;  // per sequence: first segment, number of segments
+    int32_t *chains;     // per sequence: first segment, number of segments (combine form)
+    int32_t chain_mode;  // 1: each output walk chains the maps before it; 0: a combine kernel does
 };
 
 // Segment length (in chunks) of the segmented walk, or 0 for a plain walk. A pure
@@ -147,6 +156,17 @@ __host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t
 }
 __host__ __device__ inline int64_t segment_bound(int64_t total_tokens, int64_t num_seqs, int P) {
     return (chunk_bound(total_tokens, num_seqs) + (int64_t)(P - 1) * num_seqs) / P;
+}
+// How the segmented walk finds each segment's input state. When every output walk fits in
+// one wave of the GPU (segments x heads <= 152), each one chains the maps of the segments
+// before it on the tensor cores (M as split bf16 planes): the chain of the last segment,
+// about 1.7 us per map, replaces a kernel launch and its serial chain on the critical path.
+// With more segments that replicated chain costs more SM time than it saves, and a combine
+// kernel chains the maps once per (sequence, head) in fp32 instead. A pure function of the
+// sizes, like the segment length.
+__host__ __device__ inline bool walk_chain_mode(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
+    const int P = walk_segment_chunks(total_tokens, num_seqs, num_heads);
+    return P > 0 && segment_bound(total_tokens, num_seqs, P) * num_heads <= 152;
 }
 
 // ---------------------------------------------------------------------------------

@@ -10,8 +10,8 @@
 //                     walks the chunks in order with the full state on chip, on tcgen05
 //                     tensor cores (TMEM accumulators),
 //                     U = U' - W S;  O = Qhat S + A_qk U;  S = Diag(gamma) S + Kend^T U
-//   with few long sequences the walk is segmented (two walk launches and
-//   kda_combine_kernel between them; see below)
+//   with few long sequences the walk is segmented (two walk launches, with
+//   kda_combine_kernel between them when the segments are many; see below)
 //
 // The algebra is the chunkwise form of 'From Linear Attention to KDA' (blog), §7.1-7.3
 // with the per-channel decay of §7.2 folded into the UT system, and tiles as in §8 for
@@ -48,35 +48,44 @@ namespace kda {
 // plan: seq_cu[N+1] and chunk_off[N+1] (prefix sums of ceil(len / C)) in the workspace
 // ---------------------------------------------------------------------------------
 // ---------------------------------------------------------------------------------
-// segmented walk: tables of the three phases, written by one thread of the plan kernel
-// (used only when there are few sequences). Segment g of the batch is segment sigma of sequence n, g = seg_base[n] + sigma.
-//   phase A  segment 0 from the initial state -> Sin[g0 + 1] (the next input); with one
+// segmented walk: tables of the two phases, written by one thread of the plan kernel
+// (used only when there are few sequences). Segment g of the batch is segment sigma of
+// sequence n, g = seg_base[n] + sigma; its affine map is S_out = M[g] S_in + R[g].
+//   phase A  segment 0 from the initial state -> Sin[g0 + 1] (segment 1's input); with one
 //            segment, the whole walk with o and the final state instead
 //            segment sigma (1 .. S-2) from zero     -> R[g],  with U'
-//            segment sigma (1 .. S-2) from identity -> M[g],  without U'
+//            segment sigma (1 .. S-2) from identity -> M[g],  without U' (in the chained
+//            form kept as the split bf16 planes the tensor cores read)
 //            (walks without outputs read only -W and Kend^T of the records)
-//   phase B  Sin[g + 1] = M[g] Sin[g] + R[g]  for sigma = 1 .. S-2 (kda_combine_kernel)
-//   phase C  segments 0 .. S-1 from their input states, writing o; the last one writes
-//            the final state
+//   phase B  (combine form) Sin[g + 1] = M[g] Sin[g] + R[g] for sigma = 1 .. S-2, by
+//            kda_combine_kernel
+//   phase C  segments 0 .. S-1, writing o; the last one writes the final state. Segment
+//            sigma >= 1 starts from Sin[g0 + sigma] (combine form), or (chained form) from
+//            Sin[g0 + 1], first applying X <- M[g0 + j] X + R[g0 + j] for j = 1 .. sigma - 1
+//            on the tensor cores (the chained form is taken only when all of phase C runs
+//            in one wave, so the longest chain is what it adds).
 // ---------------------------------------------------------------------------------
 __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, const int32_t *__restrict__ chunk_off,
                               int32_t N, int32_t H, const float *S0, float *Sout, const SegPlan &sp) {
     const int32_t P = sp.P;
     float *Sin = sp.Sin, *Mseg = sp.Mseg, *Rseg = sp.Rseg;
     WalkUnit *unitsA = sp.unitsA, *unitsC = sp.unitsC;
-    int32_t *chains = sp.chains;
+    auto blank = [](const float *in, float *out, int32_t c, int32_t t, int32_t flags) {
+        WalkUnit u;
+        u.in = in;
+        u.out = out;
+        u.maps = u.offs = nullptr;
+        u.c_begin = u.c_end = c;
+        u.t_begin = u.t_end = t;
+        u.flags = flags;
+        u.chain = 0;
+        return u;
+    };
     if (bad) {
         // no maps to build; phase C only marks each final state invalid (NaN)
         for (int32_t n = 0; n < N; ++n) {
-            chains[2 * n] = 0;
-            chains[2 * n + 1] = 0;
-            WalkUnit u;
-            u.in = nullptr;
-            u.out = Sout + (size_t)n * H * kStateFloats;
-            u.c_begin = u.c_end = u.t_begin = u.t_end = 0;
-            u.flags = 0;
-            u.pad = 0;
-            unitsC[n] = u;
+            unitsC[n] = blank(nullptr, Sout + (size_t)n * H * kStateFloats, 0, 0, 0);
+            sp.chains[2 * n] = sp.chains[2 * n + 1] = 0;
         }
         *sp.nA = 0;
         *sp.nC = N;
@@ -88,37 +97,26 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
         const int32_t c0 = chunk_off[n], c1 = chunk_off[n + 1];
         const int32_t t0 = seq_cu[n], t1 = seq_cu[n + 1];
         const int32_t S = (c1 - c0 + P - 1) / P;
-        chains[2 * n] = g;
-        chains[2 * n + 1] = S;
+        sp.chains[2 * n] = g;
+        sp.chains[2 * n + 1] = S;
         const float *init = S0 ? S0 + (size_t)n * seg_stride : nullptr;
-        if (S == 0) {  // an empty sequence: its final state is its initial state
-            WalkUnit u;
-            u.in = init;
-            u.out = Sout + (size_t)n * seg_stride;
-            u.c_begin = u.c_end = c0;
-            u.t_begin = u.t_end = t0;
-            u.flags = 0;
-            u.pad = 0;
-            unitsA[a++] = u;
-        }
+        float *fin = Sout + (size_t)n * seg_stride;
+        // an empty sequence: its final state is its initial state
+        if (S == 0) unitsA[a++] = blank(init, fin, c0, t0, 0);
         for (int32_t sg = 0; sg < S; ++sg) {
-            WalkUnit u;
-            u.c_begin = c0 + sg * P;
+            WalkUnit u = blank(nullptr, nullptr, c0 + sg * P, t0 + sg * P * kC, kUnitAddUp);
             u.c_end = min(c1, c0 + (sg + 1) * P);
-            u.t_begin = t0 + sg * P * kC;
             u.t_end = min(t1, t0 + (sg + 1) * P * kC);
-            u.pad = 0;
             if (sg == 0) {
                 u.in = init;
                 if (S == 1) {  // phase A: the sequence's only walk, with outputs
-                    u.out = Sout + (size_t)n * seg_stride;
+                    u.out = fin;
                     u.flags = kUnitWriteO | kUnitAddUp;
                     unitsA[a++] = u;
                     continue;
                 }
                 // phase A: the end state only (a walk without outputs is cheaper) ...
                 u.out = Sin + (size_t)(g + 1) * seg_stride;
-                u.flags = kUnitAddUp;
                 unitsA[a++] = u;
                 // ... phase C: again with outputs, alongside the other segments
                 u.out = nullptr;
@@ -127,18 +125,28 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
                 continue;
             }
             // phase C
-            u.in = Sin + (size_t)(g + sg) * seg_stride;
-            u.out = sg == S - 1 ? Sout + (size_t)n * seg_stride : nullptr;
+            if (sp.chain_mode) {  // from segment 1's input through the maps of segments 1 .. sg - 1
+                u.in = Sin + (size_t)(g + 1) * seg_stride;
+                u.chain = sg - 1;
+                if (sg > 1) {
+                    u.maps = Mseg + (size_t)(g + 1) * seg_stride;
+                    u.offs = Rseg + (size_t)(g + 1) * seg_stride;
+                }
+            } else {  // from the combine kernel's input state
+                u.in = Sin + (size_t)(g + sg) * seg_stride;
+            }
+            u.out = sg == S - 1 ? fin : nullptr;
             u.flags = kUnitWriteO | kUnitAddUp;
             unitsC[cc++] = u;
-            // phase A
+            // phase A: this segment's map
             if (sg <= S - 2) {
-                u.in = nullptr;
+                u.in = u.maps = u.offs = nullptr;
+                u.chain = 0;
                 u.out = Rseg + (size_t)(g + sg) * seg_stride;
                 u.flags = kUnitAddUp;
                 unitsA[a++] = u;
                 u.out = Mseg + (size_t)(g + sg) * seg_stride;
-                u.flags = kUnitIdentity;
+                u.flags = kUnitIdentity | (sp.chain_mode ? kUnitOutPlanes : 0);
                 unitsA[a++] = u;
             }
         }
@@ -181,9 +189,10 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
                 WalkUnit u;
                 u.in = nullptr;
                 u.out = Sout + (size_t)n * H * kStateFloats;
+                u.maps = u.offs = nullptr;
                 u.c_begin = u.c_end = u.t_begin = u.t_end = 0;
                 u.flags = 0;
-                u.pad = 0;
+                u.chain = 0;
                 units[n] = u;
             }
         }
@@ -230,8 +239,9 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
             u.c_end = chunk_off[n] + len;
             u.t_begin = start;
             u.t_end = cu_seqlens ? cu_seqlens[n + 1] : (int32_t)((n + 1) * seq_len);
+            u.maps = u.offs = nullptr;
             u.flags = kUnitWriteO | kUnitAddUp;
-            u.pad = 0;
+            u.chain = 0;
             units[n] = u;
         }
         if (tid == 255) carry += scan[255];
@@ -355,6 +365,10 @@ __global__ void __launch_bounds__(kCombineThreads)
 // Every product is split-bf16 (hi*hi + hi*lo + lo*hi). S^T and U^T, the A operands, are
 // written as split planes straight into tensor memory by the threads that own their rows
 // (tcgen05.st); the record tiles in shared memory are the B operands.
+// A segment of a segmented walk first brings its start state through the maps of the
+// segments before it: X <- M X + R, on the same tensor cores as X^T <- X^T M^T + R^T
+// (X^T in the S^T planes, M's split planes as the B operand, D in D_U | D_O1), one
+// 128 x 128 x 128 product per map, the next map's planes copied while the current one runs.
 //
 // Eight warps with fixed roles:
 //   warps 0-3  U and O: thread = value channel dv (TMEM lane dv). After group 1 they
@@ -386,12 +400,18 @@ struct WalkSmem {
     alignas(16) float up[kC * kD];       // U' of the current chunk, rows as in the record
     alignas(16) float gam[2][kD];        // gamma of chunks c (slot c & 1), the state warps' copy
     alignas(16) float gam_uo[2][kD];     // the same, the U and O warps' copy
-    unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
-    uint64_t bar_m1, bar_m2;
+    alignas(16) unsigned char ut[2 * 128 * kC * 2];  // o staging: 64 tokens x 128 channels (fp32 or bf16)
+    uint64_t bar_m1, bar_m2, bar_ch;
     uint32_t tmem_base;
     int fail;
 };
 static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
+// Before its first chunk a walk may run a chain of segment maps; their planes (hi, lo) take
+// two buffers: hi at ak + 0, lo at ak + 32 KB; hi at ak + 64 KB, lo in ut.
+constexpr int kPlaneSS = kD * kD * 2;  // one 128 x 128 bf16 plane
+static_assert(sizeof(WalkSmem::ak) >= 3 * (size_t)kPlaneSS && sizeof(WalkSmem::ut) >= (size_t)kPlaneSS,
+              "chain buffers");
+static_assert(sizeof(WalkSmem::wq) + sizeof(WalkSmem::ak) >= 2 * (size_t)kPlaneSS, "plane staging");
 
 constexpr int kWalkThreads = 256;
 // TMEM columns: accumulators D_U [0,64) D_O1 [64,128) D_O2 [128,192) D_S [192,320); the
@@ -441,6 +461,9 @@ __device__ __forceinline__ bool wait_in_order(uint64_t *bar, uint32_t parity, vo
     return !fail;
 }
 
+// kChain: the form that can chain segment maps before its first chunk and keep an end
+// state as split planes (the segmented walk's chained form); without it, neither.
+template <bool kChain>
 __global__ void __launch_bounds__(kWalkThreads, 1)
     kda_walk_kernel(int32_t *__restrict__ status, const WalkUnit *__restrict__ units,
                     const int32_t *__restrict__ n_units, int32_t H, const uint8_t *__restrict__ records,
@@ -475,6 +498,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         if (lane == 0) {
             tc::mbar_init(&s.bar_m1, 1);
             tc::mbar_init(&s.bar_m2, 1);
+            tc::mbar_init(&s.bar_ch, 1);
             tc::mbar_init_fence();
             s.fail = 0;
         }
@@ -515,31 +539,125 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 reinterpret_cast<__nv_bfloat16 *>(stage)[i * kD + dv] = __float2bfloat16_rn(ov);
         }
     };
-    if (warp < 4) {
-        // ------------- U and O warps; they also hold key rows 64 .. 127 of S -------------
-        // U' row i holds its 16-byte units (4 channels) XOR-swizzled by i % 32: a warp's
-        // reads of one row hit 32 distinct banks
-        auto up_at = [&](int i) { return i * kD + ((((dv >> 2) ^ (i & 31))) << 2) + (dv & 3); };
-        // chunk c's U' and [ -W ; Qhat ] (a map walk: -W alone) by this thread's share of
-        // 16-byte units, as one cp.async group
-        auto copy_up_wq = [&](int c) {
-            const unsigned char *rec = rec_of(c);
-            const int wq_units = (maps ? kPlaneQK : kRecWQBytes) / 16;
-            for (int u = tid; u < wq_units; u += 128) cp_async16(s.wq + 16 * u, rec + kRecW + 16 * u);
-            if (add_up)
-                for (int u = tid; u < kC * kD / 4; u += 128) cp_async16(s.up + 4 * u, rec + kRecUp + 16 * u);
-        };
+    // chunk c's U' and [ -W ; Qhat ] (a map walk: -W alone) by this U and O thread's share
+    // of 16-byte units
+    auto copy_up_wq = [&](int c) {
+        const unsigned char *rec = rec_of(c);
+        const int wq_units = (maps ? kPlaneQK : kRecWQBytes) / 16;
+        for (int u = tid; u < wq_units; u += 128) cp_async16(s.wq + 16 * u, rec + kRecW + 16 * u);
+        if (add_up)
+            for (int u = tid; u < kC * kD / 4; u += 128) cp_async16(s.up + 4 * u, rec + kRecUp + 16 * u);
+    };
+    // this thread's key rows of the start state, and their split S^T planes
+    const int r0 = warp >= 4 ? 0 : 64;
+    auto load_start = [&]() {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            const int r = 64 + 2 * j;
+            const int r = r0 + 2 * j;
             Sh[j] = S0 ? pk2(S0[(int64_t)r * kD + dv], S0[(int64_t)(r + 1) * kD + dv])
                        : pk2((identity && r == dv) ? 1.f : 0.f, (identity && r + 1 == dv) ? 1.f : 0.f);
         }
 #pragma unroll
         for (int j = 0; j < 32; j += 16)
-            split32_tmem_pk(&Sh[j], tmem + lanes + kColSHi + 32 + j, tmem + lanes + kColSLo + 32 + j);
+            split32_tmem_pk(&Sh[j], tmem + lanes + kColSHi + r0 / 2 + j, tmem + lanes + kColSLo + r0 / 2 + j);
         tc::tmem_wait_st();
-        if (c_begin < c_end) copy_up_wq(c_begin);
+    };
+
+    // the chain of segment maps before the first chunk (every thread; thread 128 issues)
+    const int chain = kChain ? unit.chain : 0;
+    int n_ch = 0;  // chain MMA groups committed (issuer)
+    if (kChain && chain > 0) {
+        unsigned char *const cb = &s.ak[0][0];
+        auto m_hi = [&](int b) { return cb + b * 2 * kPlaneSS; };
+        auto m_lo = [&](int b) { return b ? s.ut : cb + kPlaneSS; };
+        // M_j's planes into chain buffer b, in 16-byte units, by the threads outside the
+        // issuer's warp (that warp is issuing the product while the copy is due)
+        const bool copier = warp != 4;
+        const int ct = tid < 128 ? tid : tid - 32;  // 0 .. 223 over the copying threads
+        auto copy_m = [&](int j, int b) {
+            const unsigned char *src =
+                reinterpret_cast<const unsigned char *>(unit.maps + ((size_t)(j - 1) * H + h) * kStateFloats);
+            for (int u = ct; u < 2 * kPlaneSS / 16; u += kWalkThreads - 32) {
+                unsigned char *dst = u < kPlaneSS / 16 ? m_hi(b) + 16 * u : m_lo(b) + 16 * (u - kPlaneSS / 16);
+                cp_async16(dst, src + 16 * u);
+            }
+        };
+        // R_j of this thread's key rows into Sh (dead there: X is in the planes); the step's
+        // epilogue adds the product. The issuer's warp loads it a step early, before it
+        // issues; the other warps while the product runs.
+        const bool early_r = warp == 4;
+        auto load_r = [&](int j) {
+            const float *R = unit.offs + ((size_t)(j - 1) * H + h) * kStateFloats + dv;
+#pragma unroll
+            for (int p = 0; p < 32; ++p) Sh[p] = pk2(R[(int64_t)(r0 + 2 * p) * kD], R[(int64_t)(r0 + 2 * p + 1) * kD]);
+        };
+        if (copier) copy_m(1, 0);
+        cp_async_commit();
+        load_start();
+        if (early_r) load_r(1);
+        const uint32_t idc = tc::idesc_bf16_m128(kD);
+        for (int j = 1; j <= chain; ++j) {
+            const int b = (j - 1) & 1;
+            cp_async_wait<0>();  // this thread's share of M_j
+            fence_proxy_async();
+            tc::fence_before_sync();
+            __syncthreads();  // M_j in place, the S^T planes of X written
+            tc::fence_after_sync();
+            if (tid == 128) {
+                if (!fail) {
+                    const uint32_t bh = tc::smem_addr(m_hi(b)), bl = tc::smem_addr(m_lo(b));
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint64_t dh = tc::desc_k(bh, kD, ks), dl = tc::desc_k(bl, kD, ks);
+                        tc::mma_ts(D_UO, tmem + kColSHi + 8 * ks, dh, idc, ks > 0);
+                        tc::mma_ts(D_UO, tmem + kColSLo + 8 * ks, dh, idc, 1);
+                        tc::mma_ts(D_UO, tmem + kColSHi + 8 * ks, dl, idc, 1);
+                    }
+                }
+                tc::commit(&s.bar_ch);  // also after a failure, so that the count stays in step
+                ++n_ch;
+            }
+            __syncwarp();
+            // while the product runs: M_{j+1} into the other buffer (its last reader, the
+            // product of step j - 1, has completed), R_j, and at the first step the first
+            // chunk's U' and [ -W ; Qhat ]
+            if (copier && j < chain && !fail) copy_m(j + 1, b ^ 1);
+            if (j == 1 && warp < 4 && c_begin < c_end) copy_up_wq(c_begin);
+            cp_async_commit();
+            if (!early_r) load_r(j);
+            const bool ok = wait_or_fail(&s.bar_ch, (uint32_t)b, fail, wlim);
+            // X <- D + R on this thread's key rows (D column n = key row n), and the planes
+            if (ok) {
+                uint32_t d0[32], d1[32];
+                tc::fence_after_sync();
+                tc::tmem_ld32_nowait(D_UO + lanes + r0, d0);
+                tc::tmem_ld32_nowait(D_UO + lanes + r0 + 32, d1);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int p = 0; p < 16; ++p) {
+                    Sh[p] = add2(Sh[p], pk2(__uint_as_float(d0[2 * p]), __uint_as_float(d0[2 * p + 1])));
+                    Sh[16 + p] = add2(Sh[16 + p], pk2(__uint_as_float(d1[2 * p]), __uint_as_float(d1[2 * p + 1])));
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 32; q += 16)
+                split32_tmem_pk(&Sh[q], tmem + lanes + kColSHi + r0 / 2 + q, tmem + lanes + kColSLo + r0 / 2 + q);
+            tc::tmem_wait_st();
+            if (early_r && j < chain) load_r(j + 1);
+        }
+        // every map copy has landed (each was waited for at the step that used it) and the
+        // last product has completed, so the chain buffers are free for the record tiles
+    }
+
+    if (warp < 4) {
+        // ------------- U and O warps; they also hold key rows 64 .. 127 of S -------------
+        // U' row i holds its 16-byte units (4 channels) XOR-swizzled by i % 32: a warp's
+        // reads of one row hit 32 distinct banks
+        auto up_at = [&](int i) { return i * kD + ((((dv >> 2) ^ (i & 31))) << 2) + (dv & 3); };
+        if (chain == 0) {
+            load_start();
+            if (c_begin < c_end) copy_up_wq(c_begin);
+        }
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async();  // the first [ -W ; Qhat ], for group 1
@@ -718,16 +836,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         if (c_begin + 1 < c_end) copy_ak(c_begin + 1);
         cp_async_commit();
         // key rows 0 .. 63 of this thread's value column (the U and O warps hold the rest)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = 2 * j;
-            Sh[j] = S0 ? pk2(S0[(int64_t)r * kD + dv], S0[(int64_t)(r + 1) * kD + dv])
-                       : pk2((identity && r == dv) ? 1.f : 0.f, (identity && r + 1 == dv) ? 1.f : 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 32; j += 16)
-            split32_tmem_pk(&Sh[j], tmem + lanes + kColSHi + j, tmem + lanes + kColSLo + j);
-        tc::tmem_wait_st();
+        if (chain == 0) load_start();
         tc::fence_before_sync();
         named_sync(4, 128);  // initial S^T planes of rows 0 .. 63 complete
         named_sync(kBarOR, 256);
@@ -792,6 +901,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             // and TMEM are released, and report through the status word
             if (n_m1 > 0) tc::mbar_wait(&s.bar_m1, (uint32_t)((n_m1 - 1) & 1), wlim);
             if (n_m2 > 0) tc::mbar_wait(&s.bar_m2, (uint32_t)((n_m2 - 1) & 1), wlim);
+            if (n_ch > 0) tc::mbar_wait(&s.bar_ch, (uint32_t)((n_ch - 1) & 1), wlim);
             atomicExch(status, -7);
         }
     }
@@ -801,7 +911,35 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     __syncthreads();
     // the final state: rows 0 .. 63 from the state warps, 64 .. 127 from the U and O warps
     // (every wait has ended: the failure flag is final)
-    if (Sout) {
+    if (kChain && Sout && (unit.flags & kUnitOutPlanes)) {
+        // as the split planes of B[n][k] = S[n][k]: each thread's column k = dv goes into a
+        // row-major staging image (the 16-byte units of row n XOR-swizzled by n % 8, so that
+        // neither the column writes nor the unit reads below conflict), then out in the
+        // interleaved order, 16 bytes per thread and step
+        const bool failed = fail;
+        unsigned char *img = s.wq;  // 64 KB over wq and ak, free now
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float2 v = upk2(Sh[j]);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int n = r0 + 2 * j + e;
+                const float x = failed ? __int_as_float(0x7fc00000) : (e ? v.y : v.x);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+                const int off = n * 2 * kD + ((((dv >> 3) ^ (n & 7))) << 4) + (dv & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(img + off) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(img + kPlaneSS + off) = lo;
+            }
+        }
+        __syncthreads();
+        uint4 *dst = reinterpret_cast<uint4 *>(Sout);
+        for (int u = tid; u < 2 * kPlaneSS / 16; u += kWalkThreads) {
+            const int pl = u / (kPlaneSS / 16), gu = u % (kPlaneSS / 16);
+            const int n = ((gu >> 7) << 3) | (gu & 7), k8 = (gu >> 3) & 15;  // gu * 16 = il_off(n, 8 k8, 128)
+            dst[u] = *reinterpret_cast<const uint4 *>(img + pl * kPlaneSS + n * 2 * kD + ((k8 ^ (n & 7)) << 4));
+        }
+    } else if (Sout) {
         const bool failed = fail;
         float *dst = Sout + (warp >= 4 ? 0 : (int64_t)64 * kD) + dv;
 #pragma unroll
@@ -847,18 +985,21 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
 }
 
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
-                        int32_t H, const uint8_t *records, void *o, int o_f32, cudaStream_t st) {
+                        int32_t H, const uint8_t *records, void *o, int o_f32, int chained, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kda_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(kda_walk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)sizeof(WalkSmem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kda_walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sizeof(WalkSmem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
     if (max_units <= 0) return cudaSuccess;
-    dim3 grid((unsigned)max_units, (unsigned)H);
-    return launch_after(kda_walk_kernel, grid, dim3(kWalkThreads), sizeof(WalkSmem), st, status, units, n_units, H,
-                        records, o, o_f32);
+    const dim3 grid((unsigned)max_units, (unsigned)H);
+    return launch_after(chained ? kda_walk_kernel<true> : kda_walk_kernel<false>, grid, dim3(kWalkThreads),
+                        sizeof(WalkSmem), st, status, units, n_units, H, records, o, o_f32);
 }
 
 }  // namespace kda

@@ -268,10 +268,10 @@ def test_segmented_walk_random(seed):
         else:
             lens.append(int(rng.integers(2000, 4000)))
     total = int(sum(lens))
-    if kda.kda_chunk_prefill_launch_count(total, n, H) != 5:
+    if kda.kda_chunk_prefill_launch_count(total, n, H) == 3:
         lens[0] += 64 * 24 * n  # long enough on average for the segmented walk
         total = int(sum(lens))
-    assert kda.kda_chunk_prefill_launch_count(total, n, H) == 5, (lens, H)
+    assert kda.kda_chunk_prefill_launch_count(total, n, H) in (4, 5), (lens, H)
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
     inp = inputs.prefill_inputs(total, H, n, seed=200 + seed, init_state=True)
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
@@ -296,15 +296,18 @@ def _slow_memory(inp, log_a=0.001, b_mean=-3.0, seed=0):
     return inp
 
 
-@pytest.mark.parametrize("lens,H", [([3000, 1800], 2), ([5000], 1)])
-def test_segmented_walk_slow_memory(lens, H):
+@pytest.mark.parametrize("lens,H,launches", [([3000, 1800], 2, 4), ([5000], 1, 4), ([10240, 10000, 10480], 5, 5)])
+def test_segmented_walk_slow_memory(lens, H, launches):
     """The segmented walk where the segment maps matter: with weak decay and weak writes
-    the map M of a segment (its state from the identity) stays of order one, so the phase-B
+    the map M of a segment (its state from the identity) stays of order one, so the
     products M S_in carry the state from segment to segment ('From Linear Attention to
-    KDA', §7.5). Against the oracle, element by element."""
+    KDA', §7.5). Both forms: each output walk chaining the maps before it on the tensor
+    cores (4 launches; [5000] x 1 cuts ten segments, so the last one chains eight maps),
+    and the combine kernel (5 launches: 3 sequences x 5 heads in 32-segment tables).
+    Against the oracle, element by element."""
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
     n = len(lens)
-    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == 5, (lens, H)
+    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == launches, (lens, H)
     inp = _slow_memory(inputs.prefill_inputs(cu[-1], H, n, seed=31, init_state=True), seed=32)
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
                                       cu_seqlens=cu)
