@@ -96,7 +96,8 @@ struct WalkUnit {
                       // nullptr: not kept
     // maps applied to the start state before the walk, in order: X <- M_j X + R_j for
     // j = 1 .. chain. M_j of head h is at maps + ((j - 1) H + h) * 128 * 128 floats, stored
-    // as split bf16 planes (kUnitOutPlanes); R_j at offs, same indexing, fp32 rows
+    // as split bf16 planes (kUnitOutPlanes); R_j at offs, same indexing, in quads
+    // (kUnitOutQuads)
     const float *maps, *offs;
     int32_t c_begin, c_end;  // chunk-record slots
     int32_t t_begin, t_end;  // tokens of those chunks (the last chunk may be partial)
@@ -109,6 +110,11 @@ constexpr int kUnitIdentity = 4;   // start from the identity when in == nullptr
 constexpr int kUnitOutPlanes = 8;  // keep the end state S as the two bf16 planes (hi, then
                                    // lo = bf16(S - hi)) of the tensor-core operand B[n][k] =
                                    // S[n][k], interleaved K-major (il_off(n, k, 128)), 32 KB each
+// the quad layout of a state: S[r][c] at ((r / 4) * 128 + c) * 4 + r % 4, so that the walk
+// thread of value column c reads or writes four key rows with one 16-byte access, and a
+// warp's 32 columns are 512 contiguous bytes
+constexpr int kUnitOutQuads = 16;  // keep the end state in the quad layout
+constexpr int kUnitInQuads = 32;   // the start state is in the quad layout
 constexpr size_t kStateFloats = (size_t)kD * kD;
 
 // Tables of the segmented walk, built by the plan kernel when P > 0 (segment length in

@@ -117,6 +117,7 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
                 }
                 // phase A: the end state only (a walk without outputs is cheaper) ...
                 u.out = Sin + (size_t)(g + 1) * seg_stride;
+                u.flags = kUnitAddUp | (sp.chain_mode ? kUnitOutQuads : 0);
                 unitsA[a++] = u;
                 // ... phase C: again with outputs, alongside the other segments
                 u.out = nullptr;
@@ -125,8 +126,10 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
                 continue;
             }
             // phase C
+            u.flags = kUnitWriteO | kUnitAddUp;
             if (sp.chain_mode) {  // from segment 1's input through the maps of segments 1 .. sg - 1
                 u.in = Sin + (size_t)(g + 1) * seg_stride;
+                u.flags |= kUnitInQuads;
                 u.chain = sg - 1;
                 if (sg > 1) {
                     u.maps = Mseg + (size_t)(g + 1) * seg_stride;
@@ -136,14 +139,13 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
                 u.in = Sin + (size_t)(g + sg) * seg_stride;
             }
             u.out = sg == S - 1 ? fin : nullptr;
-            u.flags = kUnitWriteO | kUnitAddUp;
             unitsC[cc++] = u;
             // phase A: this segment's map
             if (sg <= S - 2) {
                 u.in = u.maps = u.offs = nullptr;
                 u.chain = 0;
                 u.out = Rseg + (size_t)(g + sg) * seg_stride;
-                u.flags = kUnitAddUp;
+                u.flags = kUnitAddUp | (sp.chain_mode ? kUnitOutQuads : 0);
                 unitsA[a++] = u;
                 u.out = Mseg + (size_t)(g + sg) * seg_stride;
                 u.flags = kUnitIdentity | (sp.chain_mode ? kUnitOutPlanes : 0);
@@ -550,12 +552,26 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     };
     // this thread's key rows of the start state, and their split S^T planes
     const int r0 = warp >= 4 ? 0 : 64;
-    auto load_start = [&]() {
+    // a state in the quad layout (the chained form's own states): 16 float4 per thread
+    auto load_quads = [&](const float *X) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(X) + (r0 / 4) * kD + dv;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = r0 + 2 * j;
-            Sh[j] = S0 ? pk2(S0[(int64_t)r * kD + dv], S0[(int64_t)(r + 1) * kD + dv])
-                       : pk2((identity && r == dv) ? 1.f : 0.f, (identity && r + 1 == dv) ? 1.f : 0.f);
+        for (int q = 0; q < 16; ++q) {
+            const float4 v = x4[q * kD];
+            Sh[2 * q] = pk2(v.x, v.y);
+            Sh[2 * q + 1] = pk2(v.z, v.w);
+        }
+    };
+    auto load_start = [&]() {
+        if (kChain && (unit.flags & kUnitInQuads)) {
+            load_quads(S0);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int r = r0 + 2 * j;
+                Sh[j] = S0 ? pk2(S0[(int64_t)r * kD + dv], S0[(int64_t)(r + 1) * kD + dv])
+                           : pk2((identity && r == dv) ? 1.f : 0.f, (identity && r + 1 == dv) ? 1.f : 0.f);
+            }
         }
 #pragma unroll
         for (int j = 0; j < 32; j += 16)
@@ -582,14 +598,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 cp_async16(dst, src + 16 * u);
             }
         };
-        // R_j of this thread's key rows into Sh (dead there: X is in the planes); the step's
-        // epilogue adds the product. The issuer's warp loads it a step early, before it
-        // issues; the other warps while the product runs.
+        // R_j of this thread's key rows, in flight in rq until the step's epilogue adds the
+        // product (nothing reads them before, so the loads do not hold the thread up). The
+        // issuer's warp loads it a step early, before it issues; the other warps first
+        // thing while the product runs.
         const bool early_r = warp == 4;
+        float4 rq[16];
         auto load_r = [&](int j) {
-            const float *R = unit.offs + ((size_t)(j - 1) * H + h) * kStateFloats + dv;
+            const float4 *x4 =
+                reinterpret_cast<const float4 *>(unit.offs + ((size_t)(j - 1) * H + h) * kStateFloats) +
+                (r0 / 4) * kD + dv;
 #pragma unroll
-            for (int p = 0; p < 32; ++p) Sh[p] = pk2(R[(int64_t)(r0 + 2 * p) * kD], R[(int64_t)(r0 + 2 * p + 1) * kD]);
+            for (int q = 0; q < 16; ++q) rq[q] = x4[q * kD];
         };
         if (copier) copy_m(1, 0);
         cp_async_commit();
@@ -618,25 +638,26 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 ++n_ch;
             }
             __syncwarp();
-            // while the product runs: M_{j+1} into the other buffer (its last reader, the
-            // product of step j - 1, has completed), R_j, and at the first step the first
+            // while the product runs: R_j, M_{j+1} into the other buffer (its last reader,
+            // the product of step j - 1, has completed), and at the first step the first
             // chunk's U' and [ -W ; Qhat ]
+            if (!early_r) load_r(j);
             if (copier && j < chain && !fail) copy_m(j + 1, b ^ 1);
             if (j == 1 && warp < 4 && c_begin < c_end) copy_up_wq(c_begin);
             cp_async_commit();
-            if (!early_r) load_r(j);
             const bool ok = wait_or_fail(&s.bar_ch, (uint32_t)b, fail, wlim);
             // X <- D + R on this thread's key rows (D column n = key row n), and the planes
             if (ok) {
-                uint32_t d0[32], d1[32];
+                uint32_t d[2][32];
                 tc::fence_after_sync();
-                tc::tmem_ld32_nowait(D_UO + lanes + r0, d0);
-                tc::tmem_ld32_nowait(D_UO + lanes + r0 + 32, d1);
+                tc::tmem_ld32_nowait(D_UO + lanes + r0, d[0]);
+                tc::tmem_ld32_nowait(D_UO + lanes + r0 + 32, d[1]);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int p = 0; p < 16; ++p) {
-                    Sh[p] = add2(Sh[p], pk2(__uint_as_float(d0[2 * p]), __uint_as_float(d0[2 * p + 1])));
-                    Sh[16 + p] = add2(Sh[16 + p], pk2(__uint_as_float(d1[2 * p]), __uint_as_float(d1[2 * p + 1])));
+                for (int q = 0; q < 16; ++q) {
+                    const uint32_t *dq = &d[q >> 3][4 * (q & 7)];
+                    Sh[2 * q] = add2(pk2(rq[q].x, rq[q].y), pk2(__uint_as_float(dq[0]), __uint_as_float(dq[1])));
+                    Sh[2 * q + 1] = add2(pk2(rq[q].z, rq[q].w), pk2(__uint_as_float(dq[2]), __uint_as_float(dq[3])));
                 }
             }
 #pragma unroll
@@ -938,6 +959,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const int pl = u / (kPlaneSS / 16), gu = u % (kPlaneSS / 16);
             const int n = ((gu >> 7) << 3) | (gu & 7), k8 = (gu >> 3) & 15;  // gu * 16 = il_off(n, 8 k8, 128)
             dst[u] = *reinterpret_cast<const uint4 *>(img + pl * kPlaneSS + n * 2 * kD + ((k8 ^ (n & 7)) << 4));
+        }
+    } else if (kChain && Sout && (unit.flags & kUnitOutQuads)) {
+        const bool failed = fail;
+        float4 *d4 = reinterpret_cast<float4 *>(Sout) + (r0 / 4) * kD + dv;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float2 a = upk2(Sh[2 * q]), b = upk2(Sh[2 * q + 1]);
+            const float nan = __int_as_float(0x7fc00000);
+            d4[q * kD] = failed ? make_float4(nan, nan, nan, nan) : make_float4(a.x, a.y, b.x, b.y);
         }
     } else if (Sout) {
         const bool failed = fail;
