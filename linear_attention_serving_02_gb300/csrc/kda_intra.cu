@@ -47,10 +47,10 @@
 //   all        Gram operands (A into TMEM, B into shared memory); MMA chain issued
 //   all        Khat (the [W | U'] operand), Qhat, Kend^T, gamma (record), while the chain runs
 //   12 warps   A_qk -> record, A_kk -> shared memory
-//   all        the next item's q, k and the z of the one after it are requested
-//   warps 0-3  the UT solve's diagonal blocks (a latency chain: running other work beside
-//              it on the same schedulers doubled its time), then all warps its other blocks
-//   all        T' split; [W | U'] chain issued; the next item's gate while it runs
+//   warps 0-1  the UT solve's diagonal blocks (one column per thread) while the others
+//              request the z of the item after next; then all warps the solve's other blocks
+//   all        T' split; [W | U'] chain issued; while it runs, the next item's q and k
+//              are requested and its gate computed
 //   all        -W and U' staged in shared memory, two bulk stores
 // Inputs arrive by cp.async; every thread arrives once per load on that load's mbarrier
 // (count 512), so any warp can wait for a whole tile.
@@ -215,9 +215,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         }
         cp_async_arrive(&s.bar_z[b]);
     };
-    auto stage_qk = [&](const Item &it, int t0 = 0, int nt = kIntraThreads) {
+    auto stage_qk = [&](const Item &it) {
 #pragma unroll 4
-        for (int e = tid - t0; e >= 0 && e < 2 * kC * (kD / 8); e += nt) {
+        for (int e = tid; e < 2 * kC * (kD / 8); e += kIntraThreads) {
             // 16 consecutive units of one row of q, then of k: q and k lie a multiple of 128
             // bytes apart, so alternating them per unit put two lanes on each bank group
             const int which = (e >> 4) & 1, i = e >> 5, c = (e & 15) * 8;
@@ -487,50 +487,41 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         const float2 pre = has_next ? gate_inputs(nxt) : make_float2(0.f, 0.f);
 
         // ---- UT transform: T = (I + A_kk)^-1, unit lower triangular ---------------------
-        // The diagonal 16 x 16 blocks on warps 0-3, warp a solving block a: lane i holds row
-        // i of A_aa and of T_aa in registers (lanes 16-31 mirror lanes 0-15 and store
-        // nothing); T starts as I and, for m = 0 .. 14 in order, every row i > m subtracts
-        // A[i][m] * (row m, now final), broadcast by shuffles. The other warps zero the
-        // blocks above the diagonal.
-        if (warp < 4) {
-            const int base = warp * kTile, i = lane & 15;
-            float a[kTile], t[kTile];
+        // The diagonal 16 x 16 blocks on warps 0-1, thread (block a, column j) solving
+        // (I + A_aa) t = e_j by forward substitution: t_i = [i = j] - sum_{m < i} A[i][m] t_m,
+        // each row of A_aa read with float4 broadcasts (the 16 threads of a block read the
+        // same row). Every row's sum can start as soon as its first terms are known, so the
+        // dependent chain is about one FMA per row. The other warps zero the blocks above
+        // the diagonal.
+        if (warp < 2) {
+            const int base = (tid >> 4) * kTile, j = tid & 15;
+            float t[kTile];
 #pragma unroll
-            for (int q4 = 0; q4 < kTile; q4 += 4) {
-                const float4 av = *reinterpret_cast<const float4 *>(&s.u.s.Akk[base + i][base + q4]);
-                a[q4] = av.x; a[q4 + 1] = av.y; a[q4 + 2] = av.z; a[q4 + 3] = av.w;
-            }
+            for (int i = 0; i < kTile; ++i) {
+                float acc = 0.f;
 #pragma unroll
-            for (int j = 0; j < kTile; ++j) t[j] = (j == i) ? 1.f : 0.f;
+                for (int m4 = 0; m4 < i; m4 += 4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(&s.u.s.Akk[base + i][base + m4]);
+                    const float am[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-            for (int m = 0; m < kTile - 1; ++m) {
-#pragma unroll
-                for (int j = 0; j <= m; ++j) {  // row m is zero beyond its diagonal
-                    const float tm = __shfl_sync(0xffffffffu, t[j], m, 16);
-                    if (i > m) t[j] = __fmaf_rn(-a[m], tm, t[j]);
+                    for (int u = 0; u < 4; ++u)
+                        if (m4 + u < i) acc = __fmaf_rn(am[u], t[m4 + u], acc);
                 }
+                t[i] = ((i == j) ? 1.f : 0.f) - acc;
             }
-            if (lane < kTile) {
 #pragma unroll
-                for (int q4 = 0; q4 < kTile; q4 += 4)
-                    *reinterpret_cast<float4 *>(&s.u.s.T[base + i][base + q4]) =
-                        make_float4(t[q4], t[q4 + 1], t[q4 + 2], t[q4 + 3]);
-            }
+            for (int i = 0; i < kTile; ++i) s.u.s.T[base + i][base + j] = t[i];
         } else {
-            for (int e = tid - 128; e < kC * kC; e += kIntraThreads - 128) {
+            for (int e = tid - 64; e < kC * kC; e += kIntraThreads - 64) {
                 const int i = e / kC, j = e % kC;
                 if ((j >> 4) > (i >> 4)) s.u.s.T[i][j] = 0.f;
             }
-            // q, k and this item's G are read no more: the next item's q and k, and the z of
-            // the item after it (into this G buffer), are requested by these warps while
-            // warps 0-3 solve (every thread still arrives on the loads' mbarriers)
-            if (has_next) stage_qk(nxt, 128, kIntraThreads - 128);
-            if (has_next2) stage_z(nxt2, b, 128, kIntraThreads - 128);
+            // this item's G is read no more: the z of the item after next is requested into
+            // its buffer by these warps while warps 0-1 solve (every thread still arrives on
+            // the load's mbarrier)
+            if (has_next2) stage_z(nxt2, b, 64, kIntraThreads - 64);
         }
-        if (warp < 4) {
-            if (has_next) cp_async_arrive(&s.bar_qk);
-            if (has_next2) cp_async_arrive(&s.bar_z[b]);
-        }
+        if (warp < 2 && has_next2) cp_async_arrive(&s.bar_z[b]);
         __syncthreads();
         // The blocks below the diagonal by doubling, the sums in k order:
         //   16 -> 32:  T_10 = -T_11 (A_10 T_00),  T_32 = -T_33 (A_32 T_22)
@@ -623,7 +614,9 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             }
             tc::commit(&s.bar_wu);
         }
-        // while the [W | U'] chain runs: the next item's gate (its z landed long before)
+        // while the [W | U'] chain runs: q and k are read no more, so the next item's are
+        // requested; then the next item's gate (its z landed long before)
+        if (has_next) stage_qk(nxt);
         if (has_next) gate(nxt, b ^ 1, ((iters + 1) >> 1) & 1, pre);
         intra_wait(&s.bar_wu, ph, fail, status);
         tc::fence_after_sync();
