@@ -51,15 +51,15 @@ namespace kda {
 // segmented walk: tables of the two phases, written by one thread of the plan kernel
 // (used only when there are few sequences). Segment g of the batch is segment sigma of
 // sequence n, g = seg_base[n] + sigma; its affine map is S_out = M[g] S_in + R[g].
-//   phase A  segment 0 from the initial state -> Sin[g0 + 1] (segment 1's input); with one
-//            segment, the whole walk with o and the final state instead
+//   phase A  segment 0 from the initial state -> Sin[g0 + 1] (segment 1's input)
 //            segment sigma (1 .. S-2) from zero     -> R[g],  with U'
 //            segment sigma (1 .. S-2) from identity -> M[g],  without U' (in the chained
 //            form kept as the split bf16 planes the tensor cores read)
 //            (walks without outputs read only -W and Kend^T of the records)
 //   phase B  (combine form) Sin[g + 1] = M[g] Sin[g] + R[g] for sigma = 1 .. S-2, by
 //            kda_combine_kernel
-//   phase C  segments 0 .. S-1, writing o; the last one writes the final state. Segment
+//   phase C  segments 0 .. S-1, writing o (a sequence of one segment only here); the last
+//            one writes the final state. Segment
 //            sigma >= 1 starts from Sin[g0 + sigma] (combine form), or (chained form) from
 //            Sin[g0 + 1], first applying X <- M[g0 + j] X + R[g0 + j] for j = 1 .. sigma - 1
 //            on the tensor cores (the chained form is taken only when all of phase C runs
@@ -109,10 +109,10 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
             u.t_end = min(t1, t0 + (sg + 1) * P * kC);
             if (sg == 0) {
                 u.in = init;
-                if (S == 1) {  // phase A: the sequence's only walk, with outputs
+                if (S == 1) {  // phase C: the sequence's only walk, with outputs
                     u.out = fin;
                     u.flags = kUnitWriteO | kUnitAddUp;
-                    unitsA[a++] = u;
+                    unitsC[cc++] = u;
                     continue;
                 }
                 // phase A: the end state only (a walk without outputs is cheaper) ...
@@ -463,9 +463,12 @@ __device__ __forceinline__ bool wait_in_order(uint64_t *bar, uint32_t parity, vo
     return !fail;
 }
 
-// kChain: the form that can chain segment maps before its first chunk and keep an end
-// state as split planes (the segmented walk's chained form); without it, neither.
-template <bool kChain>
+// Three instances, each holding only its own code (a kernel with every path in it stalled
+// on instruction fetch): kWalkOut walks with outputs; kWalkChain the same, first chaining
+// segment maps (the chained form's phase C); kWalkMaps walks without outputs (phase A:
+// segment maps, end states kept as split planes or in quads).
+constexpr int kWalkOut = 0, kWalkChain = 1, kWalkMaps = 2;
+template <int kForm>
 __global__ void __launch_bounds__(kWalkThreads, 1)
     kda_walk_kernel(int32_t *__restrict__ status, const WalkUnit *__restrict__ units,
                     const int32_t *__restrict__ n_units, int32_t H, const uint8_t *__restrict__ records,
@@ -482,7 +485,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     const int skip_commit = g_walk_skip_commit;
     const float *S0 = unit.in ? unit.in + (size_t)h * kStateFloats : nullptr;
     float *Sout = unit.out ? unit.out + (size_t)h * kStateFloats : nullptr;
-    const bool write_o = (unit.flags & kUnitWriteO) != 0;
+    constexpr bool kChain = kForm == kWalkChain, kMaps = kForm == kWalkMaps;
+    constexpr bool write_o = !kMaps;  // the plan gives every unit of an instance its form
     const bool add_up = (unit.flags & kUnitAddUp) != 0;
     const bool identity = (unit.flags & kUnitIdentity) != 0;
     const int dv = (warp & 3) * 32 + lane;  // value channel = TMEM lane (warps 0-7)
@@ -517,7 +521,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 
     // A walk without outputs (segment maps) needs only -W and Kend^T: it copies those
     // parts of the record and runs group 1 with N = 64, group 2 with N = 128.
-    const bool maps = !write_o;
+    constexpr bool maps = kMaps;
     const uint32_t ds_col = maps ? 0u : 64u;  // TMEM column of D_S within D_AK
     // this thread's half of its value column of S: key rows 0 .. 63 in the state warps,
     // 64 .. 127 in the U and O warps, so that both halves are updated at the same time
@@ -932,7 +936,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     __syncthreads();
     // the final state: rows 0 .. 63 from the state warps, 64 .. 127 from the U and O warps
     // (every wait has ended: the failure flag is final)
-    if (kChain && Sout && (unit.flags & kUnitOutPlanes)) {
+    if (kMaps && Sout && (unit.flags & kUnitOutPlanes)) {
         // as the split planes of B[n][k] = S[n][k]: each thread's column k = dv goes into a
         // row-major staging image (the 16-byte units of row n XOR-swizzled by n % 8, so that
         // neither the column writes nor the unit reads below conflict), then out in the
@@ -960,7 +964,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const int n = ((gu >> 7) << 3) | (gu & 7), k8 = (gu >> 3) & 15;  // gu * 16 = il_off(n, 8 k8, 128)
             dst[u] = *reinterpret_cast<const uint4 *>(img + pl * kPlaneSS + n * 2 * kD + ((k8 ^ (n & 7)) << 4));
         }
-    } else if (kChain && Sout && (unit.flags & kUnitOutQuads)) {
+    } else if (kMaps && Sout && (unit.flags & kUnitOutQuads)) {
         const bool failed = fail;
         float4 *d4 = reinterpret_cast<float4 *>(Sout) + (r0 / 4) * kD + dv;
 #pragma unroll
@@ -1015,21 +1019,26 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
 }
 
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
-                        int32_t H, const uint8_t *records, void *o, int o_f32, int chained, cudaStream_t st) {
+                        int32_t H, const uint8_t *records, void *o, int o_f32, int form, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kda_walk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(kda_walk_kernel<kWalkOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)sizeof(WalkSmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kda_walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(kda_walk_kernel<kWalkChain>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sizeof(WalkSmem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kda_walk_kernel<kWalkMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)sizeof(WalkSmem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
     if (max_units <= 0) return cudaSuccess;
     const dim3 grid((unsigned)max_units, (unsigned)H);
-    return launch_after(chained ? kda_walk_kernel<true> : kda_walk_kernel<false>, grid, dim3(kWalkThreads),
-                        sizeof(WalkSmem), st, status, units, n_units, H, records, o, o_f32);
+    auto kernel = form == kWalkChain ? kda_walk_kernel<kWalkChain>
+                                     : (form == kWalkMaps ? kda_walk_kernel<kWalkMaps> : kda_walk_kernel<kWalkOut>);
+    return launch_after(kernel, grid, dim3(kWalkThreads), sizeof(WalkSmem), st, status, units, n_units, H, records, o,
+                        o_f32);
 }
 
 }  // namespace kda
