@@ -96,7 +96,8 @@ def kda_chunk_prefill_workspace_size(total_tokens, num_seqs, num_heads):
 
 
 def kda_chunk_prefill_launch_count(total_tokens, num_seqs, num_heads):
-    """Kernels one kda_chunk_prefill call with these sizes launches (3, or 5 for a segmented walk)."""
+    """Kernels one kda_chunk_prefill call with these sizes launches: 3, or for a segmented
+    walk 4 (its output walks chain the segment maps) or 5 (a combine kernel chains them)."""
     return int(library().kda_chunk_prefill_launch_count(int(total_tokens), int(num_seqs), int(num_heads)))
 
 
