@@ -68,8 +68,10 @@ int kda_version(void);
 /*
  * Test hook for the state walk's failure path (no counterpart on the pages). On the
  * current device, every later kda_chunk_prefill call leaves out the MMA-completion signal
- * of chunk slot skip_commit_chunk in its state walks (-1: none), and every wait of the
- * walk gives up after wait_limit_ns nanoseconds of the GPU clock (default 2e9). A walk
+ * of chunk slot skip_commit_chunk in its state walks (-1: none; -2 - j: that of map j of
+ * the map chain that a segmented walk's output walks run first, j = 0 the first), and
+ * every wait of the walk gives up after wait_limit_ns nanoseconds of the GPU clock
+ * (default 2e9). A walk
  * whose wait gives up skips the rest of its work, writes NaN into its final state and
  * sets the workspace status word to KDA_ERR_CUDA (see kda_workspace_status); no GPU fault
  * is involved and the context stays usable. Restore with (-1, 2000000000) before normal
@@ -91,9 +93,11 @@ size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, 
 /*
  * Number of kernels one kda_chunk_prefill() call with these sizes launches on its
  * stream: 0 when num_seqs is 0, 3 (plan, intra-chunk, state walk) when every
- * (sequence, head) chain walks its chunks in one pass, 4 when the chains are too few
- * to fill the GPU and the walk is split into segments (plan, intra-chunk, segment-map
- * walk, output walk that first chains the maps). Depends only on the three sizes,
+ * (sequence, head) chain walks its chunks in one pass, 4 or 5 when the chains are too
+ * few to fill the GPU and the walk is split into segments: plan, intra-chunk, segment-map
+ * walk, then either an output walk that first chains the maps (4: every output walk fits
+ * in one wave of the GPU) or a combine kernel and the output walk (5). Depends only on
+ * the three sizes,
  * like the workspace. Returns -1 for negative arguments.
  */
 int32_t kda_chunk_prefill_launch_count(int64_t total_tokens, int32_t num_seqs, int32_t num_heads);

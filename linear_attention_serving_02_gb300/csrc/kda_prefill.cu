@@ -441,8 +441,9 @@ __device__ __forceinline__ void split32_tmem_pk(const uint64_t *x, uint32_t t_hi
 }
 
 // Test hook (kda_debug_walk_fault): the walk's MMA issuer leaves out the group-1 commit of
-// chunk g_walk_skip_commit, and every wait of the walk gives up after g_walk_wait_ns, so
-// a wait runs out with no fault; -1 and the default limit otherwise.
+// chunk g_walk_skip_commit (or, for -2 - j, the commit of map j of the map chain), and
+// every wait of the walk gives up after g_walk_wait_ns, so a wait runs out with no fault;
+// -1 and the default limit otherwise.
 __device__ int g_walk_skip_commit = -1;
 __device__ unsigned long long g_walk_wait_ns = tc::kWaitLimitNs;
 
@@ -638,8 +639,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                         tc::mma_ts(D_UO, tmem + kColSHi + 8 * ks, dl, idc, 1);
                     }
                 }
-                tc::commit(&s.bar_ch);  // also after a failure, so that the count stays in step
-                ++n_ch;
+                if (skip_commit != -2 - (j - 1)) {  // (test hook: left out for one map)
+                    tc::commit(&s.bar_ch);  // also after a failure, so that the count stays in step
+                    ++n_ch;
+                }
             }
             __syncwarp();
             // while the product runs: R_j, M_{j+1} into the other buffer (its last reader,

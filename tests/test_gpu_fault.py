@@ -1,6 +1,7 @@
 """The state walk's failure path, made to happen without a GPU fault: a host-set hook
-makes the walk's MMA issuer leave out one chunk's completion signal, so the waits behind
-it run out (after a shortened limit) while every MMA still completes. The walk must then
+makes the walk's MMA issuer leave out one chunk's (or one chained map's) completion
+signal, so the waits behind it run out (after a shortened limit) while every MMA still
+completes. The walk must then
 report KDA_ERR_CUDA through the workspace status word, fill its final state with NaN,
 leave the context usable, and a clean call afterwards must match the oracle."""
 import numpy as np
@@ -20,15 +21,22 @@ def _cuda(inp):
     return {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
-@pytest.mark.parametrize("T", [192, 4096])  # the plain walk; the segmented walk (one long sequence)
-def test_walk_wait_runs_out_and_is_reported(T):
+@pytest.mark.parametrize("T,skip", [
+    (192, 1),     # the plain walk: chunk slot 1's group-1 signal
+    (4096, 1),    # the segmented walk (one long sequence, 11 segments of 6 chunks)
+    (4096, -2),   # ... the first map of the output walks' map chain
+    (4096, -5),   # ... its fourth map (only the segments with at least four maps fail)
+])
+def test_walk_wait_runs_out_and_is_reported(T, skip):
     H = 2
     inp_cpu = inputs.prefill_inputs(T, H, 1, seed=41, init_state=True)
     inp = _cuda(inp_cpu)
     ws = torch.empty(kda.kda_chunk_prefill_workspace_size(T, 1, H), dtype=torch.uint8, device="cuda")
     o = torch.empty(inp["q"].shape, dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
-    kda.kda_debug_walk_fault(1, 1_000_000)  # chunk slot 1; waits give up after 1 ms
+    if skip < 0:  # the map chain runs only in the chained segmented form
+        assert kda.kda_chunk_prefill_launch_count(T, 1, H) == 4
+    kda.kda_debug_walk_fault(skip, 1_000_000)  # waits give up after 1 ms
     try:
         _, S = kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"],
                                      initial_state=inp["S0"], o=o, workspace=ws, o_dtype=torch.float32)
