@@ -19,7 +19,8 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
                          const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t nslots,
                          uint8_t *records, int num_sms, cudaStream_t st);
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
-                        int32_t H, const uint8_t *records, void *o, int o_f32, int form, cudaStream_t st);
+                        int32_t H, const uint8_t *records, void *o, int o_f32, int form, int head_major,
+                        cudaStream_t st);
 cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t N, int32_t H, float *Sin,
                            const float *Mseg, const float *Rseg, cudaStream_t st);
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
@@ -238,19 +239,21 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                           num_heads, cu_seqlens ? 0 : seq_len, w.nslots, records, dev.sms, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (w.P == 0) {
-        if (kda::launch_walk(status, units, counts, num_seqs, num_heads, records, o, o_f32, 0, st) != cudaSuccess)
+        // heads as the fastest grid index (the plan lists the longest sequences first)
+        if (kda::launch_walk(status, units, counts, num_seqs, num_heads, records, o, o_f32, 0, num_seqs <= 65535 ? 1 : 0,
+                             st) != cudaSuccess)
             return KDA_ERR_CUDA;
         return KDA_OK;
     }
     // segmented walk: phase A (segment maps), phase B (chain them: the combine kernel, or in
     // the chained form each output walk itself), phase C (outputs)
-    if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, 2, st) !=
+    if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, 2, 0, st) !=
         cudaSuccess)
         return KDA_ERR_CUDA;
     if (!sp.chain_mode &&
         kda::launch_combine(status, sp.chains, num_seqs, num_heads, sp.Sin, sp.Mseg, sp.Rseg, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_walk(status, sp.unitsC, sp.nC, w.seg_bound, num_heads, records, o, o_f32, sp.chain_mode ? 1 : 0,
+    if (kda::launch_walk(status, sp.unitsC, sp.nC, w.seg_bound, num_heads, records, o, o_f32, sp.chain_mode ? 1 : 0, 0,
                          st) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;

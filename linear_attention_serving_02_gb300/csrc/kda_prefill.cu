@@ -47,6 +47,7 @@ namespace kda {
 // ---------------------------------------------------------------------------------
 // plan: seq_cu[N+1] and chunk_off[N+1] (prefix sums of ceil(len / C)) in the workspace
 // ---------------------------------------------------------------------------------
+constexpr int kPlanSortMax = 1024;  // plain walks of up to this many sequences go longest first
 // ---------------------------------------------------------------------------------
 // segmented walk: tables of the two phases, written by one thread of the plan kernel
 // (used only when there are few sequences). Segment g of the batch is segment sigma of
@@ -158,10 +159,29 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
     *sp.nC = cc;
 }
 
+// the plain walk's unit of sequence n, from the finished sequence tables
+__device__ __forceinline__ WalkUnit plain_unit(int32_t n, int32_t H, const int32_t *seq_cu, const int32_t *chunk_off,
+                                               const float *S0, float *Sout) {
+    WalkUnit u;
+    u.in = S0 ? S0 + (size_t)n * H * kStateFloats : nullptr;
+    u.out = Sout + (size_t)n * H * kStateFloats;
+    u.maps = u.offs = nullptr;
+    u.c_begin = chunk_off[n];
+    u.c_end = chunk_off[n + 1];
+    u.t_begin = seq_cu[n];
+    u.t_end = seq_cu[n + 1];
+    u.flags = kUnitWriteO | kUnitAddUp;
+    u.chain = 0;
+    return u;
+}
+
 __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t N, int64_t seq_len,
                                 int64_t total_tokens, int32_t *__restrict__ status, int32_t *__restrict__ seq_cu,
                                 int32_t *__restrict__ chunk_off, int32_t H, const float *S0, float *Sout,
-                                WalkUnit *__restrict__ units, int32_t *__restrict__ n_units, SegPlan sp) {
+                                WalkUnit *__restrict__ units, int32_t *__restrict__ n_units, SegPlan sp,
+                                int sort_n) {
+    extern __shared__ uint64_t key[];  // sort_n keys (dynamic: the kernel runs beside the intra
+                                       // kernel's first CTAs and must not crowd an SM)
     __shared__ int32_t carry;
     __shared__ int32_t bad;
     __shared__ int32_t scan[256];
@@ -230,27 +250,42 @@ __global__ void kda_plan_kernel(const int32_t *__restrict__ cu_seqlens, int32_t 
         }
         // exclusive offset of sequence n = carry + inclusive(n) - len(n)
         if (n <= N) chunk_off[n] = carry + scan[tid] - len;
-        __syncthreads();
-        // the plain walk: one unit per sequence (read after this kernel, so the table
-        // entries of n + 1 written in the same pass are complete by then)
-        if (n < N) {
-            WalkUnit u;
-            u.in = S0 ? S0 + (size_t)n * H * kStateFloats : nullptr;
-            u.out = Sout + (size_t)n * H * kStateFloats;
-            u.c_begin = chunk_off[n];
-            u.c_end = chunk_off[n] + len;
-            u.t_begin = start;
-            u.t_end = cu_seqlens ? cu_seqlens[n + 1] : (int32_t)((n + 1) * seq_len);
-            u.maps = u.offs = nullptr;
-            u.flags = kUnitWriteO | kUnitAddUp;
-            u.chain = 0;
-            units[n] = u;
-        }
         if (tid == 255) carry += scan[255];
         __syncthreads();
     }
-    // the segmented walk's tables, from the offsets that the barrier above made visible
-    if (sp.P > 0 && tid == 0) plan_segments(false, seq_cu, chunk_off, N, H, S0, Sout, sp);
+    // the tables are complete and visible (barrier above)
+    if (sp.P > 0) {  // the segmented walk's tables
+        if (tid == 0) plan_segments(false, seq_cu, chunk_off, N, H, S0, Sout, sp);
+        return;
+    }
+    // the plain walk: one unit per sequence. Up to kPlanSortMax sequences are listed longest
+    // first (a bitonic sort of (chunks, sequence) keys over sort_n, the next power of two),
+    // and the walk launches heads as the fastest grid index, so that every head of the
+    // longest sequences starts in the first wave and the short ones fill in behind them.
+    if (sort_n < N) {
+        for (int32_t n = tid; n < N; n += blockDim.x) units[n] = plain_unit(n, H, seq_cu, chunk_off, S0, Sout);
+        return;
+    }
+    for (int i = tid; i < sort_n; i += blockDim.x)  // real keys above every pad key
+        key[i] = i < N ? ((uint64_t)(chunk_off[i + 1] - chunk_off[i] + 1) << 32) | (uint32_t)~i : 0ull;
+    __syncthreads();
+    for (int k = 2; k <= sort_n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < sort_n; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint64_t a = key[i], b = key[l];
+                    if (((i & k) == 0) ? (a < b) : (a > b)) {  // descending overall
+                        key[i] = b;
+                        key[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int r = tid; r < N; r += blockDim.x)
+        units[r] = plain_unit((int32_t)~(uint32_t)key[r], H, seq_cu, chunk_off, S0, Sout);
 }
 
 // Phase B: Sin[g + 1] = M[g] Sin[g] + R[g] along each sequence's segments, in fp32 on the
@@ -473,15 +508,16 @@ template <int kForm>
 __global__ void __launch_bounds__(kWalkThreads, 1)
     kda_walk_kernel(int32_t *__restrict__ status, const WalkUnit *__restrict__ units,
                     const int32_t *__restrict__ n_units, int32_t H, const uint8_t *__restrict__ records,
-                    void *__restrict__ o, int o_f32) {
+                    void *__restrict__ o, int o_f32, int head_major) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y;
+    const int h = head_major ? blockIdx.x : blockIdx.y;
+    const int ui = head_major ? blockIdx.y : blockIdx.x;
     pdl_wait();
     pdl_trigger();
-    if ((int)blockIdx.x >= *n_units) return;
-    const WalkUnit unit = units[blockIdx.x];
+    if (ui >= *n_units) return;
+    const WalkUnit unit = units[ui];
     const uint64_t wlim = g_walk_wait_ns;
     const int skip_commit = g_walk_skip_commit;
     const float *S0 = unit.in ? unit.in + (size_t)h * kStateFloats : nullptr;
@@ -1002,8 +1038,14 @@ cudaError_t set_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns) {
 cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t total, int32_t *status,
                         int32_t *seq_cu, int32_t *chunk_off, int32_t H, const float *S0, float *Sout, WalkUnit *units,
                         int32_t *n_units, const SegPlan &sp, cudaStream_t st) {
-    kda_plan_kernel<<<1, 256, 0, st>>>(cu, N, seq_len, total, status, seq_cu, chunk_off, H, S0, Sout, units,
-                                       n_units, sp);
+    int sort_n = 0;  // a plain walk of 2 .. kPlanSortMax sequences is sorted, over a power of two
+    if (sp.P == 0 && N >= 2 && N <= kPlanSortMax) {
+        sort_n = 2;
+        while (sort_n < N) sort_n <<= 1;
+    }
+    kda_plan_kernel<<<1, 256, (size_t)sort_n * sizeof(uint64_t), st>>>(cu, N, seq_len, total, status, seq_cu,
+                                                                        chunk_off, H, S0, Sout, units, n_units, sp,
+                                                                        sort_n);
     return cudaGetLastError();
 }
 
@@ -1022,7 +1064,8 @@ cudaError_t launch_combine(const int32_t *status, const int32_t *chains, int32_t
 }
 
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
-                        int32_t H, const uint8_t *records, void *o, int o_f32, int form, cudaStream_t st) {
+                        int32_t H, const uint8_t *records, void *o, int o_f32, int form, int head_major,
+                        cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kda_walk_kernel<kWalkOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1037,11 +1080,12 @@ cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n
         configured = true;
     }
     if (max_units <= 0) return cudaSuccess;
-    const dim3 grid((unsigned)max_units, (unsigned)H);
+    if (head_major && max_units > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid = head_major ? dim3((unsigned)H, (unsigned)max_units) : dim3((unsigned)max_units, (unsigned)H);
     auto kernel = form == kWalkChain ? kda_walk_kernel<kWalkChain>
                                      : (form == kWalkMaps ? kda_walk_kernel<kWalkMaps> : kda_walk_kernel<kWalkOut>);
     return launch_after(kernel, grid, dim3(kWalkThreads), sizeof(WalkSmem), st, status, units, n_units, H, records, o,
-                        o_f32);
+                        o_f32, head_major);
 }
 
 }  // namespace kda
