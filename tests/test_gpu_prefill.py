@@ -347,6 +347,23 @@ def test_plain_walk_random(seed):
     assert_prefill_close(o, S, o_ref, S_ref, "plain random %d sequences x %d" % (n, H))
 
 
+@pytest.mark.parametrize("n", [1024, 1100])
+def test_plain_walk_many_sequences(n):
+    """The plain walk's unit order: up to 1024 sequences are listed longest first (the plan
+    kernel's sort, padded to a power of two), more are left in sequence order; lengths
+    0 .. 200 with ties, one head, against the oracle."""
+    rng = np.random.default_rng(500 + n)
+    lens = [int(x) for x in rng.choice([0, 1, 5, 64, 65, 130, 200], size=n)]
+    total = int(sum(lens))
+    assert kda.kda_chunk_prefill_launch_count(total, n, 1) == 3
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    inp = inputs.prefill_inputs(total, 1, n, seed=600 + n, init_state=True)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
+                                      cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu)
+    assert_prefill_close(o, S, o_ref, S_ref, "plain walk, %d sequences" % n)
+
+
 @pytest.mark.parametrize("lens,H,o_dtype", [([300, 0, 1, 64, 129], 3, torch.bfloat16),   # plain walk
                                             ([5000, 0, 1700], 2, torch.float32)])      # segmented walk
 def test_every_output_written_over_poison(lens, H, o_dtype):
