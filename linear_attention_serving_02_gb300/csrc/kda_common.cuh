@@ -135,10 +135,12 @@ struct SegPlan {
 // the three phases, in units of one output-walk chunk step, fitted to measured walks:
 // with S segments of P chunks, phase A runs 2 S - 3 map walks per chain in
 // ceil((2 S - 3) chains / 152) waves of P + 2 steps (a map step costs about 0.83 of an
-// output step; the 2 covers a walk's start and end), the combine S - 2 chained products
-// (about 1.2 steps each), and phase C S walks per chain in ceil(S chains / 152) waves of
-// P + 2 steps. For 8192 tokens x 12 heads this keeps 7 segments of 19 chunks; for
-// 1,048,576 tokens x 12 heads it takes 38 segments of 432 chunks (phase A in six waves).
+// output step; the 2 covers a walk's start and end), the chain of S - 2 map products
+// (about 1.2 steps each as the combine kernel's; the output walks' own chain, taken when
+// phase C fits one wave, costs about 0.6 a map and keeps the same choice), and phase C S
+// walks per chain in ceil(S chains / 152) waves of P + 2 steps. For 8192 tokens x 12
+// heads this keeps 7 segments of 19 chunks; for 1,048,576 tokens x 12 heads it takes 38
+// segments of 432 chunks (phase A in six waves).
 __host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
     const int64_t chains = num_seqs * num_heads;
     if (chains <= 0) return 0;
