@@ -315,6 +315,20 @@ def test_segmented_walk_slow_memory(lens, H, launches):
     assert_prefill_close(o, S, o_ref, S_ref, "segmented, slow memory %s" % lens)
 
 
+@pytest.mark.parametrize("lens,H,launches", [([3000, 1800], 2, 4), ([10240, 10000, 10480], 5, 5)])
+def test_segmented_walk_without_initial_state(lens, H, launches):
+    """Both segmented forms with no initial state (zero): segment 0 starts from zero in
+    both phases, every later segment from what the maps carry. Weak decay and writes, so
+    the maps matter; against the oracle."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    n = len(lens)
+    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == launches, (lens, H)
+    inp = _slow_memory(inputs.prefill_inputs(cu[-1], H, n, seed=35), seed=36)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], cu_seqlens=cu)
+    o, S = gpu_prefill(inp, cu=cu, S0=None)
+    assert_prefill_close(o, S, o_ref, S_ref, "segmented, no initial state %s" % lens)
+
+
 def test_plain_walk_slow_memory():
     """The same weak decay and writes on the plain walk (many chains), 1,500 tokens."""
     lens = [1500] * 40
