@@ -823,7 +823,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // ----------------- state warps (thread 128 issues the MMAs) -----------------
         const bool issuer = (tid == 128);
         const uint32_t kIdG1 = tc::idesc_bf16_m128(maps ? 64 : 128);
-        const uint32_t kIdQl = tc::idesc_bf16_m128(64);
+        const uint32_t kIdG1w = tc::idesc_bf16_m128(192);  // [ -W ; Qhat hi ; Qhat lo ]
         // [ A_qk ; Kend^T ] is stored MN-major (its rows n contiguous per token): B transposed
         const uint32_t kIdG2 = tc::idesc_bf16(128, maps ? 128 : 192, 1);
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
@@ -842,15 +842,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 for (int u = tid - 128; u < 2 * kStackAK / 16; u += 128) cp_async16(dst + 16 * u, src + 16 * u);
             }
         };
-        // group 1 of the next chunk: [D_U | D_O1] = S^T [ -W ; Qhat ]^T
+        // group 1 of the next chunk: [D_U | D_O1 | D_O2] = S^T [ -W ; Qhat hi ; Qhat lo ]^T
         auto issue_g1 = [&](int c) {
             tc::fence_after_sync();
             if (!fail) {
-                // S^T hi and lo times the hi plane of [ -W ; Qhat ], and S^T hi times Qhat lo
-                // into the D_O1 half (W has one plane; a map walk has no Qhat)
+                // S^T hi times the three planes (N = 192: -W S, Qhat hi S, and Qhat lo S
+                // into D_O2, which group 2 then adds A_qk U to) and S^T lo times -W and
+                // Qhat hi (N = 128): 16 MMAs (W has one plane; a map walk has no Qhat)
                 // (unrolled: a loop issuing from one thread cost ~90 cycles per MMA, about
                 // what an N = 128 MMA takes to run)
-                const uint32_t b0s = tc::smem_addr(s.wq), b1s = b0s + (uint32_t)(2 * kPlaneQK);
+                const uint32_t b0s = tc::smem_addr(s.wq);
                 if (maps) {
 #pragma unroll
                     for (int ks = 0; ks < kD / 16; ++ks) {
@@ -862,9 +863,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 #pragma unroll
                     for (int ks = 0; ks < kD / 16; ++ks) {
                         const uint64_t b0 = tc::desc_k(b0s, kD, ks);
-                        tc::mma_ts(D_UO, tmem + kColSHi + 8 * ks, b0, kIdG1, ks > 0);
+                        tc::mma_ts(D_UO, tmem + kColSHi + 8 * ks, b0, kIdG1w, ks > 0);
                         tc::mma_ts(D_UO, tmem + kColSLo + 8 * ks, b0, kIdG1, 1);
-                        tc::mma_ts(D_UO + 64, tmem + kColSHi + 8 * ks, tc::desc_k(b1s, kD, ks), kIdQl, 1);
                     }
                 }
             }
@@ -873,7 +873,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 ++n_m1;
             }
         };
-        // group 2 of chunk c: [D_O2 | D_S] = U^T [ A_qk ; Kend^T ]^T
+        // group 2 of chunk c: [D_O2 | D_S] += U^T [ A_qk ; Kend^T ]^T; D_O2 holds Qhat lo S
+        // from group 1, so only D_S starts from zero: the first product is issued as two
+        // MMAs (A_qk rows accumulating, Kend^T rows not)
+        const uint32_t kIdAq = tc::idesc_bf16(128, 64, 1), kIdKe = tc::idesc_bf16(128, 128, 1);
         auto issue_g2 = [&](int c) {
             tc::fence_after_sync();
             const int slot = (c - c_begin) & 1;
@@ -883,7 +886,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint32_t a0 = tmem + kColUHi + 8 * ks, a1 = tmem + kColULo + 8 * ks;
                     const uint64_t b0 = tc::desc_k(b0s, kC, ks), b1 = tc::desc_k(b1s, kC, ks);
-                    tc::mma_ts(D_AK, a0, b0, kIdG2, ks > 0);
+                    if (ks > 0 || maps) {
+                        tc::mma_ts(D_AK, a0, b0, kIdG2, ks > 0);
+                    } else {
+                        tc::mma_ts(D_AK, a0, b0, kIdAq, 1);
+                        tc::mma_ts(D_AK + 64, a0, tc::desc_k(b0s + (uint32_t)kPlaneCC, kC, 0), kIdKe, 0);
+                    }
                     tc::mma_ts(D_AK, a0, b1, kIdG2, 1);
                     tc::mma_ts(D_AK, a1, b0, kIdG2, 1);
                 }
