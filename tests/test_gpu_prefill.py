@@ -379,7 +379,8 @@ def test_plain_walk_many_sequences(n):
 
 
 @pytest.mark.parametrize("lens,H,o_dtype", [([300, 0, 1, 64, 129], 3, torch.bfloat16),   # plain walk
-                                            ([5000, 0, 1700], 2, torch.float32)])      # segmented walk
+                                            ([5000, 0, 1700], 2, torch.float32),       # segmented, chained
+                                            ([10240, 10000, 10480], 5, torch.bfloat16)])  # segmented, combine
 def test_every_output_written_over_poison(lens, H, o_dtype):
     """o, final_state and the workspace start filled with NaN bytes: every output must be
     written (finite) and right, and nothing may read workspace that was not written."""
