@@ -32,7 +32,10 @@ constexpr int kLd64 = kC + 8;   // 64-wide tiles: 144 B per row
 //          Qh   q_i * exp(G_i), hi plane (rows 64..127)
 //          Ql   the lo plane of the same (hi + lo = the fp32 value to ~16 bits)
 //   AK  [ A_qk ; Kend^T ]  MN-major (N = 192, K = 64 tokens j), a hi and a lo plane
-//          n 0..63    decayed causal Q K^T, diagonal included (n = query token i)
+//          n 0..63    decayed causal Q K^T, diagonal included (n = query token i); its
+//                     128-byte blocks of 8 query rows x 8 keys that lie wholly above the
+//                     diagonal (key group > query group: 28 of 64) are zero and are
+//                     neither written nor read: a reader keeps them zero on its side
 //          n 64..191  k_j * exp(G_last - G_j), transposed     (n = key channel c)
 //   gam  [128]   fp32   exp(G_last), the chunk's total decay
 //   Up   [64][128] fp32 U' = T' V, token-major (row i, column = value channel); the
@@ -63,6 +66,15 @@ static_assert(kRecAK % 16 == 0 && kRecGam % 16 == 0 && kRecUp % 16 == 0, "record
 __host__ __device__ constexpr uint32_t ak_off(int n, int j) {
     return (uint32_t)((n >> 3) * 1024 + (j >> 3) * 128 + (j & 7) * 16 + (n & 7) * 2);
 }
+// whether the A_qk element (query row n, key j) lies in a 128-byte block of the plane that
+// is wholly above the diagonal (its 8 keys all come after its 8 query rows): such blocks
+// are zero and stay out of the record
+__host__ __device__ constexpr bool aqk_zero_block(int n, int j) { return (j >> 3) > (n >> 3); }
+// the same for the 16-byte unit u of an A_qk plane (u = ak_off / 16, u < 512)
+__host__ __device__ constexpr bool aqk_zero_unit(int u) { return ((u >> 3) & 7) > (u >> 6); }
+static_assert(aqk_zero_unit((int)(ak_off(7, 8) / 16)) && !aqk_zero_unit((int)(ak_off(8, 15) / 16)) &&
+                  aqk_zero_block(0, 63) && !aqk_zero_block(63, 0),
+              "zero blocks of A_qk");
 
 // byte offset of element (r, k) in an interleaved K-major tile with K elements per row
 __host__ __device__ constexpr uint32_t il_off(int r, int k, int K) {
@@ -253,6 +265,11 @@ __device__ __forceinline__ void load_b_kn(uint32_t (&r)[4], const __nv_bfloat16 
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src));
+}
+// the same with the shared-memory address given as such (unrolled copies add immediate
+// offsets to one base)
+__device__ __forceinline__ void cp_async16_s(uint32_t sdst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sdst), "l"(gmem_src));
 }
 __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src));

@@ -466,22 +466,21 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 const float a1 = (!diag || j <= i0 + 1) ? __uint_as_float(dq[2 * p2 + 1]) : 0.f;
                 split_pk(pk2(a0, a1), hi[p2], lo[p2]);
             }
-            // 8 consecutive query rows of key j: one MN-major 16-byte unit per plane
-            *reinterpret_cast<uint4 *>(rec + kRecAqk + ak_off(ib, j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(rec + kRecAqk + kStackAK + ak_off(ib, j)) =
-                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            // 8 consecutive query rows of key j: one MN-major 16-byte unit per plane (none in
+            // the blocks wholly above the diagonal, which the record leaves out)
+            if (!aqk_zero_block(ib, j)) {
+                *reinterpret_cast<uint4 *>(rec + kRecAqk + ak_off(ib, j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(rec + kRecAqk + kStackAK + ak_off(ib, j)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
             const float *be = s.beta[b];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const int i = ib + t;
                 s.u.s.Akk[i][j] = (!diag || j < i) ? be[i] * __uint_as_float(dk[t]) : 0.f;
             }
-        } else {
-            // the A_qk block above the diagonal (i < 32 <= j) is zero
-            const int ig = warp >> 2, j = 32 + lane;
-            *reinterpret_cast<uint4 *>(rec + kRecAqk + ak_off(8 * ig, j)) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4 *>(rec + kRecAqk + kStackAK + ak_off(8 * ig, j)) = make_uint4(0u, 0u, 0u, 0u);
         }
+        // (the A_qk block above the diagonal, i < 32 <= j, is zero: the record leaves it out)
         tc::fence_before_sync();
         __syncthreads();
         const float2 pre = has_next ? gate_inputs(nxt) : make_float2(0.f, 0.f);

@@ -829,7 +829,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const uint32_t ak_off = maps ? (uint32_t)kPlaneCC : 0u;  // group 2's B operand starts at Kend^T
         int n_m1 = 0, n_m2 = 0;  // MMA groups committed (issuer)
         // chunk c's [ A_qk ; Kend^T ] into slot (c - c_begin) & 1 by this thread's share of
-        // 16-byte units (a map walk: the Kend^T rows of the hi and the lo plane)
+        // 16-byte units (a map walk: the Kend^T rows of the hi and the lo plane). The A_qk
+        // blocks above the diagonal are not in the record: both slots hold zeros there.
         auto copy_ak = [&](int c) {
             unsigned char *dst = s.ak[(c - c_begin) & 1];
             const unsigned char *src = rec_of(c) + kRecAK;
@@ -839,9 +840,29 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     cp_async16(dst + kStackAK + kPlaneCC + 16 * u, src + kStackAK + kPlaneCC + 16 * u);
                 }
             } else {
-                for (int u = tid - 128; u < 2 * kStackAK / 16; u += 128) cp_async16(dst + 16 * u, src + 16 * u);
+                // unrolled from one shared and one global base: this copy is issued on the
+                // state warps' path between two chunks, where a loop with per-unit address
+                // arithmetic measured slower
+                const int t = tid - 128;
+                const uint32_t sd = smem_u32(dst) + 16u * (uint32_t)t;
+                const unsigned char *sg = src + 16 * t;
+#pragma unroll
+                for (int m = 0; m < (int)(2 * kStackAK / 2048); ++m) {
+                    const int pm = m % (int)(kStackAK / 2048);  // 2048-byte step within its plane
+                    if (pm >= (int)(kPlaneCC / 2048) || !aqk_zero_unit(t + 128 * pm))
+                        cp_async16_s(sd + 2048u * m, sg + 2048 * m);
+                }
             }
         };
+        if (!maps) {
+            // the zero blocks of A_qk in both slots (the map chain, if any, used these
+            // buffers and has completed)
+            for (int e = tid - 128; e < 4 * (int)(kPlaneCC / 16); e += 128) {
+                const int u = e & (int)(kPlaneCC / 16 - 1), sp = e / (int)(kPlaneCC / 16);  // (slot, plane)
+                if (aqk_zero_unit(u))
+                    *reinterpret_cast<uint4 *>(&s.ak[sp >> 1][(sp & 1) * kStackAK + 16 * u]) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         // group 1 of the next chunk: [D_U | D_O1 | D_O2] = S^T [ -W ; Qhat hi ; Qhat lo ]^T
         auto issue_g1 = [&](int c) {
             tc::fence_after_sync();
