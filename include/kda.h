@@ -83,6 +83,21 @@ int kda_version(void);
 int kda_debug_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns);
 
 /*
+ * Test hook for the segmented walk's long end segments (no counterpart on the pages).
+ * When a kda_chunk_prefill call takes the segmented walk with a combine kernel (5
+ * launches), a sequence of at least (2 E + 1) P chunks (P the segment length the sizes
+ * give) is cut into a first and a last segment of E P chunks and segments of P chunks
+ * between them; the sizes choose E themselves (1 = every segment P chunks), and
+ * end_factor > 0 forces E = end_factor on every later call in this process (0 restores
+ * the sizes' choice). The segment length, the workspace size and the launch count do not
+ * change; only the cut of each sequence does, so the results agree with E = 1 up to
+ * rounding. Process-global and not synchronised with calls in flight.
+ *
+ * Returns KDA_OK, or KDA_ERR_SHAPE for end_factor outside [0, 64].
+ */
+int kda_debug_segment_ends(int32_t end_factor);
+
+/*
  * Bytes of device workspace kda_chunk_prefill() needs for a batch of total_tokens
  * tokens in num_seqs sequences and num_heads heads. The size is an upper bound that
  * depends only on these three numbers, so one buffer serves every batch up to them.

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 
 #include "kda.h"
@@ -177,6 +178,15 @@ int kda_debug_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns) {
     return kda::set_walk_fault(skip_commit_chunk, wait_limit_ns) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// end factor forced by kda_debug_segment_ends (0: the cost model's)
+static std::atomic<int32_t> g_debug_segment_ends{0};
+
+int kda_debug_segment_ends(int32_t end_factor) {
+    if (end_factor < 0 || end_factor > 64) return KDA_ERR_SHAPE;
+    g_debug_segment_ends.store(end_factor);
+    return KDA_OK;
+}
+
 size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
     if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return 0;
     return ws_layout(total_tokens, num_seqs, num_heads).total;
@@ -230,6 +240,9 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
         sp.nC = counts + 2;
         sp.chains = reinterpret_cast<int32_t *>(ws + w.chains);
         sp.chain_mode = kda::walk_chain_mode(total, num_seqs, num_heads) ? 1 : 0;
+        // long end segments in the combine form only (the chained form keeps P throughout)
+        const int32_t forced = g_debug_segment_ends.load();
+        sp.E = sp.chain_mode ? 1 : (forced > 0 ? forced : kda::walk_segments(total, num_seqs, num_heads).E);
     }
     if (kda::launch_plan(cu_seqlens, num_seqs, seq_len, total, status, seq_cu, chunk_off, num_heads, initial_state,
                          final_state, units, counts, sp, st) != cudaSuccess)
@@ -246,14 +259,17 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
         return KDA_OK;
     }
     // segmented walk: phase A (segment maps), phase B (chain them: the combine kernel, or in
-    // the chained form each output walk itself), phase C (outputs)
-    if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, 2, 0, st) !=
+    // the chained form each output walk itself), phase C (outputs). With long end segments
+    // (listed first) heads are the fastest grid index, so every head's long walks start in
+    // the first wave.
+    const int hm = (sp.E > 1 && 3 * w.seg_bound <= 65535) ? 1 : 0;
+    if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, 2, hm, st) !=
         cudaSuccess)
         return KDA_ERR_CUDA;
     if (!sp.chain_mode &&
         kda::launch_combine(status, sp.chains, num_seqs, num_heads, sp.Sin, sp.Mseg, sp.Rseg, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_walk(status, sp.unitsC, sp.nC, w.seg_bound, num_heads, records, o, o_f32, sp.chain_mode ? 1 : 0, 0,
+    if (kda::launch_walk(status, sp.unitsC, sp.nC, w.seg_bound, num_heads, records, o, o_f32, sp.chain_mode ? 1 : 0, hm,
                          st) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;

@@ -138,6 +138,8 @@ struct SegPlan {
     int32_t *nA, *nC;
     int32_t *chains;     // per sequence: first segment, number of segments (combine form)
     int32_t chain_mode;  // 1: each output walk chains the maps before it; 0: a combine kernel does
+    int32_t E;           // end factor: a sequence of at least (2 E + 1) P chunks has first and
+                         // last segments of E P chunks (1: every segment P chunks)
 };
 
 // Segment length (in chunks) of the segmented walk, or 0 for a plain walk. A pure
@@ -152,8 +154,8 @@ struct SegPlan {
 // phase C fits one wave, costs about 0.6 a map and keeps the same choice), and phase C S
 // walks per chain in ceil(S chains / 152) waves of P + 2 steps. For 8192 tokens x 12
 // heads this keeps 7 segments of 19 chunks; for 1,048,576 tokens x 12 heads it takes 38
-// segments of 432 chunks (phase A in six waves).
-__host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
+// segments of 432 chunks (phase A in six waves) before the long ends below are considered.
+__host__ __device__ inline int walk_segment_uniform(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
     const int64_t chains = num_seqs * num_heads;
     if (chains <= 0) return 0;
     const int64_t slots = chunk_bound(total_tokens, num_seqs);
@@ -185,8 +187,55 @@ __host__ __device__ inline int64_t segment_bound(int64_t total_tokens, int64_t n
 // kernel chains the maps once per (sequence, head) in fp32 instead. A pure function of the
 // sizes, like the segment length.
 __host__ __device__ inline bool walk_chain_mode(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
-    const int P = walk_segment_chunks(total_tokens, num_seqs, num_heads);
+    const int P = walk_segment_uniform(total_tokens, num_seqs, num_heads);
     return P > 0 && segment_bound(total_tokens, num_seqs, P) * num_heads <= 152;
+}
+// Long ends (combine form only). The first segment of a chain needs one walk in phase A
+// (from the initial state, no map) and the last none, while every other segment needs two
+// (M and R). Making the two end segments E times as long as the others therefore takes
+// map work off phase A, and in phase C their long walks run beside several waves of short
+// ones. The walks of both phases are listed longest first. (P, E) minimises the cost model
+// above with each phase's waves counted in units of P chunks per SM (a long walk fills E of
+// them, and a phase lasts at least E); E = 1 is the uniform split. For 1,048,576 tokens x
+// 12 heads: 42 segments of 328 chunks between two of 1,312 (phase A and phase C in seven
+// and four such waves, against six and three waves of 432 chunks uniform).
+struct SegShape {
+    int P, E;
+};
+__host__ __device__ inline SegShape walk_segments(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
+    const int P1 = walk_segment_uniform(total_tokens, num_seqs, num_heads);
+    if (P1 == 0 || walk_chain_mode(total_tokens, num_seqs, num_heads)) return SegShape{P1, 1};
+    const int64_t chains = num_seqs * num_heads;
+    const int64_t avg = chunk_bound(total_tokens, num_seqs) / num_seqs;
+    auto cost = [&](int64_t P, int64_t E) {
+        // the segments a chain of avg chunks gets, and each phase's walks in P-chunk units
+        const int64_t segs = E > 1 ? 2 + (avg - 2 * E * P + P - 1) / P : (avg + P - 1) / P;
+        const int64_t ua = chains * (E > 1 ? E + 2 * (segs - 2) : 2 * segs - 3);
+        const int64_t uc = chains * (E > 1 ? 2 * E + segs - 2 : segs);
+        int64_t waves_a = (ua + 151) / 152, waves_c = (uc + 151) / 152;
+        if (waves_a < E) waves_a = E;
+        if (waves_c < E) waves_c = E;
+        return 0.83 * (double)(waves_a * (P + 2)) + 1.2 * (double)(segs - 2) + (double)(waves_c * (P + 2));
+    };
+    SegShape best{P1, 1};
+    double best_cost = cost(P1, 1);
+    for (int64_t E = 2; E <= 6; ++E) {
+        for (int64_t S = 3; S <= 96; ++S) {
+            int64_t P = (avg + 2 * E + S - 3) / (2 * E + S - 2);
+            if (P < 4) P = 4;
+            if (avg < (2 * E + 1) * P) continue;
+            const double c = cost(P, E);
+            if (c < best_cost) {
+                best_cost = c;
+                best = SegShape{(int)P, (int)E};
+            }
+        }
+    }
+    return best;
+}
+// Segment length (in chunks) of the segmented walk, or 0 for a plain walk
+__host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
+    return walk_segments(total_tokens, num_seqs, num_heads).P;
 }
 
 // ---------------------------------------------------------------------------------

@@ -93,67 +93,88 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
         return;
     }
     const size_t seg_stride = (size_t)H * kStateFloats;  // one segment's states for all heads
-    int32_t a = 0, cc = 0, g = 0;
-    for (int32_t n = 0; n < N; ++n) {
-        const int32_t c0 = chunk_off[n], c1 = chunk_off[n + 1];
-        const int32_t t0 = seq_cu[n], t1 = seq_cu[n + 1];
-        const int32_t S = (c1 - c0 + P - 1) / P;
-        sp.chains[2 * n] = g;
-        sp.chains[2 * n + 1] = S;
-        const float *init = S0 ? S0 + (size_t)n * seg_stride : nullptr;
-        float *fin = Sout + (size_t)n * seg_stride;
-        // an empty sequence: its final state is its initial state
-        if (S == 0) unitsA[a++] = blank(init, fin, c0, t0, 0);
-        for (int32_t sg = 0; sg < S; ++sg) {
-            WalkUnit u = blank(nullptr, nullptr, c0 + sg * P, t0 + sg * P * kC, kUnitAddUp);
-            u.c_end = min(c1, c0 + (sg + 1) * P);
-            u.t_end = min(t1, t0 + (sg + 1) * P * kC);
-            if (sg == 0) {
-                u.in = init;
-                if (S == 1) {  // phase C: the sequence's only walk, with outputs
-                    u.out = fin;
+    const int32_t E = sp.E;
+    int32_t a = 0, cc = 0;
+    // two passes over the same segments: the first lists the walks longer than P (the end
+    // segments of sequences cut with long ends), the second the others, so that each phase
+    // starts its longest walks first
+    for (int pass = 0; pass < 2; ++pass) {
+        int32_t g = 0;
+        for (int32_t n = 0; n < N; ++n) {
+            const int32_t c0 = chunk_off[n], c1 = chunk_off[n + 1];
+            const int32_t t0 = seq_cu[n], t1 = seq_cu[n + 1];
+            const int32_t len = c1 - c0;
+            // long ends: segments [0, E P), then P at a time up to len - E P, then [len - E P, len)
+            const bool ends = E > 1 && len >= (2 * E + 1) * P;
+            const int32_t S = ends ? 2 + (len - 2 * E * P + P - 1) / P : (len + P - 1) / P;
+            if (pass == 0) {
+                sp.chains[2 * n] = g;
+                sp.chains[2 * n + 1] = S;
+            }
+            const float *init = S0 ? S0 + (size_t)n * seg_stride : nullptr;
+            float *fin = Sout + (size_t)n * seg_stride;
+            // an empty sequence: its final state is its initial state
+            if (S == 0 && pass == 1) unitsA[a++] = blank(init, fin, c0, t0, 0);
+            for (int32_t sg = 0; sg < S; ++sg) {
+                int32_t cb, ce;  // the segment's chunks, relative to the sequence
+                if (ends) {
+                    cb = sg == 0 ? 0 : (sg == S - 1 ? len - E * P : E * P + (sg - 1) * P);
+                    ce = sg == 0 ? E * P : (sg == S - 1 ? len : min(cb + P, len - E * P));
+                } else {
+                    cb = sg * P;
+                    ce = min(len, cb + P);
+                }
+                if ((ce - cb > P) != (pass == 0)) continue;
+                WalkUnit u = blank(nullptr, nullptr, c0 + cb, t0 + cb * kC, kUnitAddUp);
+                u.c_end = c0 + ce;
+                u.t_end = min(t1, t0 + ce * kC);
+                if (sg == 0) {
+                    u.in = init;
+                    if (S == 1) {  // phase C: the sequence's only walk, with outputs
+                        u.out = fin;
+                        u.flags = kUnitWriteO | kUnitAddUp;
+                        unitsC[cc++] = u;
+                        continue;
+                    }
+                    // phase A: the end state only (a walk without outputs is cheaper) ...
+                    u.out = Sin + (size_t)(g + 1) * seg_stride;
+                    u.flags = kUnitAddUp | (sp.chain_mode ? kUnitOutQuads : 0);
+                    unitsA[a++] = u;
+                    // ... phase C: again with outputs, alongside the other segments
+                    u.out = nullptr;
                     u.flags = kUnitWriteO | kUnitAddUp;
                     unitsC[cc++] = u;
                     continue;
                 }
-                // phase A: the end state only (a walk without outputs is cheaper) ...
-                u.out = Sin + (size_t)(g + 1) * seg_stride;
-                u.flags = kUnitAddUp | (sp.chain_mode ? kUnitOutQuads : 0);
-                unitsA[a++] = u;
-                // ... phase C: again with outputs, alongside the other segments
-                u.out = nullptr;
+                // phase C
                 u.flags = kUnitWriteO | kUnitAddUp;
-                unitsC[cc++] = u;
-                continue;
-            }
-            // phase C
-            u.flags = kUnitWriteO | kUnitAddUp;
-            if (sp.chain_mode) {  // from segment 1's input through the maps of segments 1 .. sg - 1
-                u.in = Sin + (size_t)(g + 1) * seg_stride;
-                u.flags |= kUnitInQuads;
-                u.chain = sg - 1;
-                if (sg > 1) {
-                    u.maps = Mseg + (size_t)(g + 1) * seg_stride;
-                    u.offs = Rseg + (size_t)(g + 1) * seg_stride;
+                if (sp.chain_mode) {  // from segment 1's input through the maps of segments 1 .. sg - 1
+                    u.in = Sin + (size_t)(g + 1) * seg_stride;
+                    u.flags |= kUnitInQuads;
+                    u.chain = sg - 1;
+                    if (sg > 1) {
+                        u.maps = Mseg + (size_t)(g + 1) * seg_stride;
+                        u.offs = Rseg + (size_t)(g + 1) * seg_stride;
+                    }
+                } else {  // from the combine kernel's input state
+                    u.in = Sin + (size_t)(g + sg) * seg_stride;
                 }
-            } else {  // from the combine kernel's input state
-                u.in = Sin + (size_t)(g + sg) * seg_stride;
+                u.out = sg == S - 1 ? fin : nullptr;
+                unitsC[cc++] = u;
+                // phase A: this segment's map
+                if (sg <= S - 2) {
+                    u.in = u.maps = u.offs = nullptr;
+                    u.chain = 0;
+                    u.out = Rseg + (size_t)(g + sg) * seg_stride;
+                    u.flags = kUnitAddUp | (sp.chain_mode ? kUnitOutQuads : 0);
+                    unitsA[a++] = u;
+                    u.out = Mseg + (size_t)(g + sg) * seg_stride;
+                    u.flags = kUnitIdentity | (sp.chain_mode ? kUnitOutPlanes : 0);
+                    unitsA[a++] = u;
+                }
             }
-            u.out = sg == S - 1 ? fin : nullptr;
-            unitsC[cc++] = u;
-            // phase A: this segment's map
-            if (sg <= S - 2) {
-                u.in = u.maps = u.offs = nullptr;
-                u.chain = 0;
-                u.out = Rseg + (size_t)(g + sg) * seg_stride;
-                u.flags = kUnitAddUp | (sp.chain_mode ? kUnitOutQuads : 0);
-                unitsA[a++] = u;
-                u.out = Mseg + (size_t)(g + sg) * seg_stride;
-                u.flags = kUnitIdentity | (sp.chain_mode ? kUnitOutPlanes : 0);
-                unitsA[a++] = u;
-            }
+            g += S;
         }
-        g += S;
     }
     *sp.nA = a;
     *sp.nC = cc;

@@ -48,6 +48,8 @@ def library():
         lib.kda_workspace_status.restype = ctypes.c_int
         lib.kda_debug_walk_fault.argtypes = [i32, ctypes.c_uint64]
         lib.kda_debug_walk_fault.restype = ctypes.c_int
+        lib.kda_debug_segment_ends.argtypes = [i32]
+        lib.kda_debug_segment_ends.restype = ctypes.c_int
         lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
         lib.kda_recurrent_decode.restype = ctypes.c_int
         lib.kda_recurrent_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
@@ -304,6 +306,15 @@ def kda_chunk_prefill_noalloc(q, k, v, z, A, b, initial_state=None, cu_seqlens=N
     if rc != 0:
         raise KdaError("kda_chunk_prefill_noalloc", rc)
     return o, final_state
+
+
+def kda_debug_segment_ends(end_factor):
+    """Test hook of the segmented walk's long end segments (include/kda.h): end_factor > 0
+    forces the first and last segment of every long enough sequence to end_factor segment
+    lengths in the combine form; 0 restores the choice the sizes make."""
+    rc = library().kda_debug_segment_ends(ctypes.c_int32(end_factor))
+    if rc != 0:
+        raise KdaError("kda_debug_segment_ends", rc)
 
 
 def kda_debug_walk_fault(skip_commit_chunk, wait_limit_ns):

@@ -52,6 +52,14 @@ def test_status_strings_and_version():
     assert kda.kda_version() >= 100
 
 
+def test_segment_ends_hook_checks():
+    for bad in (-1, 65):
+        with pytest.raises(kda.KdaError):
+            kda.kda_debug_segment_ends(bad)
+    kda.kda_debug_segment_ends(3)
+    kda.kda_debug_segment_ends(0)
+
+
 def test_workspace_size():
     ws = kda.kda_chunk_prefill_workspace_size
     assert ws(-1, 1, 1) == 0

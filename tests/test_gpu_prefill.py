@@ -315,6 +315,31 @@ def test_segmented_walk_slow_memory(lens, H, launches):
     assert_prefill_close(o, S, o_ref, S_ref, "segmented, slow memory %s" % lens)
 
 
+@pytest.mark.parametrize("lens,H,E,init", [([10240, 10000, 10480], 5, 2, True), ([14000, 2000, 14720], 5, 3, False)])
+def test_segmented_walk_long_ends(lens, H, E, init):
+    """The combine form with long end segments, forced through the test hook on batches
+    small enough for the oracle (the sizes choose them only for much longer chains): the
+    first and last segment of each long enough sequence E segment lengths long, the
+    walks of both phases listed longest first with heads as the fastest grid index. In the
+    second batch the 2000-token sequence is too short for long ends and keeps the uniform
+    cut. Weak decay and writes, so the maps carry the state; against the oracle, and the
+    cut must change the rounding against the uniform one."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    n = len(lens)
+    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == 5, (lens, H)
+    inp = _slow_memory(inputs.prefill_inputs(cu[-1], H, n, seed=37, init_state=init), seed=38)
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"],
+                                      S0=inp["S0"] if init else None, cu_seqlens=cu)
+    o1, S1 = gpu_prefill(inp, cu=cu, S0="inp" if init else None)
+    kda.kda_debug_segment_ends(E)
+    try:
+        o, S = gpu_prefill(inp, cu=cu, S0="inp" if init else None)
+    finally:
+        kda.kda_debug_segment_ends(0)
+    assert_prefill_close(o, S, o_ref, S_ref, "segmented, long ends E=%d %s" % (E, lens))
+    assert not torch.equal(S, S1)
+
+
 @pytest.mark.parametrize("lens,H,launches", [([3000, 1800], 2, 4), ([10240, 10000, 10480], 5, 5)])
 def test_segmented_walk_without_initial_state(lens, H, launches):
     """Both segmented forms with no initial state (zero): segment 0 starts from zero in
