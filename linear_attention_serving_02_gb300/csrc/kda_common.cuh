@@ -153,7 +153,8 @@ struct SegPlan {
 // (about 1.2 steps each as the combine kernel's; the output walks' own chain, taken when
 // phase C fits one wave, costs about 0.6 a map and keeps the same choice), and phase C S
 // walks per chain in ceil(S chains / 152) waves of P + 2 steps. For 8192 tokens x 12
-// heads this keeps 7 segments of 19 chunks; for 1,048,576 tokens x 12 heads it takes 38
+// heads this keeps 7 segments of at most 19 chunks (cut to even out the output walks' map
+// chains in the chained form); for 1,048,576 tokens x 12 heads it takes 38
 // segments of 432 chunks (phase A in six waves) before the long ends below are considered.
 __host__ __device__ inline int walk_segment_uniform(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
     const int64_t chains = num_seqs * num_heads;
