@@ -477,13 +477,29 @@ def run_prefill_workload(which, steps, warmup, world, seed):
         # the decode that follows: 128 steps of one token per head on the prefilled state
         dec = [inputs.decode_step_inputs(1, H, seed=seed + 5, step=i, device="cuda", A=inp["A"]) for i in range(8)]
         o_dec = torch.empty((1, H, D), dtype=torch.float32, device="cuda")
+        def steps():
+            for i in range(128):
+                d = dec[i % len(dec)]
+                kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["z"], d["A"], d["b"], S, o=o_dec)
+
         e0.record(main)
-        for i in range(128):
-            d = dec[i % len(dec)]
-            kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["z"], d["A"], d["b"], S, o=o_dec)
+        steps()
         e1.record(main)
         e1.synchronize()
         res["decode_128_steps_ms"] = e0.elapsed_time(e1)
+        # the same steps as one CUDA graph, as a serving loop replays its launch-bound decode
+        # (each step launches one small kernel: the calls' host time dominates the loop above)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            steps()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(main)
+        graph.replay()
+        e1.record(main)
+        e1.synchronize()
+        res["decode_128_steps_graph_ms"] = e0.elapsed_time(e1)
+        del graph
     res["finite"] = bool(torch.isfinite(S).all())
     del inp, ws, o, S
     torch.cuda.empty_cache()

@@ -24,6 +24,11 @@
  *   - 'stream' is a cudaStream_t (NULL = the legacy default stream). Work is enqueued
  *     asynchronously; a return of KDA_OK means the arguments were valid and the
  *     kernels were launched, not that they have finished.
+ *   - The compute entry points only enqueue kernels on 'stream' (no allocation, copy or
+ *     synchronisation), so they can be captured into a CUDA graph and replayed; a
+ *     replay gives the bits of the same call made directly. The first call of a process
+ *     sets kernel attributes and reads the device's properties: make one call before the
+ *     first capture. kda_workspace_status synchronises and cannot be captured.
  *   - Errors are returned as kda_status codes; nothing is thrown across the ABI and no
  *     kernel traps. A failed argument check launches nothing and writes nothing.
  *   - Every pointer must be 16-byte aligned (the kernels use 128-bit accesses);
