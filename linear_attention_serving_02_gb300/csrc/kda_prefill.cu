@@ -109,7 +109,7 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
             const int32_t t0 = seq_cu[n], t1 = seq_cu[n + 1];
             const int32_t len = c1 - c0;
             // long ends: segments [0, E P), then P at a time up to len - E P, then [len - E P, len)
-            const bool ends = E > 1 && len >= (2 * E + 1) * P;
+            const bool ends = E > 1 && (int64_t)len >= (int64_t)(2 * E + 1) * P;  // then E P < len
             const int32_t S = ends ? 2 + (len - 2 * E * P + P - 1) / P : (len + P - 1) / P;
             if (pass == 0) {
                 sp.chains[2 * n] = g;
