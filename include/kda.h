@@ -89,10 +89,10 @@ int kda_debug_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns);
 
 /*
  * Test hook for the segmented walk's long end segments (no counterpart on the pages).
- * When a kda_chunk_prefill call takes the segmented walk with a combine kernel (5
- * launches), a sequence of at least (2 E + 1) P chunks (P the segment length the sizes
- * give) is cut into a first and a last segment of E P chunks and segments of P chunks
- * between them; the sizes choose E themselves (1 = every segment P chunks), and
+ * When a kda_chunk_prefill call takes the segmented walk with a combine kernel (walk
+ * form 2, see kda_chunk_prefill_walk_form), a sequence of at least (2 E + 1) P chunks
+ * (P the segment length the sizes give) is cut into a first and a last segment of E P
+ * chunks and segments of P chunks between them; the sizes choose E themselves (1 = every segment P chunks), and
  * end_factor > 0 forces E = end_factor on every later call in this process (0 restores
  * the sizes' choice). The segment length, the workspace size and the launch count do not
  * change; only the cut of each sequence does, so the results agree with E = 1 up to
@@ -113,14 +113,24 @@ size_t kda_chunk_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, 
 /*
  * Number of kernels one kda_chunk_prefill() call with these sizes launches on its
  * stream: 0 when num_seqs is 0, 3 (plan, intra-chunk, state walk) when every
- * (sequence, head) chain walks its chunks in one pass, 4 or 5 when the chains are too
- * few to fill the GPU and the walk is split into segments: plan, intra-chunk, segment-map
- * walk, then either an output walk that first chains the maps (4: every output walk fits
- * in one wave of the GPU) or a combine kernel and the output walk (5). Depends only on
- * the three sizes,
- * like the workspace. Returns -1 for negative arguments.
+ * (sequence, head) chain walks its chunks in one pass, 5 when the chains are too few to
+ * fill the GPU and the walk is split into segments: plan, intra-chunk, segment-map walk,
+ * then either a second intra-chunk launch beside the map walk (the chained form, see
+ * kda_chunk_prefill_walk_form) or a combine kernel, and the output walk. Depends only on
+ * the three sizes, like the workspace. Returns -1 for negative arguments.
  */
 int32_t kda_chunk_prefill_launch_count(int64_t total_tokens, int32_t num_seqs, int32_t num_heads);
+
+/*
+ * How a kda_chunk_prefill() call with these sizes walks the state: 0 in one pass per
+ * (sequence, head) chain; 1 in segments whose output walks first chain the segment maps
+ * before them on the tensor cores (every output walk fits in one wave of the GPU); 2 in
+ * segments whose input states a combine kernel chains. In form 1 the intra-chunk items
+ * past a whole number of rounds of the GPU's SMs that belong to the last segment of a
+ * dense batch's last sequence run in a second intra-chunk launch beside the map walk.
+ * Depends only on the three sizes. Returns -1 for negative arguments, 0 when num_seqs is 0.
+ */
+int32_t kda_chunk_prefill_walk_form(int64_t total_tokens, int32_t num_seqs, int32_t num_heads);
 
 /*
  * kda_chunk_prefill - chunkwise-parallel KDA over whole sequences.

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 
@@ -17,8 +18,8 @@ cudaError_t launch_plan(const int32_t *cu, int32_t N, int64_t seq_len, int64_t t
                         int32_t *n_units, const SegPlan &sp, cudaStream_t st);
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                          const float *A, const float *b, int32_t *status, const int32_t *seq_cu,
-                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t nslots,
-                         uint8_t *records, int num_sms, cudaStream_t st);
+                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t items,
+                         int32_t item_lo, int32_t item_hi, uint8_t *records, int num_sms, cudaStream_t st);
 cudaError_t launch_walk(int32_t *status, const WalkUnit *units, const int32_t *n_units, int64_t max_units,
                         int32_t H, const uint8_t *records, void *o, int o_f32, int form, int head_major,
                         cudaStream_t st);
@@ -173,6 +174,30 @@ const char *kda_status_string(int status) {
 
 int kda_version(void) { return 100; }
 
+namespace {
+// Intra-chunk items deferred to a second intra launch that runs beside phase A of the
+// chained segmented walk (dense batches; 0 otherwise). The first launch takes the first
+// k * sms - 1 items (k = items / sms), so that its CTAs all take k items except the last
+// CTA, which gets one fewer: that one usually starts late, on the SM that the plan kernel
+// holds. The remaining items belong to the last segment of the last sequence, which only
+// phase C reads, and they run on the SMs that phase A's walks leave free; otherwise none
+// is deferred.
+int64_t deferred_intra_items(int32_t N, int32_t H, int64_t seq_len, int P, int sms) {
+    if (N <= 0 || seq_len <= 0 || P <= 0) return 0;
+    const int64_t cps = (seq_len + kda::kC - 1) / kda::kC;
+    const int64_t items = (int64_t)N * cps * H;
+    const int64_t k = items / sms;
+    if (k < 2 || items > INT32_MAX) return 0;
+    const int64_t defer = items - (k * sms - 1);
+    const int64_t S = (cps + P - 1) / P;
+    if (S < 2) return 0;
+    const int64_t units_a = (int64_t)N * H * (2 * S - 3);  // phase A's walks, all in one wave
+    const int64_t last = S >= 3 ? kda::BalancedCut((int32_t)cps, P, (int32_t)S).last_len() : cps - (S - 1) * P;
+    if (defer > sms - units_a || defer > last * H) return 0;
+    return defer;
+}
+}  // namespace
+
 int kda_debug_walk_fault(int32_t skip_commit_chunk, uint64_t wait_limit_ns) {
     if (wait_limit_ns == 0) return KDA_ERR_SHAPE;
     return kda::set_walk_fault(skip_commit_chunk, wait_limit_ns) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -196,7 +221,13 @@ int32_t kda_chunk_prefill_launch_count(int64_t total_tokens, int32_t num_seqs, i
     if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return -1;
     if (num_seqs == 0) return 0;
     if (!kda::walk_segment_chunks(total_tokens, num_seqs, num_heads)) return 3;
-    return kda::walk_chain_mode(total_tokens, num_seqs, num_heads) ? 4 : 5;
+    return 5;  // plan, intra, phase A, then the deferred intra items or the combine kernel, phase C
+}
+
+int32_t kda_chunk_prefill_walk_form(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
+    if (total_tokens < 0 || num_seqs < 0 || num_heads < 0) return -1;
+    if (num_seqs == 0 || !kda::walk_segment_chunks(total_tokens, num_seqs, num_heads)) return 0;
+    return kda::walk_chain_mode(total_tokens, num_seqs, num_heads) ? 1 : 2;
 }
 
 int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *z, const float *A,
@@ -247,10 +278,18 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
     if (kda::launch_plan(cu_seqlens, num_seqs, seq_len, total, status, seq_cu, chunk_off, num_heads, initial_state,
                          final_state, units, counts, sp, st) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (kda::launch_intra(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k),
-                          reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, status, seq_cu, chunk_off, num_seqs,
-                          num_heads, cu_seqlens ? 0 : seq_len, w.nslots, records, dev.sms, st) != cudaSuccess)
-        return KDA_ERR_CUDA;
+    // the chained form defers the intra items past a whole number of rounds (dense batches)
+    // to a second intra launch beside phase A
+    const int64_t defer =
+        (w.P > 0 && sp.chain_mode && !cu_seqlens) ? deferred_intra_items(num_seqs, num_heads, seq_len, w.P, dev.sms) : 0;
+    const int64_t items1 = cu_seqlens ? w.nslots * num_heads
+                                      : (int64_t)num_seqs * ((seq_len + kda::kC - 1) / kda::kC) * num_heads - defer;
+    auto intra = [&](int64_t items, int32_t lo, int32_t hi) {
+        return kda::launch_intra(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k),
+                                 reinterpret_cast<const __nv_bfloat16 *>(v), z, A, b, status, seq_cu, chunk_off,
+                                 num_seqs, num_heads, cu_seqlens ? 0 : seq_len, items, lo, hi, records, dev.sms, st);
+    };
+    if (intra(items1, 0, (int32_t)std::min<int64_t>(items1, INT32_MAX)) != cudaSuccess) return KDA_ERR_CUDA;
     if (w.P == 0) {
         // heads as the fastest grid index (the plan lists the longest sequences first)
         if (kda::launch_walk(status, units, counts, num_seqs, num_heads, records, o, o_f32, 0, num_seqs <= 65535 ? 1 : 0,
@@ -265,6 +304,9 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
     const int hm = (sp.E > 1 && 3 * w.seg_bound <= 65535) ? 1 : 0;
     if (kda::launch_walk(status, sp.unitsA, sp.nA, 3 * w.seg_bound, num_heads, records, o, o_f32, 2, hm, st) !=
         cudaSuccess)
+        return KDA_ERR_CUDA;
+    // chained form: the deferred intra items (none for a cu_seqlens batch), beside phase A
+    if (sp.chain_mode && intra(defer, (int32_t)std::min<int64_t>(items1, INT32_MAX), INT32_MAX) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (!sp.chain_mode &&
         kda::launch_combine(status, sp.chains, num_seqs, num_heads, sp.Sin, sp.Mseg, sp.Rseg, st) != cudaSuccess)

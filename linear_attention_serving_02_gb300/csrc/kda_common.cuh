@@ -234,6 +234,45 @@ __host__ __device__ inline SegShape walk_segments(int64_t total_tokens, int64_t 
     }
     return best;
 }
+// Balanced cut (chained form). The output walk of segment k >= 1 first chains k - 1 maps,
+// each about kChainStep16 / 16 of a chunk step (about 1.7 against 3.1 us, measured), so a
+// sequence of len chunks in S = ceil(len / P) >= 3 segments is cut to even out chain plus
+// chunks: segment k takes min(P, (t - kChainStep16 (k - 1)) / 16) chunks (segment 0:
+// min(P, t / 16)), at least one, for the lowest level t (in 1/16 chunks) at which the
+// lengths reach len; the segments that grew at that level give back the surplus, the last
+// ones first. Used by the plan kernel and, for the last segment, by the host.
+constexpr int32_t kChainStep16 = 9;
+struct BalancedCut {
+    int32_t P = 0, S = 0, level = 0, grown = 0, surplus = 0;
+    __host__ __device__ static int32_t len_at(int32_t t16, int32_t k, int32_t P) {
+        const int32_t x = t16 - kChainStep16 * (k > 1 ? k - 1 : 0);
+        return x < 16 ? 1 : (P < (x >> 4) ? P : (x >> 4));
+    }
+    __host__ __device__ int32_t total(int32_t t16) const {
+        int32_t sum = 0;
+        for (int32_t k = 0; k < S; ++k) sum += len_at(t16, k, P);
+        return sum;
+    }
+    __host__ __device__ BalancedCut(int32_t len, int32_t P_, int32_t S_) : P(P_), S(S_) {
+        int32_t lo = 0, hi = 16 * P + kChainStep16 * S;  // total(hi) = S P >= len
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) / 2;
+            if (total(mid) >= len)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        level = lo;
+        surplus = total(level) - len;
+        for (int32_t k = 0; k < S; ++k) grown += grew(k);
+    }
+    __host__ __device__ bool grew(int32_t k) const { return len_at(level, k, P) > len_at(level - 1, k, P); }
+    // the last segment's length (it gives back first)
+    __host__ __device__ int32_t last_len() const {
+        return len_at(level, S - 1, P) - ((grew(S - 1) && surplus > 0) ? 1 : 0);
+    }
+};
+
 // Segment length (in chunks) of the segmented walk, or 0 for a plain walk
 __host__ __device__ inline int walk_segment_chunks(int64_t total_tokens, int64_t num_seqs, int64_t num_heads) {
     return walk_segments(total_tokens, num_seqs, num_heads).P;

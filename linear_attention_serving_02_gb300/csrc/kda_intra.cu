@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
                      const float *__restrict__ bgate, int32_t *__restrict__ status,
                      const int32_t *__restrict__ seq_cu, const int32_t *__restrict__ chunk_off, int32_t N, int32_t H,
-                     int64_t dense_len, uint8_t *__restrict__ records) {
+                     int64_t dense_len, uint8_t *__restrict__ records, int32_t item_lo, int32_t item_hi) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -157,9 +157,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         if (dense) pdl_wait();
         return;
     }
-    // persistent: CTA b takes items b, b + gridDim.x, ...; item = slot * H + h
-    const int n_items = (dense ? N * cps : chunk_off[N]) * H;
-    if ((int)blockIdx.x >= n_items) {
+    // persistent: CTA b takes items lo + b, lo + b + gridDim.x, ... below hi, where [lo, hi)
+    // is this launch's share of the items (item = slot * H + h)
+    const int n_all = (dense ? N * cps : chunk_off[N]) * H;
+    const int lo = min(item_lo, n_all), n_items = min(item_hi, n_all);
+    if ((int)blockIdx.x >= n_items - lo) {
         if (dense) pdl_wait();
         return;
     }
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
     };
 
     // ---- prologue: the first item's inputs and gate, the second item's z ---------------
-    int item = blockIdx.x, iters = 0;
+    int item = lo + (int)blockIdx.x, iters = 0;
     Item cur = item_of(item);
     Item nxt = item + (int)gridDim.x < n_items ? item_of(item + gridDim.x) : cur;
     stage_z(cur, 0);
@@ -692,8 +694,8 @@ size_t intra_smem_bytes() { return sizeof(IntraSmem); }
 
 cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *z,
                          const float *A, const float *b, int32_t *status, const int32_t *seq_cu,
-                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t nslots,
-                         uint8_t *records, int num_sms, cudaStream_t st) {
+                         const int32_t *chunk_off, int32_t N, int32_t H, int64_t dense_len, int64_t items,
+                         int32_t item_lo, int32_t item_hi, uint8_t *records, int num_sms, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kda_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -701,12 +703,11 @@ cudaError_t launch_intra(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    if (nslots <= 0) return cudaSuccess;
-    // persistent: one CTA per SM (the shared memory and TMEM allow no more) walks the items
-    const int64_t items = nslots * H;
-    const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)num_sms);
+    // persistent: one CTA per SM (the shared memory and TMEM allow no more) walks the items;
+    // items bounds this launch's share (at least one CTA runs, to keep the launch chain)
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)num_sms));
     return launch_after(kda_intra_kernel, dim3(grid), dim3(kIntraThreads), sizeof(IntraSmem), st, q, k, v, z, A, b,
-                        status, seq_cu, chunk_off, N, H, dense_len, records);
+                        status, seq_cu, chunk_off, N, H, dense_len, records, item_lo, item_hi);
 }
 
 }  // namespace kda

@@ -66,10 +66,6 @@ constexpr int kPlanSortMax = 1024;  // plain walks of up to this many sequences 
 //            on the tensor cores (the chained form is taken only when all of phase C runs
 //            in one wave, so the longest chain is what it adds).
 // ---------------------------------------------------------------------------------
-// cost of chaining one segment map before an output walk, in 1/16 of an output chunk step
-// (about 1.7 against 3.1 us, measured)
-constexpr int32_t kChainStep16 = 9;
-
 __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, const int32_t *__restrict__ chunk_off,
                               int32_t N, int32_t H, const float *S0, float *Sout, const SegPlan &sp) {
     const int32_t P = sp.P;
@@ -119,36 +115,9 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
             float *fin = Sout + (size_t)n * seg_stride;
             // an empty sequence: its final state is its initial state
             if (S == 0 && pass == 1) unitsA[a++] = blank(init, fin, c0, t0, 0);
-            // Chained form: the output walk of segment k >= 1 first chains k - 1 maps, each
-            // about kChainStep16 / 16 of a chunk step, so the cut evens out chain plus chunks:
-            // segment k takes min(P, (t - kChainStep16 (k - 1)) / 16) chunks (segment 0:
-            // min(P, t / 16)) for the lowest level t in 1/16 chunks whose lengths reach len,
-            // and the segments that grew at that level give back the surplus, the last ones
-            // first. Every segment keeps at least one and at most P chunks.
+            // chained form: the balanced cut (kda_common.cuh)
             const bool balanced = sp.chain_mode && !ends && S >= 3;
-            auto seg_len = [&](int32_t t16, int32_t k) {
-                const int32_t x = t16 - kChainStep16 * max(k - 1, 0);
-                return x < 16 ? 1 : min(P, x >> 4);
-            };
-            int32_t level = 0, grown = 0, surplus = 0;
-            if (balanced) {
-                auto total = [&](int32_t t16) {
-                    int32_t sum = 0;
-                    for (int32_t k = 0; k < S; ++k) sum += seg_len(t16, k);
-                    return sum;
-                };
-                int32_t lo = 0, hi = 16 * P + kChainStep16 * S;  // total(hi) = S P >= len
-                while (lo < hi) {
-                    const int32_t mid = (lo + hi) / 2;
-                    if (total(mid) >= len)
-                        hi = mid;
-                    else
-                        lo = mid + 1;
-                }
-                level = lo;
-                surplus = total(level) - len;
-                for (int32_t k = 0; k < S; ++k) grown += seg_len(level, k) > seg_len(level - 1, k);
-            }
+            const BalancedCut cut(balanced ? len : 0, P, balanced ? S : 0);
             int32_t pos = 0, grown_seen = 0;
             for (int32_t sg = 0; sg < S; ++sg) {
                 int32_t cb, ce;  // the segment's chunks, relative to the sequence
@@ -156,9 +125,9 @@ __device__ void plan_segments(bool bad, const int32_t *__restrict__ seq_cu, cons
                     cb = sg == 0 ? 0 : (sg == S - 1 ? len - E * P : E * P + (sg - 1) * P);
                     ce = sg == 0 ? E * P : (sg == S - 1 ? len : min(cb + P, len - E * P));
                 } else if (balanced) {
-                    int32_t L = seg_len(level, sg);
-                    if (L > seg_len(level - 1, sg)) {
-                        if (grown_seen >= grown - surplus) --L;
+                    int32_t L = BalancedCut::len_at(cut.level, sg, P);
+                    if (cut.grew(sg)) {
+                        if (grown_seen >= cut.grown - cut.surplus) --L;
                         ++grown_seen;
                     }
                     cb = pos;

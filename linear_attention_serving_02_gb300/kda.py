@@ -40,6 +40,8 @@ def library():
         lib.kda_chunk_prefill_workspace_size.restype = ctypes.c_size_t
         lib.kda_chunk_prefill_launch_count.argtypes = [i64, i32, i32]
         lib.kda_chunk_prefill_launch_count.restype = i32
+        lib.kda_chunk_prefill_walk_form.argtypes = [i64, i32, i32]
+        lib.kda_chunk_prefill_walk_form.restype = i32
         lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                           i32, i64, i32, i32, i32, i32,
                                           vp, i32, vp, vp, ctypes.c_size_t, vp]
@@ -98,9 +100,15 @@ def kda_chunk_prefill_workspace_size(total_tokens, num_seqs, num_heads):
 
 
 def kda_chunk_prefill_launch_count(total_tokens, num_seqs, num_heads):
-    """Kernels one kda_chunk_prefill call with these sizes launches: 3, or for a segmented
-    walk 4 (its output walks chain the segment maps) or 5 (a combine kernel chains them)."""
+    """Kernels one kda_chunk_prefill call with these sizes launches: 3, or 5 for a
+    segmented walk (include/kda.h)."""
     return int(library().kda_chunk_prefill_launch_count(int(total_tokens), int(num_seqs), int(num_heads)))
+
+
+def kda_chunk_prefill_walk_form(total_tokens, num_seqs, num_heads):
+    """How the state walk runs for these sizes: 0 one pass per chain, 1 segments whose
+    output walks chain the segment maps, 2 segments chained by a combine kernel."""
+    return int(library().kda_chunk_prefill_walk_form(int(total_tokens), int(num_seqs), int(num_heads)))
 
 
 def _prefill_args(q, k, v, z, A, b, initial_state, cu_seqlens, cu_seqlens_host, o, final_state, o_dtype):

@@ -79,10 +79,15 @@ def test_launch_count():
     assert lc(8192 * 64, 64, 32) == 3
     # short chains are not worth splitting
     assert lc(256, 1, 2) == 3
-    # one long sequence over few heads: segmented walk, every output walk in one wave
-    # chaining the maps itself (4), or more segments than that and a combine kernel (5)
-    assert lc(8192, 1, 12) == 4
+    # one long sequence over few heads: segmented walk (5 launches), every output walk in
+    # one wave chaining the maps itself (form 1), or more segments than that and a combine
+    # kernel (form 2)
+    assert lc(8192, 1, 12) == 5
     assert lc(1 << 20, 1, 12) == 5
+    wf = kda.kda_chunk_prefill_walk_form
+    assert wf(-1, 1, 1) == -1 and wf(0, 0, 4) == 0
+    assert wf(8192 * 64, 64, 32) == 0 and wf(256, 1, 2) == 0
+    assert wf(8192, 1, 12) == 1 and wf(1 << 20, 1, 12) == 2
 
 
 def _prefill(**over):

@@ -35,7 +35,7 @@ def test_walk_wait_runs_out_and_is_reported(T, skip):
     o = torch.empty(inp["q"].shape, dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
     if skip < 0:  # the map chain runs only in the chained segmented form
-        assert kda.kda_chunk_prefill_launch_count(T, 1, H) == 4
+        assert kda.kda_chunk_prefill_walk_form(T, 1, H) == 1
     kda.kda_debug_walk_fault(skip, 1_000_000)  # waits give up after 1 ms
     try:
         _, S = kda.kda_chunk_prefill(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"],

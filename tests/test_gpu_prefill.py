@@ -268,10 +268,11 @@ def test_segmented_walk_random(seed):
         else:
             lens.append(int(rng.integers(2000, 4000)))
     total = int(sum(lens))
-    if kda.kda_chunk_prefill_launch_count(total, n, H) == 3:
+    if kda.kda_chunk_prefill_walk_form(total, n, H) == 0:
         lens[0] += 64 * 24 * n  # long enough on average for the segmented walk
         total = int(sum(lens))
-    assert kda.kda_chunk_prefill_launch_count(total, n, H) in (4, 5), (lens, H)
+    assert kda.kda_chunk_prefill_walk_form(total, n, H) in (1, 2), (lens, H)
+    assert kda.kda_chunk_prefill_launch_count(total, n, H) == 5
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
     inp = inputs.prefill_inputs(total, H, n, seed=200 + seed, init_state=True)
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
@@ -296,18 +297,18 @@ def _slow_memory(inp, log_a=0.001, b_mean=-3.0, seed=0):
     return inp
 
 
-@pytest.mark.parametrize("lens,H,launches", [([3000, 1800], 2, 4), ([5000], 1, 4), ([10240, 10000, 10480], 5, 5)])
-def test_segmented_walk_slow_memory(lens, H, launches):
+@pytest.mark.parametrize("lens,H,form", [([3000, 1800], 2, 1), ([5000], 1, 1), ([10240, 10000, 10480], 5, 2)])
+def test_segmented_walk_slow_memory(lens, H, form):
     """The segmented walk where the segment maps matter: with weak decay and weak writes
     the map M of a segment (its state from the identity) stays of order one, so the
     products M S_in carry the state from segment to segment ('From Linear Attention to
     KDA', §7.5). Both forms: each output walk chaining the maps before it on the tensor
-    cores (4 launches; [5000] x 1 cuts ten segments, so the last one chains eight maps),
-    and the combine kernel (5 launches: 3 sequences x 5 heads in 32-segment tables).
+    cores (form 1; [5000] x 1 cuts ten segments, so the last one chains eight maps),
+    and the combine kernel (form 2: 3 sequences x 5 heads in 32-segment tables).
     Against the oracle, element by element."""
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
     n = len(lens)
-    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == launches, (lens, H)
+    assert kda.kda_chunk_prefill_walk_form(cu[-1], n, H) == form, (lens, H)
     inp = _slow_memory(inputs.prefill_inputs(cu[-1], H, n, seed=31, init_state=True), seed=32)
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"],
                                       cu_seqlens=cu)
@@ -326,7 +327,7 @@ def test_segmented_walk_long_ends(lens, H, E, init):
     cut must change the rounding against the uniform one."""
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
     n = len(lens)
-    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == 5, (lens, H)
+    assert kda.kda_chunk_prefill_walk_form(cu[-1], n, H) == 2, (lens, H)
     inp = _slow_memory(inputs.prefill_inputs(cu[-1], H, n, seed=37, init_state=init), seed=38)
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"],
                                       S0=inp["S0"] if init else None, cu_seqlens=cu)
@@ -340,14 +341,35 @@ def test_segmented_walk_long_ends(lens, H, E, init):
     assert not torch.equal(S, S1)
 
 
-@pytest.mark.parametrize("lens,H,launches", [([3000, 1800], 2, 4), ([10240, 10000, 10480], 5, 5)])
-def test_segmented_walk_without_initial_state(lens, H, launches):
+@pytest.mark.parametrize("T,B,H", [(4096, 2, 12), (8192, 2, 6)])
+def test_dense_segmented_walk_defers_intra_items(T, B, H):
+    """Dense batches in the chained form whose intra-chunk items pass a whole number of
+    rounds of the GPU's SMs: the items past k * SMs - 1 (the last chunks of the last
+    sequence, read only by its last output walk) run in a second intra-chunk launch beside
+    the map walk. o, final_state and the workspace start as NaN bytes, so an output walk
+    that read a record before that launch wrote it would show; against the oracle."""
+    assert kda.kda_chunk_prefill_walk_form(B * T, B, H) == 1
+    inp = inputs.prefill_inputs(B * T, H, B, seed=41, init_state=True, batch_rows=B)
+    g = _cuda(inp)
+    o = torch.full(tuple(inp["q"].shape), float("nan"), dtype=torch.float32, device="cuda")
+    S = torch.full((B, H, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.full((kda.kda_chunk_prefill_workspace_size(B * T, B, H),), 0xFF, dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_prefill(g["q"], g["k"], g["v"], g["z"], g["A"], g["b"], initial_state=g["S0"], o=o,
+                          final_state=S, workspace=ws, o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(S).all()
+    o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], S0=inp["S0"])
+    assert_prefill_close(o.cpu(), S.cpu(), o_ref, S_ref, "dense %d x %d x %d" % (B, T, H))
+
+
+@pytest.mark.parametrize("lens,H,form", [([3000, 1800], 2, 1), ([10240, 10000, 10480], 5, 2)])
+def test_segmented_walk_without_initial_state(lens, H, form):
     """Both segmented forms with no initial state (zero): segment 0 starts from zero in
     both phases, every later segment from what the maps carry. Weak decay and writes, so
     the maps matter; against the oracle."""
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
     n = len(lens)
-    assert kda.kda_chunk_prefill_launch_count(cu[-1], n, H) == launches, (lens, H)
+    assert kda.kda_chunk_prefill_walk_form(cu[-1], n, H) == form, (lens, H)
     inp = _slow_memory(inputs.prefill_inputs(cu[-1], H, n, seed=35), seed=36)
     o_ref, S_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["b"], cu_seqlens=cu)
     o, S = gpu_prefill(inp, cu=cu, S0=None)
