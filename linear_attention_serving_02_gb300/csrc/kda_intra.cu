@@ -430,11 +430,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
                 scale_split_pk(kw[p2], f[2 * p2], f[2 * p2 + 1], eh[p2], el[p2]);
             }
             *reinterpret_cast<uint4 *>(s.kv + ak_off(c, j)) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-            *reinterpret_cast<uint4 *>(rec + kRecQh + il_off(j, c, kD)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-            *reinterpret_cast<uint4 *>(rec + kRecQl + il_off(j, c, kD)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
-            *reinterpret_cast<uint4 *>(rec + kRecAK + ak_off(kC + c, j)) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
-            *reinterpret_cast<uint4 *>(rec + kRecAK + kStackAK + ak_off(kC + c, j)) =
-                make_uint4(el[0], el[1], el[2], el[3]);
+            // record stores stream past L2 (st.global.cs): the walk reads them only later
+            __stcs(reinterpret_cast<uint4 *>(rec + kRecQh + il_off(j, c, kD)), make_uint4(qh[0], qh[1], qh[2], qh[3]));
+            __stcs(reinterpret_cast<uint4 *>(rec + kRecQl + il_off(j, c, kD)), make_uint4(ql[0], ql[1], ql[2], ql[3]));
+            __stcs(reinterpret_cast<uint4 *>(rec + kRecAK + ak_off(kC + c, j)), make_uint4(eh[0], eh[1], eh[2], eh[3]));
+            __stcs(reinterpret_cast<uint4 *>(rec + kRecAK + kStackAK + ak_off(kC + c, j)),
+                   make_uint4(el[0], el[1], el[2], el[3]));
         };
         static_assert(kC * (kD / 8) == 2 * kIntraThreads, "two Khat jobs per thread");
         if (warp != 0) {
@@ -471,9 +472,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
             // 8 consecutive query rows of key j: one MN-major 16-byte unit per plane (none in
             // the blocks wholly above the diagonal, which the record leaves out)
             if (!aqk_zero_block(ib, j)) {
-                *reinterpret_cast<uint4 *>(rec + kRecAqk + ak_off(ib, j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(rec + kRecAqk + kStackAK + ak_off(ib, j)) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                __stcs(reinterpret_cast<uint4 *>(rec + kRecAqk + ak_off(ib, j)),
+                       make_uint4(hi[0], hi[1], hi[2], hi[3]));
+                __stcs(reinterpret_cast<uint4 *>(rec + kRecAqk + kStackAK + ak_off(ib, j)),
+                       make_uint4(lo[0], lo[1], lo[2], lo[3]));
             }
             const float *be = s.beta[b];
 #pragma unroll
@@ -668,8 +670,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1)
         tc::fence_before_sync();  // and the TMEM reads are ordered before the next item's writes
         __syncthreads();
         if (tid == 0) {
-            tc::bulk_s2g(rec + kRecW, s.u.e.w, (uint32_t)kPlaneQK);
-            tc::bulk_s2g(rec + kRecUp, s.u.e.up, (uint32_t)(kC * kD * 4));
+            tc::bulk_s2g_ef(rec + kRecW, s.u.e.w, (uint32_t)kPlaneQK);
+            tc::bulk_s2g_ef(rec + kRecUp, s.u.e.up, (uint32_t)(kC * kD * 4));
             tc::bulk_commit();
         }
         cur = nxt;

@@ -174,6 +174,14 @@ __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t by
                  "r"(bytes)
                  : "memory");
 }
+// the same with an L2 evict-first policy: for data that no kernel reads again soon (the
+// chunk records, read by the state walk only after the intra kernel has moved on)
+__device__ __forceinline__ void bulk_s2g_ef(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("{\n.reg .b64 pol;\ncreatepolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
+                 "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, pol;\n}\n" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // wait until the shared memory of this thread's bulk stores has been read (it may be reused)
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
